@@ -1,0 +1,163 @@
+"""Attention of a new frame's queries over the ring cache, plain CPU model.
+
+Test infrastructure only; nothing in the library imports it.
+
+"Where the Time Went" and "Blackwell and Beyond Four GPUs" on the Runway
+Characters page: every attention call of a step reads its layer's cache of
+5,788 slots, with FP8 keys and values that carry per-head scales.  Keys
+already hold their rotation (RoPE at write time), so slot order does not
+matter; queries are rotated by their own positions.  The pages give no
+softmax scale or mask; this oracle takes the usual 1/sqrt(d), no causal mask
+(every query sees every filled slot), and leaves empty slots out.
+
+``attention_exact`` is the reference the CUDA path is judged against: the
+queries in float64 without any quantisation, keys and values dequantised
+from the same FP8 cache bytes (code value times the fp32 scale, in float64),
+and a float64 softmax with the row maximum subtracted.
+
+``attention_emulated`` is a diagnostic that repeats the CUDA kernel's
+choices (queries split into FP8 terms with a per-row scale, probabilities
+scaled by 2^8 relative to a lazily updated running maximum and split into FP8
+terms, a normaliser summed from the same FP8 terms) in float64, so that
+format error and kernel bugs can be told apart.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import e4m3
+from .rope import rotate_f64
+
+INT32_MIN = -(2 ** 31)
+
+
+def softmax_attention_f64(qt: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """o[t,h,:] = sum_j softmax_j(qt[t,h]·k[h,j] / sqrt(d)) v[h,j,:] in float64.
+
+    qt [n, H, d]; k, v [H, m, d].  m = 0 gives zeros.
+    """
+    n, H, d = qt.shape
+    if k.shape[1] == 0:
+        return np.zeros((n, H, d), dtype=np.float64)
+    s = np.einsum("thd,hjd->thj", qt, k) / math.sqrt(d)
+    s = s - s.max(axis=2, keepdims=True)
+    p = np.exp(s)
+    p /= p.sum(axis=2, keepdims=True)
+    return np.einsum("thj,hjd->thd", p, v)
+
+
+def attention_exact(ring, q: np.ndarray, qpos=None) -> np.ndarray:
+    """Reference attention of queries q (float32 [n, H, d]) over ``ring``.
+
+    qpos defaults to the n positions just before ``ring.next_pos``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n = q.shape[0]
+    if qpos is None:
+        qpos = ring.next_pos - n + np.arange(n)
+    qt = rotate_f64(q, np.asarray(qpos, dtype=np.int64), ring.table.theta)
+    k, v, _ = ring.dequantised()
+    return softmax_attention_f64(qt, k, v)
+
+
+def attention_linear_window(history, q, qpos, ring) -> np.ndarray:
+    """Brute force over the last ``capacity`` written tokens in time order.
+
+    ``history`` is a list of (k_codes [n,H,d], v_codes [n,H,d], positions)
+    as they were quantised at write time.  Uses the ring's scales.
+    """
+    kc = np.concatenate([h[0] for h in history], axis=0)
+    vc = np.concatenate([h[1] for h in history], axis=0)
+    kc = kc[-ring.C:]
+    vc = vc[-ring.C:]
+    k = e4m3.decode(kc).transpose(1, 0, 2) * ring.scale_k.astype(np.float64)[:, None, None]
+    v = e4m3.decode(vc).transpose(1, 0, 2) * ring.scale_v.astype(np.float64)[:, None, None]
+    qt = rotate_f64(np.asarray(q, np.float64), np.asarray(qpos, np.int64), ring.table.theta)
+    return softmax_attention_f64(qt, k, v)
+
+
+def attention_positions_by_slot_order(raw_k, raw_v, n_valid, q, qpos, th,
+                                      first_position: int = 0) -> np.ndarray:
+    """The combination the page pins as invalid: keys cached without rotation
+    in a ring, rotated at read time with positions assigned by slot order
+    (slot j gets ``first_position + j``).
+
+    raw_k, raw_v float64 [H, C, d] (unrotated, unquantised); uses slots
+    [0, n_valid).  Correct only while slot order equals time order.
+    """
+    k = raw_k[:, :n_valid, :]
+    v = raw_v[:, :n_valid, :]
+    pos = first_position + np.arange(n_valid)
+    kt = rotate_f64(k.transpose(1, 0, 2), pos, th).transpose(1, 0, 2)
+    qt = rotate_f64(np.asarray(q, np.float64), np.asarray(qpos, np.int64), th)
+    return softmax_attention_f64(qt, kt, v)
+
+
+def attention_true_positions(raw_k, raw_v, slot_pos, q, qpos, th) -> np.ndarray:
+    """Same raw ring, each slot rotated by its own recorded position."""
+    sl = np.nonzero(np.asarray(slot_pos) != INT32_MIN)[0]
+    k = raw_k[:, sl, :]
+    v = raw_v[:, sl, :]
+    kt = rotate_f64(k.transpose(1, 0, 2), np.asarray(slot_pos)[sl], th).transpose(1, 0, 2)
+    qt = rotate_f64(np.asarray(q, np.float64), np.asarray(qpos, np.int64), th)
+    return softmax_attention_f64(qt, kt, v)
+
+
+def _split_terms(u: np.ndarray, m: int):
+    """Split float values into m FP8 terms by successive residuals."""
+    terms = []
+    r = u.astype(np.float32)
+    for _ in range(m):
+        c = e4m3.decode(e4m3.encode(r))
+        terms.append(c)
+        r = (r - c.astype(np.float32)).astype(np.float32)
+    return terms
+
+
+def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
+                       p_shift=8.0, tau=0.5) -> np.ndarray:
+    """Diagnostic: the CUDA kernel's quantisation choices, in float64.
+
+    q_terms / p_terms may be ints or per-head sequences.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n, H, d = q.shape
+    if qpos is None:
+        qpos = ring.next_pos - n + np.arange(n)
+    qt = rotate_f64(q, np.asarray(qpos, np.int64), ring.table.theta).astype(np.float32)
+    amax = np.abs(qt).max(axis=2)                                # [n, H]
+    sq = (amax / np.float32(448.0)).astype(np.float32)
+    sq = np.where(sq >= np.float32(2.0 ** -126), sq, np.float32(1.0)).astype(np.float32)
+    invq = (np.float32(1.0) / sq).astype(np.float32)
+    u = (qt * invq[:, :, None]).astype(np.float32)
+    qt_terms = np.broadcast_to(np.asarray(q_terms), (H,))
+    pt_terms = np.broadcast_to(np.asarray(p_terms), (H,))
+    out = np.zeros((n, H, d), dtype=np.float64)
+    nv = ring.n_valid
+    log2e = 1.0 / math.log(2.0)
+    for h in range(H):
+        qsum = sum(_split_terms(u[:, h, :], int(qt_terms[h])))   # float64 [n, d]
+        kc = e4m3.decode(ring.K[h, :nv, :])
+        vc = e4m3.decode(ring.V[h, :nv, :])
+        f = (sq[:, h].astype(np.float64) * float(ring.scale_k[h]) * log2e / math.sqrt(d))
+        m = np.full(n, -np.inf)
+        O = np.zeros((n, d))
+        ell = np.zeros(n)
+        for j0 in range(0, nv, tile):
+            x = (qsum @ kc[j0:j0 + tile].T) * f[:, None]
+            mt = x.max(axis=1)
+            upd = (mt > m + tau) | ~np.isfinite(m)
+            alpha = np.where(upd & np.isfinite(m), np.exp2(m - mt), 1.0)
+            alpha = np.where(np.isfinite(m), alpha, 0.0)
+            m = np.where(upd, mt, m)
+            O *= alpha[:, None]
+            ell *= alpha
+            p = np.exp2(x - m[:, None] + p_shift).astype(np.float32)
+            ps = sum(_split_terms(p, int(pt_terms[h])))
+            O += ps @ vc[j0:j0 + tile]
+            ell += ps.sum(axis=1)
+        out[:, h, :] = np.where(ell[:, None] > 0, O / np.maximum(ell, 1e-300)[:, None], 0.0) \
+            * float(ring.scale_v[h])
+    return out

@@ -1,0 +1,159 @@
+"""The rolling FP8 attention cache of one layer, as a plain CPU model.
+
+Test infrastructure only; nothing in the library imports it.
+
+Follows "Do It Once, at Write Time" on the Runway Characters page:
+* keys get RoPE at their true positions once, when they enter the cache;
+* keys and values are quantised to FP8 with per-head scales calibrated once
+  per session;
+* the cache is a ring: a new frame overwrites the oldest slots, with no
+  window copy, so after wrap-around slot order is not time order and every
+  slot carries its own position;
+* positions reset periodically; at a reset one delta rotation is applied to
+  the cached keys in place.
+
+Readings of what the pages leave open (each listed in the design notes):
+* per-head scales for K and for V, each amax/448 over the calibration frame,
+  with K measured after RoPE (the values actually quantised); a scale that
+  is not a normal fp32 number (amax 0 or tiny) is replaced by 1;
+* quantisation multiplies by the IEEE fp32 reciprocal of the scale;
+* slot = (head + t) mod capacity for the t-th new token; empty slots hold
+  position INT32_MIN; writes larger than the ring are rejected;
+* the reset's delta D defaults to the position of the oldest cached slot,
+  so the window restarts at position 0; cached keys are rotated by -D in
+  scaled (code) units, positions and the next position drop by D.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import e4m3
+from .rope import Table, rotate_pinned_f32, unrotate_pinned_f32
+
+INT32_MIN = -(2 ** 31)
+TO_OLDEST = -1
+_TINY_NORMAL = np.float32(2.0 ** -126)
+
+
+def scale_from_amax(amax: np.ndarray) -> np.ndarray:
+    """scale = fl32(amax / 448); not-normal results (0, subnormal) become 1."""
+    a = np.asarray(amax, dtype=np.float32)
+    s = a / np.float32(448.0)
+    return np.where(s >= _TINY_NORMAL, s, np.float32(1.0)).astype(np.float32)
+
+
+class Ring:
+    """One layer's cache: K and V codes as [heads][capacity][head_dim] uint8."""
+
+    def __init__(self, heads: int, head_dim: int, capacity: int,
+                 max_position: int, rope_base: float = 10000.0):
+        self.H, self.d, self.C = heads, head_dim, capacity
+        self.table = Table(head_dim, rope_base, max_position)
+        self.K = np.zeros((heads, capacity, head_dim), dtype=np.uint8)
+        self.V = np.zeros((heads, capacity, head_dim), dtype=np.uint8)
+        self.slot_pos = np.full(capacity, INT32_MIN, dtype=np.int64)
+        self.scale_k = np.ones(heads, dtype=np.float32)
+        self.scale_v = np.ones(heads, dtype=np.float32)
+        self.inv_k = np.ones(heads, dtype=np.float32)
+        self.inv_v = np.ones(heads, dtype=np.float32)
+        self.head = 0
+        self.n_valid = 0
+        self.total = 0
+        self.next_pos = 0
+        self.calibrated = False
+
+    # -- helpers -----------------------------------------------------------
+    def _positions(self, n: int, pos) -> np.ndarray:
+        if pos is None:
+            return self.next_pos + np.arange(n, dtype=np.int64)
+        pos = np.asarray(pos, dtype=np.int64).reshape(-1)
+        if pos.shape[0] != n:
+            raise ValueError("one position per token")
+        return pos
+
+    def _rope(self, k: np.ndarray, positions: np.ndarray) -> np.ndarray:
+        c, s = self.table.rows(positions)                    # [n, d/2]
+        return rotate_pinned_f32(k, c[:, None, :], s[:, None, :])
+
+    # -- the four operations --------------------------------------------------
+    def calibrate(self, k: np.ndarray, v: np.ndarray, pos=None) -> None:
+        """Per-head scales from one frame (k, v float32 [n, H, d])."""
+        k = np.asarray(k, dtype=np.float32)
+        v = np.asarray(v, dtype=np.float32)
+        n = k.shape[0]
+        if n < 1:
+            raise ValueError("calibration needs at least one token")
+        y = self._rope(k, self._positions(n, pos))
+        amax_k = np.abs(y).max(axis=(0, 2))
+        amax_v = np.abs(v).max(axis=(0, 2))
+        self.scale_k = scale_from_amax(amax_k)
+        self.scale_v = scale_from_amax(amax_v)
+        self.inv_k = (np.float32(1.0) / self.scale_k).astype(np.float32)
+        self.inv_v = (np.float32(1.0) / self.scale_v).astype(np.float32)
+        self.calibrated = True
+
+    def quantise_keys(self, k: np.ndarray, positions: np.ndarray) -> np.ndarray:
+        """Codes [n, H, d] of RoPE'd keys: e4m3(fl(rope(k, p) * inv_k[h]))."""
+        y = self._rope(np.asarray(k, dtype=np.float32), positions)
+        return e4m3.encode(y * self.inv_k[None, :, None])
+
+    def quantise_values(self, v: np.ndarray) -> np.ndarray:
+        return e4m3.encode(np.asarray(v, dtype=np.float32) * self.inv_v[None, :, None])
+
+    def slots_for(self, n: int) -> np.ndarray:
+        return (self.head + np.arange(n, dtype=np.int64)) % self.C
+
+    def write(self, k: np.ndarray, v: np.ndarray, pos=None) -> np.ndarray:
+        """Write one frame; returns the slots used."""
+        if not self.calibrated:
+            raise RuntimeError("write before calibration")
+        n = np.asarray(k).shape[0]
+        if not 1 <= n <= self.C:
+            raise ValueError("frame must hold 1..capacity tokens")
+        positions = self._positions(n, pos)
+        slots = self.slots_for(n)
+        kc = self.quantise_keys(k, positions)                # [n, H, d]
+        vc = self.quantise_values(v)
+        self.K[:, slots, :] = kc.transpose(1, 0, 2)
+        self.V[:, slots, :] = vc.transpose(1, 0, 2)
+        self.slot_pos[slots] = positions
+        self.head = int((self.head + n) % self.C)
+        self.n_valid = min(self.C, self.n_valid + n)
+        self.total += n
+        self.next_pos += n
+        return slots
+
+    def oldest_slot(self) -> int:
+        return self.head if self.n_valid == self.C else 0
+
+    def delta_rotate(self, delta: int = TO_OLDEST) -> int:
+        """Rotate every cached key by -delta in place; returns the delta used."""
+        if delta == TO_OLDEST:
+            delta = int(self.slot_pos[self.oldest_slot()]) if self.n_valid else 0
+        delta = int(delta)
+        if delta < 0:
+            raise ValueError("delta must be >= 0")
+        nv = self.n_valid
+        if nv:
+            c, s = self.table.row(delta)
+            a = e4m3.decode(self.K[:, :nv, :]).astype(np.float32)   # exact
+            y = unrotate_pinned_f32(a, c, s)
+            self.K[:, :nv, :] = e4m3.encode(y)
+            self.slot_pos[:nv] -= delta
+        self.next_pos -= delta
+        return delta
+
+    # -- read-side views ------------------------------------------------------
+    def valid_slots(self) -> np.ndarray:
+        return np.nonzero(self.slot_pos != INT32_MIN)[0]
+
+    def dequantised(self):
+        """(k, v) float64 [H, n_valid_slots, d] and their slot indices."""
+        sl = self.valid_slots()
+        k = e4m3.decode(self.K[:, sl, :]) * self.scale_k.astype(np.float64)[:, None, None]
+        v = e4m3.decode(self.V[:, sl, :]) * self.scale_v.astype(np.float64)[:, None, None]
+        return k, v, sl
+
+    def state(self):
+        return dict(head=self.head, n_valid=self.n_valid, total=self.total,
+                    next_pos=self.next_pos, calibrated=int(self.calibrated))

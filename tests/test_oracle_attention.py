@@ -1,0 +1,117 @@
+"""Pins for the oracle's float64 attention over the ring cache.
+
+Checked against: closed forms (equal keys give the mean of the values, one
+filled slot returns its value), a pure-Python brute force on a tiny case,
+and torch's scaled_dot_product_attention in float64 (a library routine).
+The kernel-mirroring diagnostic is checked to converge to the reference as
+its FP8 term counts grow.
+"""
+import math
+
+import numpy as np
+import torch
+
+from oracle import e4m3, Ring
+from oracle.attention import attention_exact, attention_emulated
+from oracle.rope import rotate_f64
+from workloads import TINY, f32_from_bf16, tiny_session, prod_session, PROD
+
+
+def _tiny_ring(frames_written=3):
+    frames = tiny_session()
+    r = Ring(TINY.heads, TINY.head_dim, TINY.capacity, TINY.max_position)
+    r.calibrate(f32_from_bf16(frames[0][1]), f32_from_bf16(frames[0][2]))
+    for f in range(frames_written):
+        r.write(f32_from_bf16(frames[f][1]), f32_from_bf16(frames[f][2]))
+    return r, frames
+
+
+def test_equal_keys_give_mean_of_values():
+    r, frames = _tiny_ring(2)
+    r.K[:, :r.n_valid, :] = r.K[:, :1, :]          # every filled slot holds the same key
+    q = f32_from_bf16(frames[2][0])
+    o = attention_exact(r, q, np.arange(12))
+    _, v, _ = r.dequantised()
+    want = v.mean(axis=1)                           # [H, d]
+    assert np.allclose(o, want[None], atol=1e-12)
+
+
+def test_single_filled_slot_returns_its_value():
+    r = Ring(2, 64, 48, 64)
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((1, 2, 64)).astype(np.float32)
+    v = rng.standard_normal((1, 2, 64)).astype(np.float32)
+    r.calibrate(k, v)
+    r.write(k, v)
+    q = rng.standard_normal((5, 2, 64)).astype(np.float32) * 10
+    o = attention_exact(r, q, np.arange(5))
+    vv = e4m3.decode(r.V[:, 0, :]) * r.scale_v.astype(np.float64)[:, None]
+    assert np.allclose(o, vv[None], atol=1e-12)
+
+
+def test_empty_ring_gives_zeros():
+    r = Ring(2, 64, 48, 64)
+    q = np.ones((3, 2, 64), np.float32)
+    assert np.all(attention_exact(r, q, np.arange(3)) == 0)
+
+
+def test_pure_python_brute_force_tiny():
+    r, frames = _tiny_ring(5)                       # 60 tokens: wrapped
+    q = f32_from_bf16(frames[5][0])[:2]
+    qpos = np.array([70, 71])
+    o = attention_exact(r, q, qpos)
+    th = r.table.theta
+    for t in range(2):
+        for h in range(TINY.heads):
+            # rotate the query by hand
+            qt = []
+            for i in range(TINY.head_dim // 2):
+                a = qpos[t] * th[i]
+                x0, x1 = float(q[t, h, 2 * i]), float(q[t, h, 2 * i + 1])
+                qt += [x0 * math.cos(a) - x1 * math.sin(a), x0 * math.sin(a) + x1 * math.cos(a)]
+            scores = []
+            for j in range(r.C):
+                kj = [float(e4m3.decode(r.K[h, j, i])) * float(r.scale_k[h]) for i in range(TINY.head_dim)]
+                scores.append(sum(a * b for a, b in zip(qt, kj)) / math.sqrt(TINY.head_dim))
+            mx = max(scores)
+            w = [math.exp(s - mx) for s in scores]
+            z = sum(w)
+            for i in range(0, TINY.head_dim, 7):
+                val = sum(w[j] * float(e4m3.decode(r.V[h, j, i])) * float(r.scale_v[h]) for j in range(r.C)) / z
+                assert math.isclose(o[t, h, i], val, rel_tol=1e-10, abs_tol=1e-12)
+
+
+def test_matches_torch_sdpa_float64():
+    r, frames = _tiny_ring(6)
+    q = f32_from_bf16(frames[6][0])
+    qpos = np.arange(72, 84)
+    o = attention_exact(r, q, qpos)
+    qt = rotate_f64(q.astype(np.float64), qpos, r.table.theta)
+    k, v, _ = r.dequantised()
+    Q = torch.from_numpy(qt.transpose(1, 0, 2).copy())[None]       # [1, H, n, d]
+    K = torch.from_numpy(k.copy())[None]
+    V = torch.from_numpy(v.copy())[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V)[0].numpy().transpose(1, 0, 2)
+    assert np.allclose(o, ref, atol=1e-12)
+
+
+def test_kernel_mirror_converges_to_reference():
+    r, frames = _tiny_ring(6)
+    q = f32_from_bf16(frames[6][0])
+    qpos = np.arange(72, 84)
+    ref = attention_exact(r, q, qpos)
+    errs = []
+    for qt, pt in [(1, 1), (2, 2), (3, 2)]:
+        errs.append(np.abs(attention_emulated(r, q, qpos, qt, pt, tile=16) - ref).max())
+    assert errs[0] > errs[1] > errs[2]
+    assert errs[2] < 1e-3
+
+
+def test_kernel_mirror_single_tile_equals_reference_structure():
+    """With enough terms the mirror's normaliser and rescaling are exact:
+    a tile size of 1 (a rescale at every slot) and of 128 agree."""
+    r, frames = _tiny_ring(6)
+    q = f32_from_bf16(frames[6][0])
+    a = attention_emulated(r, q, np.arange(72, 84), 3, 2, tile=1, tau=0.0)
+    b = attention_emulated(r, q, np.arange(72, 84), 3, 2, tile=128)
+    assert np.abs(a - b).max() < 1e-3
