@@ -1,0 +1,190 @@
+/*
+ * kvring -- a rolling FP8 attention cache for one GPU (sm_103a).
+ *
+ * One kvring_t holds one transformer layer's attention cache, as described
+ * in "Runway Characters: Serving a 57B Video Diffusion Transformer for
+ * Real-Time Conversation" (Runway research post):
+ *
+ *   - section "Do It Once, at Write Time": each new frame's keys get rotary
+ *     position embeddings (RoPE) once, as they enter the cache, and keys and
+ *     values are quantised to FP8 with per-head scales calibrated once per
+ *     session; the cache is a ring, so the window advances by overwriting
+ *     the oldest slots with no copy; at each periodic position reset a
+ *     single delta rotation is applied to the cached keys in place; after
+ *     wrap-around slot order is not time order, so every slot keeps its own
+ *     position;
+ *   - section "Where the Time Went": every attention call reads its layer's
+ *     cache (5,788 slots, 757 of them new);
+ *   - sections "What Broke in Production" and "Blackwell and Beyond Four
+ *     GPUs": no host/device synchronisation on the steady path, no buffer
+ *     per input shape, calls that chain correctly inside CUDA graphs, and an
+ *     FP8 attention kernel that takes per-head scales.
+ *
+ * Formats.  FP8 is OCP OFP8 E4M3 ("fn": bias 7, no infinities, largest
+ * finite 448), rounded to nearest even with saturation to +-448.  RoPE is
+ * the adjacent-pair form: pair (x[2i], x[2i+1]) rotates by p * base^(-2i/d).
+ *
+ * Conventions for every entry point.
+ *   - Tensors are device pointers, row-major and contiguous, 16-byte
+ *     aligned.  Token inputs are bf16 [n][num_heads][head_dim] (what a QKV
+ *     projection emits).  Positions are int32 [n] on the device.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on that stream; none synchronises with the
+ *     host, none allocates memory.  Calls on one ring must be ordered (one
+ *     stream, or the caller's events); two rings are independent.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     failed check enqueues nothing and returns an error status.  CUDA
+ *     launch failures return KVRING_ERR_CUDA.  Problems only the device can
+ *     see (a position outside the RoPE table, a timed-out wait) set bits in
+ *     an error word that kvring_export() returns in state[KVRING_STATE_ERROR];
+ *     the kernels then skip the offending element instead of faulting.
+ *   - The ring's head, fill level and next position live in device memory,
+ *     so a CUDA graph that captured a write or an attention call advances
+ *     the ring correctly on every replay.
+ */
+#ifndef KVRING_H
+#define KVRING_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvring kvring_t;   /* opaque host handle, one per layer */
+
+typedef enum {
+  KVRING_OK = 0,
+  KVRING_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size or config */
+  KVRING_ERR_NOT_CALIBRATED = 2,  /* write or attention before calibration */
+  KVRING_ERR_CAPACITY = 3,        /* more tokens than the ring or config allows */
+  KVRING_ERR_UNSUPPORTED = 4,     /* head_dim or device not supported */
+  KVRING_ERR_CUDA = 5             /* a CUDA runtime call or launch failed */
+} kvring_status;
+
+typedef struct {
+  int32_t num_heads;      /* H >= 1 */
+  int32_t head_dim;       /* d: 64 or 128 */
+  int32_t capacity;       /* C ring slots, 1 .. 2^24 */
+  int32_t max_tokens;     /* most tokens per write / calibration / attention call */
+  int32_t max_position;   /* RoPE table rows: positions lie in [0, max_position) */
+  int32_t max_kv_splits;  /* most key/value partitions one attention call may use (>= 1) */
+  int32_t attn_precision; /* 0 = automatic per tile; 1..3 = fixed FP8 term level */
+  int32_t reserved;       /* must be 0 */
+  double rope_base;       /* RoPE base, e.g. 10000 */
+} kvring_config;
+
+#define KVRING_DELTA_TO_OLDEST (-1)
+#define KVRING_OUT_F32 0
+#define KVRING_OUT_BF16 1
+
+/* Layout of the int32 state[] array returned by kvring_export(). */
+#define KVRING_STATE_HEAD 0        /* next slot to be written */
+#define KVRING_STATE_NVALID 1      /* filled slots: min(capacity, tokens written) */
+#define KVRING_STATE_TOTAL_LO 2    /* tokens written, low 32 bits */
+#define KVRING_STATE_TOTAL_HI 3    /* tokens written, high 32 bits */
+#define KVRING_STATE_NEXT_POS 4    /* position given to the next token by default */
+#define KVRING_STATE_CALIBRATED 5  /* 1 once scales are set */
+#define KVRING_STATE_ERROR 6       /* device error bits, see KVRING_DEVERR_* */
+#define KVRING_STATE_LAST_DELTA 7  /* delta used by the last delta rotation */
+#define KVRING_STATE_WORDS 8
+
+#define KVRING_DEVERR_POSITION 1u  /* a position outside [0, max_position) was skipped */
+#define KVRING_DEVERR_TIMEOUT 2u   /* a pipeline wait in the attention kernel gave up */
+#define KVRING_DEVERR_DELTA 4u     /* delta outside [0, max_position): rotation skipped */
+
+/* Bytes of device memory one ring needs (cache, scales, positions, state,
+ * RoPE table, attention workspace).  0 if the config is invalid. */
+size_t kvring_required_bytes(const kvring_config* cfg);
+
+/* Create a ring inside `dev_buf` (device memory of at least
+ * kvring_required_bytes(cfg) bytes, 256-byte aligned, owned by the caller,
+ * which must keep it alive until kvring_destroy and free it afterwards).
+ * Clears the ring, uploads the RoPE table and builds the TMA descriptors.
+ * This is the only call that synchronises (it waits for its own upload on
+ * `stream`).  On success *out receives the handle. */
+kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t bytes,
+                            void* stream, kvring_t** out);
+
+/* Free the host handle.  The device buffer stays the caller's. */
+kvring_status kvring_destroy(kvring_t* ring);
+
+/* Once per session ("Do It Once, at Write Time": per-head scales calibrated
+ * once per session).  k, v: bf16 [n][H][d]; pos: int32 [n] device positions
+ * of the keys, or NULL for next_pos + i.  For each head h:
+ *   scale_k[h] = max |rope(k)[., h, .]| / 448, scale_v[h] = max |v[., h, .]| / 448
+ * (IEEE single division; a result below 2^-126, e.g. an all-zero head,
+ * becomes 1), and the reciprocals used for quantisation.  Writes nothing
+ * into the ring; usually followed by kvring_write_frame of the same frame.
+ * Errors: INVALID_ARG (n < 1, bad pointers), CAPACITY (n > max_tokens). */
+kvring_status kvring_calibrate_scales(kvring_t* ring, const void* k_bf16, const void* v_bf16,
+                                      const int32_t* pos, int32_t n, void* stream);
+
+/* Write one frame of n new tokens ("Do It Once, at Write Time").
+ * Token t goes to slot (head + t) mod capacity:
+ *   K[h][slot][:] = e4m3(rope(k[t,h,:], pos[t]) * inv_scale_k[h])
+ *   V[h][slot][:] = e4m3(v[t,h,:] * inv_scale_v[h])
+ *   slot_pos[slot] = pos[t]
+ * then head += n (mod capacity), n_valid = min(capacity, n_valid + n),
+ * total += n, next_pos += n.  RoPE is computed in fp32 from the fp32
+ * cos/sin table with every product and sum rounded separately.
+ * pos: int32 [n] device positions, or NULL for next_pos + t.
+ * Errors: NOT_CALIBRATED, CAPACITY (n > capacity or n > max_tokens), INVALID_ARG. */
+kvring_status kvring_write_frame(kvring_t* ring, const void* k_bf16, const void* v_bf16,
+                                 const int32_t* pos, int32_t n, void* stream);
+
+/* Position reset ("Do It Once, at Write Time": one delta rotation of the
+ * cached window at each reset).  Every filled slot's key is rotated by
+ * -delta in place, in the FP8 code units (no rescaling): for each pair
+ * (a, b) of decoded codes and the table row (c, s) of delta,
+ *   a' = a*c + b*s,  b' = b*c - a*s   (fp32, each step rounded), then e4m3.
+ * slot_pos -= delta for filled slots, next_pos -= delta.  Values are not
+ * touched.  delta = KVRING_DELTA_TO_OLDEST reads, on the device, the
+ * position of the oldest slot (the next slot to be overwritten once the
+ * ring is full, slot 0 before), so the window restarts at position 0.
+ * Errors: INVALID_ARG (delta < -1 or >= max_position). */
+kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
+
+/* FP8 attention of n_q queries over the ring ("Where the Time Went";
+ * "Blackwell and Beyond Four GPUs": FP8 attention with per-head scales).
+ *   out[t,h,:] = sum_j softmax_j(rope(q[t,h,:], qpos[t]) . Kdeq[h,j,:] / sqrt(d)) Vdeq[h,j,:]
+ * over the filled slots j, with Kdeq = code * scale_k[h], Vdeq = code *
+ * scale_v[h].  Slot order does not matter: keys carry their rotation.
+ * Queries are split into FP8 terms with a per-row scale and the
+ * probabilities into FP8 terms (1 to 3 and 1 to 2 terms; the level is
+ * chosen per 128-query tile from the query and key ranges unless
+ * attn_precision fixes it); products accumulate in fp32 on the tensor cores.
+ * q: bf16 [n_q][H][d]; qpos: int32 [n_q] device positions, or NULL for
+ * next_pos - n_q + t (the positions of the last n_q tokens written with
+ * default positions).  out: [n_q][H][d], fp32 (KVRING_OUT_F32) or bf16
+ * (KVRING_OUT_BF16).  An empty ring gives zeros.
+ * Errors: NOT_CALIBRATED, CAPACITY (n_q > max_tokens), INVALID_ARG. */
+kvring_status kvring_attention(kvring_t* ring, const void* q_bf16, const int32_t* qpos,
+                               int32_t n_q, void* out, int32_t out_dtype, void* stream);
+
+/* Copy the ring out for inspection (tests, snapshots).  Any pointer may be
+ * NULL to skip that part.  k_out, v_out: uint8 [H][capacity][d] codes;
+ * scales: float [4H] = scale_k, scale_v, inv_scale_k, inv_scale_v;
+ * slot_pos: int32 [capacity] (INT32_MIN = empty); state: int32
+ * [KVRING_STATE_WORDS].  Destinations may be device or pinned host memory;
+ * the copies are enqueued on `stream` (the caller synchronises). */
+kvring_status kvring_export(kvring_t* ring, void* k_out, void* v_out, float* scales,
+                            int32_t* slot_pos, int32_t* state, void* stream);
+
+/* Test support, not part of the cache: encode n fp32 values to E4M3 codes
+ * with the same conversion the kernels use (device pointers). */
+kvring_status kvring_debug_encode_e4m3(const float* in, uint8_t* out, int64_t n, void* stream);
+
+/* Test support: the precision level (1..3) each attention tile used in the
+ * last kvring_attention call, int32 [ceil(n_q/128)][H], copied to `levels`
+ * (device or pinned host) on `stream`. */
+kvring_status kvring_debug_attention_levels(kvring_t* ring, int32_t* levels, void* stream);
+
+/* Static text for a status code. */
+const char* kvring_status_string(kvring_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVRING_H */

@@ -1,0 +1,281 @@
+"""Python binding of the kvring C ABI (``include/kvring.h``).
+
+Argument marshalling only: every step of the cache's arithmetic runs in the
+CUDA kernels of ``libkvring.so``.  PyTorch supplies device memory (one
+``uint8`` buffer per ring, allocated once), streams and tensors.  There is
+no CPU path: if the library is not built, or no sm_103a GPU is present,
+calls raise.
+
+The functions carry the C names (``kvring_create``, ``kvring_calibrate_scales``,
+``kvring_write_frame``, ``kvring_delta_rotate``, ``kvring_attention``,
+``kvring_export``); ``KvRing`` wraps them for one layer's cache.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+__all__ = [
+    "KvRing", "KvRingError", "TO_OLDEST", "lib", "library_path", "header_functions",
+    "kvring_required_bytes", "kvring_create", "kvring_destroy", "kvring_calibrate_scales",
+    "kvring_write_frame", "kvring_delta_rotate", "kvring_attention", "kvring_export",
+    "kvring_status_string", "encode_e4m3", "STATE",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+HEADER = os.path.join(ROOT, "include", "kvring.h")
+
+TO_OLDEST = -1
+OUT_F32, OUT_BF16 = 0, 1
+STATE = dict(head=0, n_valid=1, total_lo=2, total_hi=3, next_pos=4, calibrated=5, error=6,
+             last_delta=7)
+STATE_WORDS = 8
+DEVERR_POSITION, DEVERR_TIMEOUT, DEVERR_DELTA = 1, 2, 4
+
+
+class KvringConfig(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("capacity", ctypes.c_int32),
+        ("max_tokens", ctypes.c_int32),
+        ("max_position", ctypes.c_int32),
+        ("max_kv_splits", ctypes.c_int32),
+        ("attn_precision", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("rope_base", ctypes.c_double),
+    ]
+
+
+class KvRingError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {kvring_status_string(status)} (status {status})")
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return os.path.join(HERE, "libkvring.so")
+
+
+def lib():
+    """Load libkvring.so (built in-tree by ``ring_kv_cache_gb300.build``)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run `python -m ring_kv_cache_gb300.build`")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    cfgp = ctypes.POINTER(KvringConfig)
+    sig = {
+        "kvring_required_bytes": (sz, [cfgp]),
+        "kvring_create": (i32, [cfgp, vp, sz, vp, ctypes.POINTER(vp)]),
+        "kvring_destroy": (i32, [vp]),
+        "kvring_calibrate_scales": (i32, [vp, vp, vp, vp, i32, vp]),
+        "kvring_write_frame": (i32, [vp, vp, vp, vp, i32, vp]),
+        "kvring_delta_rotate": (i32, [vp, i32, vp]),
+        "kvring_attention": (i32, [vp, vp, vp, i32, vp, i32, vp]),
+        "kvring_export": (i32, [vp, vp, vp, vp, vp, vp, vp]),
+        "kvring_debug_encode_e4m3": (i32, [vp, vp, i64, vp]),
+        "kvring_debug_attention_levels": (i32, [vp, vp, vp]),
+        "kvring_status_string": (ctypes.c_char_p, [i32]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _LIB = L
+    return L
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/kvring.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(kvring_\w+)\s*\(", text, re.M)))
+
+
+def kvring_status_string(status: int) -> str:
+    return lib().kvring_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise KvRingError(status, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _tokens(x: torch.Tensor, heads: int, dim: int, name: str) -> int:
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16")
+    if x.dim() != 3 or x.shape[1] != heads or x.shape[2] != dim:
+        raise ValueError(f"{name} must have shape [n, {heads}, {dim}], got {tuple(x.shape)}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return x.shape[0]
+
+
+def _positions(pos, n: int, name: str):
+    if pos is None:
+        return None
+    if not isinstance(pos, torch.Tensor) or not pos.is_cuda or pos.dtype != torch.int32 \
+            or pos.dim() != 1 or pos.shape[0] != n or not pos.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor of {n} positions")
+    return pos
+
+
+# ---------------------------------------------------------------------------
+# C-named functions (marshalling only)
+# ---------------------------------------------------------------------------
+def make_config(heads, head_dim, capacity, max_tokens, max_position, rope_base=10000.0,
+                max_kv_splits=16, attn_precision=0) -> KvringConfig:
+    return KvringConfig(int(heads), int(head_dim), int(capacity), int(max_tokens),
+                        int(max_position), int(max_kv_splits), int(attn_precision), 0,
+                        float(rope_base))
+
+
+def kvring_required_bytes(cfg: KvringConfig) -> int:
+    return int(lib().kvring_required_bytes(ctypes.byref(cfg)))
+
+
+def kvring_create(cfg: KvringConfig, buf: torch.Tensor, stream=None) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().kvring_create(ctypes.byref(cfg), buf.data_ptr(), buf.numel() * buf.element_size(),
+                               _stream_ptr(stream, buf.device), ctypes.byref(h)), "kvring_create")
+    return h.value
+
+
+def kvring_destroy(handle: int) -> None:
+    _check(lib().kvring_destroy(handle), "kvring_destroy")
+
+
+def kvring_calibrate_scales(handle, k, v, pos, n, stream_ptr) -> None:
+    _check(lib().kvring_calibrate_scales(handle, _ptr(k), _ptr(v), _ptr(pos), int(n), stream_ptr),
+           "kvring_calibrate_scales")
+
+
+def kvring_write_frame(handle, k, v, pos, n, stream_ptr) -> None:
+    _check(lib().kvring_write_frame(handle, _ptr(k), _ptr(v), _ptr(pos), int(n), stream_ptr),
+           "kvring_write_frame")
+
+
+def kvring_delta_rotate(handle, delta, stream_ptr) -> None:
+    _check(lib().kvring_delta_rotate(handle, int(delta), stream_ptr), "kvring_delta_rotate")
+
+
+def kvring_attention(handle, q, qpos, n_q, out, out_dtype, stream_ptr) -> None:
+    _check(lib().kvring_attention(handle, _ptr(q), _ptr(qpos), int(n_q), _ptr(out), int(out_dtype),
+                                  stream_ptr), "kvring_attention")
+
+
+def kvring_export(handle, k_out, v_out, scales, slot_pos, state, stream_ptr) -> None:
+    _check(lib().kvring_export(handle, _ptr(k_out), _ptr(v_out), _ptr(scales), _ptr(slot_pos),
+                               _ptr(state), stream_ptr), "kvring_export")
+
+
+def encode_e4m3(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """E4M3 codes of a CUDA float32 tensor, with the kernels' conversion (test support)."""
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().kvring_debug_encode_e4m3(x.data_ptr(), out.data_ptr(), x.numel(),
+                                          _stream_ptr(stream, x.device)), "kvring_debug_encode_e4m3")
+    return out
+
+
+# ---------------------------------------------------------------------------
+class KvRing:
+    """One layer's rolling FP8 attention cache on the current CUDA device."""
+
+    def __init__(self, heads: int, head_dim: int, capacity: int, max_tokens: int,
+                 max_position: int, rope_base: float = 10000.0, max_kv_splits: int = 16,
+                 attn_precision: int = 0, device=None, stream=None):
+        if not torch.cuda.is_available():
+            raise RuntimeError("KvRing needs a CUDA device")
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.H, self.d, self.C = int(heads), int(head_dim), int(capacity)
+        self.max_tokens = int(max_tokens)
+        self.cfg = make_config(heads, head_dim, capacity, max_tokens, max_position, rope_base,
+                               max_kv_splits, attn_precision)
+        n = kvring_required_bytes(self.cfg)
+        if n == 0:
+            raise ValueError("invalid kvring config")
+        self.nbytes = n
+        with torch.cuda.device(self.device):
+            self.buf = torch.empty(n, dtype=torch.uint8, device=self.device)
+            self.handle = kvring_create(self.cfg, self.buf, stream)
+
+    def _s(self, stream) -> int:
+        return _stream_ptr(stream, self.device)
+
+    def calibrate(self, k, v, pos=None, stream=None) -> None:
+        n = _tokens(k, self.H, self.d, "k")
+        if _tokens(v, self.H, self.d, "v") != n:
+            raise ValueError("k and v must hold the same number of tokens")
+        kvring_calibrate_scales(self.handle, k, v, _positions(pos, n, "pos"), n, self._s(stream))
+
+    def write(self, k, v, pos=None, stream=None) -> None:
+        n = _tokens(k, self.H, self.d, "k")
+        if _tokens(v, self.H, self.d, "v") != n:
+            raise ValueError("k and v must hold the same number of tokens")
+        kvring_write_frame(self.handle, k, v, _positions(pos, n, "pos"), n, self._s(stream))
+
+    def delta_rotate(self, delta: int = TO_OLDEST, stream=None) -> None:
+        kvring_delta_rotate(self.handle, delta, self._s(stream))
+
+    def attention(self, q, qpos=None, out=None, out_dtype=torch.float32, stream=None) -> torch.Tensor:
+        n = _tokens(q, self.H, self.d, "q")
+        if out is None:
+            out = torch.empty((n, self.H, self.d), dtype=out_dtype, device=q.device)
+        if out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (n, self.H, self.d) \
+                or not out.is_contiguous() or not out.is_cuda:
+            raise ValueError("out must be a contiguous CUDA float32/bfloat16 tensor [n_q, H, d]")
+        kvring_attention(self.handle, q, _positions(qpos, n, "qpos"), n, out,
+                         OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32, self._s(stream))
+        return out
+
+    def export(self, stream=None) -> dict:
+        """Device copies of the cache, scales, positions and state (stream-ordered)."""
+        dev = self.device
+        k = torch.empty((self.H, self.C, self.d), dtype=torch.uint8, device=dev)
+        v = torch.empty_like(k)
+        scales = torch.empty(4 * self.H, dtype=torch.float32, device=dev)
+        slot_pos = torch.empty(self.C, dtype=torch.int32, device=dev)
+        state = torch.empty(STATE_WORDS, dtype=torch.int32, device=dev)
+        kvring_export(self.handle, k, v, scales, slot_pos, state, self._s(stream))
+        return dict(k=k, v=v, scales=scales, slot_pos=slot_pos, state=state)
+
+    def levels(self, stream=None) -> torch.Tensor:
+        qt = (self.max_tokens + 127) // 128
+        out = torch.empty((qt, self.H), dtype=torch.int32, device=self.device)
+        _check(lib().kvring_debug_attention_levels(self.handle, out.data_ptr(), self._s(stream)),
+               "kvring_debug_attention_levels")
+        return out
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            kvring_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

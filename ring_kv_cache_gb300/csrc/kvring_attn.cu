@@ -1,0 +1,577 @@
+// FP8 attention of a frame's queries over the ring cache, on the sm_103a
+// tensor cores (tcgen05, TMEM accumulators, TMA-fed shared memory).
+//
+// What it computes ("Where the Time Went" and "Blackwell and Beyond Four
+// GPUs" on the page "Runway Characters: Serving a 57B Video Diffusion
+// Transformer for Real-Time Conversation": FP8 attention over the cached
+// window with per-head scales):
+//   out[t,h,:] = sum_j softmax_j(rope(q[t,h], qpos[t]) . Kdeq[h,j] / sqrt(d)) Vdeq[h,j]
+// over the filled slots j, Kdeq = code * scale_k[h], Vdeq = code * scale_v[h].
+//
+// CTA = one 128-query tile x one head x one range of key/value tiles
+// (split-KV).  Six warps:
+//   warps 0-3  softmax: thread i owns query row i (= TMEM lane i).  Prologue:
+//              RoPE the row in fp32, scale by 448/amax(row), split into 1-3
+//              E4M3 terms in shared memory.  Loop: read S from TMEM, online
+//              softmax in log2 units with a lazily raised running maximum,
+//              probabilities scaled by 2^8 and split into 1-2 E4M3 terms
+//              written to shared memory; rescale O in TMEM when the maximum
+//              rises.  Epilogue: O / l, split partials and their merge.
+//   warp 4     TMA producer: K and V tiles [128 slots][d] into a 3-stage ring.
+//   warp 5     TMEM allocation and the single MMA-issuing thread:
+//              S = sum_t Q_t K^T (kind::f8f6f4, K-major operands), then
+//              O += sum_t P_t V (V MN-major straight from its [slot][d]
+//              cache layout) and l += sum_t P_t 1 (a 16-wide all-ones
+//              operand, so the softmax normaliser is summed from exactly the
+//              FP8 values that multiply V).
+// S is double-buffered in TMEM so S(j+1) is computed while the softmax
+// works on S(j); P is double-buffered in shared memory.
+//
+// Precision level per CTA (uniform, from the query tile's amax times the
+// head's key range 448*scale_k): level 1 = 1 Q term + 1 P term, level 2 =
+// 2 + 2, level 3 = 3 + 2.  Extra terms are residuals at the same scale,
+// accumulated into the same TMEM accumulator.
+//
+// Every wait is bounded (about a second of wall time); a wait that gives up
+// sets KVRING_DEVERR_TIMEOUT in the ring's error word, the CTA drains its
+// in-flight copies and MMAs, frees TMEM and returns.
+#include "kvring_internal.cuh"
+
+namespace kvr {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
+constexpr float kTau = 0.5f;      // raise the running max only when it grows by > 2^0.5
+constexpr float kPShift = 8.0f;   // probabilities carry a 2^8 factor (max 2^8.5 < 448)
+constexpr float kLevel1Max = 12.0f;   // amax(q) * amax(k) limits for levels 1 and 2
+constexpr float kLevel2Max = 100.0f;
+
+template <int D>
+struct Layout {
+  static constexpr int kQTile = kTile * D;      // one Q term tile (bytes)
+  static constexpr int kKVTile = kTile * D;
+  static constexpr int kPTile = kTile * kTile;  // one P term tile
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 3 * kQTile;
+  static constexpr int kV = kK + kStages * kKVTile;
+  static constexpr int kP = kV + kStages * kKVTile;
+  static constexpr int kOnes = kP + 2 * 2 * kPTile;
+  static constexpr int kBars = kOnes + 16 * kTile;
+  // barrier slots (8 bytes each)
+  static constexpr int kBarKvFull = 0;
+  static constexpr int kBarKvEmpty = kStages;
+  static constexpr int kBarSFull = 2 * kStages;
+  static constexpr int kBarSFree = 2 * kStages + 2;
+  static constexpr int kBarPFull = 2 * kStages + 4;
+  static constexpr int kBarPvDone = 2 * kStages + 6;
+  static constexpr int kBarMmaDone = 2 * kStages + 8;
+  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int kMisc = kBars + 8 * kNumBars;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code
+  // TMEM columns
+  static constexpr uint32_t kColS = 0;        // two 128-column S buffers
+  static constexpr uint32_t kColO = 256;      // D columns
+  static constexpr uint32_t kColL = 256 + D;  // 16 columns
+};
+
+struct Misc {
+  uint32_t tmem_base;
+  int level;
+  int abort;
+  int last;
+  float warp_qmax[4];
+};
+
+struct AttnParams {
+  RingDev r;
+  const uint16_t* q;
+  const int32_t* qpos;
+  void* out;
+  int n_q;
+  int out_bf16;
+  int nsplit;
+  int tiles_per_split;
+  int forced_level;
+};
+
+__device__ __forceinline__ void named_sync_softmax() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attention(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const AttnParams prm) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  Misc* misc = reinterpret_cast<Misc*>(sm + L::kMisc);
+  volatile int* abort = &misc->abort;
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBars + 8u * (uint32_t)i; };
+
+  const RingDev& r = prm.r;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
+  const int H = r.H;
+  const int nvalid = __ldcg(r.state + ST_NVALID);
+  const int ntile_total = (nvalid + kTile - 1) / kTile;
+  const int tile0 = split * prm.tiles_per_split;
+  int ntiles = ntile_total - tile0;
+  ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(L::kBarKvFull + s), 1);
+      mbar_init(bar(L::kBarKvEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kBarSFull + b), 1);
+      mbar_init(bar(L::kBarSFree + b), 128);
+      mbar_init(bar(L::kBarPFull + b), 128);
+      mbar_init(bar(L::kBarPvDone + b), 1);
+    }
+    mbar_init(bar(L::kBarMmaDone), 1);
+    misc->abort = 0;
+    misc->last = 0;
+    mbar_fence_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  {  // all-ones operand for the normaliser MMA (E4M3 1.0 = 0x38)
+    uint4* ones = reinterpret_cast<uint4*>(sm + L::kOnes);
+    for (int i = threadIdx.x; i < 16 * kTile / 16; i += kThreads)
+      ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+  }
+
+  // ------------------------------------------------- query prologue (0-3)
+  const int row = threadIdx.x;              // softmax threads only
+  const int t_row = qt * kTile + row;
+  float f_row = 0.f;                        // logit factor: sigma_q * scale_k * log2(e) / sqrt(d)
+  if (warp < 4) {
+    float q[D];
+    float amax = 0.f;
+    const bool live = t_row < prm.n_q;
+    if (live) {
+      int p = prm.qpos ? __ldg(prm.qpos + t_row) : __ldcg(r.state + ST_NEXT_POS) - prm.n_q + t_row;
+      if (p < 0 || p >= r.max_pos) {
+        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+        p = 0;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(prm.q + ((size_t)t_row * H + h) * D);
+      const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 w = __ldg(src + c);  // 8 bf16 = 4 pairs
+        const float4 cs0 = __ldg(tb + 2 * c), cs1 = __ldg(tb + 2 * c + 1);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
+        const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = __uint_as_float(ww[i] << 16), x1 = __uint_as_float(ww[i] & 0xFFFF0000u);
+          const float y0 = x0 * cc[i] - x1 * ss[i];
+          const float y1 = x0 * ss[i] + x1 * cc[i];
+          q[8 * c + 2 * i] = y0;
+          q[8 * c + 2 * i + 1] = y1;
+          amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < D; ++i) q[i] = 0.f;
+    }
+    float sq = amax / 448.0f;
+    if (!(sq >= 0x1p-126f)) sq = 1.0f;
+    const float invq = 1.0f / sq;
+    const float scale_k = r.scales[h];
+    f_row = sq * scale_k * (1.4426950408889634f / sqrtf((float)D));
+
+    // CTA-uniform precision level from max_row amax(q) * 448 * scale_k
+    float wm = amax;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+    if (lane == 0) misc->warp_qmax[warp] = wm;
+    named_sync_softmax();
+    int level = prm.forced_level;
+    if (level == 0) {
+      const float qm = fmaxf(fmaxf(misc->warp_qmax[0], misc->warp_qmax[1]),
+                             fmaxf(misc->warp_qmax[2], misc->warp_qmax[3]));
+      const float lg = qm * 448.0f * scale_k;
+      level = lg <= kLevel1Max ? 1 : (lg <= kLevel2Max ? 2 : 3);
+    }
+    if (threadIdx.x == 0) {
+      misc->level = level;
+      if (split == 0) r.levels[qt * H + h] = level;
+    }
+
+    // E4M3 terms of q * invq: residual splitting, written swizzled (K-major)
+#pragma unroll
+    for (int i = 0; i < D; ++i) q[i] = q[i] * invq;
+    for (int term = 0; term < level; ++term) {
+      uint8_t* qtile = sm + L::kQ + term * L::kQTile;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a0 = q[16 * c + 4 * i], a1 = q[16 * c + 4 * i + 1];
+          const float a2 = q[16 * c + 4 * i + 2], a3 = q[16 * c + 4 * i + 3];
+          const uint16_t lo = f32x2_to_e4m3x2(a0, a1), hi = f32x2_to_e4m3x2(a2, a3);
+          w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+          if (term + 1 < level) {  // keep the residual for the next term
+            const float2 dl = e4m3x2_to_f32x2(lo), dh = e4m3x2_to_f32x2(hi);
+            q[16 * c + 4 * i] = a0 - dl.x;
+            q[16 * c + 4 * i + 1] = a1 - dl.y;
+            q[16 * c + 4 * i + 2] = a2 - dh.x;
+            q[16 * c + 4 * i + 3] = a3 - dh.y;
+          }
+        }
+        *reinterpret_cast<uint4*>(qtile + swz_offset(row, c, D)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  fence_proxy_async_smem();  // the all-ones operand
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  const int level = misc->level;
+  const int n_qterms = level;
+  const int n_pterms = level >= 2 ? 2 : 1;
+
+  if (warp == 4) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait_bounded(bar(L::kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, abort, kWaitLimitNs))
+          break;
+        mbar_arrive_expect_tx(bar(L::kBarKvFull + s), 2u * kTile * D);
+        const int slot0 = (tile0 + j) * kTile;
+        tma_load_3d(sbase + L::kK + s * L::kKVTile, &tmK, 0, slot0, h, bar(L::kBarKvFull + s));
+        tma_load_3d(sbase + L::kV + s * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarKvFull + s));
+        ++issued;
+      }
+      // Drain: every issued copy must land before the CTA may exit.
+      for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j) {
+        volatile int no_abort = 0;
+        mbar_wait_bounded(bar(L::kBarKvFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
+      constexpr uint32_t idesc_pv = idesc_e4m3(128, D, true);
+      constexpr uint32_t idesc_l = idesc_e4m3(128, 16, false);
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j % kStages, b = j & 1;
+        if (!mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs)) return false;
+        if (!mbar_wait_bounded(bar(L::kBarSFree + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs)) return false;
+        tc_fence_after();
+        const uint32_t kaddr = sbase + L::kK + s * L::kKVTile;
+        for (int t = 0; t < n_qterms; ++t) {
+          const uint32_t qaddr = sbase + L::kQ + t * L::kQTile;
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            mma_e4m3(tmem + L::kColS + b * 128, smem_desc(qaddr + kk * 32, 16, 8 * D, L::kSwz),
+                     smem_desc(kaddr + kk * 32, 16, 8 * D, L::kSwz), idesc_qk, (t | kk) != 0);
+          }
+        }
+        mma_commit(bar(L::kBarSFull + b));
+        return true;
+      };
+      bool ok = issue_qk(0);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (j + 1 < ntiles && !issue_qk(j + 1)) break;
+        const int s = j % kStages, b = j & 1;
+        if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint32_t vaddr = sbase + L::kV + s * L::kKVTile;
+        for (int t = 0; t < n_pterms; ++t) {
+          const uint32_t paddr = sbase + L::kP + (b * 2 + t) * L::kPTile;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 32; ++kk) {
+            const uint32_t acc = (j > 0 || t > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t adesc = smem_desc(paddr + kk * 32, 16, 1024, 2);
+            mma_e4m3(tmem + L::kColO, adesc, smem_desc(vaddr + kk * 32 * D, 8192, 8 * D, L::kSwz),
+                     idesc_pv, acc);
+            mma_e4m3(tmem + L::kColL, adesc, smem_desc(sbase + L::kOnes + kk * 32, 16, 1024, 2),
+                     idesc_l, acc);
+          }
+        }
+        mma_commit(bar(L::kBarKvEmpty + s));
+        mma_commit(bar(L::kBarPvDone + b));
+      }
+    }
+    if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
+      mma_commit(bar(L::kBarMmaDone));
+      volatile int no_abort = 0;
+      mbar_wait_bounded(bar(L::kBarMmaDone), 0, &no_abort, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- softmax
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t trow = tmem + lane_base;
+    float m_run = -INFINITY;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j & 1;
+      ok = mbar_wait_bounded(bar(L::kBarSFull + b), (j >> 1) & 1, abort, kWaitLimitNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float x[kTile];
+      {
+        uint32_t rr[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(trow + L::kColS + b * 128 + c * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarSFree + b));
+
+      const int valid = nvalid - (tile0 + j) * kTile;  // >= 1
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTile; ++c) {
+        x[c] = c < valid ? x[c] * f_row : -INFINITY;
+        tmax = fmaxf(tmax, x[c]);
+      }
+      const bool need = tmax > m_run + kTau;
+      const float m_new = need ? tmax : m_run;
+      if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
+        // O and l already hold tiles < j; wait for PV(j-1), then rescale
+        ok = mbar_wait_bounded(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, kWaitLimitNs);
+        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+        uint32_t rr[32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          tmem_ld32(trow + L::kColO + c * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          tmem_st32(trow + L::kColO + c * 32, rr);
+        }
+        const uint32_t lv = tmem_ld1(trow + L::kColL);
+        tmem_wait_ld();
+        tmem_st1(trow + L::kColL, __float_as_uint(__uint_as_float(lv) * alpha));
+        tmem_wait_st();
+      }
+      m_run = m_new;
+      // P buffer b was last read by PV(j-2)
+      if (j >= 2) {
+        ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs);
+        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+      }
+      const float moff = kPShift - m_run;
+      uint8_t* p0 = sm + L::kP + (b * 2 + 0) * L::kPTile;
+      uint8_t* p1 = sm + L::kP + (b * 2 + 1) * L::kPTile;
+#pragma unroll
+      for (int c = 0; c < kTile / 16; ++c) {
+        uint32_t w0[4], w1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float e0 = ex2_approx(x[16 * c + 4 * i] + moff);
+          const float e1 = ex2_approx(x[16 * c + 4 * i + 1] + moff);
+          const float e2 = ex2_approx(x[16 * c + 4 * i + 2] + moff);
+          const float e3 = ex2_approx(x[16 * c + 4 * i + 3] + moff);
+          const uint16_t lo = f32x2_to_e4m3x2(e0, e1), hi = f32x2_to_e4m3x2(e2, e3);
+          w0[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+          if (n_pterms > 1) {
+            const float2 dl = e4m3x2_to_f32x2(lo), dh = e4m3x2_to_f32x2(hi);
+            const uint16_t lo2 = f32x2_to_e4m3x2(e0 - dl.x, e1 - dl.y);
+            const uint16_t hi2 = f32x2_to_e4m3x2(e2 - dh.x, e3 - dh.y);
+            w1[i] = (uint32_t)lo2 | ((uint32_t)hi2 << 16);
+          }
+        }
+        const uint32_t off = swz_offset(row, c, 128);
+        *reinterpret_cast<uint4*>(p0 + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        if (n_pterms > 1) *reinterpret_cast<uint4*>(p1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::kBarPFull + b));
+    }
+
+    // ---------------------------------------------------------- epilogue
+    float o[D];
+    float l = 0.f;
+    if (ok && ntiles > 0) {
+      const int jl = ntiles - 1;
+      ok = mbar_wait_bounded(bar(L::kBarPvDone + (jl & 1)), (jl >> 1) & 1, abort, kWaitLimitNs);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+    }
+    if (ok && ntiles > 0) {
+      tc_fence_after();
+      uint32_t rr[32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(trow + L::kColO + c * 32, rr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(rr[i]);
+      }
+      l = __uint_as_float(tmem_ld1(trow + L::kColL));
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < D; ++i) o[i] = 0.f;
+    }
+    const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+    const float scale_v = r.scales[H + h];
+    const bool live = t_row < prm.n_q;
+    if (prm.nsplit == 1) {
+      if (live) {
+        const float f = inv_l * scale_v;
+        if (prm.out_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(prm.out) + ((size_t)t_row * H + h) * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(o[8 * c + 2 * i] * f, o[8 * c + 2 * i + 1] * f);
+              w[i] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + ((size_t)t_row * H + h) * D);
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c)
+            dst[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
+        }
+      }
+    } else {
+      // partial (normalised) output and its log2-sum-exp for this split
+      const size_t prow = (((size_t)split * r.qtiles_max + qt) * H + h) * kTile + row;
+      float4* po = reinterpret_cast<float4*>(r.part_o + prow * D);
+#pragma unroll
+      for (int c = 0; c < D / 4; ++c)
+        __stcg(po + c, make_float4(o[4 * c] * inv_l, o[4 * c + 1] * inv_l, o[4 * c + 2] * inv_l, o[4 * c + 3] * inv_l));
+      __stcg(r.part_lse + prow, l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY);
+      __threadfence();
+      named_sync_softmax();
+      if (threadIdx.x == 0) {
+        const int tk = atomicAdd(r.tickets + qt * H + h, 1);
+        misc->last = tk == prm.nsplit - 1;
+      }
+      named_sync_softmax();
+      if (misc->last) {
+        __threadfence();
+        float mx = -INFINITY;
+        for (int s = 0; s < prm.nsplit; ++s) {
+          const size_t pr = (((size_t)s * r.qtiles_max + qt) * H + h) * kTile + row;
+          mx = fmaxf(mx, __ldcg(r.part_lse + pr));
+        }
+        float acc[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) acc[i] = 0.f;
+        float wsum = 0.f;
+        if (mx > -INFINITY) {
+          for (int s = 0; s < prm.nsplit; ++s) {
+            const size_t pr = (((size_t)s * r.qtiles_max + qt) * H + h) * kTile + row;
+            const float lse = __ldcg(r.part_lse + pr);
+            if (!(lse > -INFINITY)) continue;
+            const float w = ex2_approx(lse - mx);
+            wsum += w;
+            const float4* src = reinterpret_cast<const float4*>(r.part_o + pr * D);
+#pragma unroll
+            for (int c = 0; c < D / 4; ++c) {
+              const float4 vv = __ldcg(src + c);
+              acc[4 * c] += w * vv.x;
+              acc[4 * c + 1] += w * vv.y;
+              acc[4 * c + 2] += w * vv.z;
+              acc[4 * c + 3] += w * vv.w;
+            }
+          }
+        }
+        const float f = wsum > 0.f ? scale_v / wsum : 0.f;
+        if (live) {
+          if (prm.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(prm.out) + ((size_t)t_row * H + h) * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[8 * c + 2 * i] * f, acc[8 * c + 2 * i + 1] * f);
+                w[i] = *reinterpret_cast<const uint32_t*>(&bb);
+              }
+              dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + ((size_t)t_row * H + h) * D);
+#pragma unroll
+            for (int c = 0; c < D / 4; ++c)
+              dst[c] = make_float4(acc[4 * c] * f, acc[4 * c + 1] * f, acc[4 * c + 2] * f, acc[4 * c + 3] * f);
+          }
+        }
+        if (threadIdx.x == 0) r.tickets[qt * H + h] = 0;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && misc->abort)
+    atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_TIMEOUT);
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t attention_prepare(int D) {
+  const int smem = (int)attention_smem_bytes(D);
+  return D == 128 ? cudaFuncSetAttribute(k_attention<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                  : cudaFuncSetAttribute(k_attention<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+size_t attention_smem_bytes(int D) {
+  return (D == 128 ? Layout<128>::kBytes : Layout<64>::kBytes) + 1024;
+}
+
+cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                             const AttnLaunch& a, cudaStream_t s) {
+  AttnParams p;
+  p.r = r;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.qpos = a.qpos;
+  p.out = a.out;
+  p.n_q = a.n_q;
+  p.out_bf16 = a.out_bf16;
+  p.nsplit = a.nsplit;
+  p.tiles_per_split = a.tiles_per_split;
+  p.forced_level = a.forced_level;
+  const dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), (unsigned)r.H, (unsigned)a.nsplit);
+  const size_t smem = attention_smem_bytes(r.D);
+  if (r.D == 128)
+    k_attention<128><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
+  else
+    k_attention<64><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -1,0 +1,342 @@
+// Memory-bound kernels of the rolling FP8 cache: per-session scale
+// calibration, the per-frame write (RoPE + E4M3 quantisation into the ring)
+// and the in-place delta rotation at a position reset.  See the page
+// "Runway Characters: Serving a 57B Video Diffusion Transformer for
+// Real-Time Conversation", section "Do It Once, at Write Time".
+//
+// Work decomposition (all three kernels): one thread owns 16 consecutive
+// elements of one (token or slot, head) row, i.e. one 16-byte chunk of FP8
+// output; consecutive threads walk a row, then the next head, then the next
+// token, so bf16 input reads are fully contiguous and every cache row is
+// written as whole 16-byte vectors.  Completion work (ring state, scales,
+// position map) is done by the last block to finish, found with an atomic
+// ticket; no block ever waits on another.
+//
+// Arithmetic is pinned so that cache bytes are reproducible: products and
+// sums are rounded one at a time (__fmul_rn / __fadd_rn / __fsub_rn, no
+// fused multiply-add), the cos/sin table is fp32 built on the host, and the
+// E4M3 conversion is the hardware round-to-nearest-even saturating cvt.
+#include "kvring_internal.cuh"
+
+namespace kvr {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void unpack_bf16x16(const uint4& a, const uint4& b, float (&x)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack_e4m3x16(const float (&z)[16]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = f32x2_to_e4m3x2(z[4 * i], z[4 * i + 1]);
+    const uint32_t hi = f32x2_to_e4m3x2(z[4 * i + 2], z[4 * i + 3]);
+    w[i] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Rotate 8 adjacent pairs by the angles whose fp32 cos/sin are in `cs`
+// (c0, s0, c1, s1, ...): y0 = x0*c - x1*s, y1 = x0*s + x1*c, every step
+// rounded to fp32.
+__device__ __forceinline__ void rope_pinned(float (&x)[16], const float4 (&cs)[4]) {
+  const float c[8] = {cs[0].x, cs[0].z, cs[1].x, cs[1].z, cs[2].x, cs[2].z, cs[3].x, cs[3].z};
+  const float s[8] = {cs[0].y, cs[0].w, cs[1].y, cs[1].w, cs[2].y, cs[2].w, cs[3].y, cs[3].w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x0 = x[2 * i], x1 = x[2 * i + 1];
+    x[2 * i] = __fsub_rn(__fmul_rn(x0, c[i]), __fmul_rn(x1, s[i]));
+    x[2 * i + 1] = __fadd_rn(__fmul_rn(x0, s[i]), __fmul_rn(x1, c[i]));
+  }
+}
+
+__device__ __forceinline__ void load_table16(const float* table, int D, int p, int chunk,
+                                             float4 (&cs)[4]) {
+  const float4* t = reinterpret_cast<const float4*>(table + ((size_t)p * (D / 2) + chunk * 8) * 2);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cs[i] = __ldg(t + i);
+}
+
+// ------------------------------------------------------------ calibrate ---
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_calibrate(RingDev r, const uint16_t* __restrict__ k,
+                                                        const uint16_t* __restrict__ v,
+                                                        const int32_t* __restrict__ pos, int n) {
+  constexpr int CH = D / 16;
+  __shared__ int s_next;
+  __shared__ int s_last;
+  if (threadIdx.x == 0) s_next = __ldcg(r.state + ST_NEXT_POS);
+  __syncthreads();
+  const int H = r.H;
+  const long long per = (long long)n * H * CH;
+  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
+  float m = 0.f;
+  int isv = 0, h = 0, chunk = 0;
+  if (gid < 2 * per) {
+    isv = gid >= per;
+    const long long w = isv ? gid - per : gid;
+    chunk = (int)(w % CH);
+    const long long th = w / CH;
+    h = (int)(th % H);
+    const int t = (int)(th / H);
+    const uint4* src = reinterpret_cast<const uint4*>((isv ? v : k) + ((size_t)t * H + h) * D + chunk * 16);
+    float x[16];
+    unpack_bf16x16(__ldcs(src), __ldcs(src + 1), x);
+    bool ok = true;
+    if (!isv) {
+      const int p = pos ? __ldg(pos + t) : s_next + t;
+      if (p < 0 || p >= r.max_pos) {
+        ok = false;
+        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+      } else {
+        float4 cs[4];
+        load_table16(r.table, D, p, chunk, cs);
+        rope_pinned(x, cs);
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(x[i]));
+    }
+  }
+  // max over the CH lanes of one row (rows start at multiples of CH lanes)
+#pragma unroll
+  for (int off = CH / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if (gid < 2 * per && chunk == 0 && m > 0.f) atomicMax(r.amax + isv * H + h, __float_as_uint(m));
+
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int tk = atomicAdd(r.state + ST_TICKET_CALIB, 1);
+    s_last = tk == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (int i = threadIdx.x; i < 2 * H; i += kThreads) {
+      const float a = __uint_as_float(atomicExch(r.amax + i, 0u));
+      float sc = __fdiv_rn(a, 448.0f);
+      if (!(sc >= 0x1p-126f)) sc = 1.0f;
+      r.scales[i] = sc;                         // scale_k then scale_v
+      r.scales[2 * H + i] = __fdiv_rn(1.0f, sc);  // their reciprocals
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      r.state[ST_CALIBRATED] = 1;
+      r.state[ST_TICKET_CALIB] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- write ---
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* __restrict__ k,
+                                                    const uint16_t* __restrict__ v,
+                                                    const int32_t* __restrict__ pos, int n) {
+  constexpr int CH = D / 16;
+  __shared__ int s_head, s_next;
+  if (threadIdx.x == 0) {
+    s_head = __ldcg(r.state + ST_HEAD);
+    s_next = __ldcg(r.state + ST_NEXT_POS);
+  }
+  __syncthreads();
+  const int H = r.H, C = r.C;
+  const long long per = (long long)n * H * CH;
+  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
+  if (gid < 2 * per) {
+    const int isv = gid >= per;
+    const long long w = isv ? gid - per : gid;
+    const int chunk = (int)(w % CH);
+    const long long th = w / CH;
+    const int h = (int)(th % H);
+    const int t = (int)(th / H);
+    int slot = s_head + t;
+    if (slot >= C) slot -= C;  // head < C and t < n <= C
+    const uint4* src = reinterpret_cast<const uint4*>((isv ? v : k) + ((size_t)t * H + h) * D + chunk * 16);
+    float x[16];
+    unpack_bf16x16(__ldcs(src), __ldcs(src + 1), x);
+    bool ok = true;
+    int p = 0;
+    if (!isv) {
+      p = pos ? __ldg(pos + t) : s_next + t;
+      if (p < 0 || p >= r.max_pos) {
+        ok = false;
+        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+      } else {
+        float4 cs[4];
+        load_table16(r.table, D, p, chunk, cs);
+        rope_pinned(x, cs);
+      }
+      if (h == 0 && chunk == 0) r.slot_pos[slot] = p;
+    }
+    if (ok) {
+      const float inv = r.scales[(isv ? 3 : 2) * H + h];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], inv);
+      uint8_t* dst = (isv ? r.v : r.k) + ((size_t)h * C + slot) * D + chunk * 16;
+      *reinterpret_cast<uint4*>(dst) = pack_e4m3x16(x);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
+    if (tk == (int)gridDim.x - 1) {
+      __threadfence();
+      int head = s_head + n;
+      if (head >= C) head -= C;
+      const int nv = r.state[ST_NVALID] + n;
+      r.state[ST_HEAD] = head;
+      r.state[ST_NVALID] = nv < C ? nv : C;
+      const unsigned long long tot =
+          ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
+          (unsigned long long)n;
+      r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
+      r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
+      r.state[ST_NEXT_POS] = s_next + n;
+      r.state[ST_TICKET_WRITE] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- delta ---
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
+  constexpr int CH = D / 16;
+  __shared__ int s_delta, s_nv, s_last;
+  __shared__ float4 s_cs[D / 4];  // table row of delta: D/2 (cos, sin) pairs
+  if (threadIdx.x == 0) {
+    const int nv = __ldcg(r.state + ST_NVALID);
+    int d = delta_arg;
+    if (d == KVRING_DELTA_TO_OLDEST)
+      d = nv > 0 ? __ldcg(r.slot_pos + (nv == r.C ? __ldcg(r.state + ST_HEAD) : 0)) : 0;
+    if (d < 0 || d >= r.max_pos) {
+      if (blockIdx.x == 0) atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_DELTA);
+      d = -1;  // skip the rotation entirely
+    }
+    s_delta = d;
+    s_nv = nv;
+  }
+  __syncthreads();
+  const int delta = s_delta;
+  if (delta > 0) {
+    const float4* row = reinterpret_cast<const float4*>(r.table + (size_t)delta * D);
+    for (int i = threadIdx.x; i < D / 4; i += kThreads) s_cs[i] = __ldg(row + i);
+  }
+  __syncthreads();
+  const int C = r.C;
+  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const long long items = (long long)r.H * C * CH;
+  if (delta > 0 && gid < items) {
+    const int chunk = (int)(gid % CH);
+    const long long hs = gid / CH;
+    const int slot = (int)(hs % C);
+    if (slot < s_nv) {
+      uint4* p = reinterpret_cast<uint4*>(r.k + (size_t)hs * D + chunk * 16);
+      const uint4 in = *p;
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      float y[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = e4m3x2_to_f32x2((uint16_t)(w[i] & 0xFFFF));
+        const float2 b = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
+        // pairs (a.x, a.y) and (b.x, b.y); pair index chunk*8 + 2i (+1)
+        const float4 cs = s_cs[chunk * 4 + i];  // (c, s) of both pairs
+        y[4 * i + 0] = __fadd_rn(__fmul_rn(a.x, cs.x), __fmul_rn(a.y, cs.y));
+        y[4 * i + 1] = __fsub_rn(__fmul_rn(a.y, cs.x), __fmul_rn(a.x, cs.y));
+        y[4 * i + 2] = __fadd_rn(__fmul_rn(b.x, cs.z), __fmul_rn(b.y, cs.w));
+        y[4 * i + 3] = __fsub_rn(__fmul_rn(b.y, cs.z), __fmul_rn(b.x, cs.w));
+      }
+      *p = pack_e4m3x16(y);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int tk = atomicAdd(r.state + ST_TICKET_DELTA, 1);
+    s_last = tk == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    if (delta >= 0) {
+      for (int sl = threadIdx.x; sl < s_nv; sl += kThreads) r.slot_pos[sl] -= delta;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (delta >= 0) {
+        r.state[ST_NEXT_POS] -= delta;
+        r.state[ST_LAST_DELTA] = delta;
+      }
+      r.state[ST_TICKET_DELTA] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// -------------------------------------------------------- codec (tests) ---
+__global__ void k_encode(const float* __restrict__ in, uint8_t* __restrict__ out, int64_t n) {
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 2;
+  if (i + 1 < n) {
+    const uint16_t c = f32x2_to_e4m3x2(in[i], in[i + 1]);
+    out[i] = (uint8_t)(c & 0xFF);
+    out[i + 1] = (uint8_t)(c >> 8);
+  } else if (i < n) {
+    out[i] = (uint8_t)(f32x2_to_e4m3x2(in[i], 0.f) & 0xFF);
+  }
+}
+
+unsigned grid_for(long long items) { return (unsigned)((items + kThreads - 1) / kThreads); }
+
+}  // namespace
+
+cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, const int32_t* pos,
+                             int n, cudaStream_t s) {
+  const long long items = 2LL * n * r.H * (r.D / 16);
+  const unsigned g = grid_for(items);
+  if (r.D == 128)
+    k_calibrate<128><<<g, kThreads, 0, s>>>(r, (const uint16_t*)k, (const uint16_t*)v, pos, n);
+  else
+    k_calibrate<64><<<g, kThreads, 0, s>>>(r, (const uint16_t*)k, (const uint16_t*)v, pos, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
+                         cudaStream_t s) {
+  const long long items = 2LL * n * r.H * (r.D / 16);
+  const unsigned g = grid_for(items);
+  if (r.D == 128)
+    k_write<128><<<g, kThreads, 0, s>>>(r, (const uint16_t*)k, (const uint16_t*)v, pos, n);
+  else
+    k_write<64><<<g, kThreads, 0, s>>>(r, (const uint16_t*)k, (const uint16_t*)v, pos, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s) {
+  const long long items = (long long)r.H * r.C * (r.D / 16);
+  const unsigned g = grid_for(items);
+  if (r.D == 128)
+    k_delta<128><<<g, kThreads, 0, s>>>(r, delta);
+  else
+    k_delta<64><<<g, kThreads, 0, s>>>(r, delta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t pairs = (n + 1) / 2;
+  const unsigned g = (unsigned)((pairs + kThreads - 1) / kThreads);
+  k_encode<<<g, kThreads, 0, s>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -1,0 +1,329 @@
+// Host side of the kvring C ABI: argument checks, buffer carving, the RoPE
+// table, TMA descriptors and kernel launches.  Every entry point only
+// enqueues work on the caller's stream; none synchronises except
+// kvring_create (which waits for its own upload) and none allocates device
+// memory (the caller hands one buffer to kvring_create).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "kvring_internal.cuh"
+
+struct kvring {
+  kvring_config cfg;
+  kvr::RingDev dev;
+  CUtensorMap tmK;
+  CUtensorMap tmV;
+  int sm_count;
+  int qtiles_max;
+  bool calibrated;   // host mirror: a calibration has been enqueued
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool config_ok(const kvring_config* c) {
+  if (!c) return false;
+  if (c->num_heads < 1 || c->num_heads > 4096) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->capacity < 1 || c->capacity > (1 << 24)) return false;
+  if (c->max_tokens < 1 || c->max_tokens > (1 << 24)) return false;
+  if (c->max_position < 1 || c->max_position > (1 << 24)) return false;
+  if (c->max_kv_splits < 1 || c->max_kv_splits > 64) return false;
+  if (c->attn_precision < 0 || c->attn_precision > 3) return false;
+  if (c->reserved != 0) return false;
+  if (!(c->rope_base > 0.0) || !std::isfinite(c->rope_base)) return false;
+  return true;
+}
+
+struct Plan {
+  size_t k, v, slot_pos, scales, state, amax, table, part_o, part_lse, tickets, levels, total;
+  int qtiles;
+};
+
+Plan plan_for(const kvring_config* c) {
+  Plan p{};
+  const size_t H = (size_t)c->num_heads, D = (size_t)c->head_dim, C = (size_t)c->capacity;
+  p.qtiles = (c->max_tokens + kvr::kTile - 1) / kvr::kTile;
+  const size_t Q = (size_t)p.qtiles, S = (size_t)c->max_kv_splits;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  p.k = take(H * C * D);
+  p.v = take(H * C * D);
+  p.slot_pos = take(C * 4);
+  p.scales = take(4 * H * 4);
+  p.state = take(kvr::ST_WORDS_ALLOC * 4);
+  p.amax = take(2 * H * 4);
+  p.table = take((size_t)c->max_position * D * 4);
+  p.part_o = take(S * Q * H * kvr::kTile * D * 4);
+  p.part_lse = take(S * Q * H * kvr::kTile * 4);
+  p.tickets = take(Q * H * 4);
+  p.levels = take(Q * H * 4);
+  p.total = off;
+  return p;
+}
+
+kvring_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVRING_OK : KVRING_ERR_CUDA; }
+
+// Split-KV count for one attention call: the grid has qtiles * H * nsplit
+// CTAs of which one fits per SM; pick the split count with the fewest
+// "waves x (tiles per CTA + fixed per-CTA cost)".
+void choose_splits(const kvring* r, int n_q, int* nsplit, int* tiles_per_split) {
+  const int ctiles = (r->cfg.capacity + kvr::kTile - 1) / kvr::kTile;
+  const int qtiles = (n_q + kvr::kTile - 1) / kvr::kTile;
+  const long long per_split = (long long)qtiles * r->cfg.num_heads;
+  const int smax = r->cfg.max_kv_splits < ctiles ? r->cfg.max_kv_splits : ctiles;
+  double best = 1e300;
+  int best_ns = 1, best_tps = ctiles;
+  for (int ns = 1; ns <= smax; ++ns) {
+    const int tps = (ctiles + ns - 1) / ns;
+    const int ns_eff = (ctiles + tps - 1) / tps;
+    if (ns_eff != ns) continue;
+    const long long ctas = per_split * ns_eff;
+    const long long waves = (ctas + r->sm_count - 1) / r->sm_count;
+    const double cost = (double)waves * (tps + 2.0) + (ns_eff > 1 ? 0.5 : 0.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_ns = ns_eff;
+      best_tps = tps;
+    }
+  }
+  *nsplit = best_ns;
+  *tiles_per_split = best_tps;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D map over a [H][C][D] byte cache: tiles of [1][128][D] with the
+// swizzle the MMA descriptors expect (row bytes = D); rows past C read 0.
+bool make_cache_map(CUtensorMap* m, void* base, int H, int C, int D) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)C, (cuuint64_t)H};
+  const cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)C * (cuuint64_t)D};
+  const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)kvr::kTile, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult res =
+      fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvring_required_bytes(const kvring_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return plan_for(cfg).total;
+}
+
+kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t bytes, void* stream,
+                            kvring_t** out) {
+  if (!out) return KVRING_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!config_ok(cfg) || !dev_buf || !aligned(dev_buf, kAlign)) return KVRING_ERR_INVALID_ARG;
+  const Plan p = plan_for(cfg);
+  if (bytes < p.total) return KVRING_ERR_CAPACITY;
+
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVRING_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3) return KVRING_ERR_UNSUPPORTED;  // built for sm_103a only
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, dev_buf) != cudaSuccess || pa.type != cudaMemoryTypeDevice ||
+      pa.device != dev)
+    return KVRING_ERR_INVALID_ARG;
+
+  kvring* r = new (std::nothrow) kvring();
+  if (!r) return KVRING_ERR_INVALID_ARG;
+  r->cfg = *cfg;
+  r->sm_count = sms > 0 ? sms : 1;
+  r->qtiles_max = p.qtiles;
+  r->calibrated = false;
+  uint8_t* b = static_cast<uint8_t*>(dev_buf);
+  kvr::RingDev& d = r->dev;
+  d.k = b + p.k;
+  d.v = b + p.v;
+  d.slot_pos = reinterpret_cast<int32_t*>(b + p.slot_pos);
+  d.scales = reinterpret_cast<float*>(b + p.scales);
+  d.state = reinterpret_cast<int32_t*>(b + p.state);
+  d.amax = reinterpret_cast<uint32_t*>(b + p.amax);
+  d.table = reinterpret_cast<const float*>(b + p.table);
+  d.part_o = reinterpret_cast<float*>(b + p.part_o);
+  d.part_lse = reinterpret_cast<float*>(b + p.part_lse);
+  d.tickets = reinterpret_cast<int32_t*>(b + p.tickets);
+  d.levels = reinterpret_cast<int32_t*>(b + p.levels);
+  d.H = cfg->num_heads;
+  d.D = cfg->head_dim;
+  d.C = cfg->capacity;
+  d.max_pos = cfg->max_position;
+  d.max_tokens = cfg->max_tokens;
+  d.max_splits = cfg->max_kv_splits;
+  d.qtiles_max = p.qtiles;
+
+  if (kvr::attention_prepare(d.D) != cudaSuccess) {
+    delete r;
+    return KVRING_ERR_CUDA;
+  }
+  if (!make_cache_map(&r->tmK, d.k, d.H, d.C, d.D) || !make_cache_map(&r->tmV, d.v, d.H, d.C, d.D)) {
+    delete r;
+    return KVRING_ERR_UNSUPPORTED;
+  }
+
+  // Host-built contents: empty positions, unit scales, the RoPE table
+  // (theta_i = base^(-2i/d) and cos/sin of p*theta_i in double libm,
+  // rounded to fp32).
+  const int H = d.H, D = d.D, C = d.C;
+  std::vector<int32_t> slot_pos(C, kvr::kEmptyPos);
+  std::vector<float> scales(4 * H, 1.0f);
+  std::vector<float> table((size_t)cfg->max_position * D);
+  std::vector<double> theta(D / 2);
+  for (int i = 0; i < D / 2; ++i) theta[i] = std::pow(cfg->rope_base, (-2.0 * i) / (double)D);
+  for (int pos = 0; pos < cfg->max_position; ++pos) {
+    float* row = table.data() + (size_t)pos * D;
+    for (int i = 0; i < D / 2; ++i) {
+      const double a = (double)pos * theta[i];
+      row[2 * i] = (float)std::cos(a);
+      row[2 * i + 1] = (float)std::sin(a);
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t x) {
+    if (e == cudaSuccess) e = x;
+  };
+  chk(cudaMemsetAsync(b, 0, p.total, s));
+  chk(cudaMemcpyAsync(d.slot_pos, slot_pos.data(), C * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  chk(cudaMemcpyAsync(d.scales, scales.data(), scales.size() * sizeof(float), cudaMemcpyHostToDevice, s));
+  chk(cudaMemcpyAsync(b + p.table, table.data(), table.size() * sizeof(float), cudaMemcpyHostToDevice, s));
+  chk(cudaStreamSynchronize(s));  // host vectors die at return
+  if (e != cudaSuccess) {
+    delete r;
+    return KVRING_ERR_CUDA;
+  }
+  *out = r;
+  return KVRING_OK;
+}
+
+kvring_status kvring_destroy(kvring_t* ring) {
+  delete ring;
+  return KVRING_OK;
+}
+
+kvring_status kvring_calibrate_scales(kvring_t* r, const void* k, const void* v, const int32_t* pos,
+                                      int32_t n, void* stream) {
+  if (!r || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (pos && !aligned(pos, 4)) || n < 1)
+    return KVRING_ERR_INVALID_ARG;
+  if (n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+  const kvring_status st = cuda_status(kvr::launch_calibrate(r->dev, k, v, pos, n, (cudaStream_t)stream));
+  if (st == KVRING_OK) r->calibrated = true;
+  return st;
+}
+
+kvring_status kvring_write_frame(kvring_t* r, const void* k, const void* v, const int32_t* pos, int32_t n,
+                                 void* stream) {
+  if (!r || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (pos && !aligned(pos, 4)) || n < 1)
+    return KVRING_ERR_INVALID_ARG;
+  if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
+  if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+  return cuda_status(kvr::launch_write(r->dev, k, v, pos, n, (cudaStream_t)stream));
+}
+
+kvring_status kvring_delta_rotate(kvring_t* r, int32_t delta, void* stream) {
+  if (!r) return KVRING_ERR_INVALID_ARG;
+  if (delta != KVRING_DELTA_TO_OLDEST && (delta < 0 || delta >= r->cfg.max_position))
+    return KVRING_ERR_INVALID_ARG;
+  return cuda_status(kvr::launch_delta(r->dev, delta, (cudaStream_t)stream));
+}
+
+kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, int32_t n_q, void* out,
+                               int32_t out_dtype, void* stream) {
+  if (!r || !q || !out || !aligned(q, 16) || !aligned(out, 16) || (qpos && !aligned(qpos, 4)) || n_q < 1)
+    return KVRING_ERR_INVALID_ARG;
+  if (out_dtype != KVRING_OUT_F32 && out_dtype != KVRING_OUT_BF16) return KVRING_ERR_INVALID_ARG;
+  if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
+  if (n_q > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+  kvr::AttnLaunch a;
+  a.q = q;
+  a.qpos = qpos;
+  a.out = out;
+  a.n_q = n_q;
+  a.out_bf16 = out_dtype == KVRING_OUT_BF16;
+  a.forced_level = r->cfg.attn_precision;
+  choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
+  return cuda_status(kvr::launch_attention(r->dev, &r->tmK, &r->tmV, a, (cudaStream_t)stream));
+}
+
+kvring_status kvring_export(kvring_t* r, void* k_out, void* v_out, float* scales, int32_t* slot_pos,
+                            int32_t* state, void* stream) {
+  if (!r) return KVRING_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t cache = (size_t)r->dev.H * r->dev.C * r->dev.D;
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t x) {
+    if (e == cudaSuccess) e = x;
+  };
+  if (k_out) chk(cudaMemcpyAsync(k_out, r->dev.k, cache, cudaMemcpyDefault, s));
+  if (v_out) chk(cudaMemcpyAsync(v_out, r->dev.v, cache, cudaMemcpyDefault, s));
+  if (scales) chk(cudaMemcpyAsync(scales, r->dev.scales, 4 * r->dev.H * sizeof(float), cudaMemcpyDefault, s));
+  if (slot_pos) chk(cudaMemcpyAsync(slot_pos, r->dev.slot_pos, r->dev.C * sizeof(int32_t), cudaMemcpyDefault, s));
+  if (state) chk(cudaMemcpyAsync(state, r->dev.state, KVRING_STATE_WORDS * sizeof(int32_t), cudaMemcpyDefault, s));
+  return cuda_status(e);
+}
+
+kvring_status kvring_debug_encode_e4m3(const float* in, uint8_t* out, int64_t n, void* stream) {
+  if ((!in || !out) && n > 0) return KVRING_ERR_INVALID_ARG;
+  if (n < 0) return KVRING_ERR_INVALID_ARG;
+  return cuda_status(kvr::launch_encode_e4m3(in, out, n, (cudaStream_t)stream));
+}
+
+kvring_status kvring_debug_attention_levels(kvring_t* r, int32_t* levels, void* stream) {
+  if (!r || !levels) return KVRING_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)r->qtiles_max * r->dev.H * sizeof(int32_t);
+  return cuda_status(cudaMemcpyAsync(levels, r->dev.levels, bytes, cudaMemcpyDefault, (cudaStream_t)stream));
+}
+
+const char* kvring_status_string(kvring_status s) {
+  switch (s) {
+    case KVRING_OK: return "ok";
+    case KVRING_ERR_INVALID_ARG: return "invalid argument";
+    case KVRING_ERR_NOT_CALIBRATED: return "ring not calibrated";
+    case KVRING_ERR_CAPACITY: return "too many tokens for the ring or its config";
+    case KVRING_ERR_UNSUPPORTED: return "unsupported head_dim or device";
+    case KVRING_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,283 @@
+// Internal definitions shared by the kvring translation units: the device
+// layout of one ring, the int32 state words, and thin inline-PTX wrappers
+// for the sm_103a features the kernels use (E4M3 conversion, mbarrier,
+// TMA tensor copies, tcgen05 MMA / TMEM).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvring.h"
+
+namespace kvr {
+
+// State words beyond the public ones (KVRING_STATE_*): completion tickets.
+enum : int {
+  ST_HEAD = KVRING_STATE_HEAD,
+  ST_NVALID = KVRING_STATE_NVALID,
+  ST_TOTAL_LO = KVRING_STATE_TOTAL_LO,
+  ST_TOTAL_HI = KVRING_STATE_TOTAL_HI,
+  ST_NEXT_POS = KVRING_STATE_NEXT_POS,
+  ST_CALIBRATED = KVRING_STATE_CALIBRATED,
+  ST_ERROR = KVRING_STATE_ERROR,
+  ST_LAST_DELTA = KVRING_STATE_LAST_DELTA,
+  ST_TICKET_WRITE = 8,
+  ST_TICKET_CALIB = 9,
+  ST_TICKET_DELTA = 10,
+  ST_WORDS_ALLOC = 16,
+};
+
+constexpr int kTile = 128;          // slots per key/value tile, queries per query tile
+constexpr int kEmptyPos = INT32_MIN;
+
+// Device-side view of one ring (plain pointers into the caller's buffer).
+struct RingDev {
+  uint8_t* k;          // [H][C][D] E4M3 codes, keys already rotated
+  uint8_t* v;          // [H][C][D] E4M3 codes
+  int32_t* slot_pos;   // [C] position of each slot, INT32_MIN when empty
+  float* scales;       // [4H]: scale_k, scale_v, inv_scale_k, inv_scale_v
+  int32_t* state;      // [ST_WORDS_ALLOC]
+  uint32_t* amax;      // [2H] calibration maxima as float bits (0 between calls)
+  const float* table;  // [max_position][D/2][2] fp32 (cos, sin)
+  float* part_o;       // [max_splits][qtiles][H][128][D] attention partials
+  float* part_lse;     // [max_splits][qtiles][H][128]
+  int32_t* tickets;    // [qtiles][H] split completion counters (0 between calls)
+  int32_t* levels;     // [qtiles][H] precision level used per tile (debug)
+  int H, D, C, max_pos, max_tokens, max_splits, qtiles_max;
+};
+
+// ---------------------------------------------------------------- E4M3 ----
+// Two fp32 values to two E4M3 codes (round to nearest even, saturating to
+// +-448); `lo` lands in the low byte.  The PTX conversion puts its first
+// source operand in the upper half of the result.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes (low byte first) to two fp32 values, exactly (via f16).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  __half2 hh = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hh);
+}
+
+// --------------------------------------------------------------- misc -----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------- mbarrier ---
+__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(tx)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Gives up (returning
+// false and raising *abort) after `limit_ns` of wall time, or at once when
+// another thread of the CTA already raised *abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity,
+                                                  volatile int* abort, uint64_t limit_ns) {
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ TMA ---
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// -------------------------------------------------------------- tcgen05 ---
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc], E4M3 x E4M3 -> fp32.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on an mbarrier once every previously issued tcgen05 op of this
+// thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
+// (warp quarter base + i), columns [col, col + 32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+  return r;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma (sm_100 family format):
+// start address, leading / stride byte offsets (16-byte units), the fixed
+// version field, and the swizzle mode (2 = 128-byte, 4 = 64-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t swizzle_mode) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(swizzle_mode & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f8f6f4, E4M3 x E4M3 with fp32
+// accumulation; B either K-major (b_mn_major = false) or MN-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                   // D format: f32
+         | (0u << 7) | (0u << 10)                    // A, B: E4M3
+         | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+         | ((uint32_t)(N >> 3) << 17)                // N / 8
+         | ((uint32_t)(M >> 4) << 24);               // M / 16
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a tile of rows of
+// `row_bytes` (64 or 128) stored with the matching TMA / UMMA swizzle
+// (the chunk index is XOR-ed with address bits 7.. of the row start).
+__device__ __forceinline__ uint32_t swz_offset(int row, int chunk, int row_bytes) {
+  const uint32_t off = (uint32_t)row * row_bytes + (uint32_t)chunk * 16u;
+  const uint32_t mask = row_bytes == 128 ? 7u : 3u;
+  return off ^ (((off >> 7) & mask) << 4);
+}
+
+}  // namespace kvr
+
+// Launchers implemented in the kernel translation units.
+namespace kvr {
+cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, const int32_t* pos,
+                             int n, cudaStream_t s);
+cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
+                         cudaStream_t s);
+cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s);
+cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
+
+struct AttnLaunch {
+  const void* q;
+  const int32_t* qpos;
+  void* out;
+  int n_q;
+  int out_bf16;
+  int nsplit;
+  int tiles_per_split;
+  int forced_level;
+};
+cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                             const AttnLaunch& a, cudaStream_t s);
+size_t attention_smem_bytes(int D);
+// Once per process and head size, before the first launch (not capturable).
+cudaError_t attention_prepare(int D);
+}  // namespace kvr

@@ -1,0 +1,103 @@
+"""FP8 attention kernel against the oracle.
+
+* the float64 reference (unquantised queries, exact softmax) over the same
+  FP8 cache, within max-abs 2e-2 / mean-abs 2e-3, at every precision level;
+* the kernel-mirroring diagnostic (same FP8 terms, same lazy maximum, one
+  key/value split) much more tightly, which separates kernel bugs from
+  format error;
+* closed forms: an empty ring gives zeros, a single filled slot gives its
+  value, and the split-KV merge matches the single-split result.
+"""
+import numpy as np
+import pytest
+import torch
+
+import ring_kv_cache_gb300 as kv
+from oracle import Ring
+from oracle.attention import attention_emulated, attention_exact
+from workloads import RingShape, TINY, frame, tiny_session
+
+from _ringcheck import MAX_ABS, MEAN_ABS, attn_errors, dev, f, make_pair
+
+pytestmark = pytest.mark.gpu
+
+
+def _tiny_loaded(frames_written, **kw):
+    frames = tiny_session()
+    ring, orc = make_pair(TINY, Ring, **kw)
+    ring.calibrate(dev(frames[0][1]), dev(frames[0][2]))
+    orc.calibrate(f(frames[0][1]), f(frames[0][2]))
+    for i in range(frames_written):
+        ring.write(dev(frames[i][1]), dev(frames[i][2]))
+        orc.write(f(frames[i][1]), f(frames[i][2]))
+    return ring, orc, frames
+
+
+@pytest.mark.parametrize("level", [1, 2, 3])
+def test_kernel_matches_its_mirror_tightly(level):
+    ring, orc, frames = _tiny_loaded(6, max_kv_splits=1, attn_precision=level)
+    q = frames[6][0]
+    out = ring.attention(dev(q)).cpu().numpy()
+    mirror = attention_emulated(orc, f(q), None, level, 1 if level == 1 else 2)
+    mx, mn = attn_errors(out, mirror)
+    scale = np.abs(mirror).max()
+    assert mx <= 2e-3 * scale, (level, mx, scale)
+    ref = attention_exact(orc, f(q))
+    mx2, mn2 = attn_errors(out, ref)
+    assert mx2 <= MAX_ABS and mn2 <= MEAN_ABS
+
+
+def test_levels_reported_and_automatic_choice_is_in_range():
+    ring, orc, frames = _tiny_loaded(3)
+    ring.attention(dev(frames[3][0]))
+    lv = ring.levels().cpu().numpy()
+    assert lv.shape[1] == TINY.heads and np.all((lv[0] >= 1) & (lv[0] <= 3))
+
+
+def test_empty_ring_gives_zeros():
+    ring = kv.KvRing(2, 64, 48, 12, 256)
+    x = torch.randn((12, 2, 64), device="cuda").bfloat16()
+    ring.calibrate(x, x)
+    out = ring.attention(x)
+    assert torch.count_nonzero(out) == 0
+
+
+def test_single_filled_slot_returns_its_value():
+    rng = np.random.default_rng(2)
+    shape = RingShape(heads=2, head_dim=128, capacity=300, tokens=1, queries=200, max_position=1000)
+    ring, orc = make_pair(shape, Ring, max_tokens=200)
+    q, k, v = frame(rng, shape, 1)
+    ring.calibrate(dev(k), dev(v))
+    orc.calibrate(f(k), f(v))
+    ring.write(dev(k), dev(v))
+    orc.write(f(k), f(v))
+    qq, _, _ = frame(rng, shape, 200)
+    out = ring.attention(dev(qq), torch.zeros(200, dtype=torch.int32, device="cuda")).cpu().numpy()
+    want = attention_exact(orc, f(qq), np.zeros(200, int))
+    assert np.allclose(out, want, atol=1e-5 * np.abs(want).max())
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16])
+def test_split_merge_consistent(splits):
+    rng = np.random.default_rng(3)
+    shape = RingShape(heads=2, head_dim=128, capacity=2000, tokens=700, queries=300, max_position=4000)
+    ring, orc = make_pair(shape, Ring, max_tokens=700, max_kv_splits=splits)
+    for i in range(3):
+        q, k, v = frame(rng, shape, 700)
+        if i == 0:
+            ring.calibrate(dev(k), dev(v))
+            orc.calibrate(f(k), f(v))
+        ring.write(dev(k), dev(v))
+        orc.write(f(k), f(v))
+    q, _, _ = frame(rng, shape, 300)
+    out = ring.attention(dev(q)).cpu().numpy()
+    mx, mn = attn_errors(out, attention_exact(orc, f(q)))
+    assert mx <= MAX_ABS and mn <= MEAN_ABS, (splits, mx, mn)
+
+
+def test_bf16_output_close_to_f32_output():
+    ring, orc, frames = _tiny_loaded(5)
+    q = dev(frames[5][0])
+    o32 = ring.attention(q)
+    o16 = ring.attention(q, out_dtype=torch.bfloat16)
+    assert torch.allclose(o16.float(), o32, rtol=2 ** -7, atol=1e-6)
