@@ -1,0 +1,423 @@
+"""Benchmark of the rolling FP8 attention cache on one GB300 (or N replicas).
+
+Workload (the production-shaped call): one layer's ring of 5,788 slots,
+10 heads of 128, bf16 inputs; one step = one 757-token frame write (RoPE +
+E4M3 quantisation into the ring) + attention of the frame's 757 queries over
+all 5,788 slots.  The pages report 5,788 slots with 757 new per call
+("Where the Time Went", Runway Characters serving post); 10 heads of 128 is
+the assumed 4-way split of 40 heads.  Inputs are synthetic: K, V ~ N(0,1)
+times a per-head standard deviation drawn log-uniform in [0.25, 4]; Q ~ N(0,1).
+
+L2: steps rotate over 16 independent rings (and 16 input frames), so each
+step's ring, inputs and partials were last touched 15 steps earlier, after
+more than 126 MB of other traffic: every step starts L2-cold.
+
+Timing: W warm-up steps, then exactly K steps between CUDA events on the
+launching stream, with a barrier and device synchronisation on both sides;
+per-kernel durations from events around each launch on the same stream.
+The metric is time-like (microseconds per write + attention).
+
+``--impl reference`` times the CPU oracle (float64 NumPy, the test oracle)
+on this host's cores on a bounded sample of each step (see ``cpu_step``).
+Replicas only across GPUs: each rank runs its own rings; no collective is
+on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per 757-token cache write + 5788-slot FP8 attn; GB/s & TFLOP/s vs GB300 peak"
+H, D, C, N_NEW, N_Q, MAX_POS = 10, 128, 5788, 757, 757, 40960
+RINGS = 16
+# algorithmic work per step
+WRITE_BYTES = 2 * N_NEW * H * D * 2 + 2 * N_NEW * H * D + N_NEW * 4  # bf16 in, e4m3 out, slot_pos
+ATTN_FLOPS = 4.0 * H * N_Q * C * D                                   # QK^T and PV
+ATTN_BYTES = 2 * H * C * D + N_Q * H * D * 2 + N_Q * H * D * 4       # cache, q, fp32 out
+H2D_BYTES = 3 * N_NEW * H * D * 2
+D2H_BYTES = N_Q * H * D * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def attention_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current attention source; else None."""
+    src = os.path.join(ROOT, "ring_kv_cache_gb300", "csrc", "kvring_attn.cu")
+    prof = os.path.join(ROOT, "profiles", "attention_prod_traffic.json")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        p = json.load(open(prof))
+        if p.get("kvring_attn_cu_sha256") == sha:
+            return float(p["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.06)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def gpu_arm(args, rank, world):
+    import torch
+    import ring_kv_cache_gb300 as kv
+    from workloads import PROD, prod_session, to_torch_bf16
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    rings = []
+    frames = []
+    with torch.cuda.stream(stream):
+        for i in range(RINGS):
+            sk, sv, fr = prod_session(seed=2 + 1000 * rank + i, frames=9)
+            ring = kv.KvRing(H, D, C, N_NEW, MAX_POS, 10000.0, max_kv_splits=16, stream=stream)
+            t = [(to_torch_bf16(q).to(dev), to_torch_bf16(k).to(dev), to_torch_bf16(v).to(dev))
+                 for q, k, v in fr]
+            ring.calibrate(t[0][1], t[0][2], stream=stream)
+            for q, k, v in t[:8]:          # 6,056 tokens: the ring has wrapped
+                ring.write(k, v, stream=stream)
+            rings.append(ring)
+            frames.append(t[8])
+        outs = [torch.empty((N_Q, H, D), dtype=torch.float32, device=dev) for _ in range(RINGS)]
+    torch.cuda.synchronize(dev)
+
+    def step(i, ev=None):
+        r = i % RINGS
+        q, k, v = frames[r]
+        if ev is not None:
+            ev[0].record(stream)
+        rings[r].write(k, v, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        rings[r].attention(q, out=outs[r], stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # timed region: K steps, events around the whole region on the stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = start.elapsed_time(stop)
+    w_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    a_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+
+    # end to end through the public API with pinned host buffers
+    hk = [torch.empty((N_NEW, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    hout = torch.empty((N_Q, H, D), dtype=torch.float32).pin_memory()
+    for j, x in enumerate(frames[0]):
+        hk[j].copy_(x.cpu())
+    dq = torch.empty((N_Q, H, D), dtype=torch.bfloat16, device=dev)
+    dk, dv = torch.empty_like(dq), torch.empty_like(dq)
+
+    def e2e_step(i):
+        r = i % RINGS
+        dq.copy_(hk[0], non_blocking=True)
+        dk.copy_(hk[1], non_blocking=True)
+        dv.copy_(hk[2], non_blocking=True)
+        rings[r].write(dk, dv, stream=stream)
+        rings[r].attention(dq, out=outs[r], stream=stream)
+        hout.copy_(outs[r], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # precision levels used on the timed workload (for the issued-FLOP count)
+    levels = []
+    for r in rings:
+        lv = r.levels().cpu().numpy()[: (N_Q + 127) // 128]
+        levels.append(lv)
+    levels = np.concatenate(levels).ravel()
+    errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
+    return dict(total_ms=total_ms, w_ms=w_ms, a_ms=a_ms, e2e_ms=e2e_ms, clocks=clk.summary(),
+                levels=levels, device_errors=int(np.bitwise_or.reduce(errs)))
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+def cpu_step(ring_state, tokens: int, queries: int):
+    """One bounded sample of a step on the CPU oracle: write `tokens` of the
+    frame and attend `queries` of the queries; returns seconds scaled to the
+    full 757-token write + 757-query attention."""
+    from oracle.attention import attention_exact
+    orc, fr = ring_state
+    q, k, v = fr
+    t0 = time.perf_counter()
+    orc.write(k[:tokens], v[:tokens])
+    t1 = time.perf_counter()
+    attention_exact(orc, q[:queries], np.arange(orc.next_pos - queries, orc.next_pos))
+    t2 = time.perf_counter()
+    return (t1 - t0) * N_NEW / tokens + (t2 - t1) * N_Q / queries
+
+
+def cpu_setup():
+    from oracle import Ring
+    from workloads import prod_session, f32_from_bf16
+    sk, sv, fr = prod_session(seed=2, frames=9)
+    orc = Ring(H, D, C, MAX_POS)
+    orc.calibrate(f32_from_bf16(fr[0][1]), f32_from_bf16(fr[0][2]))
+    for q, k, v in fr[:8]:
+        orc.write(f32_from_bf16(k), f32_from_bf16(v))
+    q, k, v = fr[8]
+    return orc, (f32_from_bf16(q), f32_from_bf16(k), f32_from_bf16(v))
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s: float = 15.0):
+    st = cpu_setup()
+    secs = []
+    t_end = time.perf_counter() + budget_s
+    while time.perf_counter() < t_end or not secs:
+        secs.append(cpu_step(st, 64, 16))
+    us = float(np.median(secs)) * 1e6
+    return {"value": us, "unit": "µs", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{len(secs)} samples of a 64-token write + 16-query attention over the "
+                      f"wrapped 5,788-slot ring (10 heads x 128), scaled x757/64 and x757/16; median"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    st = cpu_setup()
+    tokens, queries = (8, 1) if args.steps > 50 else (64, 8)
+    for _ in range(args.warmup):
+        cpu_step(st, tokens, queries)
+    secs = [cpu_step(st, tokens, queries) for _ in range(args.steps)]
+    us = float(np.mean(secs)) * 1e6
+    line = {
+        "metric": METRIC, "value": us, "unit": "µs", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "production-shaped call: 757-token write + 757-query attention over a "
+                               "wrapped 5,788-slot ring, 10 heads x 128",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": us, "unit": "µs", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"each step writes {tokens} tokens and attends {queries} queries, "
+                                   f"scaled to 757 and 757"},
+        "e2e": {"value": us, "unit": "µs", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="kvring", choices=["kvring", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "kvring":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl" if args.impl == "kvring" else "gloo")
+
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    res = gpu_arm(args, rank, world)
+    total_ms = reduce_max(res["total_ms"], world)
+    e2e_ms = reduce_max(res["e2e_ms"], world)
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    K = args.steps
+    units = K * world
+    us_per_unit = total_ms * 1e3 / units
+    w_us = float(np.mean(res["w_ms"])) * 1e3
+    a_us = float(np.mean(res["a_ms"])) * 1e3
+    fp8_peak = 2.0 * peaks["bf16"]            # FP8 dense = 2 x bf16 (nominal 4.5 / 2.25 PF)
+    lv = res["levels"]
+    q_terms = np.where(lv >= 3, 3, np.where(lv >= 2, 2, 1))
+    p_terms = np.where(lv >= 2, 2, 1)
+    # issued MMA work relative to the algorithmic 2 units (QK, PV) per tile;
+    # the normaliser MMA (N=16) adds 16/128 of a PV per P term
+    issued = float(np.mean(q_terms + p_terms * (1 + 16.0 / D))) / 2.0
+    attn_tflops = ATTN_FLOPS / (a_us * 1e-6) / 1e12
+    write_gbs = WRITE_BYTES / (w_us * 1e-6) / 1e9
+    traffic = attention_traffic()
+    line = {
+        "metric": METRIC,
+        "value": us_per_unit,
+        "unit": "µs",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {
+            "workload": "production-shaped call: 757-token write + 757-query attention over a "
+                        "wrapped 5,788-slot ring, 10 heads x 128 (E4M3 cache, bf16 in, fp32 out)",
+            "heads": H, "head_dim": D, "capacity": C, "tokens_per_write": N_NEW, "queries": N_Q,
+            "l2": f"cold: {RINGS} rings and input frames round-robin, >126 MB between reuses",
+            "parallelism": "replicas" if world > 1 else "1 GPU",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "k_attention (FP8 attention, tcgen05)",
+            "achieved": attn_tflops,
+            "peak": fp8_peak,
+            "unit": "TFLOP/s",
+            "frac": attn_tflops / fp8_peak,
+            "traffic": traffic,
+            "peak_source": f"{peaks['src']}: FP8 = 2 x bf16 burst {peaks['bf16']} TFLOP/s",
+            "issued_mma_over_algorithmic": issued,
+            "issued_frac": attn_tflops * issued / fp8_peak,
+            "algorithmic_flops_per_launch": ATTN_FLOPS,
+            "avg_launch_us": a_us,
+            "precision_levels": {str(k): int((lv == k).sum()) for k in (1, 2, 3)},
+        },
+        "kernels": {
+            "write": {"avg_launch_us": w_us, "algorithmic_bytes": WRITE_BYTES, "GB/s": write_gbs,
+                      "frac_hbm": write_gbs / peaks["hbm"], "peak_gbs": peaks["hbm"]},
+            "attention": {"avg_launch_us": a_us, "TFLOP/s": attn_tflops,
+                          "cache_GB/s": ATTN_BYTES / (a_us * 1e-6) / 1e9},
+        },
+        "e2e": {"value": e2e_ms * 1e3 / units, "unit": "µs",
+                "h2d_bytes_per_step": H2D_BYTES, "d2h_bytes_per_step": D2H_BYTES},
+        "gpu_launches": 2 * K,
+        "clocks": res["clocks"],
+        "device_errors": res["device_errors"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

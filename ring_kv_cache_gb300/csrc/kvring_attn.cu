@@ -27,9 +27,9 @@
 // S is double-buffered in TMEM so S(j+1) is computed while the softmax
 // works on S(j); P is double-buffered in shared memory.
 //
-// Precision level per CTA (uniform, from the query tile's amax times the
-// head's key range 448*scale_k): level 1 = 1 Q term + 1 P term, level 2 =
-// 2 + 2, level 3 = 3 + 2.  Extra terms are residuals at the same scale,
+// Precision level per CTA (uniform, from the query tile's amax, the head's
+// key range 448*scale_k and value range 448*scale_v): level 1 = 1 Q term +
+// 1 P term, level 2 = 2 + 2, level 3 = 3 + 2.  Extra terms are residuals at the same scale,
 // accumulated into the same TMEM accumulator.
 //
 // Every wait is bounded (about a second of wall time); a wait that gives up
@@ -46,8 +46,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 constexpr float kTau = 0.5f;      // raise the running max only when it grows by > 2^0.5
 constexpr float kPShift = 8.0f;   // probabilities carry a 2^8 factor (max 2^8.5 < 448)
-constexpr float kLevel1Max = 12.0f;   // amax(q) * amax(k) limits for levels 1 and 2
-constexpr float kLevel2Max = 100.0f;
+// Level rule: with L = max|q| * max|k| over the tile (rotated query units
+// times 448 * scale_k) and V = 448 * scale_v, level 1 only when both are
+// small (one FP8 term of P errs by up to 2^-4 of |v|), level 2 up to L = 64,
+// level 3 beyond.  Measured against the float64 reference on the seeded
+// workloads: level 1 errs by 2-6e-2 at unit scale, level 2 by about 1e-3.
+constexpr float kLevel1MaxL = 4.0f;
+constexpr float kLevel1MaxV = 0.5f;
+constexpr float kLevel2MaxL = 64.0f;
 
 template <int D>
 struct Layout {
@@ -205,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float qm = fmaxf(fmaxf(misc->warp_qmax[0], misc->warp_qmax[1]),
                              fmaxf(misc->warp_qmax[2], misc->warp_qmax[3]));
       const float lg = qm * 448.0f * scale_k;
-      level = lg <= kLevel1Max ? 1 : (lg <= kLevel2Max ? 2 : 3);
+      const float vmax = 448.0f * r.scales[H + h];
+      level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
     }
     if (threadIdx.x == 0) {
       misc->level = level;
