@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "µs per 757-token cache write + 5788-slot FP8 attn; GB/s & TFLOP/s vs GB300 peak"
 H, D, C, N_NEW, N_Q, MAX_POS = 10, 128, 5788, 757, 757, 40960
 RINGS = 16
+RESET_PERIOD = 42   # the pages reset positions once per 42 steps (Do It Once, at Write Time)
 # algorithmic work per step
 WRITE_BYTES = 2 * N_NEW * H * D * 2 + 2 * N_NEW * H * D + N_NEW * 4  # bf16 in, e4m3 out, slot_pos
 ATTN_FLOPS = 4.0 * H * N_Q * C * D                                   # QK^T and PV
@@ -158,9 +159,16 @@ def gpu_arm(args, rank, world):
         outs = [torch.empty((N_Q, H, D), dtype=torch.float32, device=dev) for _ in range(RINGS)]
     torch.cuda.synchronize(dev)
 
+    writes = [8] * RINGS          # frames already written per ring
+
     def step(i, ev=None):
         r = i % RINGS
         q, k, v = frames[r]
+        if writes[r] % RESET_PERIOD == 0:
+            # positions reset every 42 steps: one delta rotation of the window
+            rings[r].delta_rotate(kv.TO_OLDEST, stream=stream)
+            resets[0] += 1
+        writes[r] += 1
         if ev is not None:
             ev[0].record(stream)
         rings[r].write(k, v, stream=stream)
@@ -175,6 +183,7 @@ def gpu_arm(args, rank, world):
             import torch.distributed as dist
             dist.barrier()
 
+    resets = [0]
     # warm-up
     for i in range(args.warmup):
         step(i)
@@ -185,6 +194,7 @@ def gpu_arm(args, rank, world):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
+    resets[0] = 0
     with ClockSampler(dev.index) as clk:
         start.record(stream)
         for i in range(args.steps):
@@ -193,6 +203,7 @@ def gpu_arm(args, rank, world):
         torch.cuda.synchronize(dev)
     barrier()
     total_ms = start.elapsed_time(stop)
+    timed_resets = resets[0]
     w_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
     a_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
 
@@ -206,6 +217,9 @@ def gpu_arm(args, rank, world):
 
     def e2e_step(i):
         r = i % RINGS
+        if writes[r] % RESET_PERIOD == 0:
+            rings[r].delta_rotate(kv.TO_OLDEST, stream=stream)
+        writes[r] += 1
         dq.copy_(hk[0], non_blocking=True)
         dk.copy_(hk[1], non_blocking=True)
         dv.copy_(hk[2], non_blocking=True)
@@ -235,6 +249,7 @@ def gpu_arm(args, rank, world):
     levels = np.concatenate(levels).ravel()
     errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
     return dict(total_ms=total_ms, w_ms=w_ms, a_ms=a_ms, e2e_ms=e2e_ms, clocks=clk.summary(),
+                resets=timed_resets,
                 levels=levels, device_errors=int(np.bitwise_or.reduce(errs)))
 
 
@@ -382,6 +397,8 @@ def main():
                         "wrapped 5,788-slot ring, 10 heads x 128 (E4M3 cache, bf16 in, fp32 out)",
             "heads": H, "head_dim": D, "capacity": C, "tokens_per_write": N_NEW, "queries": N_Q,
             "l2": f"cold: {RINGS} rings and input frames round-robin, >126 MB between reuses",
+            "resets": f"one delta rotation per ring every {RESET_PERIOD} writes (positions reset "
+                      f"period), inside the timed region: {res['resets']} in {K} steps",
             "parallelism": "replicas" if world > 1 else "1 GPU",
         },
         "roofline": {
@@ -407,7 +424,7 @@ def main():
         },
         "e2e": {"value": e2e_ms * 1e3 / units, "unit": "µs",
                 "h2d_bytes_per_step": H2D_BYTES, "d2h_bytes_per_step": D2H_BYTES},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 2 * K + res["resets"],
         "clocks": res["clocks"],
         "device_errors": res["device_errors"],
     }

@@ -17,7 +17,7 @@ and a float64 softmax with the row maximum subtracted.
 
 ``attention_emulated`` is a diagnostic that repeats the CUDA kernel's
 choices (queries split into FP8 terms with a per-row scale, probabilities
-scaled by 2^8 relative to a lazily updated running maximum and split into FP8
+scaled by 2^7 relative to a lazily raised running maximum and split into FP8
 terms, a normaliser summed from the same FP8 terms) in float64, so that
 format error and kernel bugs can be told apart.
 """
@@ -117,7 +117,7 @@ def _split_terms(u: np.ndarray, m: int):
 
 
 def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
-                       p_shift=8.0, tau=0.5) -> np.ndarray:
+                       p_shift=7.0, tau=1.5) -> np.ndarray:
     """Diagnostic: the CUDA kernel's quantisation choices, in float64.
 
     q_terms / p_terms may be ints or per-head sequences.

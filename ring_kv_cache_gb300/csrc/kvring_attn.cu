@@ -9,16 +9,20 @@
 // over the filled slots j, Kdeq = code * scale_k[h], Vdeq = code * scale_v[h].
 //
 // CTA = one 128-query tile x one head x one range of key/value tiles
-// (split-KV).  Six warps:
-//   warps 0-3  softmax: thread i owns query row i (= TMEM lane i).  Prologue:
-//              RoPE the row in fp32, scale by 448/amax(row), split into 1-3
-//              E4M3 terms in shared memory.  Loop: read S from TMEM, online
-//              softmax in log2 units with a lazily raised running maximum,
-//              probabilities scaled by 2^8 and split into 1-2 E4M3 terms
+// (split-KV).  Ten warps:
+//   warps 0-7  softmax.  Query row r = threadIdx % 128 (= TMEM lane r) is
+//              shared by two threads: warps 0-3 own columns [0, 64) of S and
+//              [0, d/2) of O, warps 4-7 the other halves; the pair exchanges
+//              row maxima through shared memory.  Prologue: RoPE the query
+//              in fp32, scale by 448/amax(row), split into 1-3 E4M3 terms in
+//              shared memory.  Loop: read S from TMEM, online softmax in
+//              log2 units with a lazily raised running maximum, probabilities
+//              scaled by 2^7 and split into 1-2 E4M3 terms (residual in f16x2)
 //              written to shared memory; rescale O in TMEM when the maximum
-//              rises.  Epilogue: O / l, split partials and their merge.
-//   warp 4     TMA producer: K and V tiles [128 slots][d] into a 3-stage ring.
-//   warp 5     TMEM allocation and the single MMA-issuing thread:
+//              rises by more than 2^1.5.  Epilogue: O / l, split partials and
+//              their merge.
+//   warp 8     TMA producer: K and V tiles [128 slots][d] into a 3-stage ring.
+//   warp 9     TMEM allocation and the single MMA-issuing thread:
 //              S = sum_t Q_t K^T (kind::f8f6f4, K-major operands), then
 //              O += sum_t P_t V (V MN-major straight from its [slot][d]
 //              cache layout) and l += sum_t P_t 1 (a 16-wide all-ones
@@ -29,8 +33,8 @@
 //
 // Precision level per CTA (uniform, from the query tile's amax, the head's
 // key range 448*scale_k and value range 448*scale_v): level 1 = 1 Q term +
-// 1 P term, level 2 = 2 + 2, level 3 = 3 + 2.  Extra terms are residuals at the same scale,
-// accumulated into the same TMEM accumulator.
+// 1 P term, level 2 = 2 + 2, level 3 = 3 + 2.  Extra terms are residuals at
+// the same scale, accumulated into the same TMEM accumulator.
 //
 // Every wait is bounded (about a second of wall time); a wait that gives up
 // sets KVRING_DEVERR_TIMEOUT in the ring's error word, the CTA drains its
@@ -41,11 +45,17 @@ namespace kvr {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
-constexpr float kTau = 0.5f;      // raise the running max only when it grows by > 2^0.5
-constexpr float kPShift = 8.0f;   // probabilities carry a 2^8 factor (max 2^8.5 < 448)
+// Probabilities carry a factor 2^kPShift relative to the running maximum,
+// which is raised only when a tile's maximum exceeds it by more than kTau:
+// the largest probability is 2^(kPShift + kTau) = 2^8.5 < 448 (E4M3 max).
+constexpr float kTau = 1.5f;
+constexpr float kPShift = 7.0f;
 // Level rule: with L = max|q| * max|k| over the tile (rotated query units
 // times 448 * scale_k) and V = 448 * scale_v, level 1 only when both are
 // small (one FP8 term of P errs by up to 2^-4 of |v|), level 2 up to L = 64,
@@ -65,7 +75,8 @@ struct Layout {
   static constexpr int kV = kK + kStages * kKVTile;
   static constexpr int kP = kV + kStages * kKVTile;
   static constexpr int kOnes = kP + 2 * 2 * kPTile;
-  static constexpr int kBars = kOnes + 16 * kTile;
+  static constexpr int kXch = kOnes + 16 * kTile;       // float [2 parity][2 half][128 rows]
+  static constexpr int kBars = kXch + 2 * 2 * kTile * 4;
   // barrier slots (8 bytes each)
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kStages;
@@ -76,7 +87,7 @@ struct Layout {
   static constexpr int kBarMmaDone = 2 * kStages + 8;
   static constexpr int kNumBars = 2 * kStages + 9;
   static constexpr int kMisc = kBars + 8 * kNumBars;
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kBytes = kMisc + 128;
   static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code
   // TMEM columns
   static constexpr uint32_t kColS = 0;        // two 128-column S buffers
@@ -89,7 +100,7 @@ struct Misc {
   int level;
   int abort;
   int last;
-  float warp_qmax[4];
+  float warp_qmax[8];
 };
 
 struct AttnParams {
@@ -104,8 +115,33 @@ struct AttnParams {
   int forced_level;
 };
 
-__device__ __forceinline__ void named_sync_softmax() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// Named barriers: 0 = __syncthreads, 1 = the 256 softmax threads,
+// 2..5 = the two warps that share a group of 32 query rows.
+__device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void sync_pair(int quarter) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void store_row(void* out, bool bf16, size_t elem_off, const float* o, float f) {
+  if (bf16) {
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + elem_off);
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 bb = __floats2bfloat162_rn(o[8 * c + 2 * i] * f, o[8 * c + 2 * i + 1] * f);
+        w[i] = *reinterpret_cast<const uint32_t*>(&bb);
+      }
+      dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + elem_off);
+#pragma unroll
+    for (int c = 0; c < N / 4; ++c)
+      dst[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
+  }
 }
 
 template <int D>
@@ -113,10 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnParams prm) {
   using L = Layout<D>;
+  constexpr int HD = D / 2;             // query / output columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   Misc* misc = reinterpret_cast<Misc*>(sm + L::kMisc);
+  float* xch = reinterpret_cast<float*>(sm + L::kXch);
   volatile int* abort = &misc->abort;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBars + 8u * (uint32_t)i; };
 
@@ -138,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kBarSFull + b), 1);
-      mbar_init(bar(L::kBarSFree + b), 128);
-      mbar_init(bar(L::kBarPFull + b), 128);
+      mbar_init(bar(L::kBarSFree + b), kSoftmaxThreads);
+      mbar_init(bar(L::kBarPFull + b), kSoftmaxThreads);
       mbar_init(bar(L::kBarPvDone + b), 1);
     }
     mbar_init(bar(L::kBarMmaDone), 1);
@@ -147,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc->last = 0;
     mbar_fence_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -157,24 +195,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
   }
 
-  // ------------------------------------------------- query prologue (0-3)
-  const int row = threadIdx.x;              // softmax threads only
+  // --------------------------------------------- query prologue (warps 0-7)
+  const int row = threadIdx.x & (kTile - 1);
+  const int half = threadIdx.x >> 7;        // 0 or 1 for softmax threads
+  const int quarter = warp & 3;
   const int t_row = qt * kTile + row;
   float f_row = 0.f;                        // logit factor: sigma_q * scale_k * log2(e) / sqrt(d)
-  if (warp < 4) {
-    float q[D];
+  if (warp < 8) {
+    float q[HD];
     float amax = 0.f;
-    const bool live = t_row < prm.n_q;
-    if (live) {
+    if (t_row < prm.n_q) {
       int p = prm.qpos ? __ldg(prm.qpos + t_row) : __ldcg(r.state + ST_NEXT_POS) - prm.n_q + t_row;
       if (p < 0 || p >= r.max_pos) {
         atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
         p = 0;
       }
-      const uint4* src = reinterpret_cast<const uint4*>(prm.q + ((size_t)t_row * H + h) * D);
-      const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D);
+      const uint4* src = reinterpret_cast<const uint4*>(prm.q + ((size_t)t_row * H + h) * D + half * HD);
+      const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D + half * HD);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int c = 0; c < HD / 8; ++c) {
         const uint4 w = __ldg(src + c);  // 8 bf16 = 4 pairs
         const float4 cs0 = __ldg(tb + 2 * c), cs1 = __ldg(tb + 2 * c + 1);
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
@@ -192,24 +231,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < D; ++i) q[i] = 0.f;
+      for (int i = 0; i < HD; ++i) q[i] = 0.f;
     }
+    // row amax over both halves, then the CTA-wide maximum for the level
+    xch[half * kTile + row] = amax;
+    float wm = amax;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+    if (lane == 0) misc->warp_qmax[warp] = wm;
+    sync_softmax();
+    amax = fmaxf(amax, xch[(half ^ 1) * kTile + row]);
     float sq = amax / 448.0f;
     if (!(sq >= 0x1p-126f)) sq = 1.0f;
     const float invq = 1.0f / sq;
     const float scale_k = r.scales[h];
     f_row = sq * scale_k * (1.4426950408889634f / sqrtf((float)D));
-
-    // CTA-uniform precision level from max_row amax(q) * 448 * scale_k
-    float wm = amax;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
-    if (lane == 0) misc->warp_qmax[warp] = wm;
-    named_sync_softmax();
+    f_row = fmaxf(f_row, 1e-30f);  // stays positive, so masked -inf logits stay -inf
     int level = prm.forced_level;
     if (level == 0) {
-      const float qm = fmaxf(fmaxf(misc->warp_qmax[0], misc->warp_qmax[1]),
-                             fmaxf(misc->warp_qmax[2], misc->warp_qmax[3]));
+      float qm = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) qm = fmaxf(qm, misc->warp_qmax[w]);
       const float lg = qm * 448.0f * scale_k;
       const float vmax = 448.0f * r.scales[H + h];
       level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
@@ -221,11 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // E4M3 terms of q * invq: residual splitting, written swizzled (K-major)
 #pragma unroll
-    for (int i = 0; i < D; ++i) q[i] = q[i] * invq;
+    for (int i = 0; i < HD; ++i) q[i] = q[i] * invq;
     for (int term = 0; term < level; ++term) {
       uint8_t* qtile = sm + L::kQ + term * L::kQTile;
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
+      for (int c = 0; c < HD / 16; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -241,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             q[16 * c + 4 * i + 3] = a3 - dh.y;
           }
         }
-        *reinterpret_cast<uint4*>(qtile + swz_offset(row, c, D)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(qtile + swz_offset(row, half * (HD / 16) + c, D)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     fence_proxy_async_smem();
@@ -255,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_qterms = level;
   const int n_pterms = level >= 2 ? 2 : 1;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued = 0;
@@ -276,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
@@ -330,8 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ----------------------------------------------------------- softmax
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t trow = tmem + lane_base;
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_run = -INFINITY;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -339,47 +381,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_bounded(bar(L::kBarSFull + b), (j >> 1) & 1, abort, kWaitLimitNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
       tc_fence_after();
-      float x[kTile];
+      uint32_t sr[64];
       {
-        uint32_t rr[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(trow + L::kColS + b * 128 + c * 32, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]);
-        }
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
+        tmem_ld32(trow + L::kColS + b * 128 + half * 64, s0);
+        tmem_ld32(trow + L::kColS + b * 128 + half * 64 + 32, s1);
+        tmem_wait_ld();
       }
       tc_fence_before();
       mbar_arrive(bar(L::kBarSFree + b));
 
-      const int valid = nvalid - (tile0 + j) * kTile;  // >= 1
-      float tmax = -INFINITY;
+      // mask slots past the fill level (only the ring's last tile)
+      const int valid = nvalid - (tile0 + j) * kTile - half * 64;
+      if (valid < 64) {
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        x[c] = c < valid ? x[c] * f_row : -INFINITY;
-        tmax = fmaxf(tmax, x[c]);
+        for (int c = 0; c < 64; ++c)
+          if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
       }
+      float smax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) smax = fmaxf(smax, __uint_as_float(sr[c]));
+      xch[((j & 1) * 2 + half) * kTile + row] = smax;
+      sync_pair(quarter);
+      smax = fmaxf(smax, xch[((j & 1) * 2 + (half ^ 1)) * kTile + row]);
+      const float tmax = smax * f_row;          // f_row > 0
       const bool need = tmax > m_run + kTau;
       const float m_new = need ? tmax : m_run;
       if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
-        // O and l already hold tiles < j; wait for PV(j-1), then rescale
+        // O and l hold tiles < j: wait for PV(j-1), then rescale this half
         ok = mbar_wait_bounded(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, kWaitLimitNs);
         if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
         tc_fence_after();
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
         uint32_t rr[32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(trow + L::kColO + c * 32, rr);
+        for (int c = 0; c < HD / 32; ++c) {
+          tmem_ld32(trow + L::kColO + half * HD + c * 32, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st32(trow + L::kColO + c * 32, rr);
+          tmem_st32(trow + L::kColO + half * HD + c * 32, rr);
         }
-        const uint32_t lv = tmem_ld1(trow + L::kColL);
-        tmem_wait_ld();
-        tmem_st1(trow + L::kColL, __float_as_uint(__uint_as_float(lv) * alpha));
+        if (half == 0) {
+          const uint32_t lv = tmem_ld1(trow + L::kColL);
+          tmem_wait_ld();
+          tmem_st1(trow + L::kColL, __float_as_uint(__uint_as_float(lv) * alpha));
+        }
         tmem_wait_st();
       }
       m_run = m_new;
@@ -392,24 +440,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* p0 = sm + L::kP + (b * 2 + 0) * L::kPTile;
       uint8_t* p1 = sm + L::kP + (b * 2 + 1) * L::kPTile;
 #pragma unroll
-      for (int c = 0; c < kTile / 16; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t w0[4], w1[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float e0 = ex2_approx(x[16 * c + 4 * i] + moff);
-          const float e1 = ex2_approx(x[16 * c + 4 * i + 1] + moff);
-          const float e2 = ex2_approx(x[16 * c + 4 * i + 2] + moff);
-          const float e3 = ex2_approx(x[16 * c + 4 * i + 3] + moff);
-          const uint16_t lo = f32x2_to_e4m3x2(e0, e1), hi = f32x2_to_e4m3x2(e2, e3);
-          w0[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+          const int e = 16 * c + 4 * i;
+          const float e0 = ex2_approx(fmaf(__uint_as_float(sr[e]), f_row, moff));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), f_row, moff));
+          const float e2 = ex2_approx(fmaf(__uint_as_float(sr[e + 2]), f_row, moff));
+          const float e3 = ex2_approx(fmaf(__uint_as_float(sr[e + 3]), f_row, moff));
           if (n_pterms > 1) {
-            const float2 dl = e4m3x2_to_f32x2(lo), dh = e4m3x2_to_f32x2(hi);
-            const uint16_t lo2 = f32x2_to_e4m3x2(e0 - dl.x, e1 - dl.y);
-            const uint16_t hi2 = f32x2_to_e4m3x2(e2 - dh.x, e3 - dh.y);
+            // two terms: P1 from the f16 value, P2 from its f16 residual
+            const uint32_t h01 = f32x2_to_f16x2(e0, e1), h23 = f32x2_to_f16x2(e2, e3);
+            const uint16_t lo = f16x2_to_e4m3x2(h01), hi = f16x2_to_e4m3x2(h23);
+            w0[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+            const uint16_t lo2 = f16x2_to_e4m3x2(hsub2_u32(h01, e4m3x2_to_f16x2(lo)));
+            const uint16_t hi2 = f16x2_to_e4m3x2(hsub2_u32(h23, e4m3x2_to_f16x2(hi)));
             w1[i] = (uint32_t)lo2 | ((uint32_t)hi2 << 16);
+          } else {
+            w0[i] = (uint32_t)f32x2_to_e4m3x2(e0, e1) | ((uint32_t)f32x2_to_e4m3x2(e2, e3) << 16);
           }
         }
-        const uint32_t off = swz_offset(row, c, 128);
+        const uint32_t off = swz_offset(row, half * 4 + c, 128);
         *reinterpret_cast<uint4*>(p0 + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
         if (n_pterms > 1) *reinterpret_cast<uint4*>(p1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
       }
@@ -419,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------- epilogue
-    float o[D];
+    float o[HD];
     float l = 0.f;
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
@@ -430,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t rr[32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(trow + L::kColO + c * 32, rr);
+      for (int c = 0; c < HD / 32; ++c) {
+        tmem_ld32(trow + L::kColO + half * HD + c * 32, rr);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(rr[i]);
@@ -440,48 +492,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
     } else {
 #pragma unroll
-      for (int i = 0; i < D; ++i) o[i] = 0.f;
+      for (int i = 0; i < HD; ++i) o[i] = 0.f;
     }
     const float inv_l = l > 0.f ? 1.0f / l : 0.f;
     const float scale_v = r.scales[H + h];
     const bool live = t_row < prm.n_q;
+    const size_t out_off = ((size_t)t_row * H + h) * D + half * HD;
     if (prm.nsplit == 1) {
-      if (live) {
-        const float f = inv_l * scale_v;
-        if (prm.out_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(prm.out) + ((size_t)t_row * H + h) * D);
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const __nv_bfloat162 bb = __floats2bfloat162_rn(o[8 * c + 2 * i] * f, o[8 * c + 2 * i + 1] * f);
-              w[i] = *reinterpret_cast<const uint32_t*>(&bb);
-            }
-            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + ((size_t)t_row * H + h) * D);
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c)
-            dst[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
-        }
-      }
+      if (live) store_row<HD>(prm.out, prm.out_bf16 != 0, out_off, o, inv_l * scale_v);
     } else {
       // partial (normalised) output and its log2-sum-exp for this split
       const size_t prow = (((size_t)split * r.qtiles_max + qt) * H + h) * kTile + row;
-      float4* po = reinterpret_cast<float4*>(r.part_o + prow * D);
+      float4* po = reinterpret_cast<float4*>(r.part_o + prow * D + half * HD);
 #pragma unroll
-      for (int c = 0; c < D / 4; ++c)
+      for (int c = 0; c < HD / 4; ++c)
         __stcg(po + c, make_float4(o[4 * c] * inv_l, o[4 * c + 1] * inv_l, o[4 * c + 2] * inv_l, o[4 * c + 3] * inv_l));
-      __stcg(r.part_lse + prow, l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY);
+      if (half == 0) __stcg(r.part_lse + prow, l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY);
       __threadfence();
-      named_sync_softmax();
+      sync_softmax();
       if (threadIdx.x == 0) {
         const int tk = atomicAdd(r.tickets + qt * H + h, 1);
         misc->last = tk == prm.nsplit - 1;
       }
-      named_sync_softmax();
+      sync_softmax();
       if (misc->last) {
         __threadfence();
         float mx = -INFINITY;
@@ -489,9 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const size_t pr = (((size_t)s * r.qtiles_max + qt) * H + h) * kTile + row;
           mx = fmaxf(mx, __ldcg(r.part_lse + pr));
         }
-        float acc[D];
 #pragma unroll
-        for (int i = 0; i < D; ++i) acc[i] = 0.f;
+        for (int i = 0; i < HD; ++i) o[i] = 0.f;
         float wsum = 0.f;
         if (mx > -INFINITY) {
           for (int s = 0; s < prm.nsplit; ++s) {
@@ -500,38 +532,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(lse > -INFINITY)) continue;
             const float w = ex2_approx(lse - mx);
             wsum += w;
-            const float4* src = reinterpret_cast<const float4*>(r.part_o + pr * D);
+            const float4* src = reinterpret_cast<const float4*>(r.part_o + pr * D + half * HD);
 #pragma unroll
-            for (int c = 0; c < D / 4; ++c) {
+            for (int c = 0; c < HD / 4; ++c) {
               const float4 vv = __ldcg(src + c);
-              acc[4 * c] += w * vv.x;
-              acc[4 * c + 1] += w * vv.y;
-              acc[4 * c + 2] += w * vv.z;
-              acc[4 * c + 3] += w * vv.w;
+              o[4 * c] = fmaf(w, vv.x, o[4 * c]);
+              o[4 * c + 1] = fmaf(w, vv.y, o[4 * c + 1]);
+              o[4 * c + 2] = fmaf(w, vv.z, o[4 * c + 2]);
+              o[4 * c + 3] = fmaf(w, vv.w, o[4 * c + 3]);
             }
           }
         }
-        const float f = wsum > 0.f ? scale_v / wsum : 0.f;
-        if (live) {
-          if (prm.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(prm.out) + ((size_t)t_row * H + h) * D);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-              uint32_t w[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[8 * c + 2 * i] * f, acc[8 * c + 2 * i + 1] * f);
-                w[i] = *reinterpret_cast<const uint32_t*>(&bb);
-              }
-              dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + ((size_t)t_row * H + h) * D);
-#pragma unroll
-            for (int c = 0; c < D / 4; ++c)
-              dst[c] = make_float4(acc[4 * c] * f, acc[4 * c + 1] * f, acc[4 * c + 2] * f, acc[4 * c + 3] * f);
-          }
-        }
+        if (live) store_row<HD>(prm.out, prm.out_bf16 != 0, out_off, o, wsum > 0.f ? scale_v / wsum : 0.f);
         if (threadIdx.x == 0) r.tickets[qt * H + h] = 0;
       }
     }
@@ -542,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0 && misc->abort)
     atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_TIMEOUT);
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
