@@ -10,26 +10,28 @@
 //
 // CTA = one 128-query tile x one head x one range of key/value tiles
 // (split-KV).  Ten warps:
-//   warps 0-7  softmax.  Query row r = threadIdx % 128 (= TMEM lane r) is
-//              shared by two threads: warps 0-3 own columns [0, 64) of S and
-//              [0, d/2) of O, warps 4-7 the other halves; the pair exchanges
-//              row maxima through shared memory.  Prologue: RoPE the query
-//              in fp32, scale by 448/amax(row), split into 1-3 E4M3 terms in
-//              shared memory.  Loop: read S from TMEM, online softmax in
-//              log2 units with a lazily raised running maximum, probabilities
-//              scaled by 2^7 and split into 1-2 E4M3 terms (residual in f16x2)
-//              written to shared memory; rescale O in TMEM when the maximum
-//              rises by more than 2^1.5.  Epilogue: O / l, split partials and
-//              their merge.
+//   warps 0-7  Prologue (all 256 threads, coalesced): RoPE each query chunk
+//              in fp32, scale each row by 448/amax(row), split into 1-3 E4M3
+//              terms in shared memory.  Softmax: query row r = TMEM lane r
+//              is shared by two threads (warps 0-3 own S columns [0, 64) and
+//              O columns [0, d/2); warps 4-7 the other halves), which
+//              exchange row maxima through shared memory.  Online softmax in
+//              log2 units with a lazily raised running maximum; probabilities
+//              carry 2^7 and are split into 1-2 E4M3 terms that are written
+//              back into TMEM over the S columns just read; O is rescaled in
+//              TMEM when the maximum rises by more than 1.5 (log2 units).
+//              Epilogue: O / l, split partials and their merge.
 //   warp 8     TMA producer: K and V tiles [128 slots][d] into a 3-stage ring.
 //   warp 9     TMEM allocation and the single MMA-issuing thread:
-//              S = sum_t Q_t K^T (kind::f8f6f4, K-major operands), then
-//              O += sum_t P_t V (V MN-major straight from its [slot][d]
-//              cache layout) and l += sum_t P_t 1 (a 16-wide all-ones
-//              operand, so the softmax normaliser is summed from exactly the
-//              FP8 values that multiply V).
-// S is double-buffered in TMEM so S(j+1) is computed while the softmax
-// works on S(j); P is double-buffered in shared memory.
+//              S = sum_t Q_t K^T (A and B from shared memory, K-major), then
+//              [O | l] += sum_t P_t [V | 1] with P read from TMEM and B =
+//              the V tile (MN-major, straight from its [slot][d] cache layout)
+//              extended by a 16-column block of E4M3 ones, so the softmax
+//              normaliser l is summed by the same MMA from exactly the FP8
+//              values that multiply V.
+// S is double-buffered in TMEM, so S(j+1) is computed while the softmax works
+// on S(j).  P(j) overwrites S(j)'s columns; the MMAs of one CTA run in issue
+// order, so QK(j+2) (into the same columns) always follows PV(j).
 //
 // Precision level per CTA (uniform, from the query tile's amax, the head's
 // key range 448*scale_k and value range 448*scale_v): level 1 = 1 Q term +
@@ -69,30 +71,29 @@ template <int D>
 struct Layout {
   static constexpr int kQTile = kTile * D;      // one Q term tile (bytes)
   static constexpr int kKVTile = kTile * D;
-  static constexpr int kPTile = kTile * kTile;  // one P term tile
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 3 * kQTile;
   static constexpr int kV = kK + kStages * kKVTile;
-  static constexpr int kP = kV + kStages * kKVTile;
-  static constexpr int kOnes = kP + 2 * 2 * kPTile;
-  static constexpr int kXch = kOnes + 16 * kTile;       // float [2 parity][2 half][128 rows]
-  static constexpr int kBars = kXch + 2 * 2 * kTile * 4;
+  static constexpr int kOnes = kV + kStages * kKVTile;  // 128 x 128 bytes of E4M3 1.0
+  static constexpr int kXch = kOnes + kTile * kTile;    // float [2 parity][2 half][128 rows]
+  static constexpr int kRowF = kXch + 2 * 2 * kTile * 4;  // float [128] logit factor per row
+  static constexpr int kWarpMax = kRowF + kTile * 4;      // float [8]
+  static constexpr int kBars = kWarpMax + 64;
   // barrier slots (8 bytes each)
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kStages;
   static constexpr int kBarSFull = 2 * kStages;
-  static constexpr int kBarSFree = 2 * kStages + 2;
-  static constexpr int kBarPFull = 2 * kStages + 4;
-  static constexpr int kBarPvDone = 2 * kStages + 6;
-  static constexpr int kBarMmaDone = 2 * kStages + 8;
-  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int kBarPFull = 2 * kStages + 2;
+  static constexpr int kBarPvDone = 2 * kStages + 4;
+  static constexpr int kBarMmaDone = 2 * kStages + 6;
+  static constexpr int kNumBars = 2 * kStages + 7;
   static constexpr int kMisc = kBars + 8 * kNumBars;
-  static constexpr int kBytes = kMisc + 128;
+  static constexpr int kBytes = kMisc + 64;
   static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code
   // TMEM columns
-  static constexpr uint32_t kColS = 0;        // two 128-column S buffers
-  static constexpr uint32_t kColO = 256;      // D columns
-  static constexpr uint32_t kColL = 256 + D;  // 16 columns
+  static constexpr uint32_t kColS = 0;        // two 128-column S buffers (P overwrites)
+  static constexpr uint32_t kColO = 256;      // D columns of O, then 16 of l
+  static constexpr uint32_t kColL = 256 + D;
 };
 
 struct Misc {
@@ -100,7 +101,6 @@ struct Misc {
   int level;
   int abort;
   int last;
-  float warp_qmax[8];
 };
 
 struct AttnParams {
@@ -144,17 +144,26 @@ __device__ __forceinline__ void store_row(void* out, bool bf16, size_t elem_off,
   }
 }
 
+// Four fp32 values to four E4M3 codes (first value in the low byte).
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+  return (uint32_t)f32x2_to_e4m3x2(a, b) | ((uint32_t)f32x2_to_e4m3x2(c, d) << 16);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnParams prm) {
   using L = Layout<D>;
-  constexpr int HD = D / 2;             // query / output columns per softmax thread
+  constexpr int HD = D / 2;             // O columns per softmax thread
+  constexpr int CPR = D / 8;            // 8-element query chunks per row
+  constexpr int PRO = kTile * CPR / kSoftmaxThreads;  // prologue chunks per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   Misc* misc = reinterpret_cast<Misc*>(sm + L::kMisc);
   float* xch = reinterpret_cast<float*>(sm + L::kXch);
+  float* rowf = reinterpret_cast<float*>(sm + L::kRowF);
+  float* warpmax = reinterpret_cast<float*>(sm + L::kWarpMax);
   volatile int* abort = &misc->abort;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBars + 8u * (uint32_t)i; };
 
@@ -169,14 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
 
   // ---------------------------------------------------------------- setup
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == kWarpTma * 32) {
+    // The producer initialises the barriers, so it can start the first
+    // copies before the query prologue finishes.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKvFull + s), 1);
       mbar_init(bar(L::kBarKvEmpty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kBarSFull + b), 1);
-      mbar_init(bar(L::kBarSFree + b), kSoftmaxThreads);
       mbar_init(bar(L::kBarPFull + b), kSoftmaxThreads);
       mbar_init(bar(L::kBarPvDone + b), 1);
     }
@@ -184,112 +194,110 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
+    const int first = ntiles < kStages ? ntiles : kStages;
+    for (int j = 0; j < first; ++j) {
+      mbar_arrive_expect_tx(bar(L::kBarKvFull + j), 2u * kTile * D);
+      const int slot0 = (tile0 + j) * kTile;
+      tma_load_3d(sbase + L::kK + j * L::kKVTile, &tmK, 0, slot0, h, bar(L::kBarKvFull + j));
+      tma_load_3d(sbase + L::kV + j * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarKvFull + j));
+    }
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  {  // all-ones operand for the normaliser MMA (E4M3 1.0 = 0x38)
+  {  // all-ones block that extends V for the normaliser (E4M3 1.0 = 0x38)
     uint4* ones = reinterpret_cast<uint4*>(sm + L::kOnes);
-    for (int i = threadIdx.x; i < 16 * kTile / 16; i += kThreads)
+    for (int i = threadIdx.x; i < kTile * kTile / 16; i += kThreads)
       ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
   }
 
   // --------------------------------------------- query prologue (warps 0-7)
-  const int row = threadIdx.x & (kTile - 1);
-  const int half = threadIdx.x >> 7;        // 0 or 1 for softmax threads
-  const int quarter = warp & 3;
-  const int t_row = qt * kTile + row;
-  float f_row = 0.f;                        // logit factor: sigma_q * scale_k * log2(e) / sqrt(d)
+  // Chunk task k = i * 256 + tid: row k / CPR, chunk k % CPR (8 elements,
+  // 4 RoPE pairs); a warp reads 32 consecutive 16-byte chunks.
   if (warp < 8) {
-    float q[HD];
-    float amax = 0.f;
-    if (t_row < prm.n_q) {
-      int p = prm.qpos ? __ldg(prm.qpos + t_row) : __ldcg(r.state + ST_NEXT_POS) - prm.n_q + t_row;
-      if (p < 0 || p >= r.max_pos) {
-        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
-        p = 0;
-      }
-      const uint4* src = reinterpret_cast<const uint4*>(prm.q + ((size_t)t_row * H + h) * D + half * HD);
-      const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D + half * HD);
+    float qv[PRO][8];
+    float amax[PRO];
+    const int next_pos = __ldcg(r.state + ST_NEXT_POS);
 #pragma unroll
-      for (int c = 0; c < HD / 8; ++c) {
-        const uint4 w = __ldg(src + c);  // 8 bf16 = 4 pairs
-        const float4 cs0 = __ldg(tb + 2 * c), cs1 = __ldg(tb + 2 * c + 1);
+    for (int i = 0; i < PRO; ++i) {
+      const int k = i * kSoftmaxThreads + threadIdx.x;
+      const int rrow = k / CPR, chunk = k % CPR;
+      const int t = qt * kTile + rrow;
+      amax[i] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qv[i][e] = 0.f;
+      if (t < prm.n_q) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)t * H + h) * D) + chunk);
+        int p = prm.qpos ? __ldg(prm.qpos + t) : next_pos - prm.n_q + t;
+        if (p < 0 || p >= r.max_pos) {
+          atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+          p = 0;
+        }
+        const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D) + 2 * chunk;
+        const float4 cs0 = __ldg(tb), cs1 = __ldg(tb + 1);
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
         const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
         const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x0 = __uint_as_float(ww[i] << 16), x1 = __uint_as_float(ww[i] & 0xFFFF0000u);
-          const float y0 = x0 * cc[i] - x1 * ss[i];
-          const float y1 = x0 * ss[i] + x1 * cc[i];
-          q[8 * c + 2 * i] = y0;
-          q[8 * c + 2 * i + 1] = y1;
-          amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
+          const float y0 = x0 * cc[e] - x1 * ss[e];
+          const float y1 = x0 * ss[e] + x1 * cc[e];
+          qv[i][2 * e] = y0;
+          qv[i][2 * e + 1] = y1;
+          amax[i] = fmaxf(amax[i], fmaxf(fabsf(y0), fabsf(y1)));
         }
       }
-    } else {
+      // row maximum over the CPR consecutive lanes that hold the row
 #pragma unroll
-      for (int i = 0; i < HD; ++i) q[i] = 0.f;
+      for (int off = CPR / 2; off > 0; off >>= 1) amax[i] = fmaxf(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], off));
     }
-    // row amax over both halves, then the CTA-wide maximum for the level
-    xch[half * kTile + row] = amax;
-    float wm = amax;
+    float wm = 0.f;
+#pragma unroll
+    for (int i = 0; i < PRO; ++i) wm = fmaxf(wm, amax[i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
-    if (lane == 0) misc->warp_qmax[warp] = wm;
-    sync_softmax();
-    amax = fmaxf(amax, xch[(half ^ 1) * kTile + row]);
-    float sq = amax / 448.0f;
-    if (!(sq >= 0x1p-126f)) sq = 1.0f;
-    const float invq = 1.0f / sq;
+    if (lane == 0) warpmax[warp] = wm;
     const float scale_k = r.scales[h];
-    f_row = sq * scale_k * (1.4426950408889634f / sqrtf((float)D));
-    f_row = fmaxf(f_row, 1e-30f);  // stays positive, so masked -inf logits stay -inf
+    const float vmax = 448.0f * r.scales[H + h];
+    sync_softmax();
     int level = prm.forced_level;
     if (level == 0) {
       float qm = 0.f;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) qm = fmaxf(qm, misc->warp_qmax[w]);
+      for (int w = 0; w < 8; ++w) qm = fmaxf(qm, warpmax[w]);
       const float lg = qm * 448.0f * scale_k;
-      const float vmax = 448.0f * r.scales[H + h];
       level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
     }
     if (threadIdx.x == 0) {
       misc->level = level;
       if (split == 0) r.levels[qt * H + h] = level;
     }
-
-    // E4M3 terms of q * invq: residual splitting, written swizzled (K-major)
+    // E4M3 terms of q / sigma_q (sigma_q = amax/448), residual splitting;
+    // 8 bytes per chunk per term, at the chunk's swizzled place (K-major).
 #pragma unroll
-    for (int i = 0; i < HD; ++i) q[i] = q[i] * invq;
-    for (int term = 0; term < level; ++term) {
-      uint8_t* qtile = sm + L::kQ + term * L::kQTile;
+    for (int i = 0; i < PRO; ++i) {
+      const int k = i * kSoftmaxThreads + threadIdx.x;
+      const int rrow = k / CPR, chunk = k % CPR;
+      float sq = amax[i] / 448.0f;
+      if (!(sq >= 0x1p-126f)) sq = 1.0f;
+      const float invq = 1.0f / sq;
+      if (chunk == 0) rowf[rrow] = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
+      float u[8];
 #pragma unroll
-      for (int c = 0; c < HD / 16; ++c) {
-        uint32_t w[4];
+      for (int e = 0; e < 8; ++e) u[e] = qv[i][e] * invq;
+      const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
+      for (int term = 0; term < level; ++term) {
+        const uint2 w = make_uint2(pack4_e4m3(u[0], u[1], u[2], u[3]), pack4_e4m3(u[4], u[5], u[6], u[7]));
+        *reinterpret_cast<uint2*>(sm + L::kQ + term * L::kQTile + off) = w;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float a0 = q[16 * c + 4 * i], a1 = q[16 * c + 4 * i + 1];
-          const float a2 = q[16 * c + 4 * i + 2], a3 = q[16 * c + 4 * i + 3];
-          const uint16_t lo = f32x2_to_e4m3x2(a0, a1), hi = f32x2_to_e4m3x2(a2, a3);
-          w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-          if (term + 1 < level) {  // keep the residual for the next term
-            const float2 dl = e4m3x2_to_f32x2(lo), dh = e4m3x2_to_f32x2(hi);
-            q[16 * c + 4 * i] = a0 - dl.x;
-            q[16 * c + 4 * i + 1] = a1 - dl.y;
-            q[16 * c + 4 * i + 2] = a2 - dh.x;
-            q[16 * c + 4 * i + 3] = a3 - dh.y;
-          }
-        }
-        *reinterpret_cast<uint4*>(qtile + swz_offset(row, half * (HD / 16) + c, D)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 8; ++e) u[e] -= round_mant3(u[e]);  // residual for the next term
       }
     }
     fence_proxy_async_smem();
   }
-  fence_proxy_async_smem();  // the all-ones operand
+  fence_proxy_async_smem();  // the all-ones block
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -301,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
+      int issued = ntiles < kStages ? ntiles : kStages;
+      for (int j = issued; j < ntiles; ++j) {
         const int s = j % kStages;
         if (!mbar_wait_bounded(bar(L::kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, abort, kWaitLimitNs))
           break;
@@ -323,12 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
-      constexpr uint32_t idesc_pv = idesc_e4m3(128, D, true);
-      constexpr uint32_t idesc_l = idesc_e4m3(128, 16, false);
+      constexpr uint32_t idesc_pv = idesc_e4m3(128, D + 16, true);
+      // S(j) into TMEM buffer j&1.  Its previous user, P(j-2), was consumed
+      // by PV(j-2), issued earlier by this thread: in-order execution.
       auto issue_qk = [&](int j) -> bool {
         const int s = j % kStages, b = j & 1;
         if (!mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs)) return false;
-        if (!mbar_wait_bounded(bar(L::kBarSFree + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs)) return false;
         tc_fence_after();
         const uint32_t kaddr = sbase + L::kK + s * L::kKVTile;
         for (int t = 0; t < n_qterms; ++t) {
@@ -349,16 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
         tc_fence_after();
         const uint32_t vaddr = sbase + L::kV + s * L::kKVTile;
+        const uint32_t lbo = (uint32_t)(L::kOnes - (L::kV + s * L::kKVTile));  // V tile -> ones block
         for (int t = 0; t < n_pterms; ++t) {
-          const uint32_t paddr = sbase + L::kP + (b * 2 + t) * L::kPTile;
 #pragma unroll
           for (int kk = 0; kk < kTile / 32; ++kk) {
             const uint32_t acc = (j > 0 || t > 0 || kk > 0) ? 1u : 0u;
-            const uint64_t adesc = smem_desc(paddr + kk * 32, 16, 1024, 2);
-            mma_e4m3(tmem + L::kColO, adesc, smem_desc(vaddr + kk * 32 * D, 8192, 8 * D, L::kSwz),
-                     idesc_pv, acc);
-            mma_e4m3(tmem + L::kColL, adesc, smem_desc(sbase + L::kOnes + kk * 32, 16, 1024, 2),
-                     idesc_l, acc);
+            mma_e4m3_ts(tmem + L::kColO, tmem + L::kColS + b * 128 + t * 32 + kk * 8,
+                        smem_desc(vaddr + kk * 32 * D, lbo, 8 * D, L::kSwz), idesc_pv, acc);
           }
         }
         mma_commit(bar(L::kBarKvEmpty + s));
@@ -373,6 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ----------------------------------------------------------- softmax
+    const int row = threadIdx.x & (kTile - 1);
+    const int half = threadIdx.x >> 7;
+    const int quarter = warp & 3;
+    const int t_row = qt * kTile + row;
+    const float f_row = rowf[row];
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_run = -INFINITY;
     bool ok = true;
@@ -389,9 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(trow + L::kColS + b * 128 + half * 64 + 32, s1);
         tmem_wait_ld();
       }
-      tc_fence_before();
-      mbar_arrive(bar(L::kBarSFree + b));
-
       // mask slots past the fill level (only the ring's last tile)
       const int valid = nvalid - (tile0 + j) * kTile - half * 64;
       if (valid < 64) {
@@ -403,6 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 64; ++c) smax = fmaxf(smax, __uint_as_float(sr[c]));
       xch[((j & 1) * 2 + half) * kTile + row] = smax;
+      // after this barrier both threads of the row have read their S
+      // columns, so P may overwrite any of them
       sync_pair(quarter);
       smax = fmaxf(smax, xch[((j & 1) * 2 + (half ^ 1)) * kTile + row]);
       const float tmax = smax * f_row;          // f_row > 0
@@ -428,44 +437,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           tmem_st1(trow + L::kColL, __float_as_uint(__uint_as_float(lv) * alpha));
         }
-        tmem_wait_st();
       }
       m_run = m_new;
-      // P buffer b was last read by PV(j-2)
-      if (j >= 2) {
-        ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs);
-        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-      }
+      // probabilities 2^(x - m + 7) as 1-2 E4M3 terms, written over S(j):
+      // term t, slots [64*half, 64*half + 64) -> columns 32t + 16*half + [0, 16)
       const float moff = kPShift - m_run;
-      uint8_t* p0 = sm + L::kP + (b * 2 + 0) * L::kPTile;
-      uint8_t* p1 = sm + L::kP + (b * 2 + 1) * L::kPTile;
+      uint32_t w1[16], w2[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w0[4], w1[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int e = 16 * c + 4 * i;
-          const float e0 = ex2_approx(fmaf(__uint_as_float(sr[e]), f_row, moff));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), f_row, moff));
-          const float e2 = ex2_approx(fmaf(__uint_as_float(sr[e + 2]), f_row, moff));
-          const float e3 = ex2_approx(fmaf(__uint_as_float(sr[e + 3]), f_row, moff));
-          if (n_pterms > 1) {
-            // two terms: P1 from the f16 value, P2 from its f16 residual
-            const uint32_t h01 = f32x2_to_f16x2(e0, e1), h23 = f32x2_to_f16x2(e2, e3);
-            const uint16_t lo = f16x2_to_e4m3x2(h01), hi = f16x2_to_e4m3x2(h23);
-            w0[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-            const uint16_t lo2 = f16x2_to_e4m3x2(hsub2_u32(h01, e4m3x2_to_f16x2(lo)));
-            const uint16_t hi2 = f16x2_to_e4m3x2(hsub2_u32(h23, e4m3x2_to_f16x2(hi)));
-            w1[i] = (uint32_t)lo2 | ((uint32_t)hi2 << 16);
-          } else {
-            w0[i] = (uint32_t)f32x2_to_e4m3x2(e0, e1) | ((uint32_t)f32x2_to_e4m3x2(e2, e3) << 16);
-          }
-        }
-        const uint32_t off = swz_offset(row, half * 4 + c, 128);
-        *reinterpret_cast<uint4*>(p0 + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-        if (n_pterms > 1) *reinterpret_cast<uint4*>(p1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+      for (int c = 0; c < 16; ++c) {
+        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[4 * c]), f_row, moff));
+        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 1]), f_row, moff));
+        const float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 2]), f_row, moff));
+        const float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 3]), f_row, moff));
+        w1[c] = pack4_e4m3(e0, e1, e2, e3);
+        if (n_pterms > 1)
+          w2[c] = pack4_e4m3(e0 - round_mant3(e0), e1 - round_mant3(e1), e2 - round_mant3(e2),
+                             e3 - round_mant3(e3));
       }
-      fence_proxy_async_smem();
+      tmem_st16(trow + L::kColS + b * 128 + half * 16, w1);
+      if (n_pterms > 1) tmem_st16(trow + L::kColS + b * 128 + 32 + half * 16, w2);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + b));
     }
