@@ -10,18 +10,18 @@
 //
 // CTA = one 128-query tile x one head x one range of key/value tiles
 // (split-KV).  Ten warps:
-//   warps 0-7  Prologue (all 256 threads, coalesced): RoPE each query chunk
-//              in fp32, scale each row by 448/amax(row), split into 1-3 E4M3
-//              terms in shared memory.  Softmax: query row r = TMEM lane r
-//              is shared by two threads (warps 0-3 own S columns [0, 64) and
-//              O columns [0, d/2); warps 4-7 the other halves), which
-//              exchange row maxima through shared memory.  Online softmax in
-//              log2 units with a lazily raised running maximum; probabilities
-//              carry 2^7 and are split into 1-2 E4M3 terms that are written
-//              back into TMEM over the S columns just read; O is rescaled in
-//              TMEM when the maximum rises by more than 1.5 (log2 units).
-//              Epilogue: O / l, split partials and their merge.
-//   warp 8     TMA producer: K and V tiles [128 slots][d] into a 3-stage ring.
+//   warps 0-7  Softmax: query row r = TMEM lane r is shared by two threads
+//              (warps 0-3 own S columns [0, 64) and O columns [0, d/2);
+//              warps 4-7 the other halves), which exchange row maxima
+//              through shared memory.  Online softmax in log2 units with a
+//              lazily raised running maximum; probabilities carry 2^7 and
+//              are split into 1-2 E4M3 terms (the residual in f16x2) that are
+//              written back into TMEM over the S columns just read; O is
+//              rescaled in TMEM when the maximum rises by more than 1.5 (log2
+//              units).  Epilogue: O / l, split partials and their merge.
+//   warp 8     Copy producer: the query tile's FP8 terms (one bulk copy of
+//              the images k_attn_prep wrote), then K and V tiles [128 slots][d]
+//              by TMA into a 3-stage ring.
 //   warp 9     TMEM allocation and the single MMA-issuing thread:
 //              S = sum_t Q_t K^T (A and B from shared memory, K-major), then
 //              [O | l] += sum_t P_t [V | 1] with P read from TMEM and B =
@@ -33,7 +33,12 @@
 // on S(j).  P(j) overwrites S(j)'s columns; the MMAs of one CTA run in issue
 // order, so QK(j+2) (into the same columns) always follows PV(j).
 //
-// Precision level per CTA (uniform, from the query tile's amax, the head's
+// k_attn_prep runs first, once per (query tile, head): RoPE of the queries in
+// fp32, a per-row scale 448/amax(row), the split into 1-3 E4M3 terms written
+// as ready-to-copy swizzled shared-memory images, the per-row logit factor,
+// and the tile's precision level.  Split CTAs of the same tile share them.
+//
+// Precision level per query tile (from the tile's amax, the head's
 // key range 448*scale_k and value range 448*scale_v): level 1 = 1 Q term +
 // 1 P term, level 2 = 2 + 2, level 3 = 3 + 2.  Extra terms are residuals at
 // the same scale, accumulated into the same TMEM accumulator.
@@ -76,9 +81,7 @@ struct Layout {
   static constexpr int kV = kK + kStages * kKVTile;
   static constexpr int kOnes = kV + kStages * kKVTile;  // 128 x 128 bytes of E4M3 1.0
   static constexpr int kXch = kOnes + kTile * kTile;    // float [2 parity][2 half][128 rows]
-  static constexpr int kRowF = kXch + 2 * 2 * kTile * 4;  // float [128] logit factor per row
-  static constexpr int kWarpMax = kRowF + kTile * 4;      // float [8]
-  static constexpr int kBars = kWarpMax + 64;
+  static constexpr int kBars = kXch + 2 * 2 * kTile * 4;
   // barrier slots (8 bytes each)
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kStages;
@@ -86,7 +89,8 @@ struct Layout {
   static constexpr int kBarPFull = 2 * kStages + 2;
   static constexpr int kBarPvDone = 2 * kStages + 4;
   static constexpr int kBarMmaDone = 2 * kStages + 6;
-  static constexpr int kNumBars = 2 * kStages + 7;
+  static constexpr int kBarQFull = 2 * kStages + 7;
+  static constexpr int kNumBars = 2 * kStages + 8;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 64;
   static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code
@@ -149,21 +153,112 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
   return (uint32_t)f32x2_to_e4m3x2(a, b) | ((uint32_t)f32x2_to_e4m3x2(c, d) << 16);
 }
 
+// Query preparation, one CTA per (query tile, head), 256 threads.  Chunk
+// task k = i * 256 + tid: row k / CPR, chunk k % CPR (8 elements = 4 RoPE
+// pairs); a warp reads 32 consecutive 16-byte chunks.
+template <int D>
+__global__ void __launch_bounds__(kSoftmaxThreads) k_attn_prep(const AttnParams prm) {
+  constexpr int CPR = D / 8;
+  constexpr int PRO = kTile * CPR / kSoftmaxThreads;
+  __shared__ float warpmax[8];
+  const RingDev& r = prm.r;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, H = r.H;
+  const size_t unit = (size_t)qt * H + h;
+  float qv[PRO][8];
+  float amax[PRO];
+  const int next_pos = __ldcg(r.state + ST_NEXT_POS);
+#pragma unroll
+  for (int i = 0; i < PRO; ++i) {
+    const int k = i * kSoftmaxThreads + threadIdx.x;
+    const int rrow = k / CPR, chunk = k % CPR;
+    const int t = qt * kTile + rrow;
+    amax[i] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qv[i][e] = 0.f;
+    if (t < prm.n_q) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)t * H + h) * D) + chunk);
+      int p = prm.qpos ? __ldg(prm.qpos + t) : next_pos - prm.n_q + t;
+      if (p < 0 || p >= r.max_pos) {
+        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+        p = 0;
+      }
+      const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D) + 2 * chunk;
+      const float4 cs0 = __ldg(tb), cs1 = __ldg(tb + 1);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
+      const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
+        const float y0 = x0 * cc[e] - x1 * ss[e];
+        const float y1 = x0 * ss[e] + x1 * cc[e];
+        qv[i][2 * e] = y0;
+        qv[i][2 * e + 1] = y1;
+        amax[i] = fmaxf(amax[i], fmaxf(fabsf(y0), fabsf(y1)));
+      }
+    }
+    // row maximum over the CPR consecutive lanes that hold the row
+#pragma unroll
+    for (int off = CPR / 2; off > 0; off >>= 1) amax[i] = fmaxf(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], off));
+  }
+  float wm = 0.f;
+#pragma unroll
+  for (int i = 0; i < PRO; ++i) wm = fmaxf(wm, amax[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+  if (lane == 0) warpmax[warp] = wm;
+  const float scale_k = r.scales[h];
+  const float vmax = 448.0f * r.scales[H + h];
+  __syncthreads();
+  int level = prm.forced_level;
+  if (level == 0) {
+    float qm = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) qm = fmaxf(qm, warpmax[w]);
+    const float lg = qm * 448.0f * scale_k;
+    level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
+  }
+  if (threadIdx.x == 0) r.levels[unit] = level;
+  // E4M3 terms of q / sigma_q (sigma_q = amax/448), residual splitting in
+  // f16x2; 8 bytes per chunk per term at the chunk's swizzled place.
+  uint8_t* img = r.qprep + unit * 3 * (kTile * D);
+#pragma unroll
+  for (int i = 0; i < PRO; ++i) {
+    const int k = i * kSoftmaxThreads + threadIdx.x;
+    const int rrow = k / CPR, chunk = k % CPR;
+    float sq = amax[i] / 448.0f;
+    if (!(sq >= 0x1p-126f)) sq = 1.0f;
+    const float invq = 1.0f / sq;
+    if (chunk == 0)
+      r.qrowf[unit * kTile + rrow] = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
+    uint32_t hh[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) hh[e] = f32x2_to_f16x2(qv[i][2 * e] * invq, qv[i][2 * e + 1] * invq);
+    const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
+    for (int term = 0; term < level; ++term) {
+      uint16_t c4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c4[e] = f16x2_to_e4m3x2(hh[e]);
+      *reinterpret_cast<uint2*>(img + term * (kTile * D) + off) =
+          make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hh[e] = hsub2_u32(hh[e], e4m3x2_to_f16x2(c4[e]));  // residual
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnParams prm) {
   using L = Layout<D>;
   constexpr int HD = D / 2;             // O columns per softmax thread
-  constexpr int CPR = D / 8;            // 8-element query chunks per row
-  constexpr int PRO = kTile * CPR / kSoftmaxThreads;  // prologue chunks per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   Misc* misc = reinterpret_cast<Misc*>(sm + L::kMisc);
   float* xch = reinterpret_cast<float*>(sm + L::kXch);
-  float* rowf = reinterpret_cast<float*>(sm + L::kRowF);
-  float* warpmax = reinterpret_cast<float*>(sm + L::kWarpMax);
   volatile int* abort = &misc->abort;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBars + 8u * (uint32_t)i; };
 
@@ -178,9 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
 
   // ---------------------------------------------------------------- setup
+  const size_t unit = (size_t)qt * H + h;
   if (threadIdx.x == kWarpTma * 32) {
-    // The producer initialises the barriers, so it can start the first
-    // copies before the query prologue finishes.
+    // The producer initialises the barriers and starts the query and the
+    // first key/value copies at once.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKvFull + s), 1);
       mbar_init(bar(L::kBarKvEmpty + s), 1);
@@ -191,9 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarPvDone + b), 1);
     }
     mbar_init(bar(L::kBarMmaDone), 1);
+    mbar_init(bar(L::kBarQFull), 1);
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
+    int level = __ldcg(r.levels + unit);
+    level = level < 1 ? 1 : (level > 3 ? 3 : level);
+    misc->level = level;
+    mbar_arrive_expect_tx(bar(L::kBarQFull), (uint32_t)(level * L::kQTile));
+    for (int t = 0; t < level; ++t)
+      bulk_load(sbase + L::kQ + t * L::kQTile, r.qprep + (unit * 3 + t) * L::kQTile, L::kQTile, bar(L::kBarQFull));
     const int first = ntiles < kStages ? ntiles : kStages;
     for (int j = 0; j < first; ++j) {
       mbar_arrive_expect_tx(bar(L::kBarKvFull + j), 2u * kTile * D);
@@ -210,92 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4* ones = reinterpret_cast<uint4*>(sm + L::kOnes);
     for (int i = threadIdx.x; i < kTile * kTile / 16; i += kThreads)
       ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
-  }
-
-  // --------------------------------------------- query prologue (warps 0-7)
-  // Chunk task k = i * 256 + tid: row k / CPR, chunk k % CPR (8 elements,
-  // 4 RoPE pairs); a warp reads 32 consecutive 16-byte chunks.
-  if (warp < 8) {
-    float qv[PRO][8];
-    float amax[PRO];
-    const int next_pos = __ldcg(r.state + ST_NEXT_POS);
-#pragma unroll
-    for (int i = 0; i < PRO; ++i) {
-      const int k = i * kSoftmaxThreads + threadIdx.x;
-      const int rrow = k / CPR, chunk = k % CPR;
-      const int t = qt * kTile + rrow;
-      amax[i] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qv[i][e] = 0.f;
-      if (t < prm.n_q) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)t * H + h) * D) + chunk);
-        int p = prm.qpos ? __ldg(prm.qpos + t) : next_pos - prm.n_q + t;
-        if (p < 0 || p >= r.max_pos) {
-          atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
-          p = 0;
-        }
-        const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D) + 2 * chunk;
-        const float4 cs0 = __ldg(tb), cs1 = __ldg(tb + 1);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-        const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
-        const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
-          const float y0 = x0 * cc[e] - x1 * ss[e];
-          const float y1 = x0 * ss[e] + x1 * cc[e];
-          qv[i][2 * e] = y0;
-          qv[i][2 * e + 1] = y1;
-          amax[i] = fmaxf(amax[i], fmaxf(fabsf(y0), fabsf(y1)));
-        }
-      }
-      // row maximum over the CPR consecutive lanes that hold the row
-#pragma unroll
-      for (int off = CPR / 2; off > 0; off >>= 1) amax[i] = fmaxf(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], off));
-    }
-    float wm = 0.f;
-#pragma unroll
-    for (int i = 0; i < PRO; ++i) wm = fmaxf(wm, amax[i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
-    if (lane == 0) warpmax[warp] = wm;
-    const float scale_k = r.scales[h];
-    const float vmax = 448.0f * r.scales[H + h];
-    sync_softmax();
-    int level = prm.forced_level;
-    if (level == 0) {
-      float qm = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) qm = fmaxf(qm, warpmax[w]);
-      const float lg = qm * 448.0f * scale_k;
-      level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
-    }
-    if (threadIdx.x == 0) {
-      misc->level = level;
-      if (split == 0) r.levels[qt * H + h] = level;
-    }
-    // E4M3 terms of q / sigma_q (sigma_q = amax/448), residual splitting;
-    // 8 bytes per chunk per term, at the chunk's swizzled place (K-major).
-#pragma unroll
-    for (int i = 0; i < PRO; ++i) {
-      const int k = i * kSoftmaxThreads + threadIdx.x;
-      const int rrow = k / CPR, chunk = k % CPR;
-      float sq = amax[i] / 448.0f;
-      if (!(sq >= 0x1p-126f)) sq = 1.0f;
-      const float invq = 1.0f / sq;
-      if (chunk == 0) rowf[rrow] = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
-      float u[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) u[e] = qv[i][e] * invq;
-      const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
-      for (int term = 0; term < level; ++term) {
-        const uint2 w = make_uint2(pack4_e4m3(u[0], u[1], u[2], u[3]), pack4_e4m3(u[4], u[5], u[6], u[7]));
-        *reinterpret_cast<uint2*>(sm + L::kQ + term * L::kQTile + off) = w;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] -= round_mant3(u[e]);  // residual for the next term
-      }
-    }
-    fence_proxy_async_smem();
   }
   fence_proxy_async_smem();  // the all-ones block
   tc_fence_before();
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(L::kBarSFull + b));
         return true;
       };
-      bool ok = issue_qk(0);
+      bool ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs) && issue_qk(0);
       for (int j = 0; ok && j < ntiles; ++j) {
         if (j + 1 < ntiles && !issue_qk(j + 1)) break;
         const int s = j % kStages, b = j & 1;
@@ -382,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = threadIdx.x >> 7;
     const int quarter = warp & 3;
     const int t_row = qt * kTile + row;
-    const float f_row = rowf[row];
+    const float f_row = __ldcg(r.qrowf + unit * kTile + row);
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_run = -INFINITY;
     bool ok = true;
@@ -449,10 +466,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 1]), f_row, moff));
         const float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 2]), f_row, moff));
         const float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 3]), f_row, moff));
-        w1[c] = pack4_e4m3(e0, e1, e2, e3);
-        if (n_pterms > 1)
-          w2[c] = pack4_e4m3(e0 - round_mant3(e0), e1 - round_mant3(e1), e2 - round_mant3(e2),
-                             e3 - round_mant3(e3));
+        if (n_pterms > 1) {
+          // two terms: P1 from the f16 value, P2 from its exact f16 residual
+          const uint32_t h01 = f32x2_to_f16x2(e0, e1), h23 = f32x2_to_f16x2(e2, e3);
+          const uint16_t lo = f16x2_to_e4m3x2(h01), hi = f16x2_to_e4m3x2(h23);
+          w1[c] = (uint32_t)lo | ((uint32_t)hi << 16);
+          const uint16_t lo2 = f16x2_to_e4m3x2(hsub2_u32(h01, e4m3x2_to_f16x2(lo)));
+          const uint16_t hi2 = f16x2_to_e4m3x2(hsub2_u32(h23, e4m3x2_to_f16x2(hi)));
+          w2[c] = (uint32_t)lo2 | ((uint32_t)hi2 << 16);
+        } else {
+          w1[c] = pack4_e4m3(e0, e1, e2, e3);
+        }
       }
       tmem_st16(trow + L::kColS + b * 128 + half * 16, w1);
       if (n_pterms > 1) tmem_st16(trow + L::kColS + b * 128 + 32 + half * 16, w2);
@@ -575,12 +599,17 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   p.nsplit = a.nsplit;
   p.tiles_per_split = a.tiles_per_split;
   p.forced_level = a.forced_level;
-  const dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), (unsigned)r.H, (unsigned)a.nsplit);
+  const unsigned qtiles = (unsigned)((a.n_q + kTile - 1) / kTile);
+  const dim3 pgrid(qtiles, (unsigned)r.H);
+  const dim3 grid(qtiles, (unsigned)r.H, (unsigned)a.nsplit);
   const size_t smem = attention_smem_bytes(r.D);
-  if (r.D == 128)
+  if (r.D == 128) {
+    k_attn_prep<128><<<pgrid, kSoftmaxThreads, 0, s>>>(p);
     k_attention<128><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
-  else
+  } else {
+    k_attn_prep<64><<<pgrid, kSoftmaxThreads, 0, s>>>(p);
     k_attention<64><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
+  }
   return cudaGetLastError();
 }
 

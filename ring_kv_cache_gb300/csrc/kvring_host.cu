@@ -44,7 +44,7 @@ bool config_ok(const kvring_config* c) {
 }
 
 struct Plan {
-  size_t k, v, slot_pos, scales, state, amax, table, part_o, part_lse, tickets, levels, total;
+  size_t k, v, slot_pos, scales, state, amax, table, part_o, part_lse, tickets, levels, qprep, qrowf, total;
   int qtiles;
 };
 
@@ -70,6 +70,8 @@ Plan plan_for(const kvring_config* c) {
   p.part_lse = take(S * Q * H * kvr::kTile * 4);
   p.tickets = take(Q * H * 4);
   p.levels = take(Q * H * 4);
+  p.qprep = take(Q * H * 3 * kvr::kTile * D);
+  p.qrowf = take(Q * H * kvr::kTile * 4);
   p.total = off;
   return p;
 }
@@ -184,6 +186,8 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   d.part_lse = reinterpret_cast<float*>(b + p.part_lse);
   d.tickets = reinterpret_cast<int32_t*>(b + p.tickets);
   d.levels = reinterpret_cast<int32_t*>(b + p.levels);
+  d.qprep = b + p.qprep;
+  d.qrowf = reinterpret_cast<float*>(b + p.qrowf);
   d.H = cfg->num_heads;
   d.D = cfg->head_dim;
   d.C = cfg->capacity;

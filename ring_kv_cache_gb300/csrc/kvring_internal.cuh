@@ -44,7 +44,9 @@ struct RingDev {
   float* part_o;       // [max_splits][qtiles][H][128][D] attention partials
   float* part_lse;     // [max_splits][qtiles][H][128]
   int32_t* tickets;    // [qtiles][H] split completion counters (0 between calls)
-  int32_t* levels;     // [qtiles][H] precision level used per tile (debug)
+  int32_t* levels;     // [qtiles][H] precision level of each query tile
+  uint8_t* qprep;      // [qtiles][H][3][128 * D] query E4M3 terms, swizzled tile images
+  float* qrowf;        // [qtiles][H][128] logit factor per query row
   int H, D, C, max_pos, max_tokens, max_splits, qtiles_max;
 };
 
@@ -157,6 +159,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+      : "memory");
+}
+
+// Contiguous global -> shared copy on the async proxy (16-byte aligned,
+// size a multiple of 16), completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar)
       : "memory");
 }
 
