@@ -69,7 +69,7 @@ typedef struct {
   int32_t capacity;       /* C ring slots, 1 .. 2^24 */
   int32_t max_tokens;     /* most tokens per write / calibration / attention call */
   int32_t max_position;   /* RoPE table rows: positions lie in [0, max_position) */
-  int32_t max_kv_splits;  /* most key/value partitions one attention call may use (>= 1) */
+  int32_t max_kv_splits;  /* most key/value partitions one attention call may use (1..32) */
   int32_t attn_precision; /* 0 = automatic per tile; 1..3 = fixed FP8 term level */
   int32_t reserved;       /* must be 0 */
   double rope_base;       /* RoPE base, e.g. 10000 */

@@ -126,28 +126,6 @@ __device__ __forceinline__ void sync_pair(int quarter) {
   asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
 }
 
-template <int N>
-__device__ __forceinline__ void store_row(void* out, bool bf16, size_t elem_off, const float* o, float f) {
-  if (bf16) {
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + elem_off);
-#pragma unroll
-    for (int c = 0; c < N / 8; ++c) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 bb = __floats2bfloat162_rn(o[8 * c + 2 * i] * f, o[8 * c + 2 * i + 1] * f);
-        w[i] = *reinterpret_cast<const uint32_t*>(&bb);
-      }
-      dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  } else {
-    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + elem_off);
-#pragma unroll
-    for (int c = 0; c < N / 4; ++c)
-      dst[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
-  }
-}
-
 // Four fp32 values to four E4M3 codes (first value in the low byte).
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   return (uint32_t)f32x2_to_e4m3x2(a, b) | ((uint32_t)f32x2_to_e4m3x2(c, d) << 16);
@@ -221,7 +199,7 @@ __global__ void __launch_bounds__(kSoftmaxThreads) k_attn_prep(const AttnParams 
   }
   if (threadIdx.x == 0) r.levels[unit] = level;
   // E4M3 terms of q / sigma_q (sigma_q = amax/448), residual splitting in
-  // f16x2; 8 bytes per chunk per term at the chunk's swizzled place.
+  // fp32; 8 bytes per chunk per term at the chunk's swizzled place.
   uint8_t* img = r.qprep + unit * 3 * (kTile * D);
 #pragma unroll
   for (int i = 0; i < PRO; ++i) {
@@ -232,18 +210,22 @@ __global__ void __launch_bounds__(kSoftmaxThreads) k_attn_prep(const AttnParams 
     const float invq = 1.0f / sq;
     if (chunk == 0)
       r.qrowf[unit * kTile + rrow] = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
-    uint32_t hh[4];
+    float u[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) hh[e] = f32x2_to_f16x2(qv[i][2 * e] * invq, qv[i][2 * e + 1] * invq);
+    for (int e = 0; e < 8; ++e) u[e] = qv[i][e] * invq;
     const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
     for (int term = 0; term < level; ++term) {
       uint16_t c4[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) c4[e] = f16x2_to_e4m3x2(hh[e]);
+      for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(u[2 * e], u[2 * e + 1]);
       *reinterpret_cast<uint2*>(img + term * (kTile * D) + off) =
           make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
 #pragma unroll
-      for (int e = 0; e < 4; ++e) hh[e] = hsub2_u32(hh[e], e4m3x2_to_f16x2(c4[e]));  // residual
+      for (int e = 0; e < 4; ++e) {  // exact fp32 residual for the next term
+        const float2 dq = e4m3x2_to_f32x2(c4[e]);
+        u[2 * e] -= dq.x;
+        u[2 * e + 1] -= dq.y;
+      }
     }
   }
 }
@@ -509,20 +491,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < HD; ++i) o[i] = 0.f;
     }
+    // Normalised rows go to shared memory (the key/value stages are free:
+    // every copy landed and every MMA finished), fp32 [128][d + 4], then the
+    // whole tile is stored, or merged across splits, with coalesced 16-byte
+    // accesses.
     const float inv_l = l > 0.f ? 1.0f / l : 0.f;
     const float scale_v = r.scales[H + h];
-    const bool live = t_row < prm.n_q;
-    const size_t out_off = ((size_t)t_row * H + h) * D + half * HD;
-    if (prm.nsplit == 1) {
-      if (live) store_row<HD>(prm.out, prm.out_bf16 != 0, out_off, o, inv_l * scale_v);
-    } else {
-      // partial (normalised) output and its log2-sum-exp for this split
-      const size_t prow = (((size_t)split * r.qtiles_max + qt) * H + h) * kTile + row;
-      float4* po = reinterpret_cast<float4*>(r.part_o + prow * D + half * HD);
+    const bool single = prm.nsplit == 1;
+    constexpr int SP = D + 4;                 // padded row stride (floats)
+    constexpr int F4 = kTile * D / 4;         // float4 per tile
+    float* stage = reinterpret_cast<float*>(sm + L::kK);
+    {
+      const float f = single ? inv_l * scale_v : inv_l;
+      float4* srow = reinterpret_cast<float4*>(stage + row * SP + half * HD);
 #pragma unroll
-      for (int c = 0; c < HD / 4; ++c)
-        __stcg(po + c, make_float4(o[4 * c] * inv_l, o[4 * c + 1] * inv_l, o[4 * c + 2] * inv_l, o[4 * c + 3] * inv_l));
-      if (half == 0) __stcg(r.part_lse + prow, l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY);
+      for (int c = 0; c < HD / 4; ++c) srow[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
+      if (half == 0) xch[row] = l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY;
+    }
+    sync_softmax();
+    const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
+    auto store_out = [&](int f4, float4 v) {
+      const int rrow = f4 / (D / 4), c4 = f4 % (D / 4);
+      if (rrow >= rows_live) return;
+      const size_t e = ((size_t)(qt * kTile + rrow) * H + h) * D + 4 * c4;
+      if (prm.out_bf16) {
+        const __nv_bfloat162 a0 = __floats2bfloat162_rn(v.x, v.y), a1 = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(prm.out) + e) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1));
+      } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + e) = v;
+      }
+    };
+    if (single) {
+      for (int f4 = threadIdx.x; f4 < F4; f4 += kSoftmaxThreads) {
+        const int rrow = f4 / (D / 4), c4 = f4 % (D / 4);
+        store_out(f4, *reinterpret_cast<const float4*>(stage + rrow * SP + 4 * c4));
+      }
+    } else {
+      // partial (normalised) tile and its per-row log2-sum-exp
+      const size_t pbase = ((size_t)split * r.qtiles_max + qt) * H + h;
+      float4* dst = reinterpret_cast<float4*>(r.part_o + pbase * kTile * D);
+      for (int f4 = threadIdx.x; f4 < F4; f4 += kSoftmaxThreads) {
+        const int rrow = f4 / (D / 4), c4 = f4 % (D / 4);
+        __stcg(dst + f4, *reinterpret_cast<const float4*>(stage + rrow * SP + 4 * c4));
+      }
+      if (threadIdx.x < kTile) __stcg(r.part_lse + pbase * kTile + threadIdx.x, xch[threadIdx.x]);
       __threadfence();
       sync_softmax();
       if (threadIdx.x == 0) {
@@ -531,34 +544,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       sync_softmax();
       if (misc->last) {
+        // last split of this tile: merge all splits
         __threadfence();
-        float mx = -INFINITY;
-        for (int s = 0; s < prm.nsplit; ++s) {
-          const size_t pr = (((size_t)s * r.qtiles_max + qt) * H + h) * kTile + row;
-          mx = fmaxf(mx, __ldcg(r.part_lse + pr));
-        }
-#pragma unroll
-        for (int i = 0; i < HD; ++i) o[i] = 0.f;
-        float wsum = 0.f;
-        if (mx > -INFINITY) {
-          for (int s = 0; s < prm.nsplit; ++s) {
-            const size_t pr = (((size_t)s * r.qtiles_max + qt) * H + h) * kTile + row;
-            const float lse = __ldcg(r.part_lse + pr);
-            if (!(lse > -INFINITY)) continue;
-            const float w = ex2_approx(lse - mx);
-            wsum += w;
-            const float4* src = reinterpret_cast<const float4*>(r.part_o + pr * D + half * HD);
-#pragma unroll
-            for (int c = 0; c < HD / 4; ++c) {
-              const float4 vv = __ldcg(src + c);
-              o[4 * c] = fmaf(w, vv.x, o[4 * c]);
-              o[4 * c + 1] = fmaf(w, vv.y, o[4 * c + 1]);
-              o[4 * c + 2] = fmaf(w, vv.z, o[4 * c + 2]);
-              o[4 * c + 3] = fmaf(w, vv.w, o[4 * c + 3]);
-            }
+        float* wts = reinterpret_cast<float*>(sm + L::kQ);   // [nsplit][128]
+        if (threadIdx.x < kTile) {
+          const int rr = threadIdx.x;
+          float mx = -INFINITY;
+          for (int s2 = 0; s2 < prm.nsplit; ++s2)
+            mx = fmaxf(mx, __ldcg(r.part_lse + (((size_t)s2 * r.qtiles_max + qt) * H + h) * kTile + rr));
+          float sum = 0.f;
+          for (int s2 = 0; s2 < prm.nsplit; ++s2) {
+            const float lse = __ldcg(r.part_lse + (((size_t)s2 * r.qtiles_max + qt) * H + h) * kTile + rr);
+            const float w = (mx > -INFINITY && lse > -INFINITY) ? ex2_approx(lse - mx) : 0.f;
+            wts[s2 * kTile + rr] = w;
+            sum += w;
           }
+          const float g = sum > 0.f ? scale_v / sum : 0.f;
+          for (int s2 = 0; s2 < prm.nsplit; ++s2) wts[s2 * kTile + rr] *= g;
         }
-        if (live) store_row<HD>(prm.out, prm.out_bf16 != 0, out_off, o, wsum > 0.f ? scale_v / wsum : 0.f);
+        sync_softmax();
+        for (int f4 = threadIdx.x; f4 < F4; f4 += kSoftmaxThreads) {
+          const int rrow = f4 / (D / 4);
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s2 = 0; s2 < prm.nsplit; ++s2) {
+            const float w = wts[s2 * kTile + rrow];
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                r.part_o + ((((size_t)s2 * r.qtiles_max + qt) * H + h) * kTile) * D) + f4);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+          }
+          store_out(f4, acc);
+        }
         if (threadIdx.x == 0) r.tickets[qt * H + h] = 0;
       }
     }

@@ -36,7 +36,7 @@ bool config_ok(const kvring_config* c) {
   if (c->capacity < 1 || c->capacity > (1 << 24)) return false;
   if (c->max_tokens < 1 || c->max_tokens > (1 << 24)) return false;
   if (c->max_position < 1 || c->max_position > (1 << 24)) return false;
-  if (c->max_kv_splits < 1 || c->max_kv_splits > 64) return false;
+  if (c->max_kv_splits < 1 || c->max_kv_splits > 32) return false;
   if (c->attn_precision < 0 || c->attn_precision > 3) return false;
   if (c->reserved != 0) return false;
   if (!(c->rope_base > 0.0) || !std::isfinite(c->rope_base)) return false;
