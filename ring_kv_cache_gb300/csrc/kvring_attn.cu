@@ -52,10 +52,11 @@ namespace kvr {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kPrepThreads = 256;
+constexpr int kSoftmaxThreads = 512;    // 16 warps: four threads per query row
 constexpr int kThreads = kSoftmaxThreads + 64;
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpTma = 16;
+constexpr int kWarpMma = 17;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 // Probabilities carry a factor 2^kPShift relative to the running maximum,
@@ -80,8 +81,8 @@ struct Layout {
   static constexpr int kK = kQ + 3 * kQTile;
   static constexpr int kV = kK + kStages * kKVTile;
   static constexpr int kOnes = kV + kStages * kKVTile;  // 128 x 128 bytes of E4M3 1.0
-  static constexpr int kXch = kOnes + kTile * kTile;    // float [2 parity][2 half][128 rows]
-  static constexpr int kBars = kXch + 2 * 2 * kTile * 4;
+  static constexpr int kXch = kOnes + kTile * kTile;    // float [2 parity][4 column quarters][128 rows]
+  static constexpr int kBars = kXch + 2 * 4 * kTile * 4;
   // barrier slots (8 bytes each)
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kStages;
@@ -119,11 +120,11 @@ struct AttnParams {
   int forced_level;
 };
 
-// Named barriers: 0 = __syncthreads, 1 = the 256 softmax threads,
-// 2..5 = the two warps that share a group of 32 query rows.
-__device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ void sync_pair(int quarter) {
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
+// Named barriers: 0 = __syncthreads, 1 = the 512 softmax threads,
+// 2..5 = the four warps that share a group of 32 query rows.
+__device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+__device__ __forceinline__ void sync_rowgroup(int quarter) {
+  asm volatile("bar.sync %0, 128;" ::"r"(2 + quarter) : "memory");
 }
 
 // Four fp32 values to four E4M3 codes (first value in the low byte).
@@ -135,9 +136,9 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 // task k = i * 256 + tid: row k / CPR, chunk k % CPR (8 elements = 4 RoPE
 // pairs); a warp reads 32 consecutive 16-byte chunks.
 template <int D>
-__global__ void __launch_bounds__(kSoftmaxThreads) k_attn_prep(const AttnParams prm) {
+__global__ void __launch_bounds__(kPrepThreads) k_attn_prep(const AttnParams prm) {
   constexpr int CPR = D / 8;
-  constexpr int PRO = kTile * CPR / kSoftmaxThreads;
+  constexpr int PRO = kTile * CPR / kPrepThreads;
   __shared__ float warpmax[8];
   const RingDev& r = prm.r;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(kSoftmaxThreads) k_attn_prep(const AttnParams 
   const int next_pos = __ldcg(r.state + ST_NEXT_POS);
 #pragma unroll
   for (int i = 0; i < PRO; ++i) {
-    const int k = i * kSoftmaxThreads + threadIdx.x;
+    const int k = i * kPrepThreads + threadIdx.x;
     const int rrow = k / CPR, chunk = k % CPR;
     const int t = qt * kTile + rrow;
     amax[i] = 0.f;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kSoftmaxThreads) k_attn_prep(const AttnParams 
   uint8_t* img = r.qprep + unit * 3 * (kTile * D);
 #pragma unroll
   for (int i = 0; i < PRO; ++i) {
-    const int k = i * kSoftmaxThreads + threadIdx.x;
+    const int k = i * kPrepThreads + threadIdx.x;
     const int rrow = k / CPR, chunk = k % CPR;
     float sq = amax[i] / 448.0f;
     if (!(sq >= 0x1p-126f)) sq = 1.0f;
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnParams prm) {
   using L = Layout<D>;
-  constexpr int HD = D / 2;             // O columns per softmax thread
+  constexpr int QD = D / 4;             // O columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
@@ -377,10 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ----------------------------------------------------------- softmax
+    // thread = (row, column quarter cq): S columns [32 cq, 32 cq + 32),
+    // O columns [QD cq, QD cq + QD), P bytes of its 32 slots.
     const int row = threadIdx.x & (kTile - 1);
-    const int half = threadIdx.x >> 7;
+    const int cq = threadIdx.x >> 7;
     const int quarter = warp & 3;
-    const int t_row = qt * kTile + row;
     const float f_row = __ldcg(r.qrowf + unit * kTile + row);
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_run = -INFINITY;
@@ -390,48 +392,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_bounded(bar(L::kBarSFull + b), (j >> 1) & 1, abort, kWaitLimitNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[64];
-      {
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32]);
-        tmem_ld32(trow + L::kColS + b * 128 + half * 64, s0);
-        tmem_ld32(trow + L::kColS + b * 128 + half * 64 + 32, s1);
-        tmem_wait_ld();
-      }
+      uint32_t sr[32];
+      tmem_ld32(trow + L::kColS + b * 128 + cq * 32, sr);
+      tmem_wait_ld();
       // mask slots past the fill level (only the ring's last tile)
-      const int valid = nvalid - (tile0 + j) * kTile - half * 64;
-      if (valid < 64) {
+      const int valid = nvalid - (tile0 + j) * kTile - cq * 32;
+      if (valid < 32) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < 32; ++c)
           if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
       }
       float smax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) smax = fmaxf(smax, __uint_as_float(sr[c]));
-      xch[((j & 1) * 2 + half) * kTile + row] = smax;
-      // after this barrier both threads of the row have read their S
+      for (int c = 0; c < 32; ++c) smax = fmaxf(smax, __uint_as_float(sr[c]));
+      float* xj = xch + (j & 1) * 4 * kTile;
+      xj[cq * kTile + row] = smax;
+      // after this barrier all four threads of the row have read their S
       // columns, so P may overwrite any of them
-      sync_pair(quarter);
-      smax = fmaxf(smax, xch[((j & 1) * 2 + (half ^ 1)) * kTile + row]);
+      sync_rowgroup(quarter);
+      smax = fmaxf(fmaxf(xj[row], xj[kTile + row]), fmaxf(xj[2 * kTile + row], xj[3 * kTile + row]));
       const float tmax = smax * f_row;          // f_row > 0
       const bool need = tmax > m_run + kTau;
       const float m_new = need ? tmax : m_run;
       if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
-        // O and l hold tiles < j: wait for PV(j-1), then rescale this half
+        // O and l hold tiles < j: wait for PV(j-1), then rescale this quarter
         ok = mbar_wait_bounded(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, kWaitLimitNs);
         if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
         tc_fence_after();
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-        uint32_t rr[32];
+        uint32_t rr[QD];
+        tmem_ld_n<QD>(trow + L::kColO + cq * QD, rr);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          tmem_ld32(trow + L::kColO + half * HD + c * 32, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st32(trow + L::kColO + half * HD + c * 32, rr);
-        }
-        if (half == 0) {
+        for (int i = 0; i < QD; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+        tmem_st_n<QD>(trow + L::kColO + cq * QD, rr);
+        if (cq == 0) {
           const uint32_t lv = tmem_ld1(trow + L::kColL);
           tmem_wait_ld();
           tmem_st1(trow + L::kColL, __float_as_uint(__uint_as_float(lv) * alpha));
@@ -439,11 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m_run = m_new;
       // probabilities 2^(x - m + 7) as 1-2 E4M3 terms, written over S(j):
-      // term t, slots [64*half, 64*half + 64) -> columns 32t + 16*half + [0, 16)
+      // term t, slots [32 cq, 32 cq + 32) -> columns 32 t + 8 cq + [0, 8)
       const float moff = kPShift - m_run;
-      uint32_t w1[16], w2[16];
+      uint32_t w1[8], w2[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const float e0 = ex2_approx(fmaf(__uint_as_float(sr[4 * c]), f_row, moff));
         const float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 1]), f_row, moff));
         const float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 2]), f_row, moff));
@@ -460,15 +455,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           w1[c] = pack4_e4m3(e0, e1, e2, e3);
         }
       }
-      tmem_st16(trow + L::kColS + b * 128 + half * 16, w1);
-      if (n_pterms > 1) tmem_st16(trow + L::kColS + b * 128 + 32 + half * 16, w2);
+      tmem_st_n<8>(trow + L::kColS + b * 128 + cq * 8, w1);
+      if (n_pterms > 1) tmem_st_n<8>(trow + L::kColS + b * 128 + 32 + cq * 8, w2);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + b));
     }
 
     // ---------------------------------------------------------- epilogue
-    float o[HD];
+    float o[QD];
     float l = 0.f;
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
@@ -477,19 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && ntiles > 0) {
       tc_fence_after();
-      uint32_t rr[32];
+      uint32_t rr[QD];
+      tmem_ld_n<QD>(trow + L::kColO + cq * QD, rr);
+      tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        tmem_ld32(trow + L::kColO + half * HD + c * 32, rr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c * 32 + i] = __uint_as_float(rr[i]);
-      }
+      for (int i = 0; i < QD; ++i) o[i] = __uint_as_float(rr[i]);
       l = __uint_as_float(tmem_ld1(trow + L::kColL));
       tmem_wait_ld();
     } else {
 #pragma unroll
-      for (int i = 0; i < HD; ++i) o[i] = 0.f;
+      for (int i = 0; i < QD; ++i) o[i] = 0.f;
     }
     // Normalised rows go to shared memory (the key/value stages are free:
     // every copy landed and every MMA finished), fp32 [128][d + 4], then the
@@ -500,13 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool single = prm.nsplit == 1;
     constexpr int SP = D + 4;                 // padded row stride (floats)
     constexpr int F4 = kTile * D / 4;         // float4 per tile
+    constexpr int PER = F4 / kSoftmaxThreads; // float4 per thread
     float* stage = reinterpret_cast<float*>(sm + L::kK);
     {
       const float f = single ? inv_l * scale_v : inv_l;
-      float4* srow = reinterpret_cast<float4*>(stage + row * SP + half * HD);
+      float4* srow = reinterpret_cast<float4*>(stage + row * SP + cq * QD);
 #pragma unroll
-      for (int c = 0; c < HD / 4; ++c) srow[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
-      if (half == 0) xch[row] = l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY;
+      for (int c = 0; c < QD / 4; ++c) srow[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
+      if (cq == 0) xch[row] = l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY;
     }
     sync_softmax();
     const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
@@ -522,19 +515,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + e) = v;
       }
     };
+    auto staged = [&](int f4) -> float4 {
+      return *reinterpret_cast<const float4*>(stage + (f4 / (D / 4)) * SP + 4 * (f4 % (D / 4)));
+    };
     if (single) {
-      for (int f4 = threadIdx.x; f4 < F4; f4 += kSoftmaxThreads) {
-        const int rrow = f4 / (D / 4), c4 = f4 % (D / 4);
-        store_out(f4, *reinterpret_cast<const float4*>(stage + rrow * SP + 4 * c4));
-      }
+#pragma unroll
+      for (int i = 0; i < PER; ++i) store_out(threadIdx.x + i * kSoftmaxThreads, staged(threadIdx.x + i * kSoftmaxThreads));
     } else {
       // partial (normalised) tile and its per-row log2-sum-exp
       const size_t pbase = ((size_t)split * r.qtiles_max + qt) * H + h;
       float4* dst = reinterpret_cast<float4*>(r.part_o + pbase * kTile * D);
-      for (int f4 = threadIdx.x; f4 < F4; f4 += kSoftmaxThreads) {
-        const int rrow = f4 / (D / 4), c4 = f4 % (D / 4);
-        __stcg(dst + f4, *reinterpret_cast<const float4*>(stage + rrow * SP + 4 * c4));
-      }
+#pragma unroll
+      for (int i = 0; i < PER; ++i) __stcg(dst + threadIdx.x + i * kSoftmaxThreads, staged(threadIdx.x + i * kSoftmaxThreads));
       if (threadIdx.x < kTile) __stcg(r.part_lse + pbase * kTile + threadIdx.x, xch[threadIdx.x]);
       __threadfence();
       sync_softmax();
@@ -563,20 +555,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s2 = 0; s2 < prm.nsplit; ++s2) wts[s2 * kTile + rr] *= g;
         }
         sync_softmax();
-        for (int f4 = threadIdx.x; f4 < F4; f4 += kSoftmaxThreads) {
-          const int rrow = f4 / (D / 4);
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int s2 = 0; s2 < prm.nsplit; ++s2) {
-            const float w = wts[s2 * kTile + rrow];
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                r.part_o + ((((size_t)s2 * r.qtiles_max + qt) * H + h) * kTile) * D) + f4);
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+        float4 acc[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < prm.nsplit; ++s2) {
+          // all of this split's loads in flight before any use
+          const float4* src = reinterpret_cast<const float4*>(
+              r.part_o + (((size_t)s2 * r.qtiles_max + qt) * H + h) * kTile * D);
+          float4 v[PER];
+#pragma unroll
+          for (int i = 0; i < PER; ++i) v[i] = __ldcg(src + threadIdx.x + i * kSoftmaxThreads);
+#pragma unroll
+          for (int i = 0; i < PER; ++i) {
+            const float w = wts[s2 * kTile + (threadIdx.x + i * kSoftmaxThreads) / (D / 4)];
+            acc[i].x = fmaf(w, v[i].x, acc[i].x);
+            acc[i].y = fmaf(w, v[i].y, acc[i].y);
+            acc[i].z = fmaf(w, v[i].z, acc[i].z);
+            acc[i].w = fmaf(w, v[i].w, acc[i].w);
           }
-          store_out(f4, acc);
         }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) store_out(threadIdx.x + i * kSoftmaxThreads, acc[i]);
         if (threadIdx.x == 0) r.tickets[qt * H + h] = 0;
       }
     }
@@ -622,10 +621,10 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   const dim3 grid(qtiles, (unsigned)r.H, (unsigned)a.nsplit);
   const size_t smem = attention_smem_bytes(r.D);
   if (r.D == 128) {
-    k_attn_prep<128><<<pgrid, kSoftmaxThreads, 0, s>>>(p);
+    k_attn_prep<128><<<pgrid, kPrepThreads, 0, s>>>(p);
     k_attention<128><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
   } else {
-    k_attn_prep<64><<<pgrid, kSoftmaxThreads, 0, s>>>(p);
+    k_attn_prep<64><<<pgrid, kPrepThreads, 0, s>>>(p);
     k_attention<64><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
   }
   return cudaGetLastError();
