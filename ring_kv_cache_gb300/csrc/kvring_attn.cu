@@ -332,19 +332,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_e4m3(128, D + 16, true);
+      // Descriptors are built once; per MMA only the low word (start address
+      // in 16-byte units) moves: +2 per 32-byte k-step of a K-major tile,
+      // +32*D/16 per 32-row k-step of the MN-major V tile.
+      const uint64_t dq = smem_desc(sbase + L::kQ, 16, 8 * D, L::kSwz);
+      const uint64_t dk = smem_desc(sbase + L::kK, 16, 8 * D, L::kSwz);
+      const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, kq_hi = (uint32_t)(dq >> 32);
+      // V of stage s: start address + s tiles, and the leading byte offset
+      // (to the ones block, in bits 16..29) s tiles shorter.
+      const uint64_t dv = smem_desc(sbase + L::kV, (uint32_t)(L::kOnes - L::kV), 8 * D, L::kSwz);
+      const uint32_t v_lo0 = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
+      constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4;
+      constexpr uint32_t kVStageStep = kKVStep - (kKVStep << 16);
       // S(j) into TMEM buffer j&1.  Its previous user, P(j-2), was consumed
       // by PV(j-2), issued earlier by this thread: in-order execution.
       auto issue_qk = [&](int j) -> bool {
         const int s = j % kStages, b = j & 1;
         if (!mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs)) return false;
         tc_fence_after();
-        const uint32_t kaddr = sbase + L::kK + s * L::kKVTile;
-        for (int t = 0; t < n_qterms; ++t) {
-          const uint32_t qaddr = sbase + L::kQ + t * L::kQTile;
+        const uint32_t kl = k_lo + s * kKVStep;
+        const uint32_t dst = tmem + L::kColS + b * 128;
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk) {
-            mma_e4m3(tmem + L::kColS + b * 128, smem_desc(qaddr + kk * 32, 16, 8 * D, L::kSwz),
-                     smem_desc(kaddr + kk * 32, 16, 8 * D, L::kSwz), idesc_qk, (t | kk) != 0);
+        for (int t = 0; t < 3; ++t) {
+          if (t < n_qterms) {
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk)
+              mma_e4m3_w(dst, q_lo + t * kQStep + 2 * kk, kq_hi, kl + 2 * kk, kq_hi, idesc_qk, (t | kk) != 0);
           }
         }
         mma_commit(bar(L::kBarSFull + b));
@@ -356,14 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % kStages, b = j & 1;
         if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
         tc_fence_after();
-        const uint32_t vaddr = sbase + L::kV + s * L::kKVTile;
-        const uint32_t lbo = (uint32_t)(L::kOnes - (L::kV + s * L::kKVTile));  // V tile -> ones block
-        for (int t = 0; t < n_pterms; ++t) {
+        const uint32_t vl = v_lo0 + (uint32_t)s * kVStageStep;
+        const uint32_t pa = tmem + L::kColS + b * 128;
 #pragma unroll
-          for (int kk = 0; kk < kTile / 32; ++kk) {
-            const uint32_t acc = (j > 0 || t > 0 || kk > 0) ? 1u : 0u;
-            mma_e4m3_ts(tmem + L::kColO, tmem + L::kColS + b * 128 + t * 32 + kk * 8,
-                        smem_desc(vaddr + kk * 32 * D, lbo, 8 * D, L::kSwz), idesc_pv, acc);
+        for (int t = 0; t < 2; ++t) {
+          if (t < n_pterms) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 32; ++kk)
+              mma_e4m3_ts_w(tmem + L::kColO, pa + t * 32 + kk * 8, vl + kk * (32 * D / 16), v_hi, idesc_pv,
+                            (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
           }
         }
         mma_commit(bar(L::kBarKvEmpty + s));
