@@ -15,8 +15,7 @@
 //              warps 4-7 the other halves), which exchange row maxima
 //              through shared memory.  Online softmax in log2 units with a
 //              lazily raised running maximum; probabilities carry 2^7 and
-//              are split into 1-2 E4M3 terms (the residual by Veltkamp
-//              splitting) that are
+//              are split into 1-2 E4M3 terms (the residual in f16x2) that are
 //              written back into TMEM over the S columns just read; O is
 //              rescaled in TMEM when the maximum rises by more than 1.5 (log2
 //              units).  Epilogue: O / l, split partials and their merge.
@@ -126,14 +125,6 @@ struct AttnParams {
 __device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 __device__ __forceinline__ void sync_rowgroup(int quarter) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + quarter) : "memory");
-}
-
-// x rounded to nearest with 4 significant bits (E4M3's normal precision),
-// by Veltkamp splitting with C = 2^20 + 1: c = C x, hi = c - (c - x).
-// Each step rounds on its own (no fused multiply-add).
-__device__ __forceinline__ float split_hi4(float x) {
-  const float c = __fmul_rn(x, 1048577.0f);
-  return __fsub_rn(c, __fsub_rn(c, x));
 }
 
 // Four fp32 values to four E4M3 codes (first value in the low byte).
@@ -467,11 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 1]), f_row, moff));
         const float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 2]), f_row, moff));
         const float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 3]), f_row, moff));
-        w1[c] = pack4_e4m3(e0, e1, e2, e3);
         if (n_pterms > 1) {
-          // second term: the residual of rounding to E4M3's 4 significant
-          // bits, by Veltkamp splitting (C = 2^20 + 1) in fp32
-          w2[c] = pack4_e4m3(e0 - split_hi4(e0), e1 - split_hi4(e1), e2 - split_hi4(e2), e3 - split_hi4(e3));
+          // two terms: P1 from the f16 value, P2 from its exact f16 residual
+          const uint32_t h01 = f32x2_to_f16x2(e0, e1), h23 = f32x2_to_f16x2(e2, e3);
+          const uint16_t lo = f16x2_to_e4m3x2(h01), hi = f16x2_to_e4m3x2(h23);
+          w1[c] = (uint32_t)lo | ((uint32_t)hi << 16);
+          const uint16_t lo2 = f16x2_to_e4m3x2(hsub2_u32(h01, e4m3x2_to_f16x2(lo)));
+          const uint16_t hi2 = f16x2_to_e4m3x2(hsub2_u32(h23, e4m3x2_to_f16x2(hi)));
+          w2[c] = (uint32_t)lo2 | ((uint32_t)hi2 << 16);
+        } else {
+          w1[c] = pack4_e4m3(e0, e1, e2, e3);
         }
       }
       tmem_st_n<8>(trow + L::kColS + b * 128 + cq * 8, w1);
