@@ -163,6 +163,30 @@ kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
 kvring_status kvring_attention(kvring_t* ring, const void* q_bf16, const int32_t* qpos,
                                int32_t n_q, void* out, int32_t out_dtype, void* stream);
 
+/* Attention that allocates nothing, for callers that cannot hand the library
+ * device memory.  Some callers cannot allocate device memory at all: a
+ * plugin living inside a host program that owns the whole device memory
+ * pool, or a real-time loop where an allocation would stall the device or
+ * break its memory budget.  This entry point computes exactly what
+ * kvring_attention computes, with the same arguments and errors, but its
+ * scratch (the prepared query tiles, per-row factors, precision levels,
+ * split partials and split tickets) lives in a fixed 32 MiB static device
+ * array inside the library rather than in the ring's buffer.  Every GPU
+ * that loads the library holds that array until the process exits.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - The first call on a device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - The array is shared by every call: calls that overlap on the GPU
+ *     (other streams, other rings) race and must be ordered by the caller.
+ *     Each call clears the split tickets it uses before its kernels run.
+ *   - The split count is reduced until the partials fit; a call whose
+ *     query tiles alone need more than 32 MiB (about 49 KiB per 128-query
+ *     tile per head at head_dim 128) returns KVRING_ERR_CAPACITY.
+ * The paper has no counterpart: this is a deployment variant. */
+kvring_status kvring_attention_noalloc(kvring_t* ring, const void* q_bf16, const int32_t* qpos,
+                                       int32_t n_q, void* out, int32_t out_dtype, void* stream);
+
 /* Copy the ring out for inspection (tests, snapshots).  Any pointer may be
  * NULL to skip that part.  k_out, v_out: uint8 [H][capacity][d] codes;
  * scales: float [4H] = scale_k, scale_v, inv_scale_k, inv_scale_v;

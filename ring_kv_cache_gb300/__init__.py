@@ -21,7 +21,8 @@ import torch
 __all__ = [
     "KvRing", "KvRingError", "TO_OLDEST", "lib", "library_path", "header_functions",
     "kvring_required_bytes", "kvring_create", "kvring_destroy", "kvring_calibrate_scales",
-    "kvring_write_frame", "kvring_delta_rotate", "kvring_attention", "kvring_export",
+    "kvring_write_frame", "kvring_delta_rotate", "kvring_attention", "kvring_attention_noalloc",
+    "kvring_export",
     "kvring_status_string", "encode_e4m3", "STATE",
 ]
 
@@ -83,6 +84,7 @@ def lib():
         "kvring_write_frame": (i32, [vp, vp, vp, vp, i32, vp]),
         "kvring_delta_rotate": (i32, [vp, i32, vp]),
         "kvring_attention": (i32, [vp, vp, vp, i32, vp, i32, vp]),
+        "kvring_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, vp]),
         "kvring_export": (i32, [vp, vp, vp, vp, vp, vp, vp]),
         "kvring_debug_encode_e4m3": (i32, [vp, vp, i64, vp]),
         "kvring_debug_attention_levels": (i32, [vp, vp, vp]),
@@ -183,6 +185,11 @@ def kvring_delta_rotate(handle, delta, stream_ptr) -> None:
 def kvring_attention(handle, q, qpos, n_q, out, out_dtype, stream_ptr) -> None:
     _check(lib().kvring_attention(handle, _ptr(q), _ptr(qpos), int(n_q), _ptr(out), int(out_dtype),
                                   stream_ptr), "kvring_attention")
+
+
+def kvring_attention_noalloc(handle, q, qpos, n_q, out, out_dtype, stream_ptr) -> None:
+    _check(lib().kvring_attention_noalloc(handle, _ptr(q), _ptr(qpos), int(n_q), _ptr(out),
+                                          int(out_dtype), stream_ptr), "kvring_attention_noalloc")
 
 
 def kvring_export(handle, k_out, v_out, scales, slot_pos, state, stream_ptr) -> None:

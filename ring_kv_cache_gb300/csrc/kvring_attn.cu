@@ -46,6 +46,8 @@
 // Every wait is bounded (about a second of wall time); a wait that gives up
 // sets KVRING_DEVERR_TIMEOUT in the ring's error word, the CTA drains its
 // in-flight copies and MMAs, frees TMEM and returns.
+#include <mutex>
+
 #include "kvring_internal.cuh"
 
 namespace kvr {
@@ -643,6 +645,42 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
     k_attention<64><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
   }
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Scratch for callers that cannot allocate device memory.
+//
+// kvring_attention_noalloc keeps its scratch (query images, per-row factors,
+// levels, split partials, tickets) in this file-scope array instead of the
+// ring's buffer.  It is static device memory: every GPU that loads the
+// library holds it until the process exits.  In host code the array's name
+// is only a host-side stand-in, so its device address is looked up once per
+// device (cudaGetSymbolAddress, with that device current) and then passed
+// to the kernels like any other pointer.
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+__device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
+std::mutex g_scratch_mu;
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices];
+}  // namespace
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+cudaError_t static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace kvr

@@ -289,6 +289,63 @@ kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, 
   return cuda_status(kvr::launch_attention(r->dev, &r->tmK, &r->tmV, a, (cudaStream_t)stream));
 }
 
+kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t* qpos, int32_t n_q,
+                                       void* out, int32_t out_dtype, void* stream) {
+  if (!r || !q || !out || !aligned(q, 16) || !aligned(out, 16) || (qpos && !aligned(qpos, 4)) || n_q < 1)
+    return KVRING_ERR_INVALID_ARG;
+  if (out_dtype != KVRING_OUT_F32 && out_dtype != KVRING_OUT_BF16) return KVRING_ERR_INVALID_ARG;
+  if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
+  if (n_q > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+  // Scratch plan for this call inside the static array: query images,
+  // per-row factors, levels and tickets always; split partials only when
+  // the call is split, with as many splits as fit.
+  const size_t H = (size_t)r->dev.H, D = (size_t)r->dev.D;
+  const size_t qtiles = (size_t)((n_q + kvr::kTile - 1) / kvr::kTile);
+  const size_t units = qtiles * H;
+  const size_t fixed = align_up(units * 3 * kvr::kTile * D) + align_up(units * kvr::kTile * 4) + 2 * align_up(units * 4);
+  const size_t per_split = units * kvr::kTile * D * 4;
+  const size_t per_split_lse = units * kvr::kTile * 4;
+  const size_t cap = kvr::static_scratch_bytes();
+  if (fixed > cap) return KVRING_ERR_CAPACITY;
+  kvr::AttnLaunch a;
+  a.q = q;
+  a.qpos = qpos;
+  a.out = out;
+  a.n_q = n_q;
+  a.out_bf16 = out_dtype == KVRING_OUT_BF16;
+  a.forced_level = r->cfg.attn_precision;
+  choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
+  const int ctiles = (r->cfg.capacity + kvr::kTile - 1) / kvr::kTile;
+  while (a.nsplit > 1 && fixed + align_up(a.nsplit * per_split) + align_up(a.nsplit * per_split_lse) > cap) {
+    const int want = a.nsplit - 1;
+    a.tiles_per_split = (ctiles + want - 1) / want;
+    a.nsplit = (ctiles + a.tiles_per_split - 1) / a.tiles_per_split;
+  }
+  void* base = nullptr;
+  if (kvr::static_scratch_address(&base) != cudaSuccess) return KVRING_ERR_CUDA;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  kvr::RingDev d = r->dev;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = b + off;
+    off = align_up(off + bytes);
+    return p;
+  };
+  d.qprep = take(units * 3 * kvr::kTile * D);
+  d.qrowf = reinterpret_cast<float*>(take(units * kvr::kTile * 4));
+  d.levels = reinterpret_cast<int32_t*>(take(units * 4));
+  d.tickets = reinterpret_cast<int32_t*>(take(units * 4));
+  d.part_o = reinterpret_cast<float*>(take(a.nsplit > 1 ? a.nsplit * per_split : 0));
+  d.part_lse = reinterpret_cast<float*>(take(a.nsplit > 1 ? a.nsplit * per_split_lse : 0));
+  d.qtiles_max = (int)qtiles;
+  d.max_splits = a.nsplit;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the split tickets must
+  // start at zero
+  if (cudaMemsetAsync(d.tickets, 0, units * 4, s) != cudaSuccess) return KVRING_ERR_CUDA;
+  return cuda_status(kvr::launch_attention(d, &r->tmK, &r->tmV, a, s));
+}
+
 kvring_status kvring_export(kvring_t* r, void* k_out, void* v_out, float* scales, int32_t* slot_pos,
                             int32_t* state, void* stream) {
   if (!r) return KVRING_ERR_INVALID_ARG;

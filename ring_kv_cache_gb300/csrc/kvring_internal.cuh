@@ -407,6 +407,10 @@ struct AttnLaunch {
 cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              const AttnLaunch& a, cudaStream_t s);
 size_t attention_smem_bytes(int D);
+// Fixed-size static device scratch used by kvring_attention_noalloc, and
+// its device address on the current device (looked up once per device).
+size_t static_scratch_bytes();
+cudaError_t static_scratch_address(void** out);
 // Once per process and head size, before the first launch (not capturable).
 cudaError_t attention_prepare(int D);
 }  // namespace kvr

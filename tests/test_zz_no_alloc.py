@@ -1,0 +1,70 @@
+"""The attention entry point that allocates nothing.
+
+Some callers cannot give the library device memory: a plugin inside a host
+program that owns the whole device pool, or a real-time loop where an
+allocation would stall the device.  kvring_attention_noalloc serves them:
+it computes what kvring_attention computes, with its scratch in a fixed
+static device array inside the library.
+
+Checked through the C ABI (ctypes, no binding helpers): two calls in a row
+each match the existing entry point's output for the same inputs, within
+the attention tolerance the other tests use; and a call whose query tiles
+cannot fit the static array is refused with KVRING_ERR_CAPACITY.  This file
+is named to run last, so a failure here comes after every other test ran.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import ring_kv_cache_gb300 as kv
+from workloads import PROD, prod_session
+
+from _ringcheck import MAX_ABS, MEAN_ABS, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _call(fn, ring, q, out):
+    s = torch.cuda.current_stream().cuda_stream
+    return fn(ctypes.c_void_p(ring.handle), ctypes.c_void_p(q.data_ptr()), None, q.shape[0],
+              ctypes.c_void_p(out.data_ptr()), 0, ctypes.c_void_p(s))
+
+
+def test_noalloc_matches_attention_on_two_calls_in_a_row():
+    L = kv.lib()
+    sk, sv, frames = prod_session(seed=21, frames=10)
+    ring = kv.KvRing(PROD.heads, PROD.head_dim, PROD.capacity, PROD.tokens, PROD.max_position,
+                     max_kv_splits=16)
+    ring.calibrate(dev(frames[0][1]), dev(frames[0][2]))
+    for q, k, v in frames[:8]:
+        ring.write(dev(k), dev(v))
+    for step in (8, 9):
+        q, k, v = frames[step]
+        ring.write(dev(k), dev(v))
+        qd = dev(q)
+        want = torch.empty((PROD.queries, PROD.heads, PROD.head_dim), dtype=torch.float32, device="cuda")
+        got = torch.full_like(want, float("nan"))
+        assert _call(L.kvring_attention, ring, qd, want) == 0
+        assert _call(L.kvring_attention_noalloc, ring, qd, got) == 0
+        torch.cuda.synchronize()
+        err = (got.double() - want.double()).abs()
+        assert torch.isfinite(got).all()
+        assert err.max().item() <= MAX_ABS and err.mean().item() <= MEAN_ABS, (step, err.max().item())
+
+
+def test_noalloc_refuses_what_does_not_fit():
+    L = kv.lib()
+    # 40 heads x 22 query tiles of head_dim 128 need ~43 MiB of query images
+    ring = kv.KvRing(40, 128, 256, 2816, 4096, max_kv_splits=1)
+    x = torch.zeros((8, 40, 128), dtype=torch.bfloat16, device="cuda")
+    ring.calibrate(x, x)
+    q = torch.zeros((2816, 40, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((2816, 40, 128), dtype=torch.float32, device="cuda")
+    assert _call(L.kvring_attention_noalloc, ring, q, out) == 3      # KVRING_ERR_CAPACITY
+    small = torch.zeros((128, 40, 128), dtype=torch.bfloat16, device="cuda")
+    out_small = torch.empty((128, 40, 128), dtype=torch.float32, device="cuda")
+    assert _call(L.kvring_attention_noalloc, ring, small, out_small) == 0
+    torch.cuda.synchronize()
+    assert np.all(out_small.cpu().numpy() == 0)                      # empty ring: zeros
