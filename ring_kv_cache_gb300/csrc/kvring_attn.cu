@@ -34,9 +34,11 @@
 // order, so QK(j+2) (into the same columns) always follows PV(j).
 //
 // k_attn_prep runs first, once per (query tile, head): RoPE of the queries in
-// fp32, a per-row scale 448/amax(row), the split into 1-3 E4M3 terms written
-// as ready-to-copy swizzled shared-memory images, the per-row logit factor,
-// and the tile's precision level.  Split CTAs of the same tile share them.
+// fp32, a per-row scale 448/amax(row), the split into 3 E4M3 terms written
+// as ready-to-copy swizzled shared-memory images, the per-row logit factor
+// and row maxima.  Split CTAs of the same tile share them; the attention
+// kernel is launched as a programmatic dependent of the prep kernel, so its
+// set-up and first key/value copies overlap the prep.
 //
 // Precision level per query tile (from the tile's amax, the head's
 // key range 448*scale_k and value range 448*scale_v): level 1 = 1 Q term +
@@ -55,6 +57,7 @@ namespace {
 
 constexpr int kStages = 3;
 constexpr int kPrepThreads = 256;
+constexpr int kPrepSplit = 4;           // prep CTAs per query tile (32 rows each)
 constexpr int kSoftmaxThreads = 512;    // 16 warps: four threads per query row
 constexpr int kThreads = kSoftmaxThreads + 64;
 constexpr int kWarpTma = 16;
@@ -134,29 +137,34 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
   return (uint32_t)f32x2_to_e4m3x2(a, b) | ((uint32_t)f32x2_to_e4m3x2(c, d) << 16);
 }
 
-// Query preparation, one CTA per (query tile, head), 256 threads.  Chunk
-// task k = i * 256 + tid: row k / CPR, chunk k % CPR (8 elements = 4 RoPE
-// pairs); a warp reads 32 consecutive 16-byte chunks.
+// Query preparation, one CTA per 32 rows of a (query tile, head), 256
+// threads.  Chunk task k = i * 256 + tid: row k / CPR of the block, chunk
+// k % CPR (8 elements = 4 RoPE pairs); a warp reads 32 consecutive 16-byte
+// chunks.  Writes all three E4M3 terms (the attention kernel copies as many
+// as the tile's level needs), the per-row logit factor and the row maxima
+// from which the attention kernel picks the level.
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads) k_attn_prep(const AttnParams prm) {
   constexpr int CPR = D / 8;
-  constexpr int PRO = kTile * CPR / kPrepThreads;
-  __shared__ float warpmax[8];
+  constexpr int ROWS = kTile / kPrepSplit;
+  constexpr int PRO = ROWS * CPR / kPrepThreads;
+  griddep_launch_dependents();
   const RingDev& r = prm.r;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, H = r.H;
+  const int qt = blockIdx.x / kPrepSplit, row0 = (blockIdx.x % kPrepSplit) * ROWS;
+  const int h = blockIdx.y, H = r.H;
   const size_t unit = (size_t)qt * H + h;
-  float qv[PRO][8];
-  float amax[PRO];
   const int next_pos = __ldcg(r.state + ST_NEXT_POS);
+  const float scale_k = r.scales[h];
+  uint8_t* img = r.qprep + unit * 3 * (kTile * D);
 #pragma unroll
   for (int i = 0; i < PRO; ++i) {
     const int k = i * kPrepThreads + threadIdx.x;
-    const int rrow = k / CPR, chunk = k % CPR;
+    const int rrow = row0 + k / CPR, chunk = k % CPR;
     const int t = qt * kTile + rrow;
-    amax[i] = 0.f;
+    float qv[8];
+    float amax = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qv[i][e] = 0.f;
+    for (int e = 0; e < 8; ++e) qv[e] = 0.f;
     if (t < prm.n_q) {
       const uint4 w = __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)t * H + h) * D) + chunk);
       int p = prm.qpos ? __ldg(prm.qpos + t) : next_pos - prm.n_q + t;
@@ -174,50 +182,29 @@ __global__ void __launch_bounds__(kPrepThreads) k_attn_prep(const AttnParams prm
         const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
         const float y0 = x0 * cc[e] - x1 * ss[e];
         const float y1 = x0 * ss[e] + x1 * cc[e];
-        qv[i][2 * e] = y0;
-        qv[i][2 * e + 1] = y1;
-        amax[i] = fmaxf(amax[i], fmaxf(fabsf(y0), fabsf(y1)));
+        qv[2 * e] = y0;
+        qv[2 * e + 1] = y1;
+        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
       }
     }
     // row maximum over the CPR consecutive lanes that hold the row
 #pragma unroll
-    for (int off = CPR / 2; off > 0; off >>= 1) amax[i] = fmaxf(amax[i], __shfl_xor_sync(0xFFFFFFFFu, amax[i], off));
-  }
-  float wm = 0.f;
-#pragma unroll
-  for (int i = 0; i < PRO; ++i) wm = fmaxf(wm, amax[i]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
-  if (lane == 0) warpmax[warp] = wm;
-  const float scale_k = r.scales[h];
-  const float vmax = 448.0f * r.scales[H + h];
-  __syncthreads();
-  int level = prm.forced_level;
-  if (level == 0) {
-    float qm = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) qm = fmaxf(qm, warpmax[w]);
-    const float lg = qm * 448.0f * scale_k;
-    level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
-  }
-  if (threadIdx.x == 0) r.levels[unit] = level;
-  // E4M3 terms of q / sigma_q (sigma_q = amax/448), residual splitting in
-  // fp32; 8 bytes per chunk per term at the chunk's swizzled place.
-  uint8_t* img = r.qprep + unit * 3 * (kTile * D);
-#pragma unroll
-  for (int i = 0; i < PRO; ++i) {
-    const int k = i * kPrepThreads + threadIdx.x;
-    const int rrow = k / CPR, chunk = k % CPR;
-    float sq = amax[i] / 448.0f;
+    for (int off = CPR / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    float sq = amax / 448.0f;
     if (!(sq >= 0x1p-126f)) sq = 1.0f;
     const float invq = 1.0f / sq;
-    if (chunk == 0)
-      r.qrowf[unit * kTile + rrow] = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
+    if (chunk == 0) {
+      r.qrowf[unit * 2 * kTile + rrow] = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
+      r.qrowf[unit * 2 * kTile + kTile + rrow] = amax;
+    }
+    // E4M3 terms of q / sigma_q (sigma_q = amax/448), residual splitting in
+    // fp32; 8 bytes per chunk per term at the chunk's swizzled place.
     float u[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) u[e] = qv[i][e] * invq;
+    for (int e = 0; e < 8; ++e) u[e] = qv[e] * invq;
     const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
-    for (int term = 0; term < level; ++term) {
+#pragma unroll
+    for (int term = 0; term < 3; ++term) {
       uint16_t c4[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(u[2 * e], u[2 * e + 1]);
@@ -260,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- setup
   const size_t unit = (size_t)qt * H + h;
   if (threadIdx.x == kWarpTma * 32) {
-    // The producer initialises the barriers and starts the query and the
-    // first key/value copies at once.
+    // The producer initialises the barriers and starts the first key/value
+    // copies at once; they do not depend on the query preparation.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKvFull + s), 1);
       mbar_init(bar(L::kBarKvEmpty + s), 1);
@@ -276,12 +263,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
-    int level = __ldcg(r.levels + unit);
-    level = level < 1 ? 1 : (level > 3 ? 3 : level);
-    misc->level = level;
-    mbar_arrive_expect_tx(bar(L::kBarQFull), (uint32_t)(level * L::kQTile));
-    for (int t = 0; t < level; ++t)
-      bulk_load(sbase + L::kQ + t * L::kQTile, r.qprep + (unit * 3 + t) * L::kQTile, L::kQTile, bar(L::kBarQFull));
     const int first = ntiles < kStages ? ntiles : kStages;
     for (int j = 0; j < first; ++j) {
       mbar_arrive_expect_tx(bar(L::kBarKvFull + j), 2u * kTile * D);
@@ -298,6 +279,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4* ones = reinterpret_cast<uint4*>(sm + L::kOnes);
     for (int i = threadIdx.x; i < kTile * kTile / 16; i += kThreads)
       ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+  }
+  // Everything below reads what k_attn_prep wrote.
+  griddep_wait();
+  if (warp == kWarpTma) {
+    // precision level of this query tile from its row maxima, then one bulk
+    // copy per E4M3 term of the prepared query images
+    float qm = 0.f;
+    for (int i = lane; i < kTile; i += 32) qm = fmaxf(qm, __ldcg(r.qrowf + unit * 2 * kTile + kTile + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xFFFFFFFFu, qm, off));
+    int level = prm.forced_level;
+    if (level == 0) {
+      const float lg = qm * 448.0f * r.scales[h];
+      const float vmax = 448.0f * r.scales[H + h];
+      level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
+    }
+    if (lane == 0) {
+      misc->level = level;
+      if (split == 0) r.levels[unit] = level;
+      mbar_arrive_expect_tx(bar(L::kBarQFull), (uint32_t)(level * L::kQTile));
+      for (int t = 0; t < level; ++t)
+        bulk_load(sbase + L::kQ + t * L::kQTile, r.qprep + (unit * 3 + t) * L::kQTile, L::kQTile, bar(L::kBarQFull));
+    }
   }
   fence_proxy_async_smem();  // the all-ones block
   tc_fence_before();
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = threadIdx.x & (kTile - 1);
     const int cq = threadIdx.x >> 7;
     const int quarter = warp & 3;
-    const float f_row = __ldcg(r.qrowf + unit * kTile + row);
+    const float f_row = __ldcg(r.qrowf + unit * 2 * kTile + row);
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_run = -INFINITY;
     bool ok = true;
@@ -634,17 +638,30 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   p.tiles_per_split = a.tiles_per_split;
   p.forced_level = a.forced_level;
   const unsigned qtiles = (unsigned)((a.n_q + kTile - 1) / kTile);
-  const dim3 pgrid(qtiles, (unsigned)r.H);
-  const dim3 grid(qtiles, (unsigned)r.H, (unsigned)a.nsplit);
-  const size_t smem = attention_smem_bytes(r.D);
+  const dim3 pgrid(qtiles * kPrepSplit, (unsigned)r.H);
+  // The attention kernel may start while the prep kernel still runs
+  // (programmatic dependent launch); it waits for the prep's results with
+  // griddepcontrol.wait before it reads them.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(qtiles, (unsigned)r.H, (unsigned)a.nsplit);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = attention_smem_bytes(r.D);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (r.D == 128) {
     k_attn_prep<128><<<pgrid, kPrepThreads, 0, s>>>(p);
-    k_attention<128><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
-  } else {
-    k_attn_prep<64><<<pgrid, kPrepThreads, 0, s>>>(p);
-    k_attention<64><<<grid, kThreads, smem, s>>>(*tmK, *tmV, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, k_attention<128>, *tmK, *tmV, p);
   }
-  return cudaGetLastError();
+  k_attn_prep<64><<<pgrid, kPrepThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, k_attention<64>, *tmK, *tmV, p);
 }
 
 // ---------------------------------------------------------------------------

@@ -137,21 +137,40 @@ __global__ void __launch_bounds__(kThreads) k_calibrate(RingDev r, const uint16_
 }
 
 // ---------------------------------------------------------------- write ---
+// Each thread owns kWriteU chunks, (block * kWriteU + u) * 256 + tid, so a
+// warp's accesses stay contiguous; all input loads are issued before the
+// ring state is read, which hides one DRAM round trip.
+constexpr int kWriteU = 4;
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* __restrict__ k,
                                                     const uint16_t* __restrict__ v,
                                                     const int32_t* __restrict__ pos, int n) {
   constexpr int CH = D / 16;
   __shared__ int s_head, s_next;
+  const int H = r.H, C = r.C;
+  const long long per = (long long)n * H * CH;
+  uint4 in[kWriteU][2];
+#pragma unroll
+  for (int u = 0; u < kWriteU; ++u) {
+    const long long gid = ((long long)blockIdx.x * kWriteU + u) * kThreads + threadIdx.x;
+    if (gid < 2 * per) {
+      const int isv = gid >= per;
+      const long long w = isv ? gid - per : gid;
+      const uint4* src = reinterpret_cast<const uint4*>((isv ? v : k) + (w / CH) * D + (w % CH) * 16);
+      in[u][0] = __ldcs(src);
+      in[u][1] = __ldcs(src + 1);
+    }
+  }
   if (threadIdx.x == 0) {
     s_head = __ldcg(r.state + ST_HEAD);
     s_next = __ldcg(r.state + ST_NEXT_POS);
   }
   __syncthreads();
-  const int H = r.H, C = r.C;
-  const long long per = (long long)n * H * CH;
-  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
-  if (gid < 2 * per) {
+#pragma unroll
+  for (int u = 0; u < kWriteU; ++u) {
+    const long long gid = ((long long)blockIdx.x * kWriteU + u) * kThreads + threadIdx.x;
+    if (gid >= 2 * per) continue;
     const int isv = gid >= per;
     const long long w = isv ? gid - per : gid;
     const int chunk = (int)(w % CH);
@@ -160,13 +179,11 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
     const int t = (int)(th / H);
     int slot = s_head + t;
     if (slot >= C) slot -= C;  // head < C and t < n <= C
-    const uint4* src = reinterpret_cast<const uint4*>((isv ? v : k) + ((size_t)t * H + h) * D + chunk * 16);
     float x[16];
-    unpack_bf16x16(__ldcs(src), __ldcs(src + 1), x);
+    unpack_bf16x16(in[u][0], in[u][1], x);
     bool ok = true;
-    int p = 0;
     if (!isv) {
-      p = pos ? __ldg(pos + t) : s_next + t;
+      const int p = pos ? __ldg(pos + t) : s_next + t;
       if (p < 0 || p >= r.max_pos) {
         ok = false;
         atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
@@ -313,7 +330,7 @@ cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, con
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
                          cudaStream_t s) {
   const long long items = 2LL * n * r.H * (r.D / 16);
-  const unsigned g = grid_for(items);
+  const unsigned g = grid_for((items + kWriteU - 1) / kWriteU);
   if (r.D == 128)
     k_write<128><<<g, kThreads, 0, s>>>(r, (const uint16_t*)k, (const uint16_t*)v, pos, n);
   else

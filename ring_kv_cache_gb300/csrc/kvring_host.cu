@@ -71,7 +71,7 @@ Plan plan_for(const kvring_config* c) {
   p.tickets = take(Q * H * 4);
   p.levels = take(Q * H * 4);
   p.qprep = take(Q * H * 3 * kvr::kTile * D);
-  p.qrowf = take(Q * H * kvr::kTile * 4);
+  p.qrowf = take(Q * H * 2 * kvr::kTile * 4);
   p.total = off;
   return p;
 }
@@ -302,7 +302,7 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
   const size_t H = (size_t)r->dev.H, D = (size_t)r->dev.D;
   const size_t qtiles = (size_t)((n_q + kvr::kTile - 1) / kvr::kTile);
   const size_t units = qtiles * H;
-  const size_t fixed = align_up(units * 3 * kvr::kTile * D) + align_up(units * kvr::kTile * 4) + 2 * align_up(units * 4);
+  const size_t fixed = align_up(units * 3 * kvr::kTile * D) + align_up(units * 2 * kvr::kTile * 4) + 2 * align_up(units * 4);
   const size_t per_split = units * kvr::kTile * D * 4;
   const size_t per_split_lse = units * kvr::kTile * 4;
   const size_t cap = kvr::static_scratch_bytes();
@@ -332,7 +332,7 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
     return p;
   };
   d.qprep = take(units * 3 * kvr::kTile * D);
-  d.qrowf = reinterpret_cast<float*>(take(units * kvr::kTile * 4));
+  d.qrowf = reinterpret_cast<float*>(take(units * 2 * kvr::kTile * 4));
   d.levels = reinterpret_cast<int32_t*>(take(units * 4));
   d.tickets = reinterpret_cast<int32_t*>(take(units * 4));
   d.part_o = reinterpret_cast<float*>(take(a.nsplit > 1 ? a.nsplit * per_split : 0));

@@ -46,7 +46,7 @@ struct RingDev {
   int32_t* tickets;    // [qtiles][H] split completion counters (0 between calls)
   int32_t* levels;     // [qtiles][H] precision level of each query tile
   uint8_t* qprep;      // [qtiles][H][3][128 * D] query E4M3 terms, swizzled tile images
-  float* qrowf;        // [qtiles][H][128] logit factor per query row
+  float* qrowf;        // [qtiles][H][2][128] logit factor and amax per query row
   int H, D, C, max_pos, max_tokens, max_splits, qtiles_max;
 };
 
@@ -107,6 +107,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+
+// Programmatic dependent launch: let the next kernel in the stream start,
+// and wait until the previous kernel's results are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -36,7 +36,7 @@ def test_required_bytes_matches_layout(L):
     a = lambda x: (x + 255) // 256 * 256
     want = (a(H * C * D) * 2 + a(4 * C) + a(16 * H) + a(64) + a(8 * H) + a(40960 * D * 4)
             + a(S * Q * H * 128 * D * 4) + a(S * Q * H * 128 * 4) + a(Q * H * 4) * 2
-            + a(Q * H * 3 * 128 * D) + a(Q * H * 128 * 4))
+            + a(Q * H * 3 * 128 * D) + a(Q * H * 2 * 128 * 4))
     assert n == want
 
 
