@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) k_calibrate(RingDev r, const uint16_
 // Each thread owns kWriteU chunks, (block * kWriteU + u) * 256 + tid, so a
 // warp's accesses stay contiguous; all input loads are issued before the
 // ring state is read, which hides one DRAM round trip.
-constexpr int kWriteU = 4;
+constexpr int kWriteU = 2;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* __restrict__ k,
@@ -167,6 +167,21 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
     s_next = __ldcg(r.state + ST_NEXT_POS);
   }
   __syncthreads();
+  // all table rows before any arithmetic or store, so their latencies overlap
+  float4 cs[kWriteU][4];
+  int pp[kWriteU];
+#pragma unroll
+  for (int u = 0; u < kWriteU; ++u) {
+    const long long gid = ((long long)blockIdx.x * kWriteU + u) * kThreads + threadIdx.x;
+    pp[u] = -1;
+    if (gid < per) {  // keys only
+      const int chunk = (int)(gid % CH);
+      const int t = (int)(gid / CH / H);
+      const int p = pos ? __ldg(pos + t) : s_next + t;
+      pp[u] = p;
+      if (p >= 0 && p < r.max_pos) load_table16(r.table, D, p, chunk, cs[u]);
+    }
+  }
 #pragma unroll
   for (int u = 0; u < kWriteU; ++u) {
     const long long gid = ((long long)blockIdx.x * kWriteU + u) * kThreads + threadIdx.x;
@@ -183,14 +198,12 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
     unpack_bf16x16(in[u][0], in[u][1], x);
     bool ok = true;
     if (!isv) {
-      const int p = pos ? __ldg(pos + t) : s_next + t;
+      const int p = pp[u];
       if (p < 0 || p >= r.max_pos) {
         ok = false;
         atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
       } else {
-        float4 cs[4];
-        load_table16(r.table, D, p, chunk, cs);
-        rope_pinned(x, cs);
+        rope_pinned(x, cs[u]);
       }
       if (h == 0 && chunk == 0) r.slot_pos[slot] = p;
     }
