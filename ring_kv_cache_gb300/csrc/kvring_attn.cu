@@ -132,22 +132,6 @@ __device__ __forceinline__ void sync_rowgroup(int quarter) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + quarter) : "memory");
 }
 
-// 2^x on the FMA pipe, for part of the softmax so that the special-function
-// unit (which also runs the E4M3 conversions) is not the only exp2 path.
-// x = n + f with n = round(x) (adding 1.5 * 2^23 leaves n in the low bits),
-// f in [-0.5, 0.5]; 2^f by a cubic fitted to minimise the relative error on
-// that interval (weighted least squares, max relative error 7.5e-5); 2^n by
-// adding n to the exponent field.  x is clamped at -125 (the result is then
-// far below the smallest E4M3 probability and encodes as 0).
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -125.0f);
-  const float t = __fadd_rn(x, 12582912.0f);
-  const float f = __fsub_rn(x, __fsub_rn(t, 12582912.0f));
-  const float p = fmaf(fmaf(fmaf(0.05517160892486572f, f, 0.2426111400127411f), f, 0.6932610273361206f), f,
-                       0.9999280571937561f);
-  return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
-}
-
 // Four fp32 values to four E4M3 codes (first value in the low byte).
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
   return (uint32_t)f32x2_to_e4m3x2(a, b) | ((uint32_t)f32x2_to_e4m3x2(c, d) << 16);
@@ -476,11 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t w1[8], w2[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        // half of the exponentials on the special-function unit, half on the FMA pipe
         const float e0 = ex2_approx(fmaf(__uint_as_float(sr[4 * c]), f_row, moff));
-        const float e1 = exp2_poly(fmaf(__uint_as_float(sr[4 * c + 1]), f_row, moff));
+        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 1]), f_row, moff));
         const float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 2]), f_row, moff));
-        const float e3 = exp2_poly(fmaf(__uint_as_float(sr[4 * c + 3]), f_row, moff));
+        const float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 3]), f_row, moff));
         if (n_pterms > 1) {
           // two terms: P1 from the f16 value, P2 from its exact f16 residual
           const uint32_t h01 = f32x2_to_f16x2(e0, e1), h23 = f32x2_to_f16x2(e2, e3);

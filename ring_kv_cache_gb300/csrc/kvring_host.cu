@@ -80,7 +80,9 @@ kvring_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVRING_OK :
 
 // Split-KV count for one attention call: the grid has qtiles * H * nsplit
 // CTAs of which one fits per SM; pick the split count with the fewest
-// "waves x (tiles per CTA + fixed per-CTA cost)".
+// "waves x (tiles per CTA + fixed per-CTA cost)".  The fixed cost (prologue,
+// epilogue and partial store, about four key/value tiles' time) was
+// measured on GB300.
 void choose_splits(const kvring* r, int n_q, int* nsplit, int* tiles_per_split) {
   const int ctiles = (r->cfg.capacity + kvr::kTile - 1) / kvr::kTile;
   const int qtiles = (n_q + kvr::kTile - 1) / kvr::kTile;
@@ -94,7 +96,7 @@ void choose_splits(const kvring* r, int n_q, int* nsplit, int* tiles_per_split) 
     if (ns_eff != ns) continue;
     const long long ctas = per_split * ns_eff;
     const long long waves = (ctas + r->sm_count - 1) / r->sm_count;
-    const double cost = (double)waves * (tps + 2.0) + (ns_eff > 1 ? 0.5 : 0.0);
+    const double cost = (double)waves * (tps + 4.0) + (ns_eff > 1 ? 0.5 : 0.0);
     if (cost < best - 1e-9) {
       best = cost;
       best_ns = ns_eff;
