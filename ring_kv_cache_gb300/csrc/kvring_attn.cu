@@ -465,13 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 2]), f_row, moff));
         const float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 3]), f_row, moff));
         if (n_pterms > 1) {
-          // two terms: P1 from the f16 value, P2 from its exact f16 residual
+          // two terms in f16x2: P1 = the value rounded to 4 significant bits
+          // (Veltkamp split on the FMA pipe; exact in E4M3), P2 = the exact
+          // residual
           const uint32_t h01 = f32x2_to_f16x2(e0, e1), h23 = f32x2_to_f16x2(e2, e3);
-          const uint16_t lo = f16x2_to_e4m3x2(h01), hi = f16x2_to_e4m3x2(h23);
-          w1[c] = (uint32_t)lo | ((uint32_t)hi << 16);
-          const uint16_t lo2 = f16x2_to_e4m3x2(hsub2_u32(h01, e4m3x2_to_f16x2(lo)));
-          const uint16_t hi2 = f16x2_to_e4m3x2(hsub2_u32(h23, e4m3x2_to_f16x2(hi)));
-          w2[c] = (uint32_t)lo2 | ((uint32_t)hi2 << 16);
+          const uint32_t a01 = f16x2_hi4(h01), a23 = f16x2_hi4(h23);
+          w1[c] = (uint32_t)f16x2_to_e4m3x2(a01) | ((uint32_t)f16x2_to_e4m3x2(a23) << 16);
+          w2[c] = (uint32_t)f16x2_to_e4m3x2(hsub2_u32(h01, a01)) |
+                  ((uint32_t)f16x2_to_e4m3x2(hsub2_u32(h23, a23)) << 16);
         } else {
           w1[c] = pack4_e4m3(e0, e1, e2, e3);
         }

@@ -90,6 +90,19 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Each half of h rounded to nearest with 4 significant bits (E4M3's normal
+// precision) by Veltkamp splitting in f16 (11 bits) with C = 2^7 + 1:
+// c = C h, hi = c - (c - h).  Valid for |h| < 65504 / 129.
+__device__ __forceinline__ uint32_t f16x2_hi4(uint32_t h) {
+  const uint32_t c = hmul2_u32(h, 0x58085808u);  // 129.0 in both halves
+  return hsub2_u32(c, hsub2_u32(c, h));
+}
+
 // --------------------------------------------------------------- misc -----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
