@@ -12,9 +12,11 @@ L2: steps rotate over 16 independent rings (and 16 input frames), so each
 step's ring, inputs and partials were last touched 15 steps earlier, after
 more than 126 MB of other traffic: every step starts L2-cold.
 
-Timing: W warm-up steps, then exactly K steps between CUDA events on the
-launching stream, with a barrier and device synchronisation on both sides;
-per-kernel durations from events around each launch on the same stream.
+Timing: every step is one CUDA graph replay (one ring's write + attention,
+with the delta rotation in front every 42nd write of a ring).  W warm-up
+steps, then exactly K steps between CUDA events on the launching stream,
+with a barrier and device synchronisation on both sides.  Per-kernel
+durations come from graphs of 16 back-to-back calls (one per ring).
 The metric is time-like (microseconds per write + attention).
 
 ``--impl reference`` times the CPU oracle (float64 NumPy, the test oracle)
@@ -46,6 +48,7 @@ RESET_PERIOD = 42   # the pages reset positions once per 42 steps (Do It Once, a
 WRITE_BYTES = 2 * N_NEW * H * D * 2 + 2 * N_NEW * H * D + N_NEW * 4  # bf16 in, e4m3 out, slot_pos
 ATTN_FLOPS = 4.0 * H * N_Q * C * D                                   # QK^T and PV
 ATTN_BYTES = 2 * H * C * D + N_Q * H * D * 2 + N_Q * H * D * 4       # cache, q, fp32 out
+DELTA_BYTES = 2 * H * C * D + 2 * C * 4                              # key cache read + write, positions
 H2D_BYTES = 3 * N_NEW * H * D * 2
 D2H_BYTES = N_Q * H * D * 4
 
@@ -161,51 +164,92 @@ def gpu_arm(args, rank, world):
 
     writes = [8] * RINGS          # frames already written per ring
 
-    def step(i, ev=None):
-        r = i % RINGS
-        q, k, v = frames[r]
-        if writes[r] % RESET_PERIOD == 0:
-            # positions reset every 42 steps: one delta rotation of the window
-            rings[r].delta_rotate(kv.TO_OLDEST, stream=stream)
-            resets[0] += 1
-        writes[r] += 1
-        if ev is not None:
-            ev[0].record(stream)
-        rings[r].write(k, v, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        rings[r].attention(q, out=outs[r], stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    resets = [0]
-    # warm-up
-    for i in range(args.warmup):
-        step(i)
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def do_step(r, reset):
+        q, k, v = frames[r]
+        if reset:
+            # positions reset every 42 steps: one delta rotation of the window
+            rings[r].delta_rotate(kv.TO_OLDEST, stream=stream)
+        rings[r].write(k, v, stream=stream)
+        rings[r].attention(q, out=outs[r], stream=stream)
+
+    # eager warm-up (every kernel has run once before capture)
+    for i in range(max(args.warmup, RINGS)):
+        r = i % RINGS
+        do_step(r, writes[r] % RESET_PERIOD == 0)
+        writes[r] += 1
     torch.cuda.synchronize(dev)
 
-    # timed region: K steps, events around the whole region on the stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # One CUDA graph per ring step (write + attention), and one with the
+    # position reset in front; a step is one graph replay.
+    g_step = [capture(lambda r=r: do_step(r, False)) for r in range(RINGS)]
+    g_rst = [capture(lambda r=r: do_step(r, True)) for r in range(RINGS)]
+    resets = [0]
+
+    def replay(i):
+        r = i % RINGS
+        if writes[r] % RESET_PERIOD == 0:
+            g_rst[r].replay()
+            resets[0] += 1
+        else:
+            g_step[r].replay()
+        writes[r] += 1
+
+    for i in range(args.warmup):
+        replay(i)
+    torch.cuda.synchronize(dev)
+
+    # timed region: exactly K steps, events around the whole region on the stream
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
     resets[0] = 0
     with ClockSampler(dev.index) as clk:
-        start.record(stream)
-        for i in range(args.steps):
-            step(i, evs[i])
-        stop.record(stream)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                replay(i)
+            stop.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
     total_ms = start.elapsed_time(stop)
     timed_resets = resets[0]
-    w_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
-    a_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+
+    # Per-kernel durations: graphs of 16 back-to-back calls on the 16 rings
+    # (each call L2-cold), timed with events around the replays.
+    def timed(g, reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    g_attn = capture(lambda: [rings[r].attention(frames[r][0], out=outs[r], stream=stream) for r in range(RINGS)])
+    g_write = capture(lambda: [rings[r].write(frames[r][1], frames[r][2], stream=stream) for r in range(RINGS)])
+    g_delta = capture(lambda: [rings[r].delta_rotate(kv.TO_OLDEST, stream=stream) for r in range(RINGS)])
+    timed(g_attn, 2)
+    a_reps = 8
+    a_us = timed(g_attn, a_reps) * 1e3 / (a_reps * RINGS)
+    d_ms = timed(g_delta, 1)                      # every window restarts at 0
+    w_reps = RESET_PERIOD - 1
+    w_us = timed(g_write, w_reps) * 1e3 / (w_reps * RINGS)
+    d_ms += timed(g_delta, 1)                     # delta = 41 frames of positions
+    d_us = d_ms * 1e3 / (2 * RINGS)
+    for r in range(RINGS):
+        writes[r] = RESET_PERIOD  # the next step of every ring starts with a reset
 
     # end to end through the public API with pinned host buffers
     hk = [torch.empty((N_NEW, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
@@ -248,7 +292,7 @@ def gpu_arm(args, rank, world):
         levels.append(lv)
     levels = np.concatenate(levels).ravel()
     errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
-    return dict(total_ms=total_ms, w_ms=w_ms, a_ms=a_ms, e2e_ms=e2e_ms, clocks=clk.summary(),
+    return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, e2e_ms=e2e_ms, clocks=clk.summary(),
                 resets=timed_resets,
                 levels=levels, device_errors=int(np.bitwise_or.reduce(errs)))
 
@@ -367,8 +411,7 @@ def main():
     K = args.steps
     units = K * world
     us_per_unit = total_ms * 1e3 / units
-    w_us = float(np.mean(res["w_ms"])) * 1e3
-    a_us = float(np.mean(res["a_ms"])) * 1e3
+    w_us, a_us, d_us = res["w_us"], res["a_us"], res["d_us"]
     fp8_peak = 2.0 * peaks["bf16"]            # FP8 dense = 2 x bf16 (nominal 4.5 / 2.25 PF)
     lv = res["levels"]
     q_terms = np.where(lv >= 3, 3, np.where(lv >= 2, 2, 1))
@@ -397,6 +440,7 @@ def main():
                         "wrapped 5,788-slot ring, 10 heads x 128 (E4M3 cache, bf16 in, fp32 out)",
             "heads": H, "head_dim": D, "capacity": C, "tokens_per_write": N_NEW, "queries": N_Q,
             "l2": f"cold: {RINGS} rings and input frames round-robin, >126 MB between reuses",
+            "launch": "each step is one CUDA graph replay (write + attention of one ring)",
             "resets": f"one delta rotation per ring every {RESET_PERIOD} writes (positions reset "
                       f"period), inside the timed region: {res['resets']} in {K} steps",
             "parallelism": "replicas" if world > 1 else "1 GPU",
@@ -420,11 +464,16 @@ def main():
             "write": {"avg_launch_us": w_us, "algorithmic_bytes": WRITE_BYTES, "GB/s": write_gbs,
                       "frac_hbm": write_gbs / peaks["hbm"], "peak_gbs": peaks["hbm"]},
             "attention": {"avg_launch_us": a_us, "TFLOP/s": attn_tflops,
-                          "cache_GB/s": ATTN_BYTES / (a_us * 1e-6) / 1e9},
+                          "cache_GB/s": ATTN_BYTES / (a_us * 1e-6) / 1e9,
+                          "note": "one call = query prep kernel + attention kernel"},
+            "delta_rotate": {"avg_launch_us": d_us, "algorithmic_bytes": DELTA_BYTES,
+                             "GB/s": DELTA_BYTES / (d_us * 1e-6) / 1e9,
+                             "frac_hbm": DELTA_BYTES / (d_us * 1e-6) / 1e9 / peaks["hbm"]},
+            "timing": "per-kernel: CUDA graphs of 16 back-to-back calls on 16 rings, events around replays",
         },
         "e2e": {"value": e2e_ms * 1e3 / units, "unit": "µs",
                 "h2d_bytes_per_step": H2D_BYTES, "d2h_bytes_per_step": D2H_BYTES},
-        "gpu_launches": 2 * K + res["resets"],
+        "gpu_launches": 3 * K + res["resets"],
         "clocks": res["clocks"],
         "device_errors": res["device_errors"],
     }

@@ -422,10 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 32; ++c)
           if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
       }
-      float smax = __uint_as_float(sr[0]);
+      // row maximum of this thread's 32 columns as a shallow tree
+      float m11[11];
 #pragma unroll
-      for (int c = 1; c < 31; c += 2) smax = fmax3(smax, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-      smax = fmaxf(smax, __uint_as_float(sr[31]));
+      for (int i = 0; i < 10; ++i)
+        m11[i] = fmax3(__uint_as_float(sr[3 * i]), __uint_as_float(sr[3 * i + 1]), __uint_as_float(sr[3 * i + 2]));
+      m11[10] = fmaxf(__uint_as_float(sr[30]), __uint_as_float(sr[31]));
+      float smax = fmax3(fmax3(m11[0], m11[1], m11[2]), fmax3(m11[3], m11[4], m11[5]),
+                         fmax3(m11[6], m11[7], fmax3(m11[8], m11[9], m11[10])));
       float* xj = xch + (j & 1) * 4 * kTile;
       xj[cq * kTile + row] = smax;
       // after this barrier all four threads of the row have read their S
@@ -457,25 +461,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // probabilities 2^(x - m + 7) as 1-2 E4M3 terms, written over S(j):
       // term t, slots [32 cq, 32 cq + 32) -> columns 32 t + 8 cq + [0, 8)
       const float moff = kPShift - m_run;
+      // Phases, each over all 32 columns, so that every step has 16-32
+      // independent operations in flight.
       uint32_t w1[8], w2[8];
+      float e[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float e0 = ex2_approx(fmaf(__uint_as_float(sr[4 * c]), f_row, moff));
-        const float e1 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 1]), f_row, moff));
-        const float e2 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 2]), f_row, moff));
-        const float e3 = ex2_approx(fmaf(__uint_as_float(sr[4 * c + 3]), f_row, moff));
-        if (n_pterms > 1) {
-          // two terms in f16x2: P1 = the value rounded to 4 significant bits
-          // (Veltkamp split on the FMA pipe; exact in E4M3), P2 = the exact
-          // residual
-          const uint32_t h01 = f32x2_to_f16x2(e0, e1), h23 = f32x2_to_f16x2(e2, e3);
-          const uint32_t a01 = f16x2_hi4(h01), a23 = f16x2_hi4(h23);
-          w1[c] = (uint32_t)f16x2_to_e4m3x2(a01) | ((uint32_t)f16x2_to_e4m3x2(a23) << 16);
-          w2[c] = (uint32_t)f16x2_to_e4m3x2(hsub2_u32(h01, a01)) |
-                  ((uint32_t)f16x2_to_e4m3x2(hsub2_u32(h23, a23)) << 16);
-        } else {
-          w1[c] = pack4_e4m3(e0, e1, e2, e3);
+      for (int i = 0; i < 32; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(sr[i]), f_row, moff));
+      if (n_pterms > 1) {
+        // two terms in f16x2: P1 = the value rounded to 4 significant bits
+        // (Veltkamp split on the FMA pipe; exact in E4M3), P2 = the exact
+        // residual
+        uint32_t hv[16], av[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[2 * i], e[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) av[i] = f16x2_hi4(hv[i]);
+        uint32_t c1[16], c2[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          c1[i] = f16x2_to_e4m3x2(av[i]);
+          c2[i] = f16x2_to_e4m3x2(hsub2_u32(hv[i], av[i]));
         }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          w1[c] = c1[2 * c] | (c1[2 * c + 1] << 16);
+          w2[c] = c2[2 * c] | (c2[2 * c + 1] << 16);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) w1[c] = pack4_e4m3(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
       }
       tmem_st_n<8>(trow + L::kColS + b * 128 + cq * 8, w1);
       if (n_pterms > 1) tmem_st_n<8>(trow + L::kColS + b * 128 + 32 + cq * 8, w2);
