@@ -239,6 +239,11 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
 }
 
 // ---------------------------------------------------------------- delta ---
+// A few blocks per SM, each thread looping over 16-byte chunks of filled key
+// rows (kDeltaU independent chunks in flight per iteration), so the number of
+// completion tickets stays small.
+constexpr int kDeltaU = 4;
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
   constexpr int CH = D / 16;
@@ -258,35 +263,49 @@ __global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
   }
   __syncthreads();
   const int delta = s_delta;
+  const int nv = s_nv;
   if (delta > 0) {
     const float4* row = reinterpret_cast<const float4*>(r.table + (size_t)delta * D);
     for (int i = threadIdx.x; i < D / 4; i += kThreads) s_cs[i] = __ldg(row + i);
   }
   __syncthreads();
-  const int C = r.C;
-  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
-  const long long items = (long long)r.H * C * CH;
-  if (delta > 0 && gid < items) {
-    const int chunk = (int)(gid % CH);
-    const long long hs = gid / CH;
-    const int slot = (int)(hs % C);
-    if (slot < s_nv) {
-      uint4* p = reinterpret_cast<uint4*>(r.k + (size_t)hs * D + chunk * 16);
-      const uint4 in = *p;
-      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-      float y[16];
+  if (delta > 0) {
+    // items: (head, filled slot, chunk), slot-major within a head
+    const long long per_head = (long long)nv * CH;
+    const long long items = per_head * r.H;
+    const long long stride = (long long)gridDim.x * kThreads;
+    for (long long base = (long long)blockIdx.x * kThreads + threadIdx.x; base < items; base += stride * kDeltaU) {
+      uint4 in[kDeltaU];
+      uint4* ptr[kDeltaU];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 a = e4m3x2_to_f32x2((uint16_t)(w[i] & 0xFFFF));
-        const float2 b = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
-        // pairs (a.x, a.y) and (b.x, b.y); pair index chunk*8 + 2i (+1)
-        const float4 cs = s_cs[chunk * 4 + i];  // (c, s) of both pairs
-        y[4 * i + 0] = __fadd_rn(__fmul_rn(a.x, cs.x), __fmul_rn(a.y, cs.y));
-        y[4 * i + 1] = __fsub_rn(__fmul_rn(a.y, cs.x), __fmul_rn(a.x, cs.y));
-        y[4 * i + 2] = __fadd_rn(__fmul_rn(b.x, cs.z), __fmul_rn(b.y, cs.w));
-        y[4 * i + 3] = __fsub_rn(__fmul_rn(b.y, cs.z), __fmul_rn(b.x, cs.w));
+      for (int u = 0; u < kDeltaU; ++u) {
+        const long long it = base + u * stride;
+        ptr[u] = nullptr;
+        if (it < items) {
+          const long long h = it / per_head, rem = it % per_head;
+          ptr[u] = reinterpret_cast<uint4*>(r.k + ((size_t)h * r.C + rem / CH) * D + (rem % CH) * 16);
+          in[u] = *ptr[u];
+        }
       }
-      *p = pack_e4m3x16(y);
+#pragma unroll
+      for (int u = 0; u < kDeltaU; ++u) {
+        if (!ptr[u]) continue;
+        const int chunk = (int)((base + u * stride) % per_head % CH);
+        const uint32_t w[4] = {in[u].x, in[u].y, in[u].z, in[u].w};
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 a = e4m3x2_to_f32x2((uint16_t)(w[i] & 0xFFFF));
+          const float2 b = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
+          // pairs (a.x, a.y) and (b.x, b.y); pair index chunk*8 + 2i (+1)
+          const float4 cs = s_cs[chunk * 4 + i];  // (c, s) of both pairs
+          y[4 * i + 0] = __fadd_rn(__fmul_rn(a.x, cs.x), __fmul_rn(a.y, cs.y));
+          y[4 * i + 1] = __fsub_rn(__fmul_rn(a.y, cs.x), __fmul_rn(a.x, cs.y));
+          y[4 * i + 2] = __fadd_rn(__fmul_rn(b.x, cs.z), __fmul_rn(b.y, cs.w));
+          y[4 * i + 3] = __fsub_rn(__fmul_rn(b.y, cs.z), __fmul_rn(b.x, cs.w));
+        }
+        *ptr[u] = pack_e4m3x16(y);
+      }
     }
   }
   __syncthreads();
@@ -299,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
   if (s_last) {
     __threadfence();
     if (delta >= 0) {
-      for (int sl = threadIdx.x; sl < s_nv; sl += kThreads) r.slot_pos[sl] -= delta;
+      for (int sl = threadIdx.x; sl < nv; sl += kThreads) r.slot_pos[sl] -= delta;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -352,8 +371,13 @@ cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const i
 }
 
 cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s) {
+  // the fill level is device state: size for a full ring, at most ~2 blocks per SM
   const long long items = (long long)r.H * r.C * (r.D / 16);
-  const unsigned g = grid_for(items);
+  unsigned g = grid_for((items + kDeltaU - 1) / kDeltaU);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (g > (unsigned)(2 * sms)) g = (unsigned)(2 * sms);
+  if (g < 1) g = 1;
   if (r.D == 128)
     k_delta<128><<<g, kThreads, 0, s>>>(r, delta);
   else
