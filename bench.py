@@ -400,6 +400,10 @@ def main():
 
     if args.impl == "reference":
         reference_arm(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
         return
 
     res = gpu_arm(args, rank, world)

@@ -232,6 +232,8 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
       r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
       r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
       r.state[ST_NEXT_POS] = s_next + n;
+      // oldest filled slot: the next one to be overwritten once full, else slot 0
+      r.state[ST_OLDEST_POS] = __ldcg(r.slot_pos + (nv >= C ? head : 0));
       r.state[ST_TICKET_WRITE] = 0;
       __threadfence();
     }
@@ -252,8 +254,7 @@ __global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
   if (threadIdx.x == 0) {
     const int nv = __ldcg(r.state + ST_NVALID);
     int d = delta_arg;
-    if (d == KVRING_DELTA_TO_OLDEST)
-      d = nv > 0 ? __ldcg(r.slot_pos + (nv == r.C ? __ldcg(r.state + ST_HEAD) : 0)) : 0;
+    if (d == KVRING_DELTA_TO_OLDEST) d = nv > 0 ? __ldcg(r.state + ST_OLDEST_POS) : 0;
     if (d < 0 || d >= r.max_pos) {
       if (blockIdx.x == 0) atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_DELTA);
       d = -1;  // skip the rotation entirely
@@ -264,6 +265,9 @@ __global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
   __syncthreads();
   const int delta = s_delta;
   const int nv = s_nv;
+  // positions of the filled slots, spread over all blocks (nobody reads them here)
+  if (delta > 0)
+    for (int sl = blockIdx.x * kThreads + threadIdx.x; sl < nv; sl += gridDim.x * kThreads) r.slot_pos[sl] -= delta;
   if (delta > 0) {
     const float4* row = reinterpret_cast<const float4*>(r.table + (size_t)delta * D);
     for (int i = threadIdx.x; i < D / 4; i += kThreads) s_cs[i] = __ldg(row + i);
@@ -315,20 +319,15 @@ __global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
     s_last = tk == (int)gridDim.x - 1;
   }
   __syncthreads();
-  if (s_last) {
+  if (s_last && threadIdx.x == 0) {
     __threadfence();
     if (delta >= 0) {
-      for (int sl = threadIdx.x; sl < nv; sl += kThreads) r.slot_pos[sl] -= delta;
+      r.state[ST_NEXT_POS] -= delta;
+      r.state[ST_OLDEST_POS] -= delta;
+      r.state[ST_LAST_DELTA] = delta;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      if (delta >= 0) {
-        r.state[ST_NEXT_POS] -= delta;
-        r.state[ST_LAST_DELTA] = delta;
-      }
-      r.state[ST_TICKET_DELTA] = 0;
-      __threadfence();
-    }
+    r.state[ST_TICKET_DELTA] = 0;
+    __threadfence();
   }
 }
 

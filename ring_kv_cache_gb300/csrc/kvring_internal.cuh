@@ -26,6 +26,7 @@ enum : int {
   ST_TICKET_WRITE = 8,
   ST_TICKET_CALIB = 9,
   ST_TICKET_DELTA = 10,
+  ST_OLDEST_POS = 11,   // position of the oldest filled slot (the default reset delta)
   ST_WORDS_ALLOC = 16,
 };
 

@@ -61,3 +61,41 @@ def assert_ring_equal(ring, orc, what=""):
 def attn_errors(got, want):
     err = np.abs(np.asarray(got, np.float64) - want)
     return float(err.max()), float(err.mean())
+
+
+def bf16_bits(t):
+    """bf16 CUDA tensor -> numpy uint16 bit patterns (for the oracle)."""
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def oracle_from_ring(ring, max_position, rope_base=10000.0):
+    """An oracle Ring holding exactly the device ring's current contents."""
+    from oracle import Ring
+    e = export_np(ring)
+    H = ring.H
+    orc = Ring(ring.H, ring.d, ring.C, max_position, rope_base)
+    orc.K = e["k"].copy()
+    orc.V = e["v"].copy()
+    orc.slot_pos = e["slot_pos"].astype(np.int64)
+    sc = e["scales"].astype(np.float32)
+    orc.scale_k, orc.scale_v = sc[:H].copy(), sc[H:2 * H].copy()
+    orc.inv_k, orc.inv_v = sc[2 * H:3 * H].copy(), sc[3 * H:].copy()
+    st = e["state"]
+    orc.head = int(st[kv.STATE["head"]])
+    orc.n_valid = int(st[kv.STATE["n_valid"]])
+    orc.total = int(np.uint32(st[kv.STATE["total_lo"]])) | (int(np.uint32(st[kv.STATE["total_hi"]])) << 32)
+    orc.next_pos = int(st[kv.STATE["next_pos"]])
+    orc.calibrated = bool(st[kv.STATE["calibrated"]])
+    return orc
+
+
+def sampled_attention_errors(orc, q_bits, out, rows, qpos=None):
+    """Max/mean abs error of device output rows against the float64 oracle."""
+    from oracle.attention import attention_exact
+    n = q_bits.shape[0]
+    if qpos is None:
+        qpos = orc.next_pos - n + np.arange(n)
+    ref = attention_exact(orc, f32_from_bf16(q_bits[rows]), np.asarray(qpos)[rows])
+    got = out[rows].astype(np.float64)
+    err = np.abs(got - ref)
+    return float(err.max()), float(err.mean()), ref

@@ -1,0 +1,195 @@
+"""The large workloads, checked against the oracle on sampled operations.
+
+* Full step: 60 layers (10 heads x 128, 5,788 slots), per step one 757-token
+  write per layer and 4 passes x 60 attention calls, chained in CUDA graphs
+  (the post's "Where the Time Went": 4 passes through 60 blocks, 240
+  attention calls per step).
+* Reset cycle: the same 60 layers for 84 steps with one delta rotation of
+  every layer before step 42 (positions reset every 42 steps, "Do It Once,
+  at Write Time").
+* Stress: 40 heads x 128, 60 layers, a first frame of a seeded prompt length
+  in [100, 2000], then 200 frames of 757 tokens with resets every 42 steps;
+  keys and values Student-t (3 degrees of freedom) with per-head scales
+  log-uniform in [0.1, 10], so outliers saturate at +-448.
+
+The oracle cannot replay tens of thousands of writes, so each sampled check
+loads the device ring into an oracle ring right before the sampled
+operation, applies the same operation on the CPU, and compares the device
+ring after it bit for bit; attention is checked on 64 sampled query rows of
+all heads against the float64 reference over the same FP8 cache.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import ring_kv_cache_gb300 as kv
+from oracle import TO_OLDEST
+from workloads import cuda_frame, cuda_generator, log_uniform, stress_prompt_length
+
+from _ringcheck import (MAX_ABS, MEAN_ABS, assert_ring_equal, bf16_bits, oracle_from_ring,
+                        sampled_attention_errors)
+
+pytestmark = pytest.mark.gpu
+
+LAYERS, H, D, C, N, MAXPOS = 60, 10, 128, 5788, 757, 40960
+ROWS = np.random.default_rng(99).choice(N, 64, replace=False)
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _layers(seed, heads, frames_per_layer, first=N, max_tokens=N, splits=16, dist="normal",
+            lo=0.25, hi=4.0):
+    rng = np.random.default_rng(seed)
+    gen = cuda_generator(seed)
+    rings, frames, sig = [], [], []
+    for _ in range(LAYERS):
+        sk, sv = log_uniform(rng, heads, lo, hi), log_uniform(rng, heads, lo, hi)
+        fr = [cuda_frame(gen, heads, D, N, sk, sv, dist) for _ in range(frames_per_layer)]
+        rings.append(kv.KvRing(heads, D, C, max_tokens, MAXPOS, max_kv_splits=splits))
+        frames.append(fr)
+        sig.append((sk, sv))
+    return rings, frames, sig, gen
+
+
+def test_full_step_in_cuda_graphs():
+    rings, frames, _, _ = _layers(3, H, 8)
+    for r, fr in zip(rings, frames):
+        r.calibrate(fr[0][1], fr[0][2])
+        for q, k, v in fr:                     # 6,056 tokens: wrapped
+            r.write(k, v)
+    outs = [torch.empty((N, H, D), dtype=torch.float32, device="cuda") for _ in range(LAYERS * 4)]
+    s = torch.cuda.Stream()
+
+    def step(si):
+        for l in range(LAYERS):
+            rings[l].write(frames[l][si % 8][1], frames[l][si % 8][2], stream=s)
+        for p in range(4):
+            for l in range(LAYERS):
+                rings[l].attention(frames[l][(si + p) % 8][0], out=outs[4 * l + p], stream=s)
+
+    torch.cuda.synchronize()
+    graphs = []
+    for si in range(3):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step(si)
+        graphs.append(g)
+    graphs[0].replay()
+    graphs[1].replay()
+    torch.cuda.synchronize()
+    sampled = [0, 29, 59]
+    orcs = {l: oracle_from_ring(rings[l], MAXPOS) for l in sampled}
+    graphs[2].replay()
+    torch.cuda.synchronize()
+    for l in sampled:
+        q, k, v = frames[l][2]
+        orcs[l].write(_f(k), _f(v))
+        assert_ring_equal(rings[l], orcs[l], f"full step, layer {l}")
+        for p in (0, 3):
+            qb = bf16_bits(frames[l][(2 + p) % 8][0])
+            mx, mn, _ = sampled_attention_errors(orcs[l], qb, outs[4 * l + p].cpu().numpy(), ROWS)
+            assert mx <= MAX_ABS and mn <= MEAN_ABS, (l, p, mx, mn)
+    del graphs, rings, frames, outs
+    _free()
+
+
+def _f(t):
+    from workloads import f32_from_bf16
+    return f32_from_bf16(bf16_bits(t))
+
+
+def test_reset_cycle_84_steps():
+    rings, frames, _, _ = _layers(4, H, 8)
+    for r, fr in zip(rings, frames):
+        r.calibrate(fr[0][1], fr[0][2])
+        for q, k, v in fr:
+            r.write(k, v)
+    out = torch.empty((N, H, D), dtype=torch.float32, device="cuda")
+    probe = 17
+    for st in range(84):
+        if st == 42:
+            before = oracle_from_ring(rings[probe], MAXPOS)
+            for r in rings:
+                r.delta_rotate(kv.TO_OLDEST)
+            torch.cuda.synchronize()
+            d = before.delta_rotate(TO_OLDEST)
+            assert d > 0
+            assert_ring_equal(rings[probe], before, "after the reset")
+            assert rings[probe].export()["state"][kv.STATE["last_delta"]].item() == d
+        check = st in (42, 83)
+        if check:
+            orc = oracle_from_ring(rings[probe], MAXPOS)
+        fq, fk, fv = frames[probe][st % 8]
+        for l in range(LAYERS):
+            q, k, v = frames[l][st % 8]
+            rings[l].write(k, v)
+            if l == probe:
+                rings[l].attention(q, out=out)
+        if check:
+            torch.cuda.synchronize()
+            orc.write(_f(fk), _f(fv))
+            assert_ring_equal(rings[probe], orc, f"reset cycle, step {st}")
+            mx, mn, _ = sampled_attention_errors(orc, bf16_bits(fq), out.cpu().numpy(), ROWS)
+            assert mx <= MAX_ABS and mn <= MEAN_ABS, (st, mx, mn)
+    del rings, frames
+    _free()
+
+
+def test_stress_40_heads_heavy_tails():
+    HS = 40
+    n0 = stress_prompt_length(5)
+    rng = np.random.default_rng(5)
+    gen = cuda_generator(5)
+    scales = [(log_uniform(rng, HS, 0.1, 10.0), log_uniform(rng, HS, 0.1, 10.0)) for _ in range(LAYERS)]
+    rings = [kv.KvRing(HS, D, C, 2000, MAXPOS, max_kv_splits=4) for _ in range(LAYERS)]
+    out = torch.empty((N, HS, D), dtype=torch.float32, device="cuda")
+    probe = 3
+    # first forward: a prompt of n0 tokens calibrates and fills every layer
+    for l in range(LAYERS):
+        q, k, v = cuda_frame(gen, HS, D, n0, *scales[l], dist="student_t3")
+        if l == probe:
+            orc = oracle_from_ring(rings[l], MAXPOS)
+            orc.calibrate(_f(k), _f(v))
+            orc.write(_f(k), _f(v))
+        rings[l].calibrate(k, v)
+        rings[l].write(k, v)
+    torch.cuda.synchronize()
+    assert_ring_equal(rings[probe], orc, "first forward")
+    worst = []
+    check_steps = {7, 42, 43, 199}
+    for st in range(200):
+        if st > 0 and st % 42 == 0:
+            for r in rings:
+                r.delta_rotate(kv.TO_OLDEST)
+        for l in range(LAYERS):
+            q, k, v = cuda_frame(gen, HS, D, N, *scales[l], dist="student_t3")
+            if l == probe and st in check_steps:
+                torch.cuda.synchronize()
+                orc = oracle_from_ring(rings[l], MAXPOS)
+                rings[l].write(k, v)
+                rings[l].attention(q, out=out)
+                torch.cuda.synchronize()
+                orc.write(_f(k), _f(v))
+                assert_ring_equal(rings[l], orc, f"stress step {st}")
+                mx, mn, ref = sampled_attention_errors(orc, bf16_bits(q), out.cpu().numpy(), ROWS)
+                vrms = float(np.sqrt(np.mean(ref ** 2))) + 1e-30
+                worst.append((st, mx, mn, float(np.abs(ref).max()), vrms))
+            else:
+                rings[l].write(k, v)
+                if l == probe:
+                    rings[l].attention(q, out=out)
+    torch.cuda.synchronize()
+    for r in rings:
+        assert r.export()["state"][kv.STATE["error"]].item() == 0
+    print("stress attention errors (step, max-abs, mean-abs, max|o|, rms o):", worst)
+    for st, mx, mn, omax, orms in worst:
+        # absolute bar, and the error relative to the output's own size
+        assert mn <= MEAN_ABS, (st, mn)
+        assert mx <= max(MAX_ABS, 2e-3 * omax), (st, mx, omax)
+    del rings
+    _free()

@@ -139,3 +139,45 @@ def prod_session(seed: int = 2, frames: int = 9, shape: RingShape = PROD,
 def stress_prompt_length(seed: int = 5) -> int:
     """First-forward prompt length for the stress workload, uniform in [100, 2000]."""
     return int(np.random.default_rng(seed).integers(100, 2001))
+
+
+# ---------------------------------------------------------------------------
+# Device-side draws for the large workloads (full step, reset cycle, stress):
+# a seeded torch CUDA generator, bf16 tensors [n, H, d] on the GPU.  Only
+# random numbers and the bf16 cast; nothing of the cache's arithmetic.
+def cuda_generator(seed: int, device="cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def cuda_frame(gen, heads: int, head_dim: int, n: int, sigma_k=None, sigma_v=None,
+               dist: str = "normal", device="cuda"):
+    """(q, k, v) bf16 [n, heads, head_dim] on the GPU.
+
+    dist "normal": N(0,1) draws; "student_t3": Student-t with 3 degrees of
+    freedom, built as z / sqrt((z1^2 + z2^2 + z3^2) / 3) from standard normals.
+    sigma_k / sigma_v scale each head (None = 1).
+    """
+    import torch
+
+    def draw():
+        z = torch.randn((n, heads, head_dim), generator=gen, device=device)
+        if dist == "normal":
+            return z
+        if dist == "student_t3":
+            c = torch.randn((3, n, heads, head_dim), generator=gen, device=device)
+            return z / torch.sqrt((c * c).sum(0) / 3.0)
+        raise ValueError(dist)
+
+    def scaled(sig):
+        x = draw()
+        if sig is not None:
+            x = x * torch.as_tensor(sig, dtype=torch.float32, device=device)[None, :, None]
+        return x.to(torch.bfloat16).contiguous()
+
+    q = scaled(None)
+    k = scaled(sigma_k)
+    v = scaled(sigma_v)
+    return q, k, v
