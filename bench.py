@@ -419,10 +419,9 @@ def main():
     fp8_peak = 2.0 * peaks["bf16"]            # FP8 dense = 2 x bf16 (nominal 4.5 / 2.25 PF)
     lv = res["levels"]
     q_terms = np.where(lv >= 3, 3, np.where(lv >= 2, 2, 1))
-    p_terms = np.where(lv >= 2, 2, 1)
-    # issued MMA work relative to the algorithmic 2 units (QK, PV) per tile;
-    # the normaliser MMA (N=16) adds 16/128 of a PV per P term
-    issued = float(np.mean(q_terms + p_terms * (1 + 16.0 / D))) / 2.0
+    # issued tensor work relative to the algorithmic 2 FP8 units (QK, PV) per
+    # tile: one FP8 QK per query term, and PV in f16 at half the FP8 rate
+    issued = float(np.mean(q_terms + 2.0)) / 2.0
     attn_tflops = ATTN_FLOPS / (a_us * 1e-6) / 1e12
     write_gbs = WRITE_BYTES / (w_us * 1e-6) / 1e9
     traffic = attention_traffic()

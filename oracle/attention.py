@@ -17,9 +17,9 @@ and a float64 softmax with the row maximum subtracted.
 
 ``attention_emulated`` is a diagnostic that repeats the CUDA kernel's
 choices (queries split into FP8 terms with a per-row scale, probabilities
-scaled by 2^7 relative to a lazily raised running maximum and split into FP8
-terms, a normaliser summed from the same FP8 terms) in float64, so that
-format error and kernel bugs can be told apart.
+scaled by 2^7 relative to a lazily raised running maximum and carried either
+as FP8 terms or in half precision) in float64, so that format error and
+kernel bugs can be told apart.
 """
 from __future__ import annotations
 
@@ -120,7 +120,10 @@ def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
                        p_shift=7.0, tau=1.5) -> np.ndarray:
     """Diagnostic: the CUDA kernel's quantisation choices, in float64.
 
-    q_terms / p_terms may be ints or per-head sequences.
+    q_terms may be an int or a per-head sequence.  p_terms is the number of
+    E4M3 terms of the probabilities (1 or 2; the normaliser then sums the
+    same FP8 values), or "f16": probabilities rounded to IEEE half precision
+    for the value product while the normaliser sums the unrounded values.
     """
     q = np.asarray(q, dtype=np.float64)
     n, H, d = q.shape
@@ -133,7 +136,10 @@ def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
     invq = (np.float32(1.0) / sq).astype(np.float32)
     u = (qt * invq[:, :, None]).astype(np.float32)
     qt_terms = np.broadcast_to(np.asarray(q_terms), (H,))
-    pt_terms = np.broadcast_to(np.asarray(p_terms), (H,))
+    p_f16 = isinstance(p_terms, str)
+    if p_f16 and p_terms != "f16":
+        raise ValueError(p_terms)
+    pt_terms = None if p_f16 else np.broadcast_to(np.asarray(p_terms), (H,))
     out = np.zeros((n, H, d), dtype=np.float64)
     nv = ring.n_valid
     log2e = 1.0 / math.log(2.0)
@@ -155,9 +161,13 @@ def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
             O *= alpha[:, None]
             ell *= alpha
             p = np.exp2(x - m[:, None] + p_shift).astype(np.float32)
-            ps = sum(_split_terms(p, int(pt_terms[h])))
-            O += ps @ vc[j0:j0 + tile]
-            ell += ps.sum(axis=1)
+            if p_f16:
+                O += p.astype(np.float16).astype(np.float64) @ vc[j0:j0 + tile]
+                ell += p.astype(np.float64).sum(axis=1)
+            else:
+                ps = sum(_split_terms(p, int(pt_terms[h])))
+                O += ps @ vc[j0:j0 + tile]
+                ell += ps.sum(axis=1)
         out[:, h, :] = np.where(ell[:, None] > 0, O / np.maximum(ell, 1e-300)[:, None], 0.0) \
             * float(ring.scale_v[h])
     return out

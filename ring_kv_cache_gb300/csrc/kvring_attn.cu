@@ -9,29 +9,30 @@
 // over the filled slots j, Kdeq = code * scale_k[h], Vdeq = code * scale_v[h].
 //
 // CTA = one 128-query tile x one head x one range of key/value tiles
-// (split-KV).  Ten warps:
-//   warps 0-7  Softmax: query row r = TMEM lane r is shared by two threads
-//              (warps 0-3 own S columns [0, 64) and O columns [0, d/2);
-//              warps 4-7 the other halves), which exchange row maxima
-//              through shared memory.  Online softmax in log2 units with a
-//              lazily raised running maximum; probabilities carry 2^7 and
-//              are split into 1-2 E4M3 terms (the residual in f16x2) that are
-//              written back into TMEM over the S columns just read; O is
-//              rescaled in TMEM when the maximum rises by more than 1.5 (log2
-//              units).  Epilogue: O / l, split partials and their merge.
-//   warp 8     Copy producer: the query tile's FP8 terms (one bulk copy of
-//              the images k_attn_prep wrote), then K and V tiles [128 slots][d]
-//              by TMA into a 3-stage ring.
-//   warp 9     TMEM allocation and the single MMA-issuing thread:
-//              S = sum_t Q_t K^T (A and B from shared memory, K-major), then
-//              [O | l] += sum_t P_t [V | 1] with P read from TMEM and B =
-//              the V tile (MN-major, straight from its [slot][d] cache layout)
-//              extended by a 16-column block of E4M3 ones, so the softmax
-//              normaliser l is summed by the same MMA from exactly the FP8
-//              values that multiply V.
+// (split-KV).  Twenty warps:
+//   warps 0-15  Softmax: query row r = TMEM lane r is shared by four threads
+//               (column quarter cq = warp / 4 owns S columns [32 cq, 32 cq + 32)
+//               and O columns [cq d/4, (cq + 1) d/4)), which exchange row maxima
+//               through shared memory.  Online softmax in log2 units with a
+//               lazily raised running maximum; probabilities carry 2^7 and
+//               are written back into TMEM as f16 over the S columns just read;
+//               each thread sums its fp32 probabilities into a partial
+//               normaliser in registers.  O is rescaled in TMEM when the
+//               maximum rises by more than 1.5 (log2 units).  Epilogue: O / l,
+//               split partials and their merge.
+//   warp 16     Copy producer: the query tile's FP8 terms (one bulk copy of
+//               the images k_attn_prep wrote), then K and V tiles [128 slots][d]
+//               by TMA into a 3-stage ring.
+//   warp 17     TMEM allocation and the single MMA-issuing thread:
+//               S = sum_t Q_t K^T (kind::f8f6f4, A and B from shared memory,
+//               K-major), then O += P Vh (kind::f16, P read from TMEM, B = the
+//               f16 copy of the V tile, MN-major).
+//   warps 18-19 Value converters: each landed E4M3 V tile is widened, exactly,
+//               into one of two f16 tiles (128B-swizzled MN-major atoms of 64
+//               values), which frees the E4M3 stage for the next copy.
 // S is double-buffered in TMEM, so S(j+1) is computed while the softmax works
-// on S(j).  P(j) overwrites S(j)'s columns; the MMAs of one CTA run in issue
-// order, so QK(j+2) (into the same columns) always follows PV(j).
+// on S(j).  P(j) overwrites S(j)'s first 64 columns; the MMAs of one CTA run
+// in issue order, so QK(j+2) (into the same columns) always follows PV(j).
 //
 // k_attn_prep runs first, once per (query tile, head): RoPE of the queries in
 // fp32, a per-row scale 448/amax(row), the split into 3 E4M3 terms written
@@ -40,10 +41,10 @@
 // kernel is launched as a programmatic dependent of the prep kernel, so its
 // set-up and first key/value copies overlap the prep.
 //
-// Precision level per query tile (from the tile's amax, the head's
-// key range 448*scale_k and value range 448*scale_v): level 1 = 1 Q term +
-// 1 P term, level 2 = 2 + 2, level 3 = 3 + 2.  Extra terms are residuals at
-// the same scale, accumulated into the same TMEM accumulator.
+// Precision level per query tile (from the tile's amax and the head's key
+// range 448*scale_k and value range 448*scale_v): the number of E4M3 terms of
+// the queries, 1, 2 or 3.  Extra terms are residuals at the same scale,
+// accumulated into the same TMEM accumulator.  Probabilities are always f16.
 //
 // Every wait is bounded (about a second of wall time); a wait that gives up
 // sets KVRING_DEVERR_TIMEOUT in the ring's error word, the CTA drains its
@@ -59,21 +60,24 @@ constexpr int kStages = 3;
 constexpr int kPrepThreads = 256;
 constexpr int kPrepSplit = 4;           // prep CTAs per query tile (32 rows each)
 constexpr int kSoftmaxThreads = 512;    // 16 warps: four threads per query row
-constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kCvtThreads = 64;         // 2 value-converter warps
+constexpr int kThreads = kSoftmaxThreads + 64 + kCvtThreads;
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;
+constexpr int kWarpCvt = 18;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 // Probabilities carry a factor 2^kPShift relative to the running maximum,
 // which is raised only when a tile's maximum exceeds it by more than kTau:
-// the largest probability is 2^(kPShift + kTau) = 2^8.5 < 448 (E4M3 max).
+// the largest probability is 2^(kPShift + kTau) = 2^8.5, well inside f16.
 constexpr float kTau = 1.5f;
 constexpr float kPShift = 7.0f;
 // Level rule: with L = max|q| * max|k| over the tile (rotated query units
-// times 448 * scale_k) and V = 448 * scale_v, level 1 only when both are
-// small (one FP8 term of P errs by up to 2^-4 of |v|), level 2 up to L = 64,
-// level 3 beyond.  Measured against the float64 reference on the seeded
-// workloads: level 1 errs by 2-6e-2 at unit scale, level 2 by about 1e-3.
+// times 448 * scale_k) and V = 448 * scale_v, level 1 (one E4M3 query term,
+// relative error up to 2^-4, so logits off by up to L/16) only when both are
+// small, level 2 up to L = 64, level 3 beyond.  Measured against the float64
+// reference on the seeded workloads: level 1 errs by 2e-2 at unit scale,
+// level 2 by about 1e-3.
 constexpr float kLevel1MaxL = 4.0f;
 constexpr float kLevel1MaxV = 0.5f;
 constexpr float kLevel2MaxL = 64.0f;
@@ -81,12 +85,14 @@ constexpr float kLevel2MaxL = 64.0f;
 template <int D>
 struct Layout {
   static constexpr int kQTile = kTile * D;      // one Q term tile (bytes)
-  static constexpr int kKVTile = kTile * D;
+  static constexpr int kKVTile = kTile * D;     // one E4M3 K or V tile
+  static constexpr int kVhTile = 2 * kTile * D; // one f16 V tile
+  static constexpr int kVhAtom = kTile * 128;   // 64 f16 columns x 128 rows
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 3 * kQTile;
   static constexpr int kV = kK + kStages * kKVTile;
-  static constexpr int kOnes = kV + kStages * kKVTile;  // 128 x 128 bytes of E4M3 1.0
-  static constexpr int kXch = kOnes + kTile * kTile;    // float [2 parity][4 column quarters][128 rows]
+  static constexpr int kVh = kV + kStages * kKVTile;
+  static constexpr int kXch = kVh + 2 * kVhTile;        // float [2 parity][4 column quarters][128 rows]
   static constexpr int kBars = kXch + 2 * 4 * kTile * 4;
   // barrier slots (8 bytes each)
   static constexpr int kBarKvFull = 0;
@@ -94,16 +100,17 @@ struct Layout {
   static constexpr int kBarSFull = 2 * kStages;
   static constexpr int kBarPFull = 2 * kStages + 2;
   static constexpr int kBarPvDone = 2 * kStages + 4;
-  static constexpr int kBarMmaDone = 2 * kStages + 6;
-  static constexpr int kBarQFull = 2 * kStages + 7;
-  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kBarVhFull = 2 * kStages + 6;
+  static constexpr int kBarMmaDone = 2 * kStages + 8;
+  static constexpr int kBarQFull = 2 * kStages + 9;
+  static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 64;
-  static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code
+  static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code of the E4M3 tiles
+  static_assert(kVh % 1024 == 0, "128B-swizzled atoms need 1024-byte alignment");
   // TMEM columns
-  static constexpr uint32_t kColS = 0;        // two 128-column S buffers (P overwrites)
-  static constexpr uint32_t kColO = 256;      // D columns of O, then 16 of l
-  static constexpr uint32_t kColL = 256 + D;
+  static constexpr uint32_t kColS = 0;        // two 128-column S buffers (P overwrites 64)
+  static constexpr uint32_t kColO = 256;      // D columns of O
 };
 
 struct Misc {
@@ -130,11 +137,6 @@ struct AttnParams {
 __device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 __device__ __forceinline__ void sync_rowgroup(int quarter) {
   asm volatile("bar.sync %0, 128;" ::"r"(2 + quarter) : "memory");
-}
-
-// Four fp32 values to four E4M3 codes (first value in the low byte).
-__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
-  return (uint32_t)f32x2_to_e4m3x2(a, b) | ((uint32_t)f32x2_to_e4m3x2(c, d) << 16);
 }
 
 // Query preparation, one CTA per 32 rows of a (query tile, head), 256
@@ -251,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // copies at once; they do not depend on the query preparation.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKvFull + s), 1);
-      mbar_init(bar(L::kBarKvEmpty + s), 1);
+      // freed by the QK commit and by every converter thread
+      mbar_init(bar(L::kBarKvEmpty + s), 1 + kCvtThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kBarSFull + b), 1);
       mbar_init(bar(L::kBarPFull + b), kSoftmaxThreads);
       mbar_init(bar(L::kBarPvDone + b), 1);
+      mbar_init(bar(L::kBarVhFull + b), kCvtThreads);
     }
     mbar_init(bar(L::kBarMmaDone), 1);
     mbar_init(bar(L::kBarQFull), 1);
@@ -274,11 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
-  }
-  {  // all-ones block that extends V for the normaliser (E4M3 1.0 = 0x38)
-    uint4* ones = reinterpret_cast<uint4*>(sm + L::kOnes);
-    for (int i = threadIdx.x; i < kTile * kTile / 16; i += kThreads)
-      ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
   }
   // Everything below reads what k_attn_prep wrote.
   griddep_wait();
@@ -298,19 +297,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       misc->level = level;
       if (split == 0) r.levels[unit] = level;
-      mbar_arrive_expect_tx(bar(L::kBarQFull), (uint32_t)(level * L::kQTile));
-      for (int t = 0; t < level; ++t)
-        bulk_load(sbase + L::kQ + t * L::kQTile, r.qprep + (unit * 3 + t) * L::kQTile, L::kQTile, bar(L::kBarQFull));
+      if (ntiles > 0) {   // a CTA without key/value tiles needs no queries
+        mbar_arrive_expect_tx(bar(L::kBarQFull), (uint32_t)(level * L::kQTile));
+        for (int t = 0; t < level; ++t)
+          bulk_load(sbase + L::kQ + t * L::kQTile, r.qprep + (unit * 3 + t) * L::kQTile, L::kQTile, bar(L::kBarQFull));
+      }
     }
   }
-  fence_proxy_async_smem();  // the all-ones block
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-  const int level = misc->level;
-  const int n_qterms = level;
-  const int n_pterms = level >= 2 ? 2 : 1;
+  const int n_qterms = misc->level;
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer
@@ -327,29 +325,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
       }
       // Drain: every issued copy must land before the CTA may exit.
-      for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j) {
-        volatile int no_abort = 0;
+      volatile int no_abort = 0;
+      for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
         mbar_wait_bounded(bar(L::kBarKvFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
-      }
+      if (ntiles > 0) mbar_wait_bounded(bar(L::kBarQFull), 0, &no_abort, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
-      constexpr uint32_t idesc_pv = idesc_e4m3(128, D + 16, true);
+      constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
       // Descriptors are built once; per MMA only the low word (start address
       // in 16-byte units) moves: +2 per 32-byte k-step of a K-major tile,
-      // +32*D/16 per 32-row k-step of the MN-major V tile.
+      // +16 rows x 128 bytes per 16-slot k-step of the f16 V tile.
       const uint64_t dq = smem_desc(sbase + L::kQ, 16, 8 * D, L::kSwz);
       const uint64_t dk = smem_desc(sbase + L::kK, 16, 8 * D, L::kSwz);
       const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, kq_hi = (uint32_t)(dq >> 32);
-      // V of stage s: start address + s tiles, and the leading byte offset
-      // (to the ones block, in bits 16..29) s tiles shorter.
-      const uint64_t dv = smem_desc(sbase + L::kV, (uint32_t)(L::kOnes - L::kV), 8 * D, L::kSwz);
-      const uint32_t v_lo0 = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
-      constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4;
-      constexpr uint32_t kVStageStep = kKVStep - (kKVStep << 16);
+      // f16 V: 128B-swizzled MN-major atoms of 64 columns x 8 rows (1024 B
+      // apart along the slots); the second 64 columns one atom column further
+      const uint64_t dv = smem_desc(sbase + L::kVh, (uint32_t)L::kVhAtom, 1024, 2u);
+      const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
+      constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4, kVhStep = L::kVhTile >> 4;
       // S(j) into TMEM buffer j&1.  Its previous user, P(j-2), was consumed
       // by PV(j-2), issued earlier by this thread: in-order execution.
       auto issue_qk = [&](int j) -> bool {
@@ -367,26 +364,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(bar(L::kBarSFull + b));
+        mma_commit(bar(L::kBarKvEmpty + s));   // the K stage is read
         return true;
       };
       bool ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs) && issue_qk(0);
       for (int j = 0; ok && j < ntiles; ++j) {
         if (j + 1 < ntiles && !issue_qk(j + 1)) break;
-        const int s = j % kStages, b = j & 1;
+        const int b = j & 1;
         if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
+        if (!mbar_wait_bounded(bar(L::kBarVhFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
         tc_fence_after();
-        const uint32_t vl = v_lo0 + (uint32_t)s * kVStageStep;
+        const uint32_t vl = v_lo + (uint32_t)b * kVhStep;
         const uint32_t pa = tmem + L::kColS + b * 128;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (t < n_pterms) {
-#pragma unroll
-            for (int kk = 0; kk < kTile / 32; ++kk)
-              mma_e4m3_ts_w(tmem + L::kColO, pa + t * 32 + kk * 8, vl + kk * (32 * D / 16), v_hi, idesc_pv,
-                            (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(bar(L::kBarKvEmpty + s));
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_f16_ts_w(tmem + L::kColO, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kBarPvDone + b));
       }
     }
@@ -396,25 +389,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(bar(L::kBarMmaDone), 0, &no_abort, kWaitLimitNs);
     }
     __syncwarp();
+  } else if (warp >= kWarpCvt) {
+    // ------------------------------------------------- value converters
+    // E4M3 V tile [128 slots][d] (TMA image, 128B or 64B swizzle) -> f16 tile
+    // of d/64 atoms [128 slots][64 values] (128B swizzle).  Task i: slot
+    // i / CPR, 16-value chunk i % CPR; each converter thread takes every
+    // 64th task, a batch of loads first.
+    constexpr int CPR = D / 16;
+    constexpr int PER = kTile * CPR / kCvtThreads;   // 16 (d = 128) or 8
+    constexpr int BATCH = PER < 8 ? PER : 8;
+    const int ct = threadIdx.x - kWarpCvt * 32;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages, b = j & 1;
+      bool ok = mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs);
+      if (ok && j >= 2) ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      const uint8_t* src = sm + L::kV + s * L::kKVTile;
+      uint8_t* dst = sm + L::kVh + b * L::kVhTile;
+#pragma unroll
+      for (int n0 = 0; n0 < PER; n0 += BATCH) {
+        uint4 w[BATCH];
+#pragma unroll
+        for (int n = 0; n < BATCH; ++n) {
+          const int i = ct + (n0 + n) * kCvtThreads;
+          w[n] = *reinterpret_cast<const uint4*>(src + swz_offset(i / CPR, i % CPR, D));
+        }
+#pragma unroll
+        for (int n = 0; n < BATCH; ++n) {
+          const int i = ct + (n0 + n) * kCvtThreads;
+          const int row = i / CPR, c = i % CPR;
+          const uint32_t wi[4] = {w[n].x, w[n].y, w[n].z, w[n].w};
+          uint32_t hv[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hv[2 * e] = e4m3x2_to_f16x2((uint16_t)(wi[e] & 0xFFFFu));
+            hv[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(wi[e] >> 16));
+          }
+          uint8_t* atom = dst + (c >> 2) * L::kVhAtom;
+          *reinterpret_cast<uint4*>(atom + swz_offset(row, 2 * (c & 3), 128)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(atom + swz_offset(row, 2 * (c & 3) + 1, 128)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        }
+      }
+      fence_proxy_async_smem();  // generic writes -> tensor-core reads
+      mbar_arrive(bar(L::kBarVhFull + b));
+      mbar_arrive(bar(L::kBarKvEmpty + s));
+    }
   } else {
     // ----------------------------------------------------------- softmax
     // thread = (row, column quarter cq): S columns [32 cq, 32 cq + 32),
-    // O columns [QD cq, QD cq + QD), P bytes of its 32 slots.
+    // O columns [QD cq, QD cq + QD), P columns [16 cq, 16 cq + 16).
     const int row = threadIdx.x & (kTile - 1);
     const int cq = threadIdx.x >> 7;
     const int quarter = warp & 3;
     const float f_row = __ldcg(r.qrowf + unit * 2 * kTile + row);
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_run = -INFINITY;
+    float ell = 0.f;            // this thread's part of the normaliser
+    // Once a wait has given up (ok false), the loop still runs to the end so
+    // that every softmax thread meets every named barrier; only the TMEM
+    // work is skipped.
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
-      ok = mbar_wait_bounded(bar(L::kBarSFull + b), (j >> 1) & 1, abort, kWaitLimitNs);
-      if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-      tc_fence_after();
+      ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait_bounded(bar(L::kBarSFull + b), (j >> 1) & 1, abort, kWaitLimitNs));
       uint32_t sr[32];
-      tmem_ld32(trow + L::kColS + b * 128 + cq * 32, sr);
-      tmem_wait_ld();
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(trow + L::kColS + b * 128 + cq * 32, sr);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sr[c] = 0u;
+      }
       // mask slots past the fill level (only the ring's last tile)
       const int valid = nvalid - (tile0 + j) * kTile - cq * 32;
       if (valid < 32) {
@@ -439,10 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tmax = smax * f_row;          // f_row > 0
       const bool need = tmax > m_run + kTau;
       const float m_new = need ? tmax : m_run;
-      if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
-        // O and l hold tiles < j: wait for PV(j-1), then rescale this quarter
-        ok = mbar_wait_bounded(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, kWaitLimitNs);
-        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+      const bool rescale = j > 0 && __any_sync(0xFFFFFFFFu, need);
+      if (rescale)  // O holds tiles < j: wait for PV(j-1)
+        ok = __all_sync(0xFFFFFFFFu,
+                        ok && mbar_wait_bounded(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, kWaitLimitNs));
+      if (rescale && ok) {
         tc_fence_after();
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
         uint32_t rr[QD];
@@ -451,60 +498,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < QD; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
         tmem_st_n<QD>(trow + L::kColO + cq * QD, rr);
-        if (cq == 0) {
-          const uint32_t lv = tmem_ld1(trow + L::kColL);
-          tmem_wait_ld();
-          tmem_st1(trow + L::kColL, __float_as_uint(__uint_as_float(lv) * alpha));
-        }
+        ell *= alpha;
       }
       m_run = m_new;
-      // probabilities 2^(x - m + 7) as 1-2 E4M3 terms, written over S(j):
-      // term t, slots [32 cq, 32 cq + 32) -> columns 32 t + 8 cq + [0, 8)
+      // probabilities 2^(x - m + 7): f16 pairs over S(j), slots
+      // [32 cq, 32 cq + 32) -> columns 16 cq + [0, 16), the lower slot in
+      // the low half; the normaliser takes the fp32 values
       const float moff = kPShift - m_run;
-      // Phases, each over all 32 columns, so that every step has 16-32
-      // independent operations in flight.
-      uint32_t w1[8], w2[8];
       float e[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(sr[i]), f_row, moff));
-      if (n_pterms > 1) {
-        // two terms in f16x2: P1 = the value rounded to 4 significant bits
-        // (Veltkamp split on the FMA pipe; exact in E4M3), P2 = the exact
-        // residual
-        uint32_t hv[16], av[16];
+      uint32_t hv[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[2 * i], e[2 * i + 1]);
+      for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[2 * i], e[2 * i + 1]);
+      if (ok) tmem_st_n<16>(trow + L::kColS + b * 128 + cq * 16, hv);
+      float s8[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) av[i] = f16x2_hi4(hv[i]);
-        uint32_t c1[16], c2[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          c1[i] = f16x2_to_e4m3x2(av[i]);
-          c2[i] = f16x2_to_e4m3x2(hsub2_u32(hv[i], av[i]));
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          w1[c] = c1[2 * c] | (c1[2 * c + 1] << 16);
-          w2[c] = c2[2 * c] | (c2[2 * c + 1] << 16);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) w1[c] = pack4_e4m3(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
-      }
-      tmem_st_n<8>(trow + L::kColS + b * 128 + cq * 8, w1);
-      if (n_pterms > 1) tmem_st_n<8>(trow + L::kColS + b * 128 + 32 + cq * 8, w2);
+      for (int i = 0; i < 8; ++i) s8[i] = (e[4 * i] + e[4 * i + 1]) + (e[4 * i + 2] + e[4 * i + 3]);
+      ell += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + b));
     }
 
     // ---------------------------------------------------------- epilogue
+    // the row's normaliser: sum of its four threads' parts
+    {
+      float* xl = xch + (ntiles & 1) * 4 * kTile;
+      xl[cq * kTile + row] = ell;
+      sync_rowgroup(quarter);
+      ell = (xl[row] + xl[kTile + row]) + (xl[2 * kTile + row] + xl[3 * kTile + row]);
+    }
+    const float l = ell;
     float o[QD];
-    float l = 0.f;
     if (ok && ntiles > 0) {
       const int jl = ntiles - 1;
-      ok = mbar_wait_bounded(bar(L::kBarPvDone + (jl & 1)), (jl >> 1) & 1, abort, kWaitLimitNs);
-      ok = __all_sync(0xFFFFFFFFu, ok);
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + (jl & 1)), (jl >> 1) & 1, abort, kWaitLimitNs));
     }
     if (ok && ntiles > 0) {
       tc_fence_after();
@@ -513,16 +542,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < QD; ++i) o[i] = __uint_as_float(rr[i]);
-      l = __uint_as_float(tmem_ld1(trow + L::kColL));
-      tmem_wait_ld();
     } else {
 #pragma unroll
       for (int i = 0; i < QD; ++i) o[i] = 0.f;
     }
     // Normalised rows go to shared memory (the key/value stages are free:
-    // every copy landed and every MMA finished), fp32 [128][d + 4], then the
-    // whole tile is stored, or merged across splits, with coalesced 16-byte
-    // accesses.
+    // every copy landed, was converted and read by its MMAs), fp32
+    // [128][d + 4], then the whole tile is stored, or merged across splits,
+    // with coalesced 16-byte accesses.
     const float inv_l = l > 0.f ? 1.0f / l : 0.f;
     const float scale_v = r.scales[H + h];
     const bool single = prm.nsplit == 1;
@@ -530,12 +557,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int F4 = kTile * D / 4;         // float4 per tile
     constexpr int PER = F4 / kSoftmaxThreads; // float4 per thread
     float* stage = reinterpret_cast<float*>(sm + L::kK);
+    // per-row log2-sum-exp, in the exchange buffer the normaliser did not use
+    float* lse_row = xch + ((ntiles + 1) & 1) * 4 * kTile;
     {
       const float f = single ? inv_l * scale_v : inv_l;
       float4* srow = reinterpret_cast<float4*>(stage + row * SP + cq * QD);
 #pragma unroll
       for (int c = 0; c < QD / 4; ++c) srow[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
-      if (cq == 0) xch[row] = l > 0.f ? log2f(l) + m_run - kPShift : -INFINITY;
+      if (cq == 0) lse_row[row] = (ok && l > 0.f) ? log2f(l) + m_run - kPShift : -INFINITY;
     }
     sync_softmax();
     const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
@@ -563,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4* dst = reinterpret_cast<float4*>(r.part_o + pbase * kTile * D);
 #pragma unroll
       for (int i = 0; i < PER; ++i) __stcg(dst + threadIdx.x + i * kSoftmaxThreads, staged(threadIdx.x + i * kSoftmaxThreads));
-      if (threadIdx.x < kTile) __stcg(r.part_lse + pbase * kTile + threadIdx.x, xch[threadIdx.x]);
+      if (threadIdx.x < kTile) __stcg(r.part_lse + pbase * kTile + threadIdx.x, lse_row[threadIdx.x]);
       __threadfence();
       sync_softmax();
       if (threadIdx.x == 0) {

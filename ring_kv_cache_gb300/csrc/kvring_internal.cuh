@@ -306,6 +306,19 @@ __device__ __forceinline__ void mma_e4m3_w(uint32_t d_tmem, uint32_t a_lo, uint3
       "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(0), "r"(accumulate)
       : "memory");
 }
+// D (f32, TMEM) (+)= A (f16, TMEM, two values per 32-bit column, the lower
+// k index in the low half) x B (f16, shared memory descriptor).
+__device__ __forceinline__ void mma_f16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_e4m3_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -387,6 +400,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 // Instruction descriptor for kind::f8f6f4, E4M3 x E4M3 with fp32
 // accumulation; B either K-major (b_mn_major = false) or MN-major.
+// Instruction descriptor of kind::f16 with f16 A and B and an f32
+// accumulator (the same field layout as above; f16 is type code 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                   // D format: f32
+         | (0u << 7) | (0u << 10)                    // A, B: f16
+         | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+         | ((uint32_t)(N >> 3) << 17)                // N / 8
+         | ((uint32_t)(M >> 4) << 24);               // M / 16
+}
+
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major) {
   return (1u << 4)                                   // D format: f32
          | (0u << 7) | (0u << 10)                    // A, B: E4M3
