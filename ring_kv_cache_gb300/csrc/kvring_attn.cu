@@ -9,30 +9,33 @@
 // over the filled slots j, Kdeq = code * scale_k[h], Vdeq = code * scale_v[h].
 //
 // CTA = one 128-query tile x one head x one range of key/value tiles
-// (split-KV).  Twenty warps:
-//   warps 0-15  Softmax: query row r = TMEM lane r is shared by four threads
-//               (column quarter cq = warp / 4 owns S columns [32 cq, 32 cq + 32)
-//               and O columns [cq d/4, (cq + 1) d/4)), which exchange row maxima
-//               through shared memory.  Online softmax in log2 units with a
-//               lazily raised running maximum; probabilities carry 2^7 and
-//               are written back into TMEM as f16 over the S columns just read;
-//               each thread sums its fp32 probabilities into a partial
-//               normaliser in registers.  O is rescaled in TMEM when the
-//               maximum rises by more than 1.5 (log2 units).  Epilogue: O / l,
-//               split partials and their merge.
-//   warp 16     Copy producer: the query tile's FP8 terms (one bulk copy of
+// (split-KV).  Twelve warps:
+//   warps 0-7   Softmax, two groups of four warps that take the key/value
+//               tiles in turn (group g: tiles g, g + 2, ...), each with its own
+//               S buffer and O accumulator in TMEM, so one group's MMAs run
+//               while the other group exponentiates.  One thread per query
+//               row (row r = TMEM lane r) holds all 128 scores of its row: no
+//               exchange between threads.  Online softmax in log2 units with
+//               a lazily raised running maximum; probabilities carry 2^7 and
+//               are written back into TMEM as f16 over the S columns just
+//               read, and the thread sums its fp32 probabilities into the
+//               row's normaliser.  O is rescaled in TMEM when the maximum
+//               rises by more than 1.5 (log2 units).  Epilogue: the two
+//               groups' (m, l, O) merged, O / l, split partials and their merge.
+//   warp 8      Copy producer: the query tile's FP8 terms (one bulk copy of
 //               the images k_attn_prep wrote), then K and V tiles [128 slots][d]
 //               by TMA into a 3-stage ring.
-//   warp 17     TMEM allocation and the single MMA-issuing thread:
+//   warp 9      TMEM allocation and the single MMA-issuing thread:
 //               S = sum_t Q_t K^T (kind::f8f6f4, A and B from shared memory,
-//               K-major), then O += P Vh (kind::f16, P read from TMEM, B = the
+//               K-major), then O_g += P Vh (kind::f16, P read from TMEM, B = the
 //               f16 copy of the V tile, MN-major).
-//   warps 18-19 Value converters: each landed E4M3 V tile is widened, exactly,
+//   warps 10-11 Value converters: each landed E4M3 V tile is widened, exactly,
 //               into one of two f16 tiles (128B-swizzled MN-major atoms of 64
 //               values), which frees the E4M3 stage for the next copy.
-// S is double-buffered in TMEM, so S(j+1) is computed while the softmax works
-// on S(j).  P(j) overwrites S(j)'s first 64 columns; the MMAs of one CTA run
-// in issue order, so QK(j+2) (into the same columns) always follows PV(j).
+// MMA issue order: QK(0), QK(1), then per tile j: PV(j) and QK(j + 2) into the
+// S buffer PV(j) has just read.  MMAs of one thread complete in issue order,
+// so the arrival of S(j) also means PV(j - 2) is done: group g may rescale
+// O_g as soon as S(j) is there.
 //
 // k_attn_prep runs first, once per (query tile, head): RoPE of the queries in
 // fp32, a per-row scale 448/amax(row), the split into 3 E4M3 terms written
@@ -59,12 +62,13 @@ namespace {
 constexpr int kStages = 3;
 constexpr int kPrepThreads = 256;
 constexpr int kPrepSplit = 4;           // prep CTAs per query tile (32 rows each)
-constexpr int kSoftmaxThreads = 512;    // 16 warps: four threads per query row
+constexpr int kSoftmaxThreads = 256;    // 2 groups x 4 warps, one thread per query row
+constexpr int kGroupThreads = 128;
 constexpr int kCvtThreads = 64;         // 2 value-converter warps
 constexpr int kThreads = kSoftmaxThreads + 64 + kCvtThreads;
-constexpr int kWarpTma = 16;
-constexpr int kWarpMma = 17;
-constexpr int kWarpCvt = 18;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr int kWarpCvt = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 // Probabilities carry a factor 2^kPShift relative to the running maximum,
@@ -92,8 +96,8 @@ struct Layout {
   static constexpr int kK = kQ + 3 * kQTile;
   static constexpr int kV = kK + kStages * kKVTile;
   static constexpr int kVh = kV + kStages * kKVTile;
-  static constexpr int kXch = kVh + 2 * kVhTile;        // float [2 parity][4 column quarters][128 rows]
-  static constexpr int kBars = kXch + 2 * 4 * kTile * 4;
+  static constexpr int kEpi = kVh + 2 * kVhTile;        // float m[2][128], l[2][128], lse[128]
+  static constexpr int kBars = kEpi + 5 * kTile * 4;
   // barrier slots (8 bytes each)
   static constexpr int kBarKvFull = 0;
   static constexpr int kBarKvEmpty = kStages;
@@ -109,8 +113,8 @@ struct Layout {
   static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code of the E4M3 tiles
   static_assert(kVh % 1024 == 0, "128B-swizzled atoms need 1024-byte alignment");
   // TMEM columns
-  static constexpr uint32_t kColS = 0;        // two 128-column S buffers (P overwrites 64)
-  static constexpr uint32_t kColO = 256;      // D columns of O
+  static constexpr uint32_t kColS = 0;        // S buffer of group g at 128 g (P overwrites 64 columns)
+  static constexpr uint32_t kColO = 256;      // O accumulator of group g at 256 + 128 g (D columns)
 };
 
 struct Misc {
@@ -132,12 +136,8 @@ struct AttnParams {
   int forced_level;
 };
 
-// Named barriers: 0 = __syncthreads, 1 = the 512 softmax threads,
-// 2..5 = the four warps that share a group of 32 query rows.
-__device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
-__device__ __forceinline__ void sync_rowgroup(int quarter) {
-  asm volatile("bar.sync %0, 128;" ::"r"(2 + quarter) : "memory");
-}
+// Named barriers: 0 = __syncthreads, 1 = the 256 softmax threads.
+__device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Query preparation, one CTA per 32 rows of a (query tile, head), 256
 // threads.  Chunk task k = i * 256 + tid: row k / CPR of the block, chunk
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   Misc* misc = reinterpret_cast<Misc*>(sm + L::kMisc);
-  float* xch = reinterpret_cast<float*>(sm + L::kXch);
+  float* epi = reinterpret_cast<float*>(sm + L::kEpi);
   volatile int* abort = &misc->abort;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBars + 8u * (uint32_t)i; };
 
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kBarSFull + b), 1);
-      mbar_init(bar(L::kBarPFull + b), kSoftmaxThreads);
+      mbar_init(bar(L::kBarPFull + b), kGroupThreads);
       mbar_init(bar(L::kBarPvDone + b), 1);
       mbar_init(bar(L::kBarVhFull + b), kCvtThreads);
     }
@@ -367,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(L::kBarKvEmpty + s));   // the K stage is read
         return true;
       };
-      bool ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs) && issue_qk(0);
+      bool ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs) && issue_qk(0) &&
+                (ntiles < 2 || issue_qk(1));
       for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 1 < ntiles && !issue_qk(j + 1)) break;
         const int b = j & 1;
         if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
         if (!mbar_wait_bounded(bar(L::kBarVhFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
@@ -378,9 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pa = tmem + L::kColS + b * 128;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_f16_ts_w(tmem + L::kColO, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
+                       (j > 1 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kBarPvDone + b));
+        if (j + 2 < ntiles && !issue_qk(j + 2)) break;
       }
     }
     if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
@@ -436,120 +437,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- softmax
-    // thread = (row, column quarter cq): S columns [32 cq, 32 cq + 32),
-    // O columns [QD cq, QD cq + QD), P columns [16 cq, 16 cq + 16).
+    // thread = (group g, row): S columns [0, 128) of buffer g, P columns
+    // [0, 64) of it, O_g columns [0, d).
+    const int g = warp >> 2;
     const int row = threadIdx.x & (kTile - 1);
-    const int cq = threadIdx.x >> 7;
     const int quarter = warp & 3;
     const float f_row = __ldcg(r.qrowf + unit * 2 * kTile + row);
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = trow + L::kColS + g * 128, tO = trow + L::kColO + g * 128;
     float m_run = -INFINITY;
-    float ell = 0.f;            // this thread's part of the normaliser
-    // Once a wait has given up (ok false), the loop still runs to the end so
-    // that every softmax thread meets every named barrier; only the TMEM
-    // work is skipped.
+    float ell = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait_bounded(bar(L::kBarSFull + b), (j >> 1) & 1, abort, kWaitLimitNs));
-      uint32_t sr[32];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(trow + L::kColS + b * 128 + cq * 32, sr);
-        tmem_wait_ld();
-      } else {
+    for (int j = g; j < ntiles; j += 2) {
+      const int n = j >> 1;
+      ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait_bounded(bar(L::kBarSFull + g), n & 1, abort, kWaitLimitNs));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sr[c] = 0u;
-      }
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+      tmem_wait_ld();
       // mask slots past the fill level (only the ring's last tile)
-      const int valid = nvalid - (tile0 + j) * kTile - cq * 32;
-      if (valid < 32) {
+      const int valid = nvalid - (tile0 + j) * kTile;
+      if (valid < kTile) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
+        for (int c = 0; c < 128; ++c)
           if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
       }
-      // row maximum of this thread's 32 columns as a shallow tree
-      float m11[11];
+      // row maximum: eight running three-way maxima, then a small tree
+      float mx[8];
 #pragma unroll
-      for (int i = 0; i < 10; ++i)
-        m11[i] = fmax3(__uint_as_float(sr[3 * i]), __uint_as_float(sr[3 * i + 1]), __uint_as_float(sr[3 * i + 2]));
-      m11[10] = fmaxf(__uint_as_float(sr[30]), __uint_as_float(sr[31]));
-      float smax = fmax3(fmax3(m11[0], m11[1], m11[2]), fmax3(m11[3], m11[4], m11[5]),
-                         fmax3(m11[6], m11[7], fmax3(m11[8], m11[9], m11[10])));
-      float* xj = xch + (j & 1) * 4 * kTile;
-      xj[cq * kTile + row] = smax;
-      // after this barrier all four threads of the row have read their S
-      // columns, so P may overwrite any of them
-      sync_rowgroup(quarter);
-      smax = fmaxf(fmaxf(xj[row], xj[kTile + row]), fmaxf(xj[2 * kTile + row], xj[3 * kTile + row]));
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+#pragma unroll
+      for (int i = 1; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mx[k] = fmax3(mx[k], __uint_as_float(sr[16 * i + 2 * k]), __uint_as_float(sr[16 * i + 2 * k + 1]));
+      const float smax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
       const float tmax = smax * f_row;          // f_row > 0
       const bool need = tmax > m_run + kTau;
       const float m_new = need ? tmax : m_run;
-      const bool rescale = j > 0 && __any_sync(0xFFFFFFFFu, need);
-      if (rescale)  // O holds tiles < j: wait for PV(j-1)
-        ok = __all_sync(0xFFFFFFFFu,
-                        ok && mbar_wait_bounded(bar(L::kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, kWaitLimitNs));
-      if (rescale && ok) {
-        tc_fence_after();
+      if (j > 1 && __any_sync(0xFFFFFFFFu, need)) {
+        // O_g holds this group's earlier tiles, complete (S(j) was committed
+        // after PV(j - 2)): rescale it in chunks of 16 columns (the row's
+        // scores stay in registers meanwhile)
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-        uint32_t rr[QD];
-        tmem_ld_n<QD>(trow + L::kColO + cq * QD, rr);
-        tmem_wait_ld();
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t rr[16];
+          tmem_ld_n<16>(tO + 16 * c, rr);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < QD; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-        tmem_st_n<QD>(trow + L::kColO + cq * QD, rr);
+          for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          tmem_st16(tO + 16 * c, rr);
+        }
         ell *= alpha;
       }
       m_run = m_new;
-      // probabilities 2^(x - m + 7): f16 pairs over S(j), slots
-      // [32 cq, 32 cq + 32) -> columns 16 cq + [0, 16), the lower slot in
-      // the low half; the normaliser takes the fp32 values
+      // probabilities 2^(x - m + 7): f16 pairs over S(j), slots 32 c + [0, 32)
+      // -> columns 16 c + [0, 16), the lower slot in the low half; the
+      // normaliser takes the fp32 values
       const float moff = kPShift - m_run;
-      float e[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(sr[i]), f_row, moff));
-      uint32_t hv[16];
+      for (int c = 0; c < 4; ++c) {
+        float e[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[2 * i], e[2 * i + 1]);
-      if (ok) tmem_st_n<16>(trow + L::kColS + b * 128 + cq * 16, hv);
-      float s8[8];
+        for (int i = 0; i < 32; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(sr[32 * c + i]), f_row, moff));
+        uint32_t hv[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s8[i] = (e[4 * i] + e[4 * i + 1]) + (e[4 * i + 2] + e[4 * i + 3]);
-      ell += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[2 * i], e[2 * i + 1]);
+        tmem_st16(tS + 16 * c, hv);
+        float s8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s8[i] = (e[4 * i] + e[4 * i + 1]) + (e[4 * i + 2] + e[4 * i + 3]);
+        ell += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+      }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::kBarPFull + b));
+      mbar_arrive(bar(L::kBarPFull + g));
     }
 
     // ---------------------------------------------------------- epilogue
-    // the row's normaliser: sum of its four threads' parts
-    {
-      float* xl = xch + (ntiles & 1) * 4 * kTile;
-      xl[cq * kTile + row] = ell;
-      sync_rowgroup(quarter);
-      ell = (xl[row] + xl[kTile + row]) + (xl[2 * kTile + row] + xl[3 * kTile + row]);
-    }
-    const float l = ell;
-    float o[QD];
-    if (ok && ntiles > 0) {
-      const int jl = ntiles - 1;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + (jl & 1)), (jl >> 1) & 1, abort, kWaitLimitNs));
-    }
-    if (ok && ntiles > 0) {
-      tc_fence_after();
-      uint32_t rr[QD];
-      tmem_ld_n<QD>(trow + L::kColO + cq * QD, rr);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < QD; ++i) o[i] = __uint_as_float(rr[i]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < QD; ++i) o[i] = 0.f;
-    }
+    // merge the two groups: m = max(m_0, m_1), w_g = 2^(m_g - m),
+    // l = sum w_g l_g, O = sum w_g O_g.  After this barrier both groups are
+    // done with their loops, so each PV-done barrier is at most one phase
+    // short of the group's last PV.
+    float* em = epi;                 // [2][128]
+    float* el = epi + 2 * kTile;     // [2][128]
+    float* lse_row = epi + 4 * kTile;
+    em[g * kTile + row] = m_run;
+    el[g * kTile + row] = ell;
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    sync_softmax();
+    const float m0 = em[row], m1 = em[kTile + row];
+    const float m = fmaxf(m0, m1);
+    const float w0 = m0 > -INFINITY ? ex2_approx(m0 - m) : 0.f;
+    const float w1 = m1 > -INFINITY ? ex2_approx(m1 - m) : 0.f;
+    const float l = w0 * el[row] + w1 * el[kTile + row];
+    // the last tile of each group
+    const int jl0 = ntiles > 0 ? ((ntiles - 1) & ~1) : -1;
+    const int jl1 = ntiles > 1 ? (((ntiles - 2) & ~1) + 1) : -1;
+    if (ok && jl0 >= 0)
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + 0), (jl0 >> 1) & 1, abort, kWaitLimitNs));
+    if (ok && jl1 >= 0)
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + 1), (jl1 >> 1) & 1, abort, kWaitLimitNs));
     // Normalised rows go to shared memory (the key/value stages are free:
     // every copy landed, was converted and read by its MMAs), fp32
-    // [128][d + 4], then the whole tile is stored, or merged across splits,
-    // with coalesced 16-byte accesses.
+    // [128][d + 4]: group g's thread of the row writes columns [g d/2, (g+1) d/2)
+    // from both accumulators.  Then the whole tile is stored, or merged
+    // across splits, with coalesced 16-byte accesses.
     const float inv_l = l > 0.f ? 1.0f / l : 0.f;
     const float scale_v = r.scales[H + h];
     const bool single = prm.nsplit == 1;
@@ -557,14 +553,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int F4 = kTile * D / 4;         // float4 per tile
     constexpr int PER = F4 / kSoftmaxThreads; // float4 per thread
     float* stage = reinterpret_cast<float*>(sm + L::kK);
-    // per-row log2-sum-exp, in the exchange buffer the normaliser did not use
-    float* lse_row = xch + ((ntiles + 1) & 1) * 4 * kTile;
     {
       const float f = single ? inv_l * scale_v : inv_l;
-      float4* srow = reinterpret_cast<float4*>(stage + row * SP + cq * QD);
+      const float a0 = w0 * f, a1 = w1 * f;
 #pragma unroll
-      for (int c = 0; c < QD / 4; ++c) srow[c] = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
-      if (cq == 0) lse_row[row] = (ok && l > 0.f) ? log2f(l) + m_run - kPShift : -INFINITY;
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t col = g * (D / 2) + 32 * c;
+        uint32_t r0[32], r1[32];
+        if (ok && jl0 >= 0) tmem_ld32(trow + L::kColO + col, r0);
+        if (ok && jl1 >= 0) tmem_ld32(trow + L::kColO + 128 + col, r1);
+        tmem_wait_ld();
+        float4* srow = reinterpret_cast<float4*>(stage + row * SP + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x0 = (ok && jl0 >= 0) ? __uint_as_float(r0[4 * i + k]) * a0 : 0.f;
+            const float x1 = (ok && jl1 >= 0) ? __uint_as_float(r1[4 * i + k]) * a1 : 0.f;
+            v[k] = x0 + x1;
+          }
+          srow[i] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+      }
+      if (g == 0) lse_row[row] = (ok && l > 0.f) ? log2f(l) + m - kPShift : -INFINITY;
     }
     sync_softmax();
     const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
@@ -624,19 +636,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s2 = 0; s2 < prm.nsplit; ++s2) {
-          // all of this split's loads in flight before any use
+          // a batch of this split's loads in flight before any use
           const float4* src = reinterpret_cast<const float4*>(
               r.part_o + (((size_t)s2 * r.qtiles_max + qt) * H + h) * kTile * D);
-          float4 v[PER];
+          constexpr int MB = PER < 8 ? PER : 8;
 #pragma unroll
-          for (int i = 0; i < PER; ++i) v[i] = __ldcg(src + threadIdx.x + i * kSoftmaxThreads);
+          for (int i0 = 0; i0 < PER; i0 += MB) {
+            float4 v[MB];
 #pragma unroll
-          for (int i = 0; i < PER; ++i) {
-            const float w = wts[s2 * kTile + (threadIdx.x + i * kSoftmaxThreads) / (D / 4)];
-            acc[i].x = fmaf(w, v[i].x, acc[i].x);
-            acc[i].y = fmaf(w, v[i].y, acc[i].y);
-            acc[i].z = fmaf(w, v[i].z, acc[i].z);
-            acc[i].w = fmaf(w, v[i].w, acc[i].w);
+            for (int i = 0; i < MB; ++i) v[i] = __ldcg(src + threadIdx.x + (i0 + i) * kSoftmaxThreads);
+#pragma unroll
+            for (int i = 0; i < MB; ++i) {
+              const float w = wts[s2 * kTile + (threadIdx.x + (i0 + i) * kSoftmaxThreads) / (D / 4)];
+              acc[i0 + i].x = fmaf(w, v[i].x, acc[i0 + i].x);
+              acc[i0 + i].y = fmaf(w, v[i].y, acc[i0 + i].y);
+              acc[i0 + i].z = fmaf(w, v[i].z, acc[i0 + i].z);
+              acc[i0 + i].w = fmaf(w, v[i].w, acc[i0 + i].w);
+            }
           }
         }
 #pragma unroll
