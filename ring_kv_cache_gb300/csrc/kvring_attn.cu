@@ -134,6 +134,7 @@ struct AttnParams {
   int nsplit;
   int tiles_per_split;
   int forced_level;
+  int cluster_merge;   // the splits of a query tile form one cluster (2..8 CTAs)
 };
 
 // Named barriers: 0 = __syncthreads, 1 = the 256 softmax threads.
@@ -598,6 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (single) {
 #pragma unroll
       for (int i = 0; i < PER; ++i) store_out(threadIdx.x + i * kSoftmaxThreads, staged(threadIdx.x + i * kSoftmaxThreads));
+    } else if (prm.cluster_merge) {
+      // the staged partial and its log2-sum-exp stay here; the cluster
+      // merges them after the role branches
     } else {
       // partial (normalised) tile and its per-row log2-sum-exp
       const size_t pbase = ((size_t)split * r.qtiles_max + qt) * H + h;
@@ -662,6 +666,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // ------------------------------------------------------ cluster merge
+  // The nsplit CTAs of this query tile form one cluster (rank = split).
+  // After the first cluster barrier every CTA's normalised partial and
+  // log2-sum-exp are staged in its shared memory; CTA `split` merges rows
+  // [split 128 / nsplit, (split + 1) 128 / nsplit) from all of them through
+  // distributed shared memory and stores the output rows.  The second
+  // barrier keeps every CTA's shared memory alive until its peers are done.
+  if (prm.cluster_merge) {
+    __syncwarp();
+    cluster_sync_all();
+    if (warp < kSoftmaxThreads / 32) {
+      constexpr int SP = D + 4;
+      constexpr int MT = (kTile / 2) * (D / 4) / kSoftmaxThreads;  // float4 tasks per thread (nsplit >= 2)
+      const int ns = prm.nsplit;
+      const int r0 = split * kTile / ns, r1 = (split + 1) * kTile / ns, nr = r1 - r0;
+      const uint32_t stage_a = sbase + L::kK;
+      const uint32_t lse_a = sbase + L::kEpi + 4 * kTile * 4;
+      float* wts = reinterpret_cast<float*>(sm + L::kQ);   // [nsplit][128]
+      const float scale_v = r.scales[H + h];
+      if ((int)threadIdx.x < nr) {
+        const int row = r0 + threadIdx.x;
+        float lv[8];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2)
+          if (s2 < ns) {
+            lv[s2] = ld_dsmem_f32(dsmem_addr(lse_a + 4u * row, s2));
+            mx = fmaxf(mx, lv[s2]);
+          }
+        float sum = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2)
+          if (s2 < ns) {
+            lv[s2] = (mx > -INFINITY && lv[s2] > -INFINITY) ? ex2_approx(lv[s2] - mx) : 0.f;
+            sum += lv[s2];
+          }
+        const float gsc = sum > 0.f ? scale_v / sum : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2)
+          if (s2 < ns) wts[s2 * kTile + threadIdx.x] = lv[s2] * gsc;
+      }
+      sync_softmax();
+      const int ntask = nr * (D / 4);
+      const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
+      float4 acc[MT];
+#pragma unroll
+      for (int i = 0; i < MT; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s2 = 0; s2 < ns; ++s2) {
+        float4 v[MT];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          const int idx = threadIdx.x + i * kSoftmaxThreads;
+          const int row = r0 + idx / (D / 4), c4 = idx % (D / 4);
+          v[i] = idx < ntask ? ld_dsmem_f4(dsmem_addr(stage_a + 4u * (row * SP + 4 * c4), s2))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          const int idx = threadIdx.x + i * kSoftmaxThreads;
+          const float w = idx < ntask ? wts[s2 * kTile + idx / (D / 4)] : 0.f;
+          acc[i].x = fmaf(w, v[i].x, acc[i].x);
+          acc[i].y = fmaf(w, v[i].y, acc[i].y);
+          acc[i].z = fmaf(w, v[i].z, acc[i].z);
+          acc[i].w = fmaf(w, v[i].w, acc[i].w);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        const int idx = threadIdx.x + i * kSoftmaxThreads;
+        const int row = r0 + idx / (D / 4), c4 = idx % (D / 4);
+        if (idx >= ntask || row >= rows_live) continue;
+        const size_t e = ((size_t)(qt * kTile + row) * H + h) * D + 4 * c4;
+        if (prm.out_bf16) {
+          const __nv_bfloat162 a0 = __floats2bfloat162_rn(acc[i].x, acc[i].y), a1 = __floats2bfloat162_rn(acc[i].z, acc[i].w);
+          *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(prm.out) + e) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1));
+        } else {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + e) = acc[i];
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();
+  }
+
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
@@ -697,6 +786,7 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   p.nsplit = a.nsplit;
   p.tiles_per_split = a.tiles_per_split;
   p.forced_level = a.forced_level;
+  p.cluster_merge = (a.nsplit >= 2 && a.nsplit <= 8) ? 1 : 0;
   const unsigned qtiles = (unsigned)((a.n_q + kTile - 1) / kTile);
   const dim3 pgrid(qtiles * kPrepSplit, (unsigned)r.H);
   // The attention kernel may start while the prep kernel still runs
@@ -707,11 +797,18 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = attention_smem_bytes(r.D);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.cluster_merge) {  // the splits of one query tile as one cluster
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = (unsigned)a.nsplit;
+    cfg.numAttrs = 2;
+  }
   if (r.D == 128) {
     k_attn_prep<128><<<pgrid, kPrepThreads, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();

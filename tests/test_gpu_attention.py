@@ -80,8 +80,10 @@ def test_single_filled_slot_returns_its_value():
     assert np.allclose(out, want, atol=1e-5 * np.abs(want).max())
 
 
-@pytest.mark.parametrize("splits", [1, 3, 16])
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8, 16])
 def test_split_merge_consistent(splits):
+    """2..8 splits merge inside a thread-block cluster, more through global
+    partials; both must agree with the float64 reference."""
     rng = np.random.default_rng(3)
     shape = RingShape(heads=2, head_dim=128, capacity=2000, tokens=700, queries=300, max_position=4000)
     ring, orc = make_pair(shape, Ring, max_tokens=700, max_kv_splits=splits)
@@ -104,3 +106,26 @@ def test_bf16_output_close_to_f32_output():
     o32 = ring.attention(q)
     o16 = ring.attention(q, out_dtype=torch.bfloat16)
     assert torch.allclose(o16.float(), o32, rtol=2 ** -7, atol=1e-6)
+
+
+@pytest.mark.parametrize("splits", [4, 8, 12])
+def test_split_merge_with_empty_splits_and_bf16_output(splits):
+    """A ring one-third full: the last splits of each query tile own no
+    key/value tiles and contribute nothing; the merged bf16 output must
+    still match the reference, and so must the f32 output."""
+    rng = np.random.default_rng(4)
+    shape = RingShape(heads=2, head_dim=128, capacity=2000, tokens=700, queries=300, max_position=4000)
+    ring, orc = make_pair(shape, Ring, max_tokens=700, max_kv_splits=splits)
+    q, k, v = frame(rng, shape, 700)
+    ring.calibrate(dev(k), dev(v))
+    orc.calibrate(f(k), f(v))
+    ring.write(dev(k), dev(v))
+    orc.write(f(k), f(v))
+    q, _, _ = frame(rng, shape, 300)
+    want = attention_exact(orc, f(q))
+    out = ring.attention(dev(q)).cpu().numpy()
+    mx, mn = attn_errors(out, want)
+    assert mx <= MAX_ABS and mn <= MEAN_ABS, (splits, mx, mn)
+    outb = ring.attention(dev(q), out_dtype=torch.bfloat16).float().cpu().numpy()
+    mx, mn = attn_errors(outb, want)
+    assert mx <= MAX_ABS + 2.0 ** -8 * np.abs(want).max() and mn <= MEAN_ABS + 1e-3, (splits, mx, mn)
