@@ -146,6 +146,34 @@ kvring_status kvring_write_frame(kvring_t* ring, const void* k_bf16, const void*
  * Errors: INVALID_ARG (delta < -1 or >= max_position). */
 kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
 
+/* Largest number of rings one batched call takes (a model's layers). */
+#define KVRING_MAX_BATCH 64
+
+/* kvring_write_frame on num_rings rings at once, in one launch: ring i gets
+ * k_bf16[i], v_bf16[i] and pos[i] (pos may be NULL, or any pos[i] NULL, for
+ * next_pos + t of that ring).  Every ring must have the same num_heads,
+ * head_dim and capacity; n applies to all.  The result on each ring is
+ * byte-for-byte that of kvring_write_frame.  The reset of the page
+ * ("Do It Once, at Write Time") and the per-step upkeep touch every layer,
+ * and one launch over all of them moves hundreds of megabytes instead of a
+ * few per launch.  `rings`, `k_bf16`, `v_bf16` and `pos` are host arrays of
+ * num_rings entries (the pointers in them are device pointers); rings must
+ * be distinct.
+ * Errors: INVALID_ARG (num_rings outside 1..KVRING_MAX_BATCH, a NULL or
+ * repeated ring, mismatched shapes, unaligned pointers), NOT_CALIBRATED,
+ * CAPACITY; nothing is launched on an error. */
+kvring_status kvring_write_frames_many(kvring_t* const* rings, int32_t num_rings,
+                                       const void* const* k_bf16, const void* const* v_bf16,
+                                       const int32_t* const* pos, int32_t n, void* stream);
+
+/* kvring_delta_rotate on num_rings rings of the same num_heads, head_dim and
+ * capacity in one launch (delta, or KVRING_DELTA_TO_OLDEST read per ring on
+ * the device).  Each ring ends byte-for-byte as after kvring_delta_rotate.
+ * Errors: INVALID_ARG (as above, or delta < -1 or >= a ring's max_position);
+ * nothing is launched on an error. */
+kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t num_rings, int32_t delta,
+                                       void* stream);
+
 /* FP8 attention of n_q queries over the ring ("Where the Time Went";
  * "Blackwell and Beyond Four GPUs": FP8 attention with per-head scales).
  *   out[t,h,:] = sum_j softmax_j(rope(q[t,h,:], qpos[t]) . Kdeq[h,j,:] / sqrt(d)) Vdeq[h,j,:]

@@ -22,6 +22,7 @@ __all__ = [
     "KvRing", "KvRingError", "TO_OLDEST", "lib", "library_path", "header_functions",
     "kvring_required_bytes", "kvring_create", "kvring_destroy", "kvring_calibrate_scales",
     "kvring_write_frame", "kvring_delta_rotate", "kvring_attention", "kvring_attention_noalloc",
+    "kvring_write_frames_many", "kvring_delta_rotate_many", "write_frames_many", "delta_rotate_many",
     "kvring_export",
     "kvring_status_string", "encode_e4m3", "STATE",
 ]
@@ -83,6 +84,8 @@ def lib():
         "kvring_calibrate_scales": (i32, [vp, vp, vp, vp, i32, vp]),
         "kvring_write_frame": (i32, [vp, vp, vp, vp, i32, vp]),
         "kvring_delta_rotate": (i32, [vp, i32, vp]),
+        "kvring_write_frames_many": (i32, [vp, i32, vp, vp, vp, i32, vp]),
+        "kvring_delta_rotate_many": (i32, [vp, i32, i32, vp]),
         "kvring_attention": (i32, [vp, vp, vp, i32, vp, i32, vp]),
         "kvring_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, vp]),
         "kvring_export": (i32, [vp, vp, vp, vp, vp, vp, vp]),
@@ -180,6 +183,48 @@ def kvring_write_frame(handle, k, v, pos, n, stream_ptr) -> None:
 
 def kvring_delta_rotate(handle, delta, stream_ptr) -> None:
     _check(lib().kvring_delta_rotate(handle, int(delta), stream_ptr), "kvring_delta_rotate")
+
+
+def _ptr_array(values):
+    arr = (ctypes.c_void_p * len(values))()
+    for i, x in enumerate(values):
+        arr[i] = x
+    return arr
+
+
+def kvring_write_frames_many(handles, ks, vs, poss, n, stream_ptr) -> None:
+    """Batched write: host arrays of ring handles and device pointers."""
+    m = len(handles)
+    pos_arr = None if poss is None else _ptr_array([_ptr(p) for p in poss])
+    _check(lib().kvring_write_frames_many(_ptr_array(handles), m, _ptr_array([_ptr(k) for k in ks]),
+                                          _ptr_array([_ptr(v) for v in vs]), pos_arr, int(n), stream_ptr),
+           "kvring_write_frames_many")
+
+
+def kvring_delta_rotate_many(handles, delta, stream_ptr) -> None:
+    _check(lib().kvring_delta_rotate_many(_ptr_array(handles), len(handles), int(delta), stream_ptr),
+           "kvring_delta_rotate_many")
+
+
+def write_frames_many(rings, ks, vs, poss=None, stream=None) -> None:
+    """kvring_write_frame on several rings of one shape in one launch."""
+    if not rings or len(ks) != len(rings) or len(vs) != len(rings) or (poss is not None and len(poss) != len(rings)):
+        raise ValueError("one k, v (and pos) per ring")
+    r0 = rings[0]
+    n = _tokens(ks[0], r0.H, r0.d, "k")
+    for i, r in enumerate(rings):
+        if _tokens(ks[i], r.H, r.d, "k") != n or _tokens(vs[i], r.H, r.d, "v") != n:
+            raise ValueError("every k and v must hold the same number of tokens")
+        if poss is not None:
+            _positions(poss[i], n, "pos")
+    kvring_write_frames_many([r.handle for r in rings], ks, vs, poss, n, r0._s(stream))
+
+
+def delta_rotate_many(rings, delta: int = TO_OLDEST, stream=None) -> None:
+    """kvring_delta_rotate on several rings of one shape in one launch."""
+    if not rings:
+        raise ValueError("no rings")
+    kvring_delta_rotate_many([r.handle for r in rings], delta, rings[0]._s(stream))
 
 
 def kvring_attention(handle, q, qpos, n_q, out, out_dtype, stream_ptr) -> None:

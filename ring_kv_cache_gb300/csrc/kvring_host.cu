@@ -273,6 +273,59 @@ kvring_status kvring_delta_rotate(kvring_t* r, int32_t delta, void* stream) {
   return cuda_status(kvr::launch_delta(r->dev, delta, (cudaStream_t)stream));
 }
 
+namespace {
+// Common checks of a batch: count, distinct non-NULL rings of one shape.
+kvring_status check_batch(kvring_t* const* rings, int32_t count) {
+  if (!rings || count < 1 || count > KVRING_MAX_BATCH || count > kvr::kMaxBatch) return KVRING_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    const kvring* r = rings[i];
+    if (!r) return KVRING_ERR_INVALID_ARG;
+    const kvring* r0 = rings[0];
+    if (r->cfg.num_heads != r0->cfg.num_heads || r->cfg.head_dim != r0->cfg.head_dim ||
+        r->cfg.capacity != r0->cfg.capacity)
+      return KVRING_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)
+      if (rings[j] == r) return KVRING_ERR_INVALID_ARG;
+  }
+  return KVRING_OK;
+}
+}  // namespace
+
+kvring_status kvring_write_frames_many(kvring_t* const* rings, int32_t count, const void* const* k,
+                                       const void* const* v, const int32_t* const* pos, int32_t n,
+                                       void* stream) {
+  kvring_status st = check_batch(rings, count);
+  if (st != KVRING_OK) return st;
+  if (!k || !v || n < 1) return KVRING_ERR_INVALID_ARG;
+  static thread_local kvr::WriteMany b;   // ~10 KB: kernel parameters, not device memory
+  for (int i = 0; i < count; ++i) {
+    const kvring* r = rings[i];
+    const int32_t* p = pos ? pos[i] : nullptr;
+    if (!k[i] || !v[i] || !aligned(k[i], 16) || !aligned(v[i], 16) || (p && !aligned(p, 4)))
+      return KVRING_ERR_INVALID_ARG;
+    if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
+    if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+    b.r[i] = r->dev;
+    b.k[i] = static_cast<const uint16_t*>(k[i]);
+    b.v[i] = static_cast<const uint16_t*>(v[i]);
+    b.pos[i] = p;
+  }
+  return cuda_status(kvr::launch_write_many(b, count, n, (cudaStream_t)stream));
+}
+
+kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, int32_t delta, void* stream) {
+  kvring_status st = check_batch(rings, count);
+  if (st != KVRING_OK) return st;
+  static thread_local kvr::DeltaMany b;
+  for (int i = 0; i < count; ++i) {
+    const kvring* r = rings[i];
+    if (delta != KVRING_DELTA_TO_OLDEST && (delta < 0 || delta >= r->cfg.max_position))
+      return KVRING_ERR_INVALID_ARG;
+    b.r[i] = r->dev;
+  }
+  return cuda_status(kvr::launch_delta_many(b, count, delta, (cudaStream_t)stream));
+}
+
 kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, int32_t n_q, void* out,
                                int32_t out_dtype, void* stream) {
   if (!r || !q || !out || !aligned(q, 16) || !aligned(out, 16) || (qpos && !aligned(qpos, 4)) || n_q < 1)

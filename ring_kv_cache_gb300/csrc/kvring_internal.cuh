@@ -474,6 +474,20 @@ struct AttnLaunch {
   int tiles_per_split;
   int forced_level;
 };
+// Batched write / delta over rings of one shape (kernel parameters: no
+// device memory is needed to describe the batch).
+constexpr int kMaxBatch = 64;
+struct WriteMany {
+  RingDev r[kMaxBatch];
+  const uint16_t* k[kMaxBatch];
+  const uint16_t* v[kMaxBatch];
+  const int32_t* pos[kMaxBatch];
+};
+struct DeltaMany {
+  RingDev r[kMaxBatch];
+};
+cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t s);
+cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStream_t s);
 cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              const AttnLaunch& a, cudaStream_t s);
 size_t attention_smem_bytes(int D);

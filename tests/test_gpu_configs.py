@@ -6,7 +6,8 @@
   attention calls per step).
 * Reset cycle: the same 60 layers for 84 steps with one delta rotation of
   every layer before step 42 (positions reset every 42 steps, "Do It Once,
-  at Write Time").
+  at Write Time"), done as one batched launch over all 60 rings; after it
+  each step's 60 writes also go in one batched launch.
 * Stress: 40 heads x 128, 60 layers, a first frame of a seeded prompt length
   in [100, 2000], then 200 frames of 757 tokens with resets every 42 steps;
   keys and values Student-t (3 degrees of freedom) with per-head scales
@@ -114,8 +115,7 @@ def test_reset_cycle_84_steps():
     for st in range(84):
         if st == 42:
             before = oracle_from_ring(rings[probe], MAXPOS)
-            for r in rings:
-                r.delta_rotate(kv.TO_OLDEST)
+            kv.delta_rotate_many(rings, kv.TO_OLDEST)     # every layer in one launch
             torch.cuda.synchronize()
             d = before.delta_rotate(TO_OLDEST)
             assert d > 0
@@ -125,11 +125,16 @@ def test_reset_cycle_84_steps():
         if check:
             orc = oracle_from_ring(rings[probe], MAXPOS)
         fq, fk, fv = frames[probe][st % 8]
-        for l in range(LAYERS):
-            q, k, v = frames[l][st % 8]
-            rings[l].write(k, v)
-            if l == probe:
-                rings[l].attention(q, out=out)
+        if st < 42:
+            for l in range(LAYERS):
+                q, k, v = frames[l][st % 8]
+                rings[l].write(k, v)
+                if l == probe:
+                    rings[l].attention(q, out=out)
+        else:      # after the reset the whole step's writes go in one launch
+            kv.write_frames_many(rings, [frames[l][st % 8][1] for l in range(LAYERS)],
+                                 [frames[l][st % 8][2] for l in range(LAYERS)])
+            rings[probe].attention(fq, out=out)
         if check:
             torch.cuda.synchronize()
             orc.write(_f(fk), _f(fv))
