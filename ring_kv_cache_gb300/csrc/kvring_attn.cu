@@ -151,11 +151,27 @@ __global__ void __launch_bounds__(kPrepThreads) k_attn_prep(const AttnParams prm
   constexpr int CPR = D / 8;
   constexpr int ROWS = kTile / kPrepSplit;
   constexpr int PRO = ROWS * CPR / kPrepThreads;
-  griddep_launch_dependents();
   const RingDev& r = prm.r;
   const int qt = blockIdx.x / kPrepSplit, row0 = (blockIdx.x % kPrepSplit) * ROWS;
   const int h = blockIdx.y, H = r.H;
   const size_t unit = (size_t)qt * H + h;
+  // The queries were complete before the preceding kernel started, so they
+  // load now; the ring state (next position) may still be changing in a
+  // preceding write kernel, which this kernel may overlap (programmatic
+  // dependent launch): it is read only after griddepcontrol.wait.
+  uint4 wq[PRO];
+#pragma unroll
+  for (int i = 0; i < PRO; ++i) {
+    const int k = i * kPrepThreads + threadIdx.x;
+    const int t = qt * kTile + row0 + k / CPR;
+    wq[i] = t < prm.n_q ? __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)t * H + h) * D) + k % CPR)
+                        : make_uint4(0u, 0u, 0u, 0u);
+  }
+  griddep_wait();
+  // Only now may the attention kernel start: before its own wait it reads
+  // the fill level and copies key/value tiles, which must not precede the
+  // preceding write's completion.
+  griddep_launch_dependents();
   const int next_pos = __ldcg(r.state + ST_NEXT_POS);
   const float scale_k = r.scales[h];
   uint8_t* img = r.qprep + unit * 3 * (kTile * D);
@@ -169,7 +185,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_attn_prep(const AttnParams prm
 #pragma unroll
     for (int e = 0; e < 8; ++e) qv[e] = 0.f;
     if (t < prm.n_q) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)t * H + h) * D) + chunk);
+      const uint4 w = wq[i];
       int p = prm.qpos ? __ldg(prm.qpos + t) : next_pos - prm.n_q + t;
       if (p < 0 || p >= r.max_pos) {
         atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
@@ -809,15 +825,18 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
     attr[1].val.clusterDim.z = (unsigned)a.nsplit;
     cfg.numAttrs = 2;
   }
-  if (r.D == 128) {
-    k_attn_prep<128><<<pgrid, kPrepThreads, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, k_attention<128>, *tmK, *tmV, p);
-  }
-  k_attn_prep<64><<<pgrid, kPrepThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // The prep kernel is itself a programmatic dependent of whatever precedes
+  // it: a write kernel lets it start early (see k_attn_prep).
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = pgrid;
+  pcfg.blockDim = dim3(kPrepThreads);
+  pcfg.dynamicSmemBytes = 0;
+  pcfg.stream = s;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = 1;
+  cudaError_t e = r.D == 128 ? cudaLaunchKernelEx(&pcfg, k_attn_prep<128>, p) : cudaLaunchKernelEx(&pcfg, k_attn_prep<64>, p);
   if (e != cudaSuccess) return e;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_attention<128>, *tmK, *tmV, p);
   return cudaLaunchKernelEx(&cfg, k_attention<64>, *tmK, *tmV, p);
 }
 

@@ -151,6 +151,9 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
                                            int n, int blk, int nblk) {
   constexpr int CH = D / 16;
   __shared__ int s_head, s_next;
+  // a following attention's query preparation may start now: it waits for
+  // this grid before it reads the ring state
+  griddep_launch_dependents();
   const int H = r.H, C = r.C;
   const long long per = (long long)n * H * CH;
   uint4 in[U][2];
