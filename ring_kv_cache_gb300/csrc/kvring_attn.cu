@@ -246,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<D>;
   constexpr int QD = D / 4;             // O columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base by pointer arithmetic on the shared array itself,
+  // so the compiler keeps shared-memory (not generic) loads and stores
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(sm);
   Misc* misc = reinterpret_cast<Misc*>(sm + L::kMisc);
   float* epi = reinterpret_cast<float*>(sm + L::kEpi);
