@@ -326,6 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // A following write (or query preparation) launched as a programmatic
+  // dependent may start on the idle SMs now: it loads its inputs and waits
+  // for this grid before it touches the ring.
+  griddep_launch_dependents();
   const uint32_t tmem = misc->tmem_base;
   const int n_qterms = misc->level;
 

@@ -151,8 +151,9 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
                                            int n, int blk, int nblk) {
   constexpr int CH = D / 16;
   __shared__ int s_head, s_next;
-  // a following attention's query preparation may start now: it waits for
-  // this grid before it reads the ring state
+  // A following kernel launched as a programmatic dependent (an attention's
+  // query preparation, or the next write) may start now: each waits for
+  // this grid before it touches the ring.
   griddep_launch_dependents();
   const int H = r.H, C = r.C;
   const long long per = (long long)n * H * CH;
@@ -168,6 +169,10 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
       in[u][1] = __ldcs(src + 1);
     }
   }
+  // This kernel is launched as a programmatic dependent of the preceding
+  // kernel: the inputs above were complete before that kernel started; the
+  // ring (state, cache, positions) is read and written only after it is done.
+  griddep_wait();
   if (threadIdx.x == 0) {
     s_head = __ldcg(r.state + ST_HEAD);
     s_next = __ldcg(r.state + ST_NEXT_POS);
@@ -399,26 +404,39 @@ cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, con
   return cudaGetLastError();
 }
 
+// Writes launch as programmatic dependents of the preceding kernel (they
+// load their inputs early and wait before touching the ring).
+cudaLaunchConfig_t pdl_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
                          cudaStream_t s) {
   const long long items = 2LL * n * r.H * (r.D / 16);
-  const unsigned g = grid_for((items + kWriteU - 1) / kWriteU);
-  if (r.D == 128)
-    k_write<128><<<g, kThreads, 0, s>>>(r, (const uint16_t*)k, (const uint16_t*)v, pos, n);
-  else
-    k_write<64><<<g, kThreads, 0, s>>>(r, (const uint16_t*)k, (const uint16_t*)v, pos, n);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteU - 1) / kWriteU)), s, attr);
+  const uint16_t* kk = static_cast<const uint16_t*>(k);
+  const uint16_t* vv = static_cast<const uint16_t*>(v);
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write<128>, r, kk, vv, pos, n);
+  return cudaLaunchKernelEx(&cfg, k_write<64>, r, kk, vv, pos, n);
 }
 
 cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t s) {
   const RingDev& r = b.r[0];
   const long long items = 2LL * n * r.H * (r.D / 16);
-  const dim3 g(grid_for((items + kWriteManyU - 1) / kWriteManyU), (unsigned)count);
-  if (r.D == 128)
-    k_write_many<128><<<g, kThreads, 0, s>>>(b, n);
-  else
-    k_write_many<64><<<g, kThreads, 0, s>>>(b, n);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteManyU - 1) / kWriteManyU), (unsigned)count), s, attr);
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write_many<128>, b, n);
+  return cudaLaunchKernelEx(&cfg, k_write_many<64>, b, n);
 }
 
 cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStream_t s) {
