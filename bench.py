@@ -555,7 +555,7 @@ def main():
                       "frac_hbm": write_gbs / peaks["hbm"], "peak_gbs": peaks["hbm"]},
             "attention": {"avg_launch_us": a_us, "TFLOP/s": attn_tflops,
                           "cache_GB/s": ATTN_BYTES / (a_us * 1e-6) / 1e9,
-                          "note": "one call = query prep kernel + attention kernel"},
+                          "note": "one call = one attention kernel (query prologue fused)"},
             "delta_rotate": {"avg_launch_us": d_us, "algorithmic_bytes": DELTA_BYTES,
                              "GB/s": DELTA_BYTES / (d_us * 1e-6) / 1e9,
                              "frac_hbm": DELTA_BYTES / (d_us * 1e-6) / 1e9 / peaks["hbm"]},
@@ -575,7 +575,7 @@ def main():
         },
         "e2e": {"value": e2e_ms * 1e3 / units, "unit": "µs",
                 "h2d_bytes_per_step": H2D_BYTES, "d2h_bytes_per_step": D2H_BYTES},
-        "gpu_launches": 3 * K + res["resets"],
+        "gpu_launches": 2 * K + res["resets"],   # per step: write + attention; a delta rotation per reset
         "clocks": res["clocks"],
         "device_errors": res["device_errors"],
     }

@@ -179,10 +179,11 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t num_rings
  *   out[t,h,:] = sum_j softmax_j(rope(q[t,h,:], qpos[t]) . Kdeq[h,j,:] / sqrt(d)) Vdeq[h,j,:]
  * over the filled slots j, with Kdeq = code * scale_k[h], Vdeq = code *
  * scale_v[h].  Slot order does not matter: keys carry their rotation.
- * Queries are split into FP8 terms with a per-row scale and the
- * probabilities into FP8 terms (1 to 3 and 1 to 2 terms; the level is
- * chosen per 128-query tile from the query and key ranges unless
- * attn_precision fixes it); products accumulate in fp32 on the tensor cores.
+ * Queries are split into 1 to 3 FP8 terms with a per-row scale (the level
+ * is chosen per 128-query tile from the query and key ranges unless
+ * attn_precision fixes it); the probabilities multiply V in half precision
+ * (V widened exactly from its E4M3 codes); products accumulate in fp32 on
+ * the tensor cores.
  * q: bf16 [n_q][H][d]; qpos: int32 [n_q] device positions, or NULL for
  * next_pos - n_q + t (the positions of the last n_q tokens written with
  * default positions).  out: [n_q][H][d], fp32 (KVRING_OUT_F32) or bf16
@@ -197,20 +198,22 @@ kvring_status kvring_attention(kvring_t* ring, const void* q_bf16, const int32_t
  * pool, or a real-time loop where an allocation would stall the device or
  * break its memory budget.  This entry point computes exactly what
  * kvring_attention computes, with the same arguments and errors, but its
- * scratch (the prepared query tiles, per-row factors, precision levels,
- * split partials and split tickets) lives in a fixed 32 MiB static device
- * array inside the library rather than in the ring's buffer.  Every GPU
- * that loads the library holds that array until the process exits.
+ * scratch (the precision level chosen for each 128-query tile and head)
+ * lives in a fixed 128 KiB static device array inside the library rather
+ * than in the ring's buffer.  Every GPU that loads the library holds that
+ * array until the process exits.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
  *   - The first call on a device looks up the array's device address
  *     (once per device, with that device current); make that first call
  *     before any stream capture.
  *   - The array is shared by every call: calls that overlap on the GPU
  *     (other streams, other rings) race and must be ordered by the caller.
- *     Each call clears the split tickets it uses before its kernels run.
- *   - The split count is reduced until the partials fit; a call whose
- *     query tiles alone need more than 32 MiB (about 49 KiB per 128-query
- *     tile per head at head_dim 128) returns KVRING_ERR_CAPACITY.
+ *     Nothing in it needs to start at zero (each call writes every level
+ *     it uses before reading it).
+ *   - It uses at most 8 key/value splits, which merge inside their
+ *     thread-block cluster, so it needs no split partials.  A call with more
+ *     than 32,768 (128-query tile, head) units, i.e. more than 4 bytes of
+ *     levels per unit beyond 128 KiB, returns KVRING_ERR_CAPACITY.
  * The paper has no counterpart: this is a deployment variant. */
 kvring_status kvring_attention_noalloc(kvring_t* ring, const void* q_bf16, const int32_t* qpos,
                                        int32_t n_q, void* out, int32_t out_dtype, void* stream);

@@ -22,9 +22,8 @@
 //               row's normaliser.  O is rescaled in TMEM when the maximum
 //               rises by more than 1.5 (log2 units).  Epilogue: the two
 //               groups' (m, l, O) merged, O / l, split partials and their merge.
-//   warp 8      Copy producer: the query tile's FP8 terms (one bulk copy of
-//               the images k_attn_prep wrote), then K and V tiles [128 slots][d]
-//               by TMA into a 3-stage ring.
+//   warp 8      Copy producer: K and V tiles [128 slots][d] by TMA into a
+//               3-stage ring (the third stage once the query prologue is done).
 //   warp 9      TMEM allocation and the single MMA-issuing thread:
 //               S = sum_t Q_t K^T (kind::f8f6f4, A and B from shared memory,
 //               K-major), then O_g += P Vh (kind::f16, P read from TMEM, B = the
@@ -37,12 +36,13 @@
 // so the arrival of S(j) also means PV(j - 2) is done: group g may rescale
 // O_g as soon as S(j) is there.
 //
-// k_attn_prep runs first, once per (query tile, head): RoPE of the queries in
-// fp32, a per-row scale 448/amax(row), the split into 3 E4M3 terms written
-// as ready-to-copy swizzled shared-memory images, the per-row logit factor
-// and row maxima.  Split CTAs of the same tile share them; the attention
-// kernel is launched as a programmatic dependent of the prep kernel, so its
-// set-up and first key/value copies overlap the prep.
+// Query prologue, by the softmax threads at the start of every CTA: the
+// tile's query rows and their RoPE-table rows are copied into shared memory
+// (cp.async, into the third K/V stage and the f16 V tiles, unused until then),
+// rotated in fp32, scaled per row by 448/amax(row), split into up to 3 E4M3
+// terms written straight into the swizzled images the QK MMA reads; the
+// per-row logit factor stays in the thread's register, and the tile's
+// maximum picks the level.  Split CTAs of a tile each do their own.
 //
 // Precision level per query tile (from the tile's amax and the head's key
 // range 448*scale_k and value range 448*scale_v): the number of E4M3 terms of
@@ -60,8 +60,6 @@ namespace kvr {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kPrepThreads = 256;
-constexpr int kPrepSplit = 4;           // prep CTAs per query tile (32 rows each)
 constexpr int kSoftmaxThreads = 256;    // 2 groups x 4 warps, one thread per query row
 constexpr int kGroupThreads = 128;
 constexpr int kCvtThreads = 64;         // 2 value-converter warps
@@ -140,105 +138,6 @@ struct AttnParams {
 // Named barriers: 0 = __syncthreads, 1 = the 256 softmax threads.
 __device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Query preparation, one CTA per 32 rows of a (query tile, head), 256
-// threads.  Chunk task k = i * 256 + tid: row k / CPR of the block, chunk
-// k % CPR (8 elements = 4 RoPE pairs); a warp reads 32 consecutive 16-byte
-// chunks.  Writes all three E4M3 terms (the attention kernel copies as many
-// as the tile's level needs), the per-row logit factor and the row maxima
-// from which the attention kernel picks the level.
-template <int D>
-__global__ void __launch_bounds__(kPrepThreads) k_attn_prep(const AttnParams prm) {
-  constexpr int CPR = D / 8;
-  constexpr int ROWS = kTile / kPrepSplit;
-  constexpr int PRO = ROWS * CPR / kPrepThreads;
-  const RingDev& r = prm.r;
-  const int qt = blockIdx.x / kPrepSplit, row0 = (blockIdx.x % kPrepSplit) * ROWS;
-  const int h = blockIdx.y, H = r.H;
-  const size_t unit = (size_t)qt * H + h;
-  // The queries were complete before the preceding kernel started, so they
-  // load now; the ring state (next position) may still be changing in a
-  // preceding write kernel, which this kernel may overlap (programmatic
-  // dependent launch): it is read only after griddepcontrol.wait.
-  uint4 wq[PRO];
-#pragma unroll
-  for (int i = 0; i < PRO; ++i) {
-    const int k = i * kPrepThreads + threadIdx.x;
-    const int t = qt * kTile + row0 + k / CPR;
-    wq[i] = t < prm.n_q ? __ldg(reinterpret_cast<const uint4*>(prm.q + ((size_t)t * H + h) * D) + k % CPR)
-                        : make_uint4(0u, 0u, 0u, 0u);
-  }
-  griddep_wait();
-  // Only now may the attention kernel start: before its own wait it reads
-  // the fill level and copies key/value tiles, which must not precede the
-  // preceding write's completion.
-  griddep_launch_dependents();
-  const int next_pos = __ldcg(r.state + ST_NEXT_POS);
-  const float scale_k = r.scales[h];
-  uint8_t* img = r.qprep + unit * 3 * (kTile * D);
-#pragma unroll
-  for (int i = 0; i < PRO; ++i) {
-    const int k = i * kPrepThreads + threadIdx.x;
-    const int rrow = row0 + k / CPR, chunk = k % CPR;
-    const int t = qt * kTile + rrow;
-    float qv[8];
-    float amax = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qv[e] = 0.f;
-    if (t < prm.n_q) {
-      const uint4 w = wq[i];
-      int p = prm.qpos ? __ldg(prm.qpos + t) : next_pos - prm.n_q + t;
-      if (p < 0 || p >= r.max_pos) {
-        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
-        p = 0;
-      }
-      const float4* tb = reinterpret_cast<const float4*>(r.table + (size_t)p * D) + 2 * chunk;
-      const float4 cs0 = __ldg(tb), cs1 = __ldg(tb + 1);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-      const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
-      const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
-        const float y0 = x0 * cc[e] - x1 * ss[e];
-        const float y1 = x0 * ss[e] + x1 * cc[e];
-        qv[2 * e] = y0;
-        qv[2 * e + 1] = y1;
-        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
-      }
-    }
-    // row maximum over the CPR consecutive lanes that hold the row
-#pragma unroll
-    for (int off = CPR / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    float sq = amax / 448.0f;
-    if (!(sq >= 0x1p-126f)) sq = 1.0f;
-    const float invq = 1.0f / sq;
-    if (chunk == 0) {
-      r.qrowf[unit * 2 * kTile + rrow] = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
-      r.qrowf[unit * 2 * kTile + kTile + rrow] = amax;
-    }
-    // E4M3 terms of q / sigma_q (sigma_q = amax/448), residual splitting in
-    // fp32; 8 bytes per chunk per term at the chunk's swizzled place.
-    float u[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) u[e] = qv[e] * invq;
-    const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
-#pragma unroll
-    for (int term = 0; term < 3; ++term) {
-      uint16_t c4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(u[2 * e], u[2 * e + 1]);
-      *reinterpret_cast<uint2*>(img + term * (kTile * D) + off) =
-          make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {  // exact fp32 residual for the next term
-        const float2 dq = e4m3x2_to_f32x2(c4[e]);
-        u[2 * e] -= dq.x;
-        u[2 * e + 1] -= dq.y;
-      }
-    }
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -259,6 +158,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
   const int H = r.H;
+  // Query rows of this tile that exist, and where they are staged in shared
+  // memory until the query prologue has made E4M3 terms of them: the third
+  // K and V stages (rows 0-63, 64-127), which hold no copy before then.
+  const int rows_in = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
+  auto q_stage = [&](int rr) -> uint32_t {
+    return sbase + (rr < 64 ? L::kK : L::kV) + 2 * L::kKVTile + (uint32_t)(rr & 63) * (2 * D);
+  };
+  if (warp < kSoftmaxThreads / 32) {
+    // the queries were complete before the preceding kernel started
+    for (int k = threadIdx.x; k < rows_in * (D / 8); k += kSoftmaxThreads) {
+      const int rr = k / (D / 8), c = k % (D / 8);
+      cp_async16(q_stage(rr) + 16u * c, prm.q + ((size_t)(qt * kTile + rr) * H + h) * D + 8 * c);
+    }
+    cp_async_commit();
+  }
+  // This kernel is a programmatic dependent of the preceding kernel (a write,
+  // or an earlier attention): the ring (state, cache) is read only after it.
+  griddep_wait();
   const int nvalid = __ldcg(r.state + ST_NVALID);
   const int ntile_total = (nvalid + kTile - 1) / kTile;
   const int tile0 = split * prm.tiles_per_split;
@@ -268,8 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- setup
   const size_t unit = (size_t)qt * H + h;
   if (threadIdx.x == kWarpTma * 32) {
-    // The producer initialises the barriers and starts the first key/value
-    // copies at once; they do not depend on the query preparation.
+    // The producer initialises the barriers and starts the first two
+    // key/value copies at once; the third stage's space holds query rows
+    // until the query prologue is done.
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(L::kBarKvFull + s), 1);
       // freed by the QK commit and by every converter thread
@@ -282,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarVhFull + b), kCvtThreads);
     }
     mbar_init(bar(L::kBarMmaDone), 1);
-    mbar_init(bar(L::kBarQFull), 1);
+    mbar_init(bar(L::kBarQFull), kSoftmaxThreads);   // the query prologue
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
-    const int first = ntiles < kStages ? ntiles : kStages;
+    const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
     for (int j = 0; j < first; ++j) {
       mbar_arrive_expect_tx(bar(L::kBarKvFull + j), 2u * kTile * D);
       const int slot0 = (tile0 + j) * kTile;
@@ -298,31 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  // Everything below reads what k_attn_prep wrote.
-  griddep_wait();
-  if (warp == kWarpTma) {
-    // precision level of this query tile from its row maxima, then one bulk
-    // copy per E4M3 term of the prepared query images
-    float qm = 0.f;
-    for (int i = lane; i < kTile; i += 32) qm = fmaxf(qm, __ldcg(r.qrowf + unit * 2 * kTile + kTile + i));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xFFFFFFFFu, qm, off));
-    int level = prm.forced_level;
-    if (level == 0) {
-      const float lg = qm * 448.0f * r.scales[h];
-      const float vmax = 448.0f * r.scales[H + h];
-      level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
-    }
-    if (lane == 0) {
-      misc->level = level;
-      if (split == 0) r.levels[unit] = level;
-      if (ntiles > 0) {   // a CTA without key/value tiles needs no queries
-        mbar_arrive_expect_tx(bar(L::kBarQFull), (uint32_t)(level * L::kQTile));
-        for (int t = 0; t < level; ++t)
-          bulk_load(sbase + L::kQ + t * L::kQTile, r.qprep + (unit * 3 + t) * L::kQTile, L::kQTile, bar(L::kBarQFull));
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -331,13 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for this grid before it touches the ring.
   griddep_launch_dependents();
   const uint32_t tmem = misc->tmem_base;
-  const int n_qterms = misc->level;
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = ntiles < kStages ? ntiles : kStages;
-      for (int j = issued; j < ntiles; ++j) {
+      int issued = ntiles < kStages - 1 ? ntiles : kStages - 1;
+      const bool go = issued >= ntiles || mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs);
+      for (int j = issued; go && j < ntiles; ++j) {
         const int s = j % kStages;
         if (!mbar_wait_bounded(bar(L::kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, abort, kWaitLimitNs))
           break;
@@ -351,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
         mbar_wait_bounded(bar(L::kBarKvFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
-      if (ntiles > 0) mbar_wait_bounded(bar(L::kBarQFull), 0, &no_abort, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -370,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv = smem_desc(sbase + L::kVh, (uint32_t)L::kVhAtom, 1024, 2u);
       const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
       constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4, kVhStep = L::kVhTile >> 4;
+      int n_qterms = 3;
       // S(j) into TMEM buffer j&1.  Its previous user, P(j-2), was consumed
       // by PV(j-2), issued earlier by this thread: in-order execution.
       auto issue_qk = [&](int j) -> bool {
@@ -390,8 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(L::kBarKvEmpty + s));   // the K stage is read
         return true;
       };
-      bool ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs) && issue_qk(0) &&
-                (ntiles < 2 || issue_qk(1));
+      bool ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs);
+      n_qterms = misc->level;   // written before the prologue's arrivals
+      ok = ok && issue_qk(0) && (ntiles < 2 || issue_qk(1));
       for (int j = 0; ok && j < ntiles; ++j) {
         const int b = j & 1;
         if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
@@ -426,6 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages, b = j & 1;
       bool ok = mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs);
+      // the f16 tiles hold RoPE-table rows until the query prologue is done
+      if (ok && j == 0) ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs);
       if (ok && j >= 2) ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       const uint8_t* src = sm + L::kV + s * L::kKVTile;
@@ -465,7 +361,136 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = warp >> 2;
     const int row = threadIdx.x & (kTile - 1);
     const int quarter = warp & 3;
-    const float f_row = __ldcg(r.qrowf + unit * 2 * kTile + row);
+    float f_row;
+    {
+      // ---------------------------------------------- query prologue
+      // (1) one position per query row; (2) the RoPE-table rows of those
+      // positions copied into the f16 V tiles' space with 16-byte cp.async
+      // (the query rows are already on their way, see above); (3) pass 1, a
+      // small rolled loop over 8-value chunks: chunk task k = i * 256 + tid
+      // is query row k / CPR, chunk k % CPR, so a warp holds every chunk of
+      // its rows and a row's amax is a shuffle reduction, and the warps'
+      // maxima give the tile's precision level; (4) pass 2 rotates again and
+      // writes the level's E4M3 terms straight into the swizzled images the
+      // QK MMA reads.
+      constexpr int CPR = D / 8;                           // 16-byte q chunks per row
+      constexpr int TPR = D / 4;                           // 16-byte table chunks per row
+      constexpr int PQ = kTile * CPR / kSoftmaxThreads;    // 8 (d = 128) or 4
+      int* qpos_s = reinterpret_cast<int*>(epi + 2 * kTile);   // [128]
+      if (threadIdx.x < kTile) {
+        const int tq = qt * kTile + threadIdx.x;
+        int p = 0;
+        if (tq < prm.n_q) {
+          p = prm.qpos ? __ldg(prm.qpos + tq) : __ldcg(r.state + ST_NEXT_POS) - prm.n_q + tq;
+          if (p < 0 || p >= r.max_pos) {
+            atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+            p = 0;
+          }
+        }
+        qpos_s[threadIdx.x] = p;
+      }
+      sync_softmax();
+      for (int k = threadIdx.x; k < rows_in * TPR; k += kSoftmaxThreads) {
+        const int rr = k / TPR, c = k % TPR;
+        cp_async16(sbase + L::kVh + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)qpos_s[rr] * D + 4 * c);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      sync_softmax();
+      auto rotate = [&](int rrow, int chunk, float (&u)[8]) -> float {
+        float cmax = 0.f;
+        if (rrow < rows_in) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sm + (q_stage(rrow) - sbase) + 16 * chunk);
+          const float4* tb = reinterpret_cast<const float4*>(sm + L::kVh + (size_t)rrow * (4 * D)) + 2 * chunk;
+          const float4 cs0 = tb[0], cs1 = tb[1];
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
+          const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
+            u[2 * e] = x0 * cc[e] - x1 * ss[e];
+            u[2 * e + 1] = x0 * ss[e] + x1 * cc[e];
+            cmax = fmaxf(cmax, fmaxf(fabsf(u[2 * e]), fabsf(u[2 * e + 1])));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[e] = 0.f;          // rows past n_q: zero queries
+        }
+        return cmax;
+      };
+      float wmax = 0.f;
+#pragma unroll 4
+      for (int i = 0; i < PQ; ++i) {
+        const int k = i * kSoftmaxThreads + threadIdx.x;
+        const int rrow = k / CPR, chunk = k % CPR;
+        float u[8];
+        float cmax = rotate(rrow, chunk, u);
+        // row maximum over the CPR consecutive lanes that hold the row
+#pragma unroll
+        for (int off = CPR / 2; off > 0; off >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, off));
+        if (chunk == 0) epi[rrow] = cmax;
+        wmax = fmaxf(wmax, cmax);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xFFFFFFFFu, wmax, off));
+      if (lane == 0) epi[kTile + warp] = wmax;
+      sync_softmax();
+      float qm = epi[kTile];
+#pragma unroll
+      for (int i = 1; i < kSoftmaxThreads / 32; ++i) qm = fmaxf(qm, epi[kTile + i]);
+      int level = prm.forced_level;
+      if (level == 0) {
+        const float lg = qm * 448.0f * r.scales[h];
+        const float vmax = 448.0f * r.scales[H + h];
+        level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
+      }
+#pragma unroll 2
+      for (int i = 0; i < PQ; ++i) {
+        const int k = i * kSoftmaxThreads + threadIdx.x;
+        const int rrow = k / CPR, chunk = k % CPR;
+        float u[8];
+        rotate(rrow, chunk, u);
+        // E4M3 terms of q / sigma_q (sigma_q = amax/448 of the row), exact
+        // fp32 residuals; 8 bytes per chunk per term at the chunk's swizzled
+        // place in the query images
+        float sq = epi[rrow] / 448.0f;
+        if (!(sq >= 0x1p-126f)) sq = 1.0f;
+        const float invq = 1.0f / sq;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] *= invq;
+        const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
+#pragma unroll
+        for (int term = 0; term < 3; ++term) {
+          if (term < level) {
+            uint16_t c4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(u[2 * e], u[2 * e + 1]);
+            *reinterpret_cast<uint2*>(sm + L::kQ + term * L::kQTile + off) =
+                make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
+            if (term + 1 < level) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 dq = e4m3x2_to_f32x2(c4[e]);
+                u[2 * e] -= dq.x;
+                u[2 * e + 1] -= dq.y;
+              }
+            }
+          }
+        }
+      }
+      {
+        float sq = epi[row] / 448.0f;       // this thread's softmax row
+        if (!(sq >= 0x1p-126f)) sq = 1.0f;
+        f_row = fmaxf(sq * r.scales[h] * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
+      }
+      if (threadIdx.x == 0) {
+        misc->level = level;
+        if (split == 0) r.levels[unit] = level;
+      }
+      fence_proxy_async_smem();   // generic writes -> tensor-core reads
+      mbar_arrive(bar(L::kBarQFull));
+    }
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = trow + L::kColS + g * 128, tO = trow + L::kColO + g * 128;
     float m_run = -INFINITY;
@@ -810,10 +835,9 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   p.forced_level = a.forced_level;
   p.cluster_merge = (a.nsplit >= 2 && a.nsplit <= 8) ? 1 : 0;
   const unsigned qtiles = (unsigned)((a.n_q + kTile - 1) / kTile);
-  const dim3 pgrid(qtiles * kPrepSplit, (unsigned)r.H);
-  // The attention kernel may start while the prep kernel still runs
-  // (programmatic dependent launch); it waits for the prep's results with
-  // griddepcontrol.wait before it reads them.
+  // A programmatic dependent of the preceding kernel: it may start while
+  // that kernel still runs, copies its query rows, and waits
+  // (griddepcontrol.wait) before it reads the ring.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(qtiles, (unsigned)r.H, (unsigned)a.nsplit);
   cfg.blockDim = dim3(kThreads);
@@ -831,17 +855,6 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
     attr[1].val.clusterDim.z = (unsigned)a.nsplit;
     cfg.numAttrs = 2;
   }
-  // The prep kernel is itself a programmatic dependent of whatever precedes
-  // it: a write kernel lets it start early (see k_attn_prep).
-  cudaLaunchConfig_t pcfg = {};
-  pcfg.gridDim = pgrid;
-  pcfg.blockDim = dim3(kPrepThreads);
-  pcfg.dynamicSmemBytes = 0;
-  pcfg.stream = s;
-  pcfg.attrs = attr;
-  pcfg.numAttrs = 1;
-  cudaError_t e = r.D == 128 ? cudaLaunchKernelEx(&pcfg, k_attn_prep<128>, p) : cudaLaunchKernelEx(&pcfg, k_attn_prep<64>, p);
-  if (e != cudaSuccess) return e;
   if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_attention<128>, *tmK, *tmV, p);
   return cudaLaunchKernelEx(&cfg, k_attention<64>, *tmK, *tmV, p);
 }
@@ -849,15 +862,15 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
 // ---------------------------------------------------------------------------
 // Scratch for callers that cannot allocate device memory.
 //
-// kvring_attention_noalloc keeps its scratch (query images, per-row factors,
-// levels, split partials, tickets) in this file-scope array instead of the
-// ring's buffer.  It is static device memory: every GPU that loads the
+// kvring_attention_noalloc keeps its scratch (the precision level of every
+// query tile and head; its splits merge in a cluster, so it needs no
+// partials) in this file-scope array instead of the ring's buffer.  It is static device memory: every GPU that loads the
 // library holds it until the process exits.  In host code the array's name
 // is only a host-side stand-in, so its device address is looked up once per
 // device (cudaGetSymbolAddress, with that device current) and then passed
 // to the kernels like any other pointer.
 namespace {
-constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+constexpr size_t kStaticScratchBytes = size_t(128) << 10;   // 32,768 units
 __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
 std::mutex g_scratch_mu;
 constexpr int kMaxDevices = 64;

@@ -44,7 +44,7 @@ bool config_ok(const kvring_config* c) {
 }
 
 struct Plan {
-  size_t k, v, slot_pos, scales, state, amax, table, part_o, part_lse, tickets, levels, qprep, qrowf, total;
+  size_t k, v, slot_pos, scales, state, amax, table, part_o, part_lse, tickets, levels, total;
   int qtiles;
 };
 
@@ -52,7 +52,9 @@ Plan plan_for(const kvring_config* c) {
   Plan p{};
   const size_t H = (size_t)c->num_heads, D = (size_t)c->head_dim, C = (size_t)c->capacity;
   p.qtiles = (c->max_tokens + kvr::kTile - 1) / kvr::kTile;
-  const size_t Q = (size_t)p.qtiles, S = (size_t)c->max_kv_splits;
+  // split partials go through global memory only beyond 8 splits (up to 8
+  // splits merge inside a thread-block cluster)
+  const size_t Q = (size_t)p.qtiles, S = c->max_kv_splits > 8 ? (size_t)c->max_kv_splits : 0;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -70,8 +72,6 @@ Plan plan_for(const kvring_config* c) {
   p.part_lse = take(S * Q * H * kvr::kTile * 4);
   p.tickets = take(Q * H * 4);
   p.levels = take(Q * H * 4);
-  p.qprep = take(Q * H * 3 * kvr::kTile * D);
-  p.qrowf = take(Q * H * 2 * kvr::kTile * 4);
   p.total = off;
   return p;
 }
@@ -188,8 +188,6 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   d.part_lse = reinterpret_cast<float*>(b + p.part_lse);
   d.tickets = reinterpret_cast<int32_t*>(b + p.tickets);
   d.levels = reinterpret_cast<int32_t*>(b + p.levels);
-  d.qprep = b + p.qprep;
-  d.qrowf = reinterpret_cast<float*>(b + p.qrowf);
   d.H = cfg->num_heads;
   d.D = cfg->head_dim;
   d.C = cfg->capacity;
@@ -351,17 +349,13 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
   if (out_dtype != KVRING_OUT_F32 && out_dtype != KVRING_OUT_BF16) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n_q > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
-  // Scratch plan for this call inside the static array: query images,
-  // per-row factors, levels and tickets always; split partials only when
-  // the call is split, with as many splits as fit.
-  const size_t H = (size_t)r->dev.H, D = (size_t)r->dev.D;
+  // Scratch for this call inside the static array: the precision level of
+  // each (query tile, head).  At most 8 splits, which merge inside their
+  // thread-block cluster, so no split partials or tickets are needed.
+  const size_t H = (size_t)r->dev.H;
   const size_t qtiles = (size_t)((n_q + kvr::kTile - 1) / kvr::kTile);
   const size_t units = qtiles * H;
-  const size_t fixed = align_up(units * 3 * kvr::kTile * D) + align_up(units * 2 * kvr::kTile * 4) + 2 * align_up(units * 4);
-  const size_t per_split = units * kvr::kTile * D * 4;
-  const size_t per_split_lse = units * kvr::kTile * 4;
-  const size_t cap = kvr::static_scratch_bytes();
-  if (fixed > cap) return KVRING_ERR_CAPACITY;
+  if (units * 4 > kvr::static_scratch_bytes()) return KVRING_ERR_CAPACITY;
   kvr::AttnLaunch a;
   a.q = q;
   a.qpos = qpos;
@@ -371,33 +365,20 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
   a.forced_level = r->cfg.attn_precision;
   choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
   const int ctiles = (r->cfg.capacity + kvr::kTile - 1) / kvr::kTile;
-  while (a.nsplit > 1 && fixed + align_up(a.nsplit * per_split) + align_up(a.nsplit * per_split_lse) > cap) {
-    const int want = a.nsplit - 1;
-    a.tiles_per_split = (ctiles + want - 1) / want;
+  if (a.nsplit > 8) {
+    a.tiles_per_split = (ctiles + 7) / 8;
     a.nsplit = (ctiles + a.tiles_per_split - 1) / a.tiles_per_split;
   }
   void* base = nullptr;
   if (kvr::static_scratch_address(&base) != cudaSuccess) return KVRING_ERR_CUDA;
-  uint8_t* b = static_cast<uint8_t*>(base);
   kvr::RingDev d = r->dev;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    uint8_t* p = b + off;
-    off = align_up(off + bytes);
-    return p;
-  };
-  d.qprep = take(units * 3 * kvr::kTile * D);
-  d.qrowf = reinterpret_cast<float*>(take(units * 2 * kvr::kTile * 4));
-  d.levels = reinterpret_cast<int32_t*>(take(units * 4));
-  d.tickets = reinterpret_cast<int32_t*>(take(units * 4));
-  d.part_o = reinterpret_cast<float*>(take(a.nsplit > 1 ? a.nsplit * per_split : 0));
-  d.part_lse = reinterpret_cast<float*>(take(a.nsplit > 1 ? a.nsplit * per_split_lse : 0));
+  d.levels = static_cast<int32_t*>(base);
+  d.tickets = nullptr;
+  d.part_o = nullptr;
+  d.part_lse = nullptr;
   d.qtiles_max = (int)qtiles;
   d.max_splits = a.nsplit;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: the split tickets must
-  // start at zero
-  if (cudaMemsetAsync(d.tickets, 0, units * 4, s) != cudaSuccess) return KVRING_ERR_CUDA;
   return cuda_status(kvr::launch_attention(d, &r->tmK, &r->tmV, a, s));
 }
 

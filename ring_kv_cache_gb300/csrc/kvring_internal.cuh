@@ -42,12 +42,10 @@ struct RingDev {
   int32_t* state;      // [ST_WORDS_ALLOC]
   uint32_t* amax;      // [2H] calibration maxima as float bits (0 between calls)
   const float* table;  // [max_position][D/2][2] fp32 (cos, sin)
-  float* part_o;       // [max_splits][qtiles][H][128][D] attention partials
+  float* part_o;       // [max_splits][qtiles][H][128][D] attention partials (more than 8 splits)
   float* part_lse;     // [max_splits][qtiles][H][128]
   int32_t* tickets;    // [qtiles][H] split completion counters (0 between calls)
   int32_t* levels;     // [qtiles][H] precision level of each query tile
-  uint8_t* qprep;      // [qtiles][H][3][128 * D] query E4M3 terms, swizzled tile images
-  float* qrowf;        // [qtiles][H][2][128] logit factor and amax per query row
   int H, D, C, max_pos, max_tokens, max_splits, qtiles_max;
 };
 
@@ -179,6 +177,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity
     }
   }
 }
+
+// ------------------------------------------------------------ cp.async ---
+// 16-byte global -> shared copy that bypasses registers (and L1); grouped by
+// cp_async_commit, complete for the issuing thread after cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // -------------------------------------------------------------- cluster ---
 // Barrier over every thread of every CTA of the cluster (all warps

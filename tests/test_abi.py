@@ -34,10 +34,14 @@ def test_required_bytes_matches_layout(L):
     n = kv.kvring_required_bytes(cfg)
     H, D, C, Q, S = 10, 128, 5788, 6, 8
     a = lambda x: (x + 255) // 256 * 256
+    # up to 8 splits merge in a thread-block cluster: no split partials
     want = (a(H * C * D) * 2 + a(4 * C) + a(16 * H) + a(64) + a(8 * H) + a(40960 * D * 4)
-            + a(S * Q * H * 128 * D * 4) + a(S * Q * H * 128 * 4) + a(Q * H * 4) * 2
-            + a(Q * H * 3 * 128 * D) + a(Q * H * 2 * 128 * 4))
+            + a(Q * H * 4) * 2)
     assert n == want
+    cfg = kv.make_config(10, 128, 5788, 757, 40960, max_kv_splits=16)
+    S = 16
+    want += a(S * Q * H * 128 * D * 4) + a(S * Q * H * 128 * 4)
+    assert kv.kvring_required_bytes(cfg) == want
 
 
 @pytest.mark.parametrize("field,value", [

@@ -8,8 +8,9 @@ static device array inside the library.
 
 Checked through the C ABI (ctypes, no binding helpers): two calls in a row
 each match the existing entry point's output for the same inputs, within
-the attention tolerance the other tests use; and a call whose query tiles
-cannot fit the static array is refused with KVRING_ERR_CAPACITY.  This file
+the attention tolerance the other tests use; and a call with more
+(query tile, head) units than the static array holds levels for is refused
+with KVRING_ERR_CAPACITY before anything is launched.  This file
 is named to run last, so a failure here comes after every other test ran.
 """
 import ctypes
@@ -56,15 +57,16 @@ def test_noalloc_matches_attention_on_two_calls_in_a_row():
 
 def test_noalloc_refuses_what_does_not_fit():
     L = kv.lib()
-    # 40 heads x 22 query tiles of head_dim 128 need ~43 MiB of query images
-    ring = kv.KvRing(40, 128, 256, 2816, 4096, max_kv_splits=1)
-    x = torch.zeros((8, 40, 128), dtype=torch.bfloat16, device="cuda")
+    # 64 heads x 513 query tiles = 32,832 (tile, head) levels > 128 KiB / 4 B
+    n_big = 513 * 128
+    ring = kv.KvRing(64, 128, 256, n_big, 4096, max_kv_splits=1)
+    x = torch.zeros((8, 64, 128), dtype=torch.bfloat16, device="cuda")
     ring.calibrate(x, x)
-    q = torch.zeros((2816, 40, 128), dtype=torch.bfloat16, device="cuda")
-    out = torch.empty((2816, 40, 128), dtype=torch.float32, device="cuda")
+    q = torch.zeros((n_big, 64, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((n_big, 64, 128), dtype=torch.float32, device="cuda")
     assert _call(L.kvring_attention_noalloc, ring, q, out) == 3      # KVRING_ERR_CAPACITY
-    small = torch.zeros((128, 40, 128), dtype=torch.bfloat16, device="cuda")
-    out_small = torch.empty((128, 40, 128), dtype=torch.float32, device="cuda")
+    small = torch.zeros((128, 64, 128), dtype=torch.bfloat16, device="cuda")
+    out_small = torch.empty((128, 64, 128), dtype=torch.float32, device="cuda")
     assert _call(L.kvring_attention_noalloc, ring, small, out_small) == 0
     torch.cuda.synchronize()
     assert np.all(out_small.cpu().numpy() == 0)                      # empty ring: zeros
