@@ -75,14 +75,15 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 constexpr float kTau = 1.5f;
 constexpr float kPShift = 7.0f;
 // Level rule: with L = max|q| * max|k| over the tile (rotated query units
-// times 448 * scale_k) and V = 448 * scale_v, level 1 (one E4M3 query term,
-// relative error up to 2^-4, so logits off by up to L/16) only when both are
-// small, level 2 up to L = 64, level 3 beyond.  Measured against the float64
-// reference on the seeded workloads: level 1 errs by 2e-2 at unit scale,
-// level 2 by about 1e-3.
+// times 448 * scale_k) and V = 448 * scale_v (the largest value), level 1
+// (one E4M3 query term, relative error up to 2^-4) only when both are small,
+// level 2 while L * V <= 435, level 3 beyond.  The output error of level 2
+// grows about as 2.3e-5 * L * V (measured against the float64 reference for
+// L from 20 to 550), so level 2 stays within 1e-2 max-abs, half the 2e-2 bar;
+// level 3 errs about 25 times less.
 constexpr float kLevel1MaxL = 4.0f;
 constexpr float kLevel1MaxV = 0.5f;
-constexpr float kLevel2MaxL = 64.0f;
+constexpr float kLevel2MaxLV = 435.0f;
 
 template <int D>
 struct Layout {
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (level == 0) {
         const float lg = qm * 448.0f * r.scales[h];
         const float vmax = 448.0f * r.scales[H + h];
-        level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg <= kLevel2MaxL ? 2 : 3);
+        level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg * vmax <= kLevel2MaxLV ? 2 : 3);
       }
 #pragma unroll 2
       for (int i = 0; i < PQ; ++i) {
