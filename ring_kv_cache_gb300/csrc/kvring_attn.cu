@@ -166,14 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto q_stage = [&](int rr) -> uint32_t {
     return sbase + (rr < 64 ? L::kK : L::kV) + 2 * L::kKVTile + (uint32_t)(rr & 63) * (2 * D);
   };
-  if (warp < kSoftmaxThreads / 32) {
-    // the queries were complete before the preceding kernel started
-    for (int k = threadIdx.x; k < rows_in * (D / 8); k += kSoftmaxThreads) {
-      const int rr = k / (D / 8), c = k % (D / 8);
-      cp_async16(q_stage(rr) + 16u * c, prm.q + ((size_t)(qt * kTile + rr) * H + h) * D + 8 * c);
-    }
-    cp_async_commit();
+  // the queries were complete before the preceding kernel started
+  for (int k = threadIdx.x; k < rows_in * (D / 8); k += kThreads) {
+    const int rr = k / (D / 8), c = k % (D / 8);
+    cp_async16(q_stage(rr) + 16u * c, prm.q + ((size_t)(qt * kTile + rr) * H + h) * D + 8 * c);
   }
+  cp_async_commit();
   // This kernel is a programmatic dependent of the preceding kernel (a write,
   // or an earlier attention): the ring (state, cache) is read only after it.
   griddep_wait();
@@ -201,7 +199,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarVhFull + b), kCvtThreads);
     }
     mbar_init(bar(L::kBarMmaDone), 1);
-    mbar_init(bar(L::kBarQFull), kSoftmaxThreads);   // the query prologue
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
@@ -226,12 +223,140 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   const uint32_t tmem = misc->tmem_base;
 
+  {
+    // ------------------------------------------------ query prologue
+    // All twelve warps, before the roles split up (nothing can proceed
+    // without the query terms anyway).
+      // (1) one position per query row; (2) the RoPE-table rows of those
+      // positions copied into the f16 V tiles' space with 16-byte cp.async
+      // (the query rows are already on their way, see above); (3) pass 1, a
+      // small rolled loop over 8-value chunks: chunk task k = i * 384 + tid
+      // is query row k / CPR, chunk k % CPR, so a warp holds every chunk of
+      // its rows and a row's amax is a shuffle reduction, and the warps'
+      // maxima give the tile's precision level; (4) pass 2 rotates again and
+      // writes the level's E4M3 terms straight into the swizzled images the
+      // QK MMA reads.
+      constexpr int CPR = D / 8;                           // 16-byte q chunks per row
+      constexpr int TPR = D / 4;                           // 16-byte table chunks per row
+      constexpr int PQ = (kTile * CPR + kThreads - 1) / kThreads;   // chunk tasks per thread
+      int* qpos_s = reinterpret_cast<int*>(epi + 2 * kTile);   // [128]
+      if (threadIdx.x < kTile) {
+        const int tq = qt * kTile + threadIdx.x;
+        int p = 0;
+        if (tq < prm.n_q) {
+          p = prm.qpos ? __ldg(prm.qpos + tq) : __ldcg(r.state + ST_NEXT_POS) - prm.n_q + tq;
+          if (p < 0 || p >= r.max_pos) {
+            atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+            p = 0;
+          }
+        }
+        qpos_s[threadIdx.x] = p;
+      }
+      __syncthreads();
+      for (int k = threadIdx.x; k < rows_in * TPR; k += kThreads) {
+        const int rr = k / TPR, c = k % TPR;
+        cp_async16(sbase + L::kVh + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)qpos_s[rr] * D + 4 * c);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      __syncthreads();
+      auto rotate = [&](int rrow, int chunk, float (&u)[8]) -> float {
+        float cmax = 0.f;
+        if (rrow < rows_in) {
+          const uint4 w = *reinterpret_cast<const uint4*>(sm + (q_stage(rrow) - sbase) + 16 * chunk);
+          const float4* tb = reinterpret_cast<const float4*>(sm + L::kVh + (size_t)rrow * (4 * D)) + 2 * chunk;
+          const float4 cs0 = tb[0], cs1 = tb[1];
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
+          const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
+            u[2 * e] = x0 * cc[e] - x1 * ss[e];
+            u[2 * e + 1] = x0 * ss[e] + x1 * cc[e];
+            cmax = fmaxf(cmax, fmaxf(fabsf(u[2 * e]), fabsf(u[2 * e + 1])));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[e] = 0.f;          // rows past n_q: zero queries
+        }
+        return cmax;
+      };
+      float wmax = 0.f;
+#pragma unroll 4
+      for (int i = 0; i < PQ; ++i) {
+        const int k = i * kThreads + threadIdx.x;
+        if (k >= kTile * CPR) break;                       // whole warps leave together
+        const int rrow = k / CPR, chunk = k % CPR;
+        float u[8];
+        float cmax = rotate(rrow, chunk, u);
+        // row maximum over the CPR consecutive lanes that hold the row
+#pragma unroll
+        for (int off = CPR / 2; off > 0; off >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, off));
+        if (chunk == 0) epi[rrow] = cmax;
+        wmax = fmaxf(wmax, cmax);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xFFFFFFFFu, wmax, off));
+      if (lane == 0) epi[kTile + warp] = wmax;
+      __syncthreads();
+      float qm = epi[kTile];
+#pragma unroll
+      for (int i = 1; i < kThreads / 32; ++i) qm = fmaxf(qm, epi[kTile + i]);
+      int level = prm.forced_level;
+      if (level == 0) {
+        const float lg = qm * 448.0f * r.scales[h];
+        const float vmax = 448.0f * r.scales[H + h];
+        level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg * vmax <= kLevel2MaxLV ? 2 : 3);
+      }
+#pragma unroll 2
+      for (int i = 0; i < PQ; ++i) {
+        const int k = i * kThreads + threadIdx.x;
+        if (k >= kTile * CPR) break;
+        const int rrow = k / CPR, chunk = k % CPR;
+        float u[8];
+        rotate(rrow, chunk, u);
+        // E4M3 terms of q / sigma_q (sigma_q = amax/448 of the row), exact
+        // fp32 residuals; 8 bytes per chunk per term at the chunk's swizzled
+        // place in the query images
+        float sq = epi[rrow] / 448.0f;
+        if (!(sq >= 0x1p-126f)) sq = 1.0f;
+        const float invq = 1.0f / sq;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] *= invq;
+        const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
+#pragma unroll
+        for (int term = 0; term < 3; ++term) {
+          if (term < level) {
+            uint16_t c4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(u[2 * e], u[2 * e + 1]);
+            *reinterpret_cast<uint2*>(sm + L::kQ + term * L::kQTile + off) =
+                make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
+            if (term + 1 < level) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 dq = e4m3x2_to_f32x2(c4[e]);
+                u[2 * e] -= dq.x;
+                u[2 * e + 1] -= dq.y;
+              }
+            }
+          }
+        }
+      }
+      if (threadIdx.x == 0) {
+        misc->level = level;
+        if (split == 0) r.levels[unit] = level;
+      }
+      fence_proxy_async_smem();   // generic writes -> tensor-core reads
+      __syncthreads();
+  }
+
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued = ntiles < kStages - 1 ? ntiles : kStages - 1;
-      const bool go = issued >= ntiles || mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs);
-      for (int j = issued; go && j < ntiles; ++j) {
+      for (int j = issued; j < ntiles; ++j) {
         const int s = j % kStages;
         if (!mbar_wait_bounded(bar(L::kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, abort, kWaitLimitNs))
           break;
@@ -284,9 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(L::kBarKvEmpty + s));   // the K stage is read
         return true;
       };
-      bool ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs);
-      n_qterms = misc->level;   // written before the prologue's arrivals
-      ok = ok && issue_qk(0) && (ntiles < 2 || issue_qk(1));
+      n_qterms = misc->level;   // the prologue ended with a CTA barrier
+      bool ok = issue_qk(0) && (ntiles < 2 || issue_qk(1));
       for (int j = 0; ok && j < ntiles; ++j) {
         const int b = j & 1;
         if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
@@ -321,8 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages, b = j & 1;
       bool ok = mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs);
-      // the f16 tiles hold RoPE-table rows until the query prologue is done
-      if (ok && j == 0) ok = mbar_wait_bounded(bar(L::kBarQFull), 0, abort, kWaitLimitNs);
       if (ok && j >= 2) ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       const uint8_t* src = sm + L::kV + s * L::kKVTile;
@@ -362,135 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = warp >> 2;
     const int row = threadIdx.x & (kTile - 1);
     const int quarter = warp & 3;
+    // the logit factor of this thread's query row (row amax from the prologue)
     float f_row;
     {
-      // ---------------------------------------------- query prologue
-      // (1) one position per query row; (2) the RoPE-table rows of those
-      // positions copied into the f16 V tiles' space with 16-byte cp.async
-      // (the query rows are already on their way, see above); (3) pass 1, a
-      // small rolled loop over 8-value chunks: chunk task k = i * 256 + tid
-      // is query row k / CPR, chunk k % CPR, so a warp holds every chunk of
-      // its rows and a row's amax is a shuffle reduction, and the warps'
-      // maxima give the tile's precision level; (4) pass 2 rotates again and
-      // writes the level's E4M3 terms straight into the swizzled images the
-      // QK MMA reads.
-      constexpr int CPR = D / 8;                           // 16-byte q chunks per row
-      constexpr int TPR = D / 4;                           // 16-byte table chunks per row
-      constexpr int PQ = kTile * CPR / kSoftmaxThreads;    // 8 (d = 128) or 4
-      int* qpos_s = reinterpret_cast<int*>(epi + 2 * kTile);   // [128]
-      if (threadIdx.x < kTile) {
-        const int tq = qt * kTile + threadIdx.x;
-        int p = 0;
-        if (tq < prm.n_q) {
-          p = prm.qpos ? __ldg(prm.qpos + tq) : __ldcg(r.state + ST_NEXT_POS) - prm.n_q + tq;
-          if (p < 0 || p >= r.max_pos) {
-            atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
-            p = 0;
-          }
-        }
-        qpos_s[threadIdx.x] = p;
-      }
-      sync_softmax();
-      for (int k = threadIdx.x; k < rows_in * TPR; k += kSoftmaxThreads) {
-        const int rr = k / TPR, c = k % TPR;
-        cp_async16(sbase + L::kVh + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)qpos_s[rr] * D + 4 * c);
-      }
-      cp_async_commit();
-      cp_async_wait_all();
-      sync_softmax();
-      auto rotate = [&](int rrow, int chunk, float (&u)[8]) -> float {
-        float cmax = 0.f;
-        if (rrow < rows_in) {
-          const uint4 w = *reinterpret_cast<const uint4*>(sm + (q_stage(rrow) - sbase) + 16 * chunk);
-          const float4* tb = reinterpret_cast<const float4*>(sm + L::kVh + (size_t)rrow * (4 * D)) + 2 * chunk;
-          const float4 cs0 = tb[0], cs1 = tb[1];
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-          const float cc[4] = {cs0.x, cs0.z, cs1.x, cs1.z};
-          const float ss[4] = {cs0.y, cs0.w, cs1.y, cs1.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = __uint_as_float(ww[e] << 16), x1 = __uint_as_float(ww[e] & 0xFFFF0000u);
-            u[2 * e] = x0 * cc[e] - x1 * ss[e];
-            u[2 * e + 1] = x0 * ss[e] + x1 * cc[e];
-            cmax = fmaxf(cmax, fmaxf(fabsf(u[2 * e]), fabsf(u[2 * e + 1])));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) u[e] = 0.f;          // rows past n_q: zero queries
-        }
-        return cmax;
-      };
-      float wmax = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < PQ; ++i) {
-        const int k = i * kSoftmaxThreads + threadIdx.x;
-        const int rrow = k / CPR, chunk = k % CPR;
-        float u[8];
-        float cmax = rotate(rrow, chunk, u);
-        // row maximum over the CPR consecutive lanes that hold the row
-#pragma unroll
-        for (int off = CPR / 2; off > 0; off >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, off));
-        if (chunk == 0) epi[rrow] = cmax;
-        wmax = fmaxf(wmax, cmax);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xFFFFFFFFu, wmax, off));
-      if (lane == 0) epi[kTile + warp] = wmax;
-      sync_softmax();
-      float qm = epi[kTile];
-#pragma unroll
-      for (int i = 1; i < kSoftmaxThreads / 32; ++i) qm = fmaxf(qm, epi[kTile + i]);
-      int level = prm.forced_level;
-      if (level == 0) {
-        const float lg = qm * 448.0f * r.scales[h];
-        const float vmax = 448.0f * r.scales[H + h];
-        level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg * vmax <= kLevel2MaxLV ? 2 : 3);
-      }
-#pragma unroll 2
-      for (int i = 0; i < PQ; ++i) {
-        const int k = i * kSoftmaxThreads + threadIdx.x;
-        const int rrow = k / CPR, chunk = k % CPR;
-        float u[8];
-        rotate(rrow, chunk, u);
-        // E4M3 terms of q / sigma_q (sigma_q = amax/448 of the row), exact
-        // fp32 residuals; 8 bytes per chunk per term at the chunk's swizzled
-        // place in the query images
-        float sq = epi[rrow] / 448.0f;
-        if (!(sq >= 0x1p-126f)) sq = 1.0f;
-        const float invq = 1.0f / sq;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] *= invq;
-        const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
-#pragma unroll
-        for (int term = 0; term < 3; ++term) {
-          if (term < level) {
-            uint16_t c4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(u[2 * e], u[2 * e + 1]);
-            *reinterpret_cast<uint2*>(sm + L::kQ + term * L::kQTile + off) =
-                make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
-            if (term + 1 < level) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 dq = e4m3x2_to_f32x2(c4[e]);
-                u[2 * e] -= dq.x;
-                u[2 * e + 1] -= dq.y;
-              }
-            }
-          }
-        }
-      }
-      {
-        float sq = epi[row] / 448.0f;       // this thread's softmax row
-        if (!(sq >= 0x1p-126f)) sq = 1.0f;
-        f_row = fmaxf(sq * r.scales[h] * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
-      }
-      if (threadIdx.x == 0) {
-        misc->level = level;
-        if (split == 0) r.levels[unit] = level;
-      }
-      fence_proxy_async_smem();   // generic writes -> tensor-core reads
-      mbar_arrive(bar(L::kBarQFull));
+      float sq = epi[row] / 448.0f;
+      if (!(sq >= 0x1p-126f)) sq = 1.0f;
+      f_row = fmaxf(sq * r.scales[h] * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
     }
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = trow + L::kColS + g * 128, tO = trow + L::kColO + g * 128;
