@@ -16,10 +16,12 @@ Modules:
   attention  float64 attention over the cache (the reference), brute-force
              linear window, the slot-order-positions negative case, and a
              diagnostic that mirrors the kernel's FP8 operand choices.
+  legacy     the original upkeep the ring replaced (window copy, RoPE of
+             every cached key and re-quantisation at every call).
 
 Parity pins: every function here is checked in tests/test_oracle_*.py
 against closed forms, invariants, library routines or brute force.  Nothing
 in this package is "parity unpinned".
 """
-from . import e4m3, rope, ring, attention  # noqa: F401
+from . import e4m3, rope, ring, attention, legacy  # noqa: F401
 from .ring import Ring, INT32_MIN, TO_OLDEST  # noqa: F401
