@@ -50,6 +50,10 @@ ATTN_FLOPS = 4.0 * H * N_Q * C * D                                   # QK^T and 
 ATTN_BYTES = 2 * H * C * D + N_Q * H * D * 2 + N_Q * H * D * 4       # cache, q, fp32 out
 DELTA_BYTES = 2 * H * C * D + 2 * C * 4                              # key cache read + write, positions
 LAYERS = 60         # one ring per layer: the batched write / reset of a whole step
+CALLS_PER_STEP = 240  # attention calls per step (4 passes x 60 blocks): where the old upkeep ran
+# the original upkeep per call with a full window: copy the shifted bf16 window
+# (read + write), read it again to rotate and quantise, write the FP8 cache
+LEGACY_BYTES = 3 * 2 * C * H * D * 2 + 2 * C * H * D
 H2D_BYTES = 3 * N_NEW * H * D * 2
 D2H_BYTES = N_Q * H * D * 4
 
@@ -331,8 +335,9 @@ def gpu_arm(args, rank, world):
     levels = np.concatenate(levels).ravel()
     errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
     batched = batched_upkeep(args, dev, stream) if not args.no_batched else None
+    legacy_us = legacy_upkeep_us(dev, stream) if not args.no_batched else None
     return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, e2e_ms=e2e_ms, clocks=clk.summary(),
-                batched=batched,
+                batched=batched, legacy_us=legacy_us,
                 resets=timed_resets,
                 levels=levels, device_errors=int(np.bitwise_or.reduce(errs)))
 
@@ -381,6 +386,43 @@ def batched_upkeep(args, dev, stream):
     del rings, ks, vs
     torch.cuda.empty_cache()
     return dict(write_us=w_us, delta_us=d_us)
+
+
+def legacy_upkeep_us(dev, stream):
+    """The upkeep the ring replaced, per call with a full 5,788-slot window:
+    window copy, RoPE of every cached key, window scales, re-quantisation of
+    the whole cache (two kernels).  Four rings round-robin, so each call's
+    104 MB is L2-cold; a CUDA graph of four calls, replayed."""
+    import torch
+    import ring_kv_cache_gb300 as kv
+    with torch.cuda.stream(stream):
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        rings = [kv.KvRing(H, D, C, N_NEW, MAX_POS, 10000.0, max_kv_splits=1, stream=stream) for _ in range(4)]
+        wins = [kv.LegacyWindows(r) for r in rings]
+        ks = [torch.randn((N_NEW, H, D), generator=g, device=dev).bfloat16() for _ in range(4)]
+        vs = [torch.randn((N_NEW, H, D), generator=g, device=dev).bfloat16() for _ in range(4)]
+        for _ in range(8):                       # fill every window
+            for w, k, v in zip(wins, ks, vs):
+                w.upkeep(k, v, stream=stream)
+        torch.cuda.synchronize(dev)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for _ in range(2):                   # two calls per ring: the buffers alternate back
+                for w, k, v in zip(wins, ks, vs):
+                    w.upkeep(k, v, stream=stream)
+        gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 4
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / (reps * 8)
+    del rings, wins, ks, vs
+    torch.cuda.empty_cache()
+    return us
 
 
 def reduce_max(x: float, world: int) -> float:
@@ -560,6 +602,20 @@ def main():
                              "GB/s": DELTA_BYTES / (d_us * 1e-6) / 1e9,
                              "frac_hbm": DELTA_BYTES / (d_us * 1e-6) / 1e9 / peaks["hbm"]},
             "timing": "per-kernel: CUDA graphs of 16 back-to-back calls on 16 rings, events around replays",
+            **({} if res["legacy_us"] is None else {
+                "legacy_upkeep": {
+                    "avg_call_us": res["legacy_us"], "algorithmic_bytes": LEGACY_BYTES,
+                    "GB/s": LEGACY_BYTES / (res["legacy_us"] * 1e-6) / 1e9,
+                    "frac_hbm": LEGACY_BYTES / (res["legacy_us"] * 1e-6) / 1e9 / peaks["hbm"],
+                    "per_step_us": {
+                        "legacy (upkeep in each of 240 attention calls)": CALLS_PER_STEP * res["legacy_us"],
+                        "ring (one write per layer, 60 launches)": LAYERS * w_us,
+                        **({} if res["batched"] is None else {
+                            "ring (60 layers in one batched write)": res["batched"]["write_us"]}),
+                    },
+                    "note": "the original upkeep (window copy, RoPE of every key, re-quantisation) per call; "
+                            "the pages' step went from 69.7 ms to 6.2 ms of upkeep on 4 H100s",
+                }}),
             **({} if res["batched"] is None else {
                 "write_batched_60_layers": {
                     "avg_launch_us": res["batched"]["write_us"], "algorithmic_bytes": LAYERS * WRITE_BYTES,

@@ -146,6 +146,26 @@ kvring_status kvring_write_frame(kvring_t* ring, const void* k_bf16, const void*
  * Errors: INVALID_ARG (delta < -1 or >= max_position). */
 kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
 
+/* The cache upkeep the ring replaced, kept as the comparison path ("Where
+ * the Time Went": before the ring, every attention call re-applied RoPE to
+ * every cached key, re-quantised the cache to FP8 and shifted the window by
+ * copying it).  The caller keeps the window of the last `capacity` tokens,
+ * unrotated bf16 [capacity][H][d] in time order, in two buffer pairs and
+ * alternates them: this call copies wk_in/wv_in shifted by the n new tokens
+ * (the n oldest leave once the window is full) plus the frame k/v (bf16
+ * [n][H][d]) into wk_out/wv_out, takes per-head scales from the whole new
+ * window (amax of the rotated keys, of the values, over 448), and rewrites
+ * the ring's FP8 cache from it: window slot i -> ring slot i, key rotated at
+ * position base + i (base = position of the oldest token in the window,
+ * positions counting the tokens given so far from 0), same pinned fp32 RoPE
+ * and E4M3 conversion as kvring_write_frame.  Afterwards kvring_attention
+ * reads the ring as usual.  Do not mix with kvring_write_frame on one ring.
+ * Errors: INVALID_ARG (NULL, unaligned or aliased buffers), CAPACITY
+ * (n > capacity or n > max_tokens). */
+kvring_status kvring_legacy_upkeep(kvring_t* ring, const void* wk_in, const void* wv_in, void* wk_out,
+                                   void* wv_out, const void* k_bf16, const void* v_bf16, int32_t n,
+                                   void* stream);
+
 /* Largest number of rings one batched call takes (a model's layers). */
 #define KVRING_MAX_BATCH 64
 

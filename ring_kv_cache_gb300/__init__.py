@@ -23,6 +23,7 @@ __all__ = [
     "kvring_required_bytes", "kvring_create", "kvring_destroy", "kvring_calibrate_scales",
     "kvring_write_frame", "kvring_delta_rotate", "kvring_attention", "kvring_attention_noalloc",
     "kvring_write_frames_many", "kvring_delta_rotate_many", "write_frames_many", "delta_rotate_many",
+    "kvring_legacy_upkeep", "LegacyWindows",
     "kvring_export",
     "kvring_status_string", "encode_e4m3", "STATE",
 ]
@@ -85,6 +86,7 @@ def lib():
         "kvring_write_frame": (i32, [vp, vp, vp, vp, i32, vp]),
         "kvring_delta_rotate": (i32, [vp, i32, vp]),
         "kvring_write_frames_many": (i32, [vp, i32, vp, vp, vp, i32, vp]),
+        "kvring_legacy_upkeep": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, vp]),
         "kvring_delta_rotate_many": (i32, [vp, i32, i32, vp]),
         "kvring_attention": (i32, [vp, vp, vp, i32, vp, i32, vp]),
         "kvring_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, vp]),
@@ -225,6 +227,36 @@ def delta_rotate_many(rings, delta: int = TO_OLDEST, stream=None) -> None:
     if not rings:
         raise ValueError("no rings")
     kvring_delta_rotate_many([r.handle for r in rings], delta, rings[0]._s(stream))
+
+
+def kvring_legacy_upkeep(handle, wk_in, wv_in, wk_out, wv_out, k, v, n, stream_ptr) -> None:
+    _check(lib().kvring_legacy_upkeep(handle, _ptr(wk_in), _ptr(wv_in), _ptr(wk_out), _ptr(wv_out), _ptr(k),
+                                      _ptr(v), int(n), stream_ptr), "kvring_legacy_upkeep")
+
+
+class LegacyWindows:
+    """The two bf16 window buffer pairs the legacy upkeep alternates between."""
+
+    def __init__(self, ring: "KvRing"):
+        shape = (ring.C, ring.H, ring.d)
+        self.ring = ring
+        self.k = [torch.zeros(shape, dtype=torch.bfloat16, device=ring.device) for _ in range(2)]
+        self.v = [torch.zeros(shape, dtype=torch.bfloat16, device=ring.device) for _ in range(2)]
+        self.cur = 0
+
+    def upkeep(self, k, v, stream=None) -> None:
+        """One call of the original upkeep on `ring` with the frame (k, v)."""
+        r = self.ring
+        n = _tokens(k, r.H, r.d, "k")
+        if _tokens(v, r.H, r.d, "v") != n:
+            raise ValueError("k and v must hold the same number of tokens")
+        a, b = self.cur, 1 - self.cur
+        kvring_legacy_upkeep(r.handle, self.k[a], self.v[a], self.k[b], self.v[b], k, v, n, r._s(stream))
+        self.cur = b
+
+    def window(self):
+        """The current (k, v) bf16 windows [capacity, H, d]."""
+        return self.k[self.cur], self.v[self.cur]
 
 
 def kvring_attention(handle, q, qpos, n_q, out, out_dtype, stream_ptr) -> None:

@@ -377,6 +377,171 @@ __global__ void __launch_bounds__(kThreads) k_delta_many(const __grid_constant__
   delta_body<D, kDeltaManyU>(b.r[blockIdx.y], delta_arg, blockIdx.x, gridDim.x);
 }
 
+// ------------------------------------------------------- legacy upkeep ---
+// The upkeep the ring replaced ("Where the Time Went": every call re-applied
+// RoPE to every cached key, re-quantised the cache and shifted the window by
+// copying it), kept as the comparison path.  The window holds the unrotated
+// bf16 keys and values of the last C tokens in time order ([C][H][d], token-
+// major like the frames).  Ring state words reused: n_valid = tokens in the
+// window, next_pos = tokens seen (the next token's position).
+//
+// Pass 1, one thread per 16-value chunk of every (window slot, head): copy
+// the shifted window (the oldest tokens leave once it is full, the frame
+// enters at its end) into the other window buffer, and take each head's
+// maximum of the rotated keys (RoPE at position base + slot) and of the
+// values; the last block turns the maxima into scales.
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_legacy_shift(RingDev r, const uint16_t* __restrict__ wk_in,
+                                                           const uint16_t* __restrict__ wv_in,
+                                                           uint16_t* __restrict__ wk_out, uint16_t* __restrict__ wv_out,
+                                                           const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                                                           int n) {
+  constexpr int CH = D / 16;
+  __shared__ int s_fill, s_total, s_last;
+  if (threadIdx.x == 0) {
+    s_fill = __ldcg(r.state + ST_NVALID);
+    s_total = __ldcg(r.state + ST_NEXT_POS);
+  }
+  __syncthreads();
+  const int H = r.H, C = r.C;
+  const int fill = s_fill, total = s_total;
+  const int nf = fill + n < C ? fill + n : C;          // tokens in the new window
+  const int keep = nf - n;                             // old tokens that stay
+  const int base = total + n - nf;                     // position of window slot 0
+  const long long per = (long long)nf * H * CH;
+  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
+  float m = 0.f;
+  int isv = 0, h = 0, chunk = 0;
+  if (gid < 2 * per) {
+    isv = gid >= per;
+    const long long w = isv ? gid - per : gid;
+    chunk = (int)(w % CH);
+    const long long th = w / CH;
+    h = (int)(th % H);
+    const int i = (int)(th / H);                       // window slot
+    const uint16_t* src = i < keep ? (isv ? wv_in : wk_in) + ((size_t)(fill - keep + i) * H + h) * D
+                                   : (isv ? v : k) + ((size_t)(i - keep) * H + h) * D;
+    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(src) + 2 * chunk);
+    const uint4 b = __ldcs(reinterpret_cast<const uint4*>(src) + 2 * chunk + 1);
+    uint4* dst = reinterpret_cast<uint4*>((isv ? wv_out : wk_out) + ((size_t)i * H + h) * D) + 2 * chunk;
+    dst[0] = a;
+    dst[1] = b;
+    float x[16];
+    unpack_bf16x16(a, b, x);
+    bool ok = true;
+    if (!isv) {
+      const int p = base + i;
+      if (p < 0 || p >= r.max_pos) {
+        ok = false;
+        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+      } else {
+        float4 cs[4];
+        load_table16(r.table, D, p, chunk, cs);
+        rope_pinned(x, cs);
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(x[e]));
+    }
+  }
+#pragma unroll
+  for (int off = CH / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if (gid < 2 * per && chunk == 0 && m > 0.f) atomicMax(r.amax + isv * H + h, __float_as_uint(m));
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int tk = atomicAdd(r.state + ST_TICKET_CALIB, 1);
+    s_last = tk == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (int i = threadIdx.x; i < 2 * H; i += kThreads) {
+      const float a = __uint_as_float(atomicExch(r.amax + i, 0u));
+      float sc = __fdiv_rn(a, 448.0f);
+      if (!(sc >= 0x1p-126f)) sc = 1.0f;
+      r.scales[i] = sc;
+      r.scales[2 * H + i] = __fdiv_rn(1.0f, sc);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      r.state[ST_TICKET_CALIB] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// Pass 2: the whole window rotated again and quantised with the new scales
+// into the FP8 ring (slot = window slot), positions base + slot; the last
+// block advances the state.
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_legacy_quantise(RingDev r, const uint16_t* __restrict__ wk,
+                                                              const uint16_t* __restrict__ wv, int n) {
+  constexpr int CH = D / 16;
+  __shared__ int s_fill, s_total;
+  if (threadIdx.x == 0) {
+    s_fill = __ldcg(r.state + ST_NVALID);
+    s_total = __ldcg(r.state + ST_NEXT_POS);
+  }
+  __syncthreads();
+  const int H = r.H, C = r.C;
+  const int fill = s_fill, total = s_total;
+  const int nf = fill + n < C ? fill + n : C;
+  const int base = total + n - nf;
+  const long long per = (long long)nf * H * CH;
+  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
+  if (gid < 2 * per) {
+    const int isv = gid >= per;
+    const long long w = isv ? gid - per : gid;
+    const int chunk = (int)(w % CH);
+    const long long th = w / CH;
+    const int h = (int)(th % H);
+    const int i = (int)(th / H);
+    const uint4* src = reinterpret_cast<const uint4*>((isv ? wv : wk) + ((size_t)i * H + h) * D) + 2 * chunk;
+    float x[16];
+    unpack_bf16x16(__ldcs(src), __ldcs(src + 1), x);
+    bool ok = true;
+    if (!isv) {
+      const int p = base + i;
+      if (p < 0 || p >= r.max_pos) {
+        ok = false;
+      } else {
+        float4 cs[4];
+        load_table16(r.table, D, p, chunk, cs);
+        rope_pinned(x, cs);
+      }
+      if (h == 0 && chunk == 0) r.slot_pos[i] = p;
+    }
+    if (ok) {
+      const float inv = r.scales[(isv ? 3 : 2) * H + h];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = __fmul_rn(x[e], inv);
+      *reinterpret_cast<uint4*>((isv ? r.v : r.k) + ((size_t)h * C + i) * D + chunk * 16) = pack_e4m3x16(x);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
+    if (tk == (int)gridDim.x - 1) {
+      __threadfence();
+      r.state[ST_NVALID] = nf;
+      r.state[ST_HEAD] = nf % C;
+      r.state[ST_NEXT_POS] = total + n;
+      const unsigned long long tot =
+          ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
+          (unsigned long long)n;
+      r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
+      r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
+      r.state[ST_OLDEST_POS] = base;
+      r.state[ST_CALIBRATED] = 1;
+      r.state[ST_TICKET_WRITE] = 0;
+      __threadfence();
+    }
+  }
+}
+
 // -------------------------------------------------------- codec (tests) ---
 __global__ void k_encode(const float* __restrict__ in, uint8_t* __restrict__ out, int64_t n) {
   const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 2;
@@ -471,6 +636,27 @@ cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s) {
     k_delta<128><<<g, kThreads, 0, s>>>(r, delta);
   else
     k_delta<64><<<g, kThreads, 0, s>>>(r, delta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_legacy_upkeep(const RingDev& r, const void* wk_in, const void* wv_in, void* wk_out,
+                                 void* wv_out, const void* k, const void* v, int n, cudaStream_t s) {
+  // sized for a full window; threads past the current fill exit at once
+  const long long items = 2LL * r.C * r.H * (r.D / 16);
+  const unsigned g = grid_for(items);
+  const auto* ki = static_cast<const uint16_t*>(wk_in);
+  const auto* vi = static_cast<const uint16_t*>(wv_in);
+  auto* ko = static_cast<uint16_t*>(wk_out);
+  auto* vo = static_cast<uint16_t*>(wv_out);
+  const auto* kn = static_cast<const uint16_t*>(k);
+  const auto* vn = static_cast<const uint16_t*>(v);
+  if (r.D == 128) {
+    k_legacy_shift<128><<<g, kThreads, 0, s>>>(r, ki, vi, ko, vo, kn, vn, n);
+    k_legacy_quantise<128><<<g, kThreads, 0, s>>>(r, ko, vo, n);
+  } else {
+    k_legacy_shift<64><<<g, kThreads, 0, s>>>(r, ki, vi, ko, vo, kn, vn, n);
+    k_legacy_quantise<64><<<g, kThreads, 0, s>>>(r, ko, vo, n);
+  }
   return cudaGetLastError();
 }
 

@@ -324,6 +324,20 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, in
   return cuda_status(kvr::launch_delta_many(b, count, delta, (cudaStream_t)stream));
 }
 
+kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* wv_in, void* wk_out, void* wv_out,
+                                   const void* k, const void* v, int32_t n, void* stream) {
+  if (!r || !wk_in || !wv_in || !wk_out || !wv_out || !k || !v || n < 1) return KVRING_ERR_INVALID_ARG;
+  const void* ptrs[6] = {wk_in, wv_in, wk_out, wv_out, k, v};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return KVRING_ERR_INVALID_ARG;
+  if (wk_in == wk_out || wv_in == wv_out || wk_out == wv_out) return KVRING_ERR_INVALID_ARG;
+  if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+  const kvring_status st = cuda_status(
+      kvr::launch_legacy_upkeep(r->dev, wk_in, wv_in, wk_out, wv_out, k, v, n, (cudaStream_t)stream));
+  if (st == KVRING_OK) r->calibrated = true;   // the path sets its own scales
+  return st;
+}
+
 kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, int32_t n_q, void* out,
                                int32_t out_dtype, void* stream) {
   if (!r || !q || !out || !aligned(q, 16) || !aligned(out, 16) || (qpos && !aligned(qpos, 4)) || n_q < 1)

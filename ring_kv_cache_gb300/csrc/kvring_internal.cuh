@@ -495,6 +495,8 @@ struct DeltaMany {
 };
 cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t s);
 cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStream_t s);
+cudaError_t launch_legacy_upkeep(const RingDev& r, const void* wk_in, const void* wv_in, void* wk_out,
+                                 void* wv_out, const void* k, const void* v, int n, cudaStream_t s);
 cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              const AttnLaunch& a, cudaStream_t s);
 size_t attention_smem_bytes(int D);
