@@ -64,6 +64,15 @@ __device__ __forceinline__ void load_table16(const float* table, int D, int p, i
   for (int i = 0; i < 4; ++i) cs[i] = __ldg(t + i);
 }
 
+// The same rotation for 2 adjacent pairs, cos/sin in `cs` as (c0, s0, c1, s1).
+__device__ __forceinline__ void rope_pinned2(float (&x)[4], const float4& cs) {
+  const float x0 = x[0], x1 = x[1], x2 = x[2], x3 = x[3];
+  x[0] = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+  x[1] = __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+  x[2] = __fsub_rn(__fmul_rn(x2, cs.z), __fmul_rn(x3, cs.w));
+  x[3] = __fadd_rn(__fmul_rn(x2, cs.w), __fmul_rn(x3, cs.z));
+}
+
 // ------------------------------------------------------------ calibrate ---
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_calibrate(RingDev r, const uint16_t* __restrict__ k,
@@ -258,16 +267,299 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
   write_body<D, kWriteU>(r, k, v, pos, n, blockIdx.x, gridDim.x);
 }
 
-// Many rings of one shape in one launch: ring blockIdx.y, the same blocks
-// per ring as a single-ring write.
-// Batched: two chunks per thread and four blocks per SM (a few registers
-// spill); over 60 rings this measured 108.8 us against 152.8 us at three
-// blocks per SM and 205 us at four chunks per thread.
-constexpr int kWriteManyU = 2;
+// Many rings of one shape in one launch, as a bulk-copy pipeline.  The work
+// is cut into units of whole tokens (TU = RU / H tokens of all H heads, RU =
+// 8192 / D rows, 16 KB of bf16) -- or, when one token's heads exceed RU rows,
+// of one token's heads in groups of RU -- so every unit is a contiguous run of
+// the frame; each ring's key and value units alternate, and block b of G
+// takes the b-th G-th of the unit list.  One producer thread streams each
+// unit into a shared-memory stage with cp.async.bulk: the rows, and for keys
+// the RoPE rows of the unit's tokens (one copy when their positions are
+// consecutive); sixteen consumer warps rotate, scale and quantise them (the
+// single-ring write's arithmetic, byte for byte) and store the codes.
+//
+// A unit has RU x D/16 = 512 places of 16 values; consumer thread `tid`
+// keeps place tid in every unit: row tid / CH (CH = D/16), lane k = tid % CH
+// in the row, and of the row's D/8 runs of 8 values the runs k and k + CH.
+// A quarter-warp then reads 128 contiguous input bytes and writes 64
+// contiguous output bytes per run; all shared-memory offsets are constants of
+// the thread, so a unit costs its arithmetic and little else.
+//
+// Stage layout: [TU][HU][D] bf16 | [TU][D] fp32 RoPE rows | the unit's token
+// positions (explicit positions only), head and next_pos.
+constexpr int kWmConsumerWarps = 16;
+constexpr int kWmThreads = 32 * (kWmConsumerWarps + 1);  // one block per SM at 120 registers
+constexpr int kWmStageBudget = 200 * 1024;               // bytes of stages per block
+constexpr int kWmMaxStages = 16;
+constexpr uint64_t kWmWaitLimitNs = 1000000000ull;       // one second
+static_assert(32 * kWmConsumerWarps == 512, "one place per consumer thread and unit");
+
+struct WmGeom {
+  int HU, TU, NG, tab_off, pos_off, stage_bytes, stages;
+};
+__host__ __device__ inline WmGeom wm_geom(int H, int D) {
+  WmGeom g;
+  const int RU = 8192 / D;
+  if (H <= RU) {
+    g.HU = H;
+    g.TU = RU / H;
+    g.NG = 1;
+  } else {
+    g.HU = RU;
+    g.TU = 1;
+    g.NG = (H + RU - 1) / RU;
+  }
+  g.tab_off = g.TU * g.HU * D * 2;
+  g.pos_off = g.tab_off + g.TU * D * 4;
+  g.stage_bytes = (g.pos_off + (g.TU + 2) * 4 + 127) / 128 * 128;
+  g.stages = kWmStageBudget / g.stage_bytes;
+  if (g.stages > kWmMaxStages) g.stages = kWmMaxStages;
+  if (g.stages < 2) g.stages = 2;
+  return g;
+}
+// units per kind and ring
+__host__ __device__ inline long long wm_units(const WmGeom& g, int n) {
+  return (long long)((n + g.TU - 1) / g.TU) * g.NG;
+}
+
+// One consumer thread's place in one unit: read its two runs (and for keys
+// their RoPE words) from the stage, hand the stage back (once per warp),
+// then rotate, scale, quantise and store.
+template <int D, bool KEY>
+__device__ __forceinline__ void wm_place(const RingDev& r, const uint8_t* st, const int* hdr, bool act, bool expl,
+                                         int in_off, int tab_off, int dt, int k, int h, int slot, int p_impl,
+                                         float inv, uint32_t empty_bar, int lane) {
+  constexpr int CH = D / 16;
+  uint4 in[2];
+  float4 cs[2][2];
+  int p = 0;
+  bool ok = act;
+  if (act) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) in[j] = *reinterpret_cast<const uint4*>(st + in_off + 16 * CH * j);
+    if (KEY) {
+      p = expl ? hdr[dt] : p_impl;
+      ok = p >= 0 && p < r.max_pos;
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          cs[j][0] = *reinterpret_cast<const float4*>(st + tab_off + 32 * CH * j);
+          cs[j][1] = *reinterpret_cast<const float4*>(st + tab_off + 32 * CH * j + 16);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+  if (!act) return;
+  if (KEY) {
+    if (!ok) atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+    if (h == 0 && k == 0) r.slot_pos[slot] = p;
+    if (!ok) return;
+  }
+  uint8_t* out = (KEY ? r.k : r.v) + ((size_t)h * r.C + slot) * D + 8 * k;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t wv[4] = {in[j].x, in[j].y, in[j].z, in[j].w};
+    uint32_t code[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float x[4] = {__uint_as_float(wv[2 * i] << 16), __uint_as_float(wv[2 * i] & 0xFFFF0000u),
+                    __uint_as_float(wv[2 * i + 1] << 16), __uint_as_float(wv[2 * i + 1] & 0xFFFF0000u)};
+      if (KEY) rope_pinned2(x, cs[j][i]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) x[c] = __fmul_rn(x[c], inv);
+      code[i] = (uint32_t)f32x2_to_e4m3x2(x[0], x[1]) | ((uint32_t)f32x2_to_e4m3x2(x[2], x[3]) << 16);
+    }
+    *reinterpret_cast<uint2*>(out + 8 * CH * j) = make_uint2(code[0], code[1]);
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 4) k_write_many(const __grid_constant__ WriteMany b, int n) {
-  const int i = blockIdx.y;
-  write_body<D, kWriteManyU>(b.r[i], b.k[i], b.v[i], b.pos[i], n, blockIdx.x, gridDim.x);
+__global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany b, int count, int n) {
+  constexpr int CH = D / 16;
+  extern __shared__ __align__(128) uint8_t wsm[];
+  __shared__ __align__(8) uint64_t full[kWmMaxStages], empty[kWmMaxStages];
+  __shared__ int s_abort;
+  const int H = b.r[0].H, C = b.r[0].C;
+  const WmGeom g = wm_geom(H, D);
+  const int S = g.stages;
+  const long long ur = wm_units(g, n);
+  const long long up = 2 * ur;  // units per ring: key and value units alternate
+  const long long total = up * count;
+  const long long u_begin = total * blockIdx.x / gridDim.x;
+  const long long u_end = total * (blockIdx.x + 1) / gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kWmConsumerWarps);
+    }
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  griddep_launch_dependents();
+  griddep_wait();  // the rings are touched only after the preceding kernel
+  __syncthreads();
+  if (u_begin >= u_end) return;
+  volatile int* abort = &s_abort;
+  const uint32_t base = smem_u32(wsm);
+  // unit u = ring * up + jv; jv = 2 (tb NG + hg) + (1 for values)
+  int ring = (int)(u_begin / up), jv = (int)(u_begin % up);
+  int tb = (jv >> 1) / g.NG, hg = (jv >> 1) % g.NG;
+  int s = 0;
+  uint32_t ph = 0;
+
+  if (warp == kWmConsumerWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane != 0) return;
+    int cur = -1, head = 0, next = 0;
+    long long i = 0;
+    for (long long u = u_begin; u < u_end; ++u, ++i) {
+      if (i >= S && !mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abort, kWmWaitLimitNs)) break;
+      const bool isv = jv & 1;
+      const int t0 = tb * g.TU;
+      const int ntok = min(g.TU, n - t0), nh = min(g.HU, H - hg * g.HU);
+      const RingDev& r = b.r[ring];
+      if (ring != cur) {
+        cur = ring;
+        head = __ldcg(r.state + ST_HEAD);
+        next = __ldcg(r.state + ST_NEXT_POS);
+      }
+      int* hdr = reinterpret_cast<int*>(wsm + (size_t)s * g.stage_bytes + g.pos_off);
+      hdr[g.TU] = head;
+      hdr[g.TU + 1] = next;
+      const uint32_t in_bytes = (uint32_t)(ntok * nh) * D * 2;
+      uint32_t bytes = in_bytes;
+      const int32_t* pos = b.pos[ring];
+      const int p0 = next + t0;
+      const bool one_copy = !isv && !pos && p0 >= 0 && p0 + ntok <= r.max_pos;
+      if (!isv) {
+        if (one_copy) {
+          bytes += (uint32_t)ntok * D * 4;
+        } else {
+          for (int t = 0; t < ntok; ++t) {
+            const int p = pos ? __ldg(pos + t0 + t) : p0 + t;
+            hdr[t] = p;
+            if (p >= 0 && p < r.max_pos) bytes += D * 4;
+          }
+        }
+      }
+      const uint32_t fb = smem_u32(&full[s]);
+      const uint32_t sa = base + (uint32_t)s * g.stage_bytes;
+      mbar_arrive_expect_tx(fb, bytes);
+      bulk_load(sa, (isv ? b.v[ring] : b.k[ring]) + ((size_t)t0 * H + hg * g.HU) * D, in_bytes, fb);
+      if (one_copy) {
+        bulk_load(sa + g.tab_off, r.table + (size_t)p0 * D, (uint32_t)ntok * D * 4, fb);
+      } else if (!isv) {
+        for (int t = 0; t < ntok; ++t) {
+          const int p = hdr[t];
+          if (p >= 0 && p < r.max_pos) bulk_load(sa + g.tab_off + t * D * 4, r.table + (size_t)p * D, D * 4, fb);
+        }
+      }
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+      if (++jv == (int)up) {
+        jv = 0;
+        tb = hg = 0;
+        ++ring;
+      } else if (!(jv & 1) && ++hg == g.NG) {
+        hg = 0;
+        ++tb;
+      }
+    }
+    if (*abort) {
+      // leave no copy in flight: wait (bounded) for the stages issued last
+      int no_abort = 0;
+      for (long long q = i > S ? i - S : 0; q < i; ++q)
+        mbar_wait_bounded(smem_u32(&full[q % S]), (uint32_t)((q / S) & 1), &no_abort, kWmWaitLimitNs);
+      atomicOr(reinterpret_cast<unsigned*>(b.r[cur < 0 ? 0 : cur].state + ST_ERROR), KVRING_DEVERR_TIMEOUT);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int row = threadIdx.x / CH, k = threadIdx.x % CH;
+  const int dt = row / g.HU, hl = row % g.HU;
+  const int in_off = row * D * 2 + 16 * k;
+  const int tab_off = g.tab_off + dt * D * 4 + 32 * k;
+  float invk = 1.0f, invv = 1.0f;
+  int done = 0, head = 0, next = 0, cur = -1, cur_hg = -1;
+  for (long long u = u_begin; u < u_end; ++u) {
+    if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abort, kWmWaitLimitNs)) {
+      if (lane == 0) atomicOr(reinterpret_cast<unsigned*>(b.r[ring].state + ST_ERROR), KVRING_DEVERR_TIMEOUT);
+      break;
+    }
+    const bool isv = jv & 1;
+    const int t0 = tb * g.TU;
+    const int ntok = min(g.TU, n - t0), nh = min(g.HU, H - hg * g.HU);
+    const RingDev& r = b.r[ring];
+    const int h = hg * g.HU + hl;
+    if (ring != cur || hg != cur_hg) {
+      cur = ring;
+      cur_hg = hg;
+      const int hc = min(h, H - 1);
+      invk = r.scales[2 * H + hc];
+      invv = r.scales[3 * H + hc];
+    }
+    const uint8_t* st = wsm + (size_t)s * g.stage_bytes;
+    const int* hdr = reinterpret_cast<const int*>(st + g.pos_off);
+    head = hdr[g.TU];
+    next = hdr[g.TU + 1];
+    const bool act = dt < ntok && hl < nh;
+    int slot = head + t0 + dt;
+    if (slot >= C) slot -= C;
+    const uint32_t eb = smem_u32(&empty[s]);
+    if (isv)
+      wm_place<D, false>(r, st, hdr, act, false, in_off, tab_off, dt, k, h, slot, 0, invv, eb, lane);
+    else
+      wm_place<D, true>(r, st, hdr, act, b.pos[ring] != nullptr, in_off, tab_off, dt, k, h, slot, next + t0 + dt,
+                        invk, eb, lane);
+    ++done;
+    if (++s == S) {
+      s = 0;
+      ph ^= 1;
+    }
+    // Ring done for this block: every consumer warp adds its units to the
+    // ring's ticket; the warp that completes (consumer warps) x (units per
+    // ring) publishes the new ring state.
+    const bool ring_end = jv + 1 == (int)up;
+    if (ring_end || u + 1 == u_end) {
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        const int tk = atomicAdd(r.state + ST_TICKET_WRITE, done);
+        if (tk + done == kWmConsumerWarps * (int)up) {
+          __threadfence();
+          int nh2 = head + n;
+          if (nh2 >= C) nh2 -= C;
+          const int nv = r.state[ST_NVALID] + n;
+          r.state[ST_HEAD] = nh2;
+          r.state[ST_NVALID] = nv < C ? nv : C;
+          const unsigned long long tot =
+              ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
+              (unsigned long long)n;
+          r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
+          r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
+          r.state[ST_NEXT_POS] = next + n;
+          r.state[ST_OLDEST_POS] = __ldcg(r.slot_pos + (nv >= C ? nh2 : 0));
+          r.state[ST_TICKET_WRITE] = 0;
+          __threadfence();
+        }
+      }
+      done = 0;
+    }
+    if (ring_end) {
+      jv = 0;
+      tb = hg = 0;
+      ++ring;
+    } else if (!(++jv & 1) && ++hg == g.NG) {
+      hg = 0;
+      ++tb;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- delta ---
@@ -596,12 +888,21 @@ cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const i
 }
 
 cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t s) {
+  // one block per SM, each streaming its share of the units
   const RingDev& r = b.r[0];
-  const long long items = 2LL * n * r.H * (r.D / 16);
+  const WmGeom g = wm_geom(r.H, r.D);
+  const long long units = 2LL * count * wm_units(g, n);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long grid = sms;
+  if (grid > units) grid = units;
+  if (grid < 1) grid = 1;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteManyU - 1) / kWriteManyU), (unsigned)count), s, attr);
-  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write_many<128>, b, n);
-  return cudaLaunchKernelEx(&cfg, k_write_many<64>, b, n);
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)grid), s, attr);
+  cfg.blockDim = dim3(kWmThreads);
+  cfg.dynamicSmemBytes = (size_t)g.stages * g.stage_bytes;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write_many<128>, b, count, n);
+  return cudaLaunchKernelEx(&cfg, k_write_many<64>, b, count, n);
 }
 
 cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStream_t s) {
@@ -637,6 +938,12 @@ cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s) {
   else
     k_delta<64><<<g, kThreads, 0, s>>>(r, delta);
   return cudaGetLastError();
+}
+
+cudaError_t cache_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(k_write_many<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWmStageBudget);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_write_many<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWmStageBudget);
 }
 
 cudaError_t launch_legacy_upkeep(const RingDev& r, const void* wk_in, const void* wv_in, void* wk_out,

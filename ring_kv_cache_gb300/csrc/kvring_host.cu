@@ -196,7 +196,7 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   d.max_splits = cfg->max_kv_splits;
   d.qtiles_max = p.qtiles;
 
-  if (kvr::attention_prepare(d.D) != cudaSuccess) {
+  if (kvr::attention_prepare(d.D) != cudaSuccess || kvr::cache_prepare() != cudaSuccess) {
     delete r;
     return KVRING_ERR_CUDA;
   }

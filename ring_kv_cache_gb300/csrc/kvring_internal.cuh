@@ -186,6 +186,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Wait until at most N of this thread's most recent groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_stages() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // -------------------------------------------------------------- cluster ---
 // Barrier over every thread of every CTA of the cluster (all warps
@@ -493,6 +498,7 @@ struct WriteMany {
 struct DeltaMany {
   RingDev r[kMaxBatch];
 };
+cudaError_t cache_prepare();   // kernel attributes (shared-memory size) of the cache kernels
 cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t s);
 cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStream_t s);
 cudaError_t launch_legacy_upkeep(const RingDev& r, const void* wk_in, const void* wv_in, void* wk_out,
