@@ -4,13 +4,17 @@
 // "Runway Characters: Serving a 57B Video Diffusion Transformer for
 // Real-Time Conversation", section "Do It Once, at Write Time".
 //
-// Work decomposition (all three kernels): one thread owns 16 consecutive
-// elements of one (token or slot, head) row, i.e. one 16-byte chunk of FP8
-// output; consecutive threads walk a row, then the next head, then the next
-// token, so bf16 input reads are fully contiguous and every cache row is
-// written as whole 16-byte vectors.  Completion work (ring state, scales,
-// position map) is done by the last block to finish, found with an atomic
-// ticket; no block ever waits on another.
+// Work decomposition.  Calibration and the single-ring write: one thread
+// owns 16 consecutive elements of one (token, head) row, i.e. one 16-byte
+// chunk of FP8 output; consecutive threads walk a row, then the next head,
+// then the next token, so bf16 input reads are fully contiguous and every
+// cache row is written as whole 16-byte vectors.  The batched write and the
+// delta rotation are bulk-copy pipelines: one block per SM, one producer
+// thread streaming contiguous 16 KB units into shared-memory stages, sixteen
+// consumer warps doing the arithmetic and storing whole 16-byte vectors.
+// Completion work (ring state, scales, position map) is done by the last
+// block (or warp) to finish, found with an atomic ticket; no block ever
+// waits on another.
 //
 // Arithmetic is pinned so that cache bytes are reproducible: products and
 // sums are rounded one at a time (__fmul_rn / __fadd_rn / __fsub_rn, no
@@ -563,110 +567,201 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
 }
 
 // ---------------------------------------------------------------- delta ---
-// A few blocks per SM, each thread looping over 16-byte chunks of filled key
-// rows (kDeltaU independent chunks in flight per iteration), so the number of
-// completion tickets stays small.
-constexpr int kDeltaU = 4;
+// Delta rotation of one or many rings as a bulk-copy pipeline.  A unit is
+// RU = 16384 / D consecutive slots of one head of one ring, i.e. one
+// contiguous 16 KB run of key codes; ring r contributes H x ceil(C / RU)
+// units (sized for a full ring: rows at or past the fill level are neither
+// copied nor written).  Block b of G takes the b-th G-th of the unit list.
+// One producer thread resolves each ring's delta and fill level from its
+// state and streams the unit's filled rows into a shared-memory stage with
+// cp.async.bulk; sixteen consumer warps decode, rotate and re-encode them
+// (the single-ring arithmetic, byte for byte) and store the codes back in
+// place with 16-byte stores.  Consumer thread `tid` keeps chunk tid % CH of
+// rows tid / CH + j * (512 / CH), so its table values are fixed per ring.
+constexpr int kDpConsumerWarps = 16;
+constexpr int kDpThreads = 32 * (kDpConsumerWarps + 1);
+constexpr int kDpUnitBytes = 16384;
+constexpr int kDpStages = 12;
+constexpr int kDpSmemBytes = kDpStages * kDpUnitBytes;
+static_assert(32 * kDpConsumerWarps == 512, "512 consumer threads");
 
-// One ring's share of a delta rotation: block `blk` of `nblk`, U chunks in
-// flight per thread and iteration.
-template <int D, int U>
-__device__ __forceinline__ void delta_body(const RingDev& r, int delta_arg, int blk, int nblk) {
-  constexpr int CH = D / 16;
-  __shared__ int s_delta, s_nv, s_last;
-  __shared__ float4 s_cs[D / 4];  // table row of delta: D/2 (cos, sin) pairs
+template <int D>
+__global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_constant__ DeltaMany b, int count,
+                                                              int delta_arg) {
+  constexpr int CH = D / 16;             // 16-byte chunks per row
+  constexpr int RU = kDpUnitBytes / D;   // rows per unit
+  constexpr int RSTEP = 512 / CH;        // rows between a thread's chunks
+  constexpr int PASSES = RU / RSTEP;
+  static_assert(PASSES * RSTEP == RU && RU <= 512, "unit shape");
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[kDpStages], empty[kDpStages];
+  __shared__ int hdr[kDpStages][2];  // filled rows of the unit, its ring's delta (-1: none)
+  __shared__ int s_abort;
+  const int H = b.r[0].H, C = b.r[0].C;
+  const int runs = (C + RU - 1) / RU;
+  const long long up = (long long)H * runs;  // units per ring
+  const long long total = up * count;
+  const long long u_begin = total * blockIdx.x / gridDim.x;
+  const long long u_end = total * (blockIdx.x + 1) / gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    const int nv = __ldcg(r.state + ST_NVALID);
-    int d = delta_arg;
-    if (d == KVRING_DELTA_TO_OLDEST) d = nv > 0 ? __ldcg(r.state + ST_OLDEST_POS) : 0;
-    if (d < 0 || d >= r.max_pos) {
-      if (blk == 0) atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_DELTA);
-      d = -1;  // skip the rotation entirely
+    for (int i = 0; i < kDpStages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kDpConsumerWarps);
     }
-    s_delta = d;
-    s_nv = nv;
+    s_abort = 0;
+    mbar_fence_init();
   }
+  griddep_launch_dependents();
+  griddep_wait();  // the rings are touched only after the preceding kernel
   __syncthreads();
-  const int delta = s_delta;
-  const int nv = s_nv;
-  // positions of the filled slots, spread over all blocks (nobody reads them here)
-  if (delta > 0)
-    for (int sl = blk * kThreads + threadIdx.x; sl < nv; sl += nblk * kThreads) r.slot_pos[sl] -= delta;
-  if (delta > 0) {
-    const float4* row = reinterpret_cast<const float4*>(r.table + (size_t)delta * D);
-    for (int i = threadIdx.x; i < D / 4; i += kThreads) s_cs[i] = __ldg(row + i);
+  if (u_begin >= u_end) return;
+  volatile int* abort = &s_abort;
+  const uint32_t base = smem_u32(dsm);
+  // unit u = ring * up + h * runs + run
+  int ring = (int)(u_begin / up);
+  int h = (int)(u_begin % up) / runs, run = (int)(u_begin % up) % runs;
+  int s = 0;
+  uint32_t ph = 0;
+
+  if (warp == kDpConsumerWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane != 0) return;
+    int cur = -1, nv = 0, d = -1;
+    long long i = 0;
+    for (long long u = u_begin; u < u_end; ++u, ++i) {
+      if (i >= kDpStages && !mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abort, kWmWaitLimitNs)) break;
+      const RingDev& r = b.r[ring];
+      if (ring != cur) {
+        cur = ring;
+        nv = __ldcg(r.state + ST_NVALID);
+        d = delta_arg;
+        if (d == KVRING_DELTA_TO_OLDEST) d = nv > 0 ? __ldcg(r.state + ST_OLDEST_POS) : 0;
+        if (d < 0 || d >= r.max_pos) {
+          atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_DELTA);
+          d = -1;  // skip the rotation entirely
+        }
+      }
+      const int r0 = run * RU;
+      int rows = d > 0 ? nv - r0 : 0;
+      rows = rows < 0 ? 0 : (rows > RU ? RU : rows);
+      hdr[s][0] = rows;
+      hdr[s][1] = d;
+      const uint32_t fb = smem_u32(&full[s]);
+      mbar_arrive_expect_tx(fb, (uint32_t)rows * D);
+      if (rows > 0)
+        bulk_load(base + (uint32_t)s * kDpUnitBytes, r.k + ((size_t)h * C + r0) * D, (uint32_t)rows * D, fb);
+      if (++s == kDpStages) {
+        s = 0;
+        ph ^= 1;
+      }
+      if (++run == runs) {
+        run = 0;
+        if (++h == H) {
+          h = 0;
+          ++ring;
+        }
+      }
+    }
+    if (*abort) {
+      // leave no copy in flight: wait (bounded) for the stages issued last
+      int no_abort = 0;
+      for (long long q = i > kDpStages ? i - kDpStages : 0; q < i; ++q)
+        mbar_wait_bounded(smem_u32(&full[q % kDpStages]), (uint32_t)((q / kDpStages) & 1), &no_abort,
+                          kWmWaitLimitNs);
+      atomicOr(reinterpret_cast<unsigned*>(b.r[cur < 0 ? 0 : cur].state + ST_ERROR), KVRING_DEVERR_TIMEOUT);
+    }
+    return;
   }
-  __syncthreads();
-  if (delta > 0) {
-    // items: (head, filled slot, chunk), slot-major within a head
-    const long long per_head = (long long)nv * CH;
-    const long long items = per_head * r.H;
-    const long long stride = (long long)nblk * kThreads;
-    for (long long base = (long long)blk * kThreads + threadIdx.x; base < items; base += stride * U) {
-      uint4 in[U];
-      uint4* ptr[U];
+
+  // ------------------------------------------------------------ consumers
+  const int k = threadIdx.x % CH, row0 = threadIdx.x / CH;
+  float c[8], sn[8];  // cos / sin of this thread's 8 pairs at the ring's delta
+  int cur_d = 0, done = 0, d = -1;
+  for (long long u = u_begin; u < u_end; ++u) {
+    if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abort, kWmWaitLimitNs)) {
+      if (lane == 0) atomicOr(reinterpret_cast<unsigned*>(b.r[ring].state + ST_ERROR), KVRING_DEVERR_TIMEOUT);
+      break;
+    }
+    const int rows = hdr[s][0];
+    d = hdr[s][1];
+    uint4 in[PASSES];
+    const uint8_t* st = dsm + (size_t)s * kDpUnitBytes;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const long long it = base + u * stride;
-        ptr[u] = nullptr;
-        if (it < items) {
-          const long long h = it / per_head, rem = it % per_head;
-          ptr[u] = reinterpret_cast<uint4*>(r.k + ((size_t)h * r.C + rem / CH) * D + (rem % CH) * 16);
-          in[u] = *ptr[u];
+    for (int j = 0; j < PASSES; ++j)
+      if (row0 + j * RSTEP < rows) in[j] = *reinterpret_cast<const uint4*>(st + (row0 + j * RSTEP) * D + 16 * k);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    const RingDev& r = b.r[ring];
+    const int r0 = run * RU;
+    if (rows > 0) {
+      if (d != cur_d) {
+        cur_d = d;
+        const float4* t = reinterpret_cast<const float4*>(r.table + (size_t)d * D + 16 * k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 cs = __ldg(t + i);  // (c, s) of pairs 8k + 2i and 8k + 2i + 1
+          c[2 * i] = cs.x;
+          sn[2 * i] = cs.y;
+          c[2 * i + 1] = cs.z;
+          sn[2 * i + 1] = cs.w;
         }
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (!ptr[u]) continue;
-        const int chunk = (int)((base + u * stride) % per_head % CH);
-        const uint32_t w[4] = {in[u].x, in[u].y, in[u].z, in[u].w};
+      for (int j = 0; j < PASSES; ++j) {
+        const int row = row0 + j * RSTEP;
+        if (row >= rows) continue;
+        const uint32_t w[4] = {in[j].x, in[j].y, in[j].z, in[j].w};
         float y[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 a = e4m3x2_to_f32x2((uint16_t)(w[i] & 0xFFFF));
-          const float2 b = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
-          // pairs (a.x, a.y) and (b.x, b.y); pair index chunk*8 + 2i (+1)
-          const float4 cs = s_cs[chunk * 4 + i];  // (c, s) of both pairs
-          y[4 * i + 0] = __fadd_rn(__fmul_rn(a.x, cs.x), __fmul_rn(a.y, cs.y));
-          y[4 * i + 1] = __fsub_rn(__fmul_rn(a.y, cs.x), __fmul_rn(a.x, cs.y));
-          y[4 * i + 2] = __fadd_rn(__fmul_rn(b.x, cs.z), __fmul_rn(b.y, cs.w));
-          y[4 * i + 3] = __fsub_rn(__fmul_rn(b.y, cs.z), __fmul_rn(b.x, cs.w));
+          const float2 bb = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
+          y[4 * i + 0] = __fadd_rn(__fmul_rn(a.x, c[2 * i]), __fmul_rn(a.y, sn[2 * i]));
+          y[4 * i + 1] = __fsub_rn(__fmul_rn(a.y, c[2 * i]), __fmul_rn(a.x, sn[2 * i]));
+          y[4 * i + 2] = __fadd_rn(__fmul_rn(bb.x, c[2 * i + 1]), __fmul_rn(bb.y, sn[2 * i + 1]));
+          y[4 * i + 3] = __fsub_rn(__fmul_rn(bb.y, c[2 * i + 1]), __fmul_rn(bb.x, sn[2 * i + 1]));
         }
-        *ptr[u] = pack_e4m3x16(y);
+        *reinterpret_cast<uint4*>(r.k + ((size_t)h * C + r0 + row) * D + 16 * k) = pack_e4m3x16(y);
+      }
+      if (h == 0 && (int)threadIdx.x < rows) r.slot_pos[r0 + threadIdx.x] -= d;
+    }
+    ++done;
+    if (++s == kDpStages) {
+      s = 0;
+      ph ^= 1;
+    }
+    // Ring done for this block: every consumer warp adds its units to the
+    // ring's ticket; the warp that completes (consumer warps) x (units per
+    // ring) publishes the new positions.
+    const bool ring_end = h == H - 1 && run == runs - 1;
+    if (ring_end || u + 1 == u_end) {
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        const int tk = atomicAdd(r.state + ST_TICKET_DELTA, done);
+        if (tk + done == kDpConsumerWarps * (int)up) {
+          __threadfence();
+          if (d >= 0) {
+            r.state[ST_NEXT_POS] -= d;
+            r.state[ST_OLDEST_POS] -= d;
+            r.state[ST_LAST_DELTA] = d;
+          }
+          r.state[ST_TICKET_DELTA] = 0;
+          __threadfence();
+        }
+      }
+      done = 0;
+    }
+    if (++run == runs) {
+      run = 0;
+      if (++h == H) {
+        h = 0;
+        ++ring;
+        cur_d = 0;
       }
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int tk = atomicAdd(r.state + ST_TICKET_DELTA, 1);
-    s_last = tk == nblk - 1;
-  }
-  __syncthreads();
-  if (s_last && threadIdx.x == 0) {
-    __threadfence();
-    if (delta >= 0) {
-      r.state[ST_NEXT_POS] -= delta;
-      r.state[ST_OLDEST_POS] -= delta;
-      r.state[ST_LAST_DELTA] = delta;
-    }
-    r.state[ST_TICKET_DELTA] = 0;
-    __threadfence();
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads) k_delta(RingDev r, int delta_arg) {
-  delta_body<D, kDeltaU>(r, delta_arg, blockIdx.x, gridDim.x);
-}
-
-// Batched: four chunks in flight per thread, about eight blocks per SM over
-// the batch (measured best of 4/6/8/16 chunks and 4/8/12/16/32 blocks).
-constexpr int kDeltaManyU = 4;
-constexpr int kDeltaManyBlocksPerSm = 8;
-template <int D>
-__global__ void __launch_bounds__(kThreads) k_delta_many(const __grid_constant__ DeltaMany b, int delta_arg) {
-  delta_body<D, kDeltaManyU>(b.r[blockIdx.y], delta_arg, blockIdx.x, gridDim.x);
 }
 
 // ------------------------------------------------------- legacy upkeep ---
@@ -905,45 +1000,44 @@ cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t
   return cudaLaunchKernelEx(&cfg, k_write_many<64>, b, count, n);
 }
 
-cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStream_t s) {
-  // per ring the single-ring grid capped so that the batch gives about
-  // kDeltaManyBlocksPerSm blocks per SM, at least 8 per ring
+// One block per SM (or per unit, if fewer), each streaming its share of the
+// units; launched as a programmatic dependent like the writes.
+cudaError_t launch_delta_pipe(const DeltaMany& b, int count, int delta, cudaStream_t s) {
   const RingDev& r = b.r[0];
-  const long long items = (long long)r.H * r.C * (r.D / 16);
-  unsigned g = grid_for((items + kDeltaManyU - 1) / kDeltaManyU);
+  const int ru = kDpUnitBytes / r.D;
+  const long long units = (long long)count * r.H * ((r.C + ru - 1) / ru);
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  unsigned per = (unsigned)((kDeltaManyBlocksPerSm * sms + count - 1) / count);
-  if (per < 8) per = 8;
-  if (g > per) g = per;
-  if (g < 1) g = 1;
-  const dim3 grid(g, (unsigned)count);
-  if (r.D == 128)
-    k_delta_many<128><<<grid, kThreads, 0, s>>>(b, delta);
-  else
-    k_delta_many<64><<<grid, kThreads, 0, s>>>(b, delta);
-  return cudaGetLastError();
+  long long grid = sms;
+  if (grid > units) grid = units;
+  if (grid < 1) grid = 1;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)grid), s, attr);
+  cfg.blockDim = dim3(kDpThreads);
+  cfg.dynamicSmemBytes = kDpSmemBytes;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_delta_pipe<128>, b, count, delta);
+  return cudaLaunchKernelEx(&cfg, k_delta_pipe<64>, b, count, delta);
+}
+
+cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStream_t s) {
+  return launch_delta_pipe(b, count, delta, s);
 }
 
 cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s) {
-  // the fill level is device state: size for a full ring, at most ~2 blocks per SM
-  const long long items = (long long)r.H * r.C * (r.D / 16);
-  unsigned g = grid_for((items + kDeltaU - 1) / kDeltaU);
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (g > (unsigned)(2 * sms)) g = (unsigned)(2 * sms);
-  if (g < 1) g = 1;
-  if (r.D == 128)
-    k_delta<128><<<g, kThreads, 0, s>>>(r, delta);
-  else
-    k_delta<64><<<g, kThreads, 0, s>>>(r, delta);
-  return cudaGetLastError();
+  DeltaMany b;
+  b.r[0] = r;
+  return launch_delta_pipe(b, 1, delta, s);
 }
 
 cudaError_t cache_prepare() {
   cudaError_t e = cudaFuncSetAttribute(k_write_many<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWmStageBudget);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_write_many<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWmStageBudget);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_write_many<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWmStageBudget);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_delta_pipe<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDpSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_delta_pipe<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDpSmemBytes);
+  return e;
 }
 
 cudaError_t launch_legacy_upkeep(const RingDev& r, const void* wk_in, const void* wv_in, void* wk_out,
