@@ -12,14 +12,15 @@
 // (split-KV).  Twelve warps:
 //   warps 0-7   Softmax, two groups of four warps that take the key/value
 //               tiles in turn (group g: tiles g, g + 2, ...), each with its own
-//               S buffer and O accumulator in TMEM, so one group's MMAs run
-//               while the other group exponentiates.  One thread per query
-//               row (row r = TMEM lane r) holds all 128 scores of its row: no
-//               exchange between threads.  Online softmax in log2 units with
-//               a lazily raised running maximum; probabilities carry 2^7 and
-//               are written back into TMEM as f16 over the S columns just
-//               read, and the thread sums its fp32 probabilities into the
-//               row's normaliser.  O is rescaled in TMEM when the maximum
+//               probability buffer P_g and O accumulator O_g in TMEM.  The one
+//               S buffer passes from tile to tile: a group loads S(j) into
+//               registers and hands the buffer back at once, so QK(j + 1) runs
+//               while it exponentiates.  One thread per query row (row r =
+//               TMEM lane r) holds all 128 scores of its row: no exchange
+//               between threads.  Online softmax in log2 units with a lazily
+//               raised running maximum; probabilities carry 2^7 and are
+//               written into P_g as f16, and the thread sums its fp32
+//               probabilities into the row's normaliser.  O is rescaled in TMEM when the maximum
 //               rises by more than 1.5 (log2 units).  Epilogue: the two
 //               groups' (m, l, O) merged, O / l, split partials and their merge.
 //   warp 8      Copy producer: K and V tiles [128 slots][d] by TMA into a
@@ -31,10 +32,10 @@
 //   warps 10-11 Value converters: each landed E4M3 V tile is widened, exactly,
 //               into one of two f16 tiles (128B-swizzled MN-major atoms of 64
 //               values), which frees the E4M3 stage for the next copy.
-// MMA issue order: QK(0), QK(1), then per tile j: PV(j) and QK(j + 2) into the
-// S buffer PV(j) has just read.  MMAs of one thread complete in issue order,
-// so the arrival of S(j) also means PV(j - 2) is done: group g may rescale
-// O_g as soon as S(j) is there.
+// MMA issue: QK(j) as soon as S(j - 1) is in its group's registers and the
+// K/V stage has landed; PV(j) as soon as P(j) and its f16 V tile are written.
+// A group waits for PV(j - 2) (its previous tile) before it rescales O_g or
+// writes P_g for tile j.
 //
 // Query prologue, by the softmax threads at the start of every CTA: the
 // tile's query rows and their RoPE-table rows are copied into shared memory
@@ -105,14 +106,15 @@ struct Layout {
   static constexpr int kBarPvDone = 2 * kStages + 4;
   static constexpr int kBarVhFull = 2 * kStages + 6;
   static constexpr int kBarMmaDone = 2 * kStages + 8;
-  static constexpr int kBarQFull = 2 * kStages + 9;
+  static constexpr int kBarSFree = 2 * kStages + 9;
   static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 64;
   static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code of the E4M3 tiles
   static_assert(kVh % 1024 == 0, "128B-swizzled atoms need 1024-byte alignment");
   // TMEM columns
-  static constexpr uint32_t kColS = 0;        // S buffer of group g at 128 g (P overwrites 64 columns)
+  static constexpr uint32_t kColS = 0;        // the S buffer (128 columns, one tile's scores)
+  static constexpr uint32_t kColP = 128;      // f16 probabilities of group g at 128 + 64 g
   static constexpr uint32_t kColO = 256;      // O accumulator of group g at 256 + 128 g (D columns)
 };
 
@@ -193,12 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::kBarKvEmpty + s), 1 + kCvtThreads);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(L::kBarSFull + b), 1);
+      mbar_init(bar(L::kBarSFull + b), 1);     // S of a group-b tile is in TMEM
       mbar_init(bar(L::kBarPFull + b), kGroupThreads);
       mbar_init(bar(L::kBarPvDone + b), 1);
       mbar_init(bar(L::kBarVhFull + b), kCvtThreads);
     }
     mbar_init(bar(L::kBarMmaDone), 1);
+    mbar_init(bar(L::kBarSFree), kGroupThreads / 32);  // a tile's S is in its group's registers
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
@@ -388,15 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv = smem_desc(sbase + L::kVh, (uint32_t)L::kVhAtom, 1024, 2u);
       const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
       constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4, kVhStep = L::kVhTile >> 4;
-      int n_qterms = 3;
-      // S(j) into TMEM buffer j&1.  Its previous user, P(j-2), was consumed
-      // by PV(j-2), issued earlier by this thread: in-order execution.
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j % kStages, b = j & 1;
-        if (!mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs)) return false;
+      const int n_qterms = misc->level;   // the prologue ended with a CTA barrier
+      // S(j) into the S buffer, whose previous tile its group has already
+      // loaded into registers; the K stage is freed by the commit.
+      auto issue_qk = [&](int j) {
+        const int s = j % kStages;
         tc_fence_after();
         const uint32_t kl = k_lo + s * kKVStep;
-        const uint32_t dst = tmem + L::kColS + b * 128;
+        const uint32_t dst = tmem + L::kColS;
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
           if (t < n_qterms) {
@@ -405,25 +407,56 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_e4m3_w(dst, q_lo + t * kQStep + 2 * kk, kq_hi, kl + 2 * kk, kq_hi, idesc_qk, (t | kk) != 0);
           }
         }
-        mma_commit(bar(L::kBarSFull + b));
+        mma_commit(bar(L::kBarSFull + (j & 1)));
         mma_commit(bar(L::kBarKvEmpty + s));   // the K stage is read
-        return true;
       };
-      n_qterms = misc->level;   // the prologue ended with a CTA barrier
-      bool ok = issue_qk(0) && (ntiles < 2 || issue_qk(1));
-      for (int j = 0; ok && j < ntiles; ++j) {
+      // O_b += P_b(j) Vh_b(j), b = j & 1.
+      auto issue_pv = [&](int j) {
         const int b = j & 1;
-        if (!mbar_wait_bounded(bar(L::kBarPFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
-        if (!mbar_wait_bounded(bar(L::kBarVhFull + b), (j >> 1) & 1, abort, kWaitLimitNs)) break;
         tc_fence_after();
         const uint32_t vl = v_lo + (uint32_t)b * kVhStep;
-        const uint32_t pa = tmem + L::kColS + b * 128;
+        const uint32_t pa = tmem + L::kColP + 64u * b;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
                        (j > 1 || kk > 0) ? 1u : 0u);
         mma_commit(bar(L::kBarPvDone + b));
-        if (j + 2 < ntiles && !issue_qk(j + 2)) break;
+      };
+      // Issue each MMA group as soon as its inputs are there: QK(nq) once
+      // S(nq - 1) is in its group's registers and the K/V stage has landed,
+      // PV(np) once P(np) and its f16 V tile are written.  The thread polls
+      // without sleeping (a sleep, however short it asks for, delays the
+      // issue by about a microsecond).
+      int nq = 0, np = 0;
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (np < ntiles) {
+        bool prog = false;
+        if (nq < ntiles && (nq == 0 || mbar_test_wait(bar(L::kBarSFree), (nq - 1) & 1)) &&
+            mbar_test_wait(bar(L::kBarKvFull + nq % kStages), (nq / kStages) & 1)) {
+          issue_qk(nq++);
+          prog = true;
+        }
+        if (np < nq && mbar_test_wait(bar(L::kBarPFull + (np & 1)), (np >> 1) & 1) &&
+            mbar_test_wait(bar(L::kBarVhFull + (np & 1)), (np >> 1) & 1)) {
+          issue_pv(np++);
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+          continue;
+        }
+        if (idle++ == 0) {
+          t_idle = globaltimer_ns();
+        } else {
+          if ((idle & 15u) == 0) {
+            if (*abort) break;
+            if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+              *abort = 1;
+              break;
+            }
+          }
+        }
       }
     }
     if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
@@ -479,8 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- softmax
-    // thread = (group g, row): S columns [0, 128) of buffer g, P columns
-    // [0, 64) of it, O_g columns [0, d).
+    // thread = (group g, row): S columns [0, 128), P_g columns [0, 64),
+    // O_g columns [0, d).
     const int g = warp >> 2;
     const int row = threadIdx.x & (kTile - 1);
     const int quarter = warp & 3;
@@ -492,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       f_row = fmaxf(sq * r.scales[h] * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
     }
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tS = trow + L::kColS + g * 128, tO = trow + L::kColO + g * 128;
+    const uint32_t tS = trow + L::kColS, tP = trow + L::kColP + 64 * g, tO = trow + L::kColO + g * 128;
     float m_run = -INFINITY;
     float ell = 0.f;
     bool ok = true;
@@ -505,6 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
       tmem_wait_ld();
+      // the scores are in registers: the S buffer may take the next tile
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kBarSFree));
       // mask slots past the fill level (only the ring's last tile)
       const int valid = nvalid - (tile0 + j) * kTile;
       if (valid < kTile) {
@@ -525,10 +562,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tmax = smax * f_row;          // f_row > 0
       const bool need = tmax > m_run + kTau;
       const float m_new = need ? tmax : m_run;
+      // O_g and P_g are touched only once PV(j - 2), this group's previous
+      // tile, has completed
+      if (j > 1) {
+        ok = __all_sync(0xFFFFFFFFu,
+                        mbar_wait_bounded(bar(L::kBarPvDone + g), ((j - 2) >> 1) & 1, abort, kWaitLimitNs));
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (j > 1 && __any_sync(0xFFFFFFFFu, need)) {
-        // O_g holds this group's earlier tiles, complete (S(j) was committed
-        // after PV(j - 2)): rescale it in chunks of 16 columns (the row's
-        // scores stay in registers meanwhile)
+        // O_g holds this group's earlier tiles: rescale it in chunks of 16
+        // columns (the row's scores stay in registers meanwhile)
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < D / 16; ++c) {
@@ -542,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ell *= alpha;
       }
       m_run = m_new;
-      // probabilities 2^(x - m + 7): f16 pairs over S(j), slots 32 c + [0, 32)
+      // probabilities 2^(x - m + 7): f16 pairs into P_g, slots 32 c + [0, 32)
       // -> columns 16 c + [0, 16), the lower slot in the low half; the
       // normaliser takes the fp32 values
       const float moff = kPShift - m_run;
@@ -554,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t hv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[2 * i], e[2 * i + 1]);
-        tmem_st16(tS + 16 * c, hv);
+        tmem_st16(tP + 16 * c, hv);
         float s8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) s8[i] = (e[4 * i] + e[4 * i + 1]) + (e[4 * i + 2] + e[4 * i + 3]);
