@@ -99,17 +99,22 @@ struct Layout {
   static constexpr int kEpi = kVh + 2 * kVhTile;        // float m[2][128], l[2][128], lse[128]
   static constexpr int kBars = kEpi + 5 * kTile * 4;
   // barrier slots (8 bytes each)
-  static constexpr int kBarKvFull = 0;
-  static constexpr int kBarKvEmpty = kStages;
+  static constexpr int kBarKFull = 0;                   // K tile of a stage landed
+  static constexpr int kBarKEmpty = kStages;            // ... read by its QK
   static constexpr int kBarSFull = 2 * kStages;
   static constexpr int kBarPFull = 2 * kStages + 2;
   static constexpr int kBarPvDone = 2 * kStages + 4;
   static constexpr int kBarVhFull = 2 * kStages + 6;
   static constexpr int kBarMmaDone = 2 * kStages + 8;
   static constexpr int kBarSFree = 2 * kStages + 9;
-  static constexpr int kNumBars = 2 * kStages + 10;
+  static constexpr int kBarMerge = 2 * kStages + 10;    // peers' partial rows have landed
+  static constexpr int kBarPvIssuerDone = 2 * kStages + 11;  // every PV of the PV issuer has finished
+  static constexpr int kBarVFull = 2 * kStages + 12;    // V tile of a stage landed
+  static constexpr int kBarVEmpty = 3 * kStages + 12;   // ... widened to f16 by the converters
+  static constexpr int kNumBars = 4 * kStages + 12;
   static constexpr int kMisc = kBars + 8 * kNumBars;
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kLseAll = kMisc + 64;             // float [8 splits][128]: the cluster's log2-sum-exps
+  static constexpr int kBytes = kLseAll + 8 * kTile * 4;
   static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code of the E4M3 tiles
   static_assert(kVh % 1024 == 0, "128B-swizzled atoms need 1024-byte alignment");
   // TMEM columns
@@ -174,25 +179,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async16(q_stage(rr) + 16u * c, prm.q + ((size_t)(qt * kTile + rr) * H + h) * D + 8 * c);
   }
   cp_async_commit();
-  // This kernel is a programmatic dependent of the preceding kernel (a write,
-  // or an earlier attention): the ring (state, cache) is read only after it.
-  griddep_wait();
-  const int nvalid = __ldcg(r.state + ST_NVALID);
-  const int ntile_total = (nvalid + kTile - 1) / kTile;
-  const int tile0 = split * prm.tiles_per_split;
-  int ntiles = ntile_total - tile0;
-  ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
-
-  // ---------------------------------------------------------------- setup
-  const size_t unit = (size_t)qt * H + h;
+  // Set-up that touches nothing a preceding kernel writes runs before the
+  // wait: barriers, TMEM, and an L2 prefetch of the RoPE rows the default
+  // query positions will most likely need (a hint only: the state word is
+  // read before the preceding write may have advanced it, so both the
+  // positions before and after a write of n_q tokens are prefetched).
   if (threadIdx.x == kWarpTma * 32) {
-    // The producer initialises the barriers and starts the first two
-    // key/value copies at once; the third stage's space holds query rows
-    // until the query prologue is done.
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    // K and V stages are loaded and freed separately: a K stage as soon as
+    // its QK has read it, a V stage once the converters have widened it
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(L::kBarKvFull + s), 1);
-      // freed by the QK commit and by every converter thread
-      mbar_init(bar(L::kBarKvEmpty + s), 1 + kCvtThreads);
+      mbar_init(bar(L::kBarKFull + s), 1);
+      mbar_init(bar(L::kBarKEmpty + s), 1);
+      mbar_init(bar(L::kBarVFull + s), 1);
+      mbar_init(bar(L::kBarVEmpty + s), kCvtThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kBarSFull + b), 1);     // S of a group-b tile is in TMEM
@@ -202,20 +203,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(L::kBarMmaDone), 1);
     mbar_init(bar(L::kBarSFree), kGroupThreads / 32);  // a tile's S is in its group's registers
+    mbar_init(bar(L::kBarMerge), 1);
+    mbar_init(bar(L::kBarPvIssuerDone), 1);
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
-    const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
-    for (int j = 0; j < first; ++j) {
-      mbar_arrive_expect_tx(bar(L::kBarKvFull + j), 2u * kTile * D);
-      const int slot0 = (tile0 + j) * kTile;
-      tma_load_3d(sbase + L::kK + j * L::kKVTile, &tmK, 0, slot0, h, bar(L::kBarKvFull + j));
-      tma_load_3d(sbase + L::kV + j * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarKvFull + j));
-    }
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
+  }
+  if (!prm.qpos && threadIdx.x < 2 * kTile) {
+    const int t = qt * kTile + (threadIdx.x & (kTile - 1));
+    if (t < prm.n_q) {
+      int p = __ldcg(r.state + ST_NEXT_POS) - prm.n_q + t + (threadIdx.x >= kTile ? prm.n_q : 0);
+      p = p < 0 ? 0 : (p >= r.max_pos ? r.max_pos - 1 : p);
+      bulk_prefetch_l2(r.table + (size_t)p * D, D * 4);
+    }
+  }
+  // This kernel is a programmatic dependent of the preceding kernel (a write,
+  // or an earlier attention): the ring (state, cache) is read only after it.
+  griddep_wait();
+  const int nvalid = __ldcg(r.state + ST_NVALID);
+  // the head's scales, loaded once here (the level choice, the softmax, the
+  // epilogue and the split merge need them; a load there would sit on
+  // their critical path)
+  const float scale_k = r.scales[h], scale_v = r.scales[H + h];
+  const int ntile_total = (nvalid + kTile - 1) / kTile;
+  const int tile0 = split * prm.tiles_per_split;
+  int ntiles = ntile_total - tile0;
+  ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
+
+  // ---------------------------------------------------------------- setup
+  const size_t unit = (size_t)qt * H + h;
+  if (threadIdx.x == kWarpTma * 32) {
+    // The producer starts the first two key/value copies at once; the third
+    // stage's space holds query rows until the query prologue is done.
+    const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
+    for (int j = 0; j < first; ++j) {
+      const int slot0 = (tile0 + j) * kTile;
+      mbar_arrive_expect_tx(bar(L::kBarKFull + j), (uint32_t)(kTile * D));
+      tma_load_3d(sbase + L::kK + j * L::kKVTile, &tmK, 0, slot0, h, bar(L::kBarKFull + j));
+      mbar_arrive_expect_tx(bar(L::kBarVFull + j), (uint32_t)(kTile * D));
+      tma_load_3d(sbase + L::kV + j * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarVFull + j));
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -232,13 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // without the query terms anyway).
       // (1) one position per query row; (2) the RoPE-table rows of those
       // positions copied into the f16 V tiles' space with 16-byte cp.async
-      // (the query rows are already on their way, see above); (3) pass 1, a
-      // small rolled loop over 8-value chunks: chunk task k = i * 384 + tid
-      // is query row k / CPR, chunk k % CPR, so a warp holds every chunk of
-      // its rows and a row's amax is a shuffle reduction, and the warps'
-      // maxima give the tile's precision level; (4) pass 2 rotates again and
-      // writes the level's E4M3 terms straight into the swizzled images the
-      // QK MMA reads.
+      // (the query rows are already on their way, see above); (3) pass 1
+      // over 8-value chunks: chunk task k = i * 384 + tid is query row
+      // k / CPR, chunk k % CPR, so a warp holds every chunk of its rows and a
+      // row's amax is a shuffle reduction, and the warps' maxima give the
+      // tile's precision level; (4) pass 2 writes the level's E4M3 terms of
+      // the rotated values it kept in registers straight into the swizzled
+      // images the QK MMA reads.
       constexpr int CPR = D / 8;                           // 16-byte q chunks per row
       constexpr int TPR = D / 4;                           // 16-byte table chunks per row
       constexpr int PQ = (kTile * CPR + kThreads - 1) / kThreads;   // chunk tasks per thread
@@ -285,18 +316,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return cmax;
       };
+      // Pass 1 rotates every chunk once and keeps the values in registers
+      // (u[i], the row maximum in rm[i]); after the CTA barrier that gives
+      // the tile's maximum and level, pass 2 scales them and writes the terms.
+      // Chunk tasks of one iteration cover whole warps (rows x CPR is a
+      // multiple of 32), so every shuffle has all lanes.
+      float u[PQ][8], rm[PQ];
       float wmax = 0.f;
-#pragma unroll 4
+#pragma unroll
       for (int i = 0; i < PQ; ++i) {
         const int k = i * kThreads + threadIdx.x;
-        if (k >= kTile * CPR) break;                       // whole warps leave together
         const int rrow = k / CPR, chunk = k % CPR;
-        float u[8];
-        float cmax = rotate(rrow, chunk, u);
+        float cmax = 0.f;
+        if (k < kTile * CPR) {
+          cmax = rotate(rrow, chunk, u[i]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[i][e] = 0.f;
+        }
         // row maximum over the CPR consecutive lanes that hold the row
 #pragma unroll
         for (int off = CPR / 2; off > 0; off >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, off));
-        if (chunk == 0) epi[rrow] = cmax;
+        rm[i] = cmax;
+        if (k < kTile * CPR && chunk == 0) epi[rrow] = cmax;
         wmax = fmaxf(wmax, cmax);
       }
 #pragma unroll
@@ -308,40 +350,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 1; i < kThreads / 32; ++i) qm = fmaxf(qm, epi[kTile + i]);
       int level = prm.forced_level;
       if (level == 0) {
-        const float lg = qm * 448.0f * r.scales[h];
-        const float vmax = 448.0f * r.scales[H + h];
+        const float lg = qm * 448.0f * scale_k;
+        const float vmax = 448.0f * scale_v;
         level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg * vmax <= kLevel2MaxLV ? 2 : 3);
       }
-#pragma unroll 2
+#pragma unroll
       for (int i = 0; i < PQ; ++i) {
         const int k = i * kThreads + threadIdx.x;
         if (k >= kTile * CPR) break;
         const int rrow = k / CPR, chunk = k % CPR;
-        float u[8];
-        rotate(rrow, chunk, u);
         // E4M3 terms of q / sigma_q (sigma_q = amax/448 of the row), exact
         // fp32 residuals; 8 bytes per chunk per term at the chunk's swizzled
         // place in the query images
-        float sq = epi[rrow] / 448.0f;
+        float sq = rm[i] / 448.0f;
         if (!(sq >= 0x1p-126f)) sq = 1.0f;
         const float invq = 1.0f / sq;
+        float* v = u[i];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] *= invq;
+        for (int e = 0; e < 8; ++e) v[e] *= invq;
         const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
 #pragma unroll
         for (int term = 0; term < 3; ++term) {
           if (term < level) {
             uint16_t c4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(u[2 * e], u[2 * e + 1]);
+            for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(v[2 * e], v[2 * e + 1]);
             *reinterpret_cast<uint2*>(sm + L::kQ + term * L::kQTile + off) =
                 make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
             if (term + 1 < level) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float2 dq = e4m3x2_to_f32x2(c4[e]);
-                u[2 * e] -= dq.x;
-                u[2 * e + 1] -= dq.y;
+                v[2 * e] -= dq.x;
+                v[2 * e + 1] -= dq.y;
               }
             }
           }
@@ -356,46 +397,100 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp == kWarpTma) {
-    // ------------------------------------------------------ TMA producer
+    // ------------------------------------------ TMA producer + PV issuer
+    // One thread loads the key/value tiles and issues PV(j) = P_b(j) Vh_b(j)
+    // into O_b (b = j & 1) as soon as P(j) and its f16 V tile are written;
+    // the MMA warp issues only QK, so the two kinds of MMA are issued from
+    // two warps and neither waits behind the other's issue (a single thread
+    // needs longer to issue an M = 128, N = 128 MMA than the tensor core
+    // needs to run it).
     if (lane == 0) {
-      int issued = ntiles < kStages - 1 ? ntiles : kStages - 1;
-      for (int j = issued; j < ntiles; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait_bounded(bar(L::kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, abort, kWaitLimitNs))
-          break;
-        mbar_arrive_expect_tx(bar(L::kBarKvFull + s), 2u * kTile * D);
-        const int slot0 = (tile0 + j) * kTile;
-        tma_load_3d(sbase + L::kK + s * L::kKVTile, &tmK, 0, slot0, h, bar(L::kBarKvFull + s));
-        tma_load_3d(sbase + L::kV + s * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarKvFull + s));
-        ++issued;
-      }
-      // Drain: every issued copy must land before the CTA may exit.
-      volatile int no_abort = 0;
-      for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
-        mbar_wait_bounded(bar(L::kBarKvFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
-    }
-    __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------- MMA issuer
-    if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
-      // Descriptors are built once; per MMA only the low word (start address
-      // in 16-byte units) moves: +2 per 32-byte k-step of a K-major tile,
-      // +16 rows x 128 bytes per 16-slot k-step of the f16 V tile.
-      const uint64_t dq = smem_desc(sbase + L::kQ, 16, 8 * D, L::kSwz);
-      const uint64_t dk = smem_desc(sbase + L::kK, 16, 8 * D, L::kSwz);
-      const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, kq_hi = (uint32_t)(dq >> 32);
       // f16 V: 128B-swizzled MN-major atoms of 64 columns x 8 rows (1024 B
       // apart along the slots); the second 64 columns one atom column further
       const uint64_t dv = smem_desc(sbase + L::kVh, (uint32_t)L::kVhAtom, 1024, 2u);
       const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
-      constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4, kVhStep = L::kVhTile >> 4;
+      constexpr uint32_t kVhStep = L::kVhTile >> 4;
+      auto issue_pv = [&](int j) {
+        const int b = j & 1;
+        tc_fence_after();
+        const uint32_t vl = v_lo + (uint32_t)b * kVhStep;
+        const uint32_t pa = tmem + L::kColP + 64u * b;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
+                       (j > 1 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::kBarPvDone + b));
+      };
+      const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
+      int k_issued = first, v_issued = first, np = 0;
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (np < ntiles) {
+        bool prog = false;
+        if (mbar_test_wait(bar(L::kBarPFull + (np & 1)), (np >> 1) & 1) &&
+            mbar_test_wait(bar(L::kBarVhFull + (np & 1)), (np >> 1) & 1)) {
+          issue_pv(np++);
+          prog = true;
+        }
+        if (k_issued < ntiles &&
+            mbar_test_wait(bar(L::kBarKEmpty + k_issued % kStages), ((k_issued / kStages) & 1) ^ 1)) {
+          const int s = k_issued % kStages;
+          mbar_arrive_expect_tx(bar(L::kBarKFull + s), (uint32_t)(kTile * D));
+          tma_load_3d(sbase + L::kK + s * L::kKVTile, &tmK, 0, (tile0 + k_issued) * kTile, h, bar(L::kBarKFull + s));
+          ++k_issued;
+          prog = true;
+        }
+        if (v_issued < ntiles &&
+            mbar_test_wait(bar(L::kBarVEmpty + v_issued % kStages), ((v_issued / kStages) & 1) ^ 1)) {
+          const int s = v_issued % kStages;
+          mbar_arrive_expect_tx(bar(L::kBarVFull + s), (uint32_t)(kTile * D));
+          tma_load_3d(sbase + L::kV + s * L::kKVTile, &tmV, 0, (tile0 + v_issued) * kTile, h, bar(L::kBarVFull + s));
+          ++v_issued;
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+          continue;
+        }
+        if (idle++ == 0) {
+          t_idle = globaltimer_ns();
+        } else if ((idle & 15u) == 0) {
+          if (*abort) break;
+          if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+            *abort = 1;
+            break;
+          }
+        }
+      }
+      // Drain: every issued copy must land before the CTA may exit.
+      volatile int no_abort = 0;
+      for (int j = k_issued - kStages < 0 ? 0 : k_issued - kStages; j < k_issued; ++j)
+        mbar_wait_bounded(bar(L::kBarKFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
+      for (int j = v_issued - kStages < 0 ? 0 : v_issued - kStages; j < v_issued; ++j)
+        mbar_wait_bounded(bar(L::kBarVFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
+      // and every PV this thread issued has finished before TMEM is freed
+      mma_commit(bar(L::kBarPvIssuerDone));
+      mbar_wait_bounded(bar(L::kBarPvIssuerDone), 0, &no_abort, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------- QK issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
+      // Descriptors are built once; per MMA only the low word (start address
+      // in 16-byte units) moves: +2 per 32-byte k-step of a K-major tile.
+      const uint64_t dq = smem_desc(sbase + L::kQ, 16, 8 * D, L::kSwz);
+      const uint64_t dk = smem_desc(sbase + L::kK, 16, 8 * D, L::kSwz);
+      const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, kq_hi = (uint32_t)(dq >> 32);
+      constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4;
       const int n_qterms = misc->level;   // the prologue ended with a CTA barrier
-      // S(j) into the S buffer, whose previous tile its group has already
-      // loaded into registers; the K stage is freed by the commit.
-      auto issue_qk = [&](int j) {
+      // S(j) into the S buffer once its group has S(j - 1) in registers and
+      // the K/V stage has landed; the K stage is freed by the commit.
+      for (int j = 0; j < ntiles; ++j) {
         const int s = j % kStages;
+        if (j > 0 && !mbar_wait_bounded(bar(L::kBarSFree), (j - 1) & 1, abort, kWaitLimitNs)) break;
+        if (!mbar_wait_bounded(bar(L::kBarKFull + s), (j / kStages) & 1, abort, kWaitLimitNs)) break;
         tc_fence_after();
         const uint32_t kl = k_lo + s * kKVStep;
         const uint32_t dst = tmem + L::kColS;
@@ -408,55 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(bar(L::kBarSFull + (j & 1)));
-        mma_commit(bar(L::kBarKvEmpty + s));   // the K stage is read
-      };
-      // O_b += P_b(j) Vh_b(j), b = j & 1.
-      auto issue_pv = [&](int j) {
-        const int b = j & 1;
-        tc_fence_after();
-        const uint32_t vl = v_lo + (uint32_t)b * kVhStep;
-        const uint32_t pa = tmem + L::kColP + 64u * b;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
-                       (j > 1 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::kBarPvDone + b));
-      };
-      // Issue each MMA group as soon as its inputs are there: QK(nq) once
-      // S(nq - 1) is in its group's registers and the K/V stage has landed,
-      // PV(np) once P(np) and its f16 V tile are written.  The thread polls
-      // without sleeping (a sleep, however short it asks for, delays the
-      // issue by about a microsecond).
-      int nq = 0, np = 0;
-      uint32_t idle = 0;
-      uint64_t t_idle = 0;
-      while (np < ntiles) {
-        bool prog = false;
-        if (nq < ntiles && (nq == 0 || mbar_test_wait(bar(L::kBarSFree), (nq - 1) & 1)) &&
-            mbar_test_wait(bar(L::kBarKvFull + nq % kStages), (nq / kStages) & 1)) {
-          issue_qk(nq++);
-          prog = true;
-        }
-        if (np < nq && mbar_test_wait(bar(L::kBarPFull + (np & 1)), (np >> 1) & 1) &&
-            mbar_test_wait(bar(L::kBarVhFull + (np & 1)), (np >> 1) & 1)) {
-          issue_pv(np++);
-          prog = true;
-        }
-        if (prog) {
-          idle = 0;
-          continue;
-        }
-        if (idle++ == 0) {
-          t_idle = globaltimer_ns();
-        } else {
-          if ((idle & 15u) == 0) {
-            if (*abort) break;
-            if (globaltimer_ns() - t_idle > kWaitLimitNs) {
-              *abort = 1;
-              break;
-            }
-          }
-        }
+        mma_commit(bar(L::kBarKEmpty + s));   // the K stage is read
       }
     }
     if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
@@ -477,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ct = threadIdx.x - kWarpCvt * 32;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages, b = j & 1;
-      bool ok = mbar_wait_bounded(bar(L::kBarKvFull + s), (j / kStages) & 1, abort, kWaitLimitNs);
+      bool ok = mbar_wait_bounded(bar(L::kBarVFull + s), (j / kStages) & 1, abort, kWaitLimitNs);
       if (ok && j >= 2) ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       const uint8_t* src = sm + L::kV + s * L::kKVTile;
@@ -508,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();  // generic writes -> tensor-core reads
       mbar_arrive(bar(L::kBarVhFull + b));
-      mbar_arrive(bar(L::kBarKvEmpty + s));
+      mbar_arrive(bar(L::kBarVEmpty + s));
     }
   } else {
     // ----------------------------------------------------------- softmax
@@ -522,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       float sq = epi[row] / 448.0f;
       if (!(sq >= 0x1p-126f)) sq = 1.0f;
-      f_row = fmaxf(sq * r.scales[h] * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
+      f_row = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
     }
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = trow + L::kColS, tP = trow + L::kColP + 64 * g, tO = trow + L::kColO + g * 128;
@@ -580,7 +627,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_n<16>(tO + 16 * c, rr);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          for (int i = 0; i < 16; i += 2) {
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                        make_float2(alpha, alpha));
+            rr[i] = __float_as_uint(y.x);
+            rr[i + 1] = __float_as_uint(y.y);
+          }
           tmem_st16(tO + 16 * c, rr);
         }
         ell *= alpha;
@@ -589,21 +641,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // probabilities 2^(x - m + 7): f16 pairs into P_g, slots 32 c + [0, 32)
       // -> columns 16 c + [0, 16), the lower slot in the low half; the
       // normaliser takes the fp32 values
+      // (pairs of scores through the packed two-lane fp32 FMA and add)
       const float moff = kPShift - m_run;
+      const float2 fr2 = make_float2(f_row, f_row), mo2 = make_float2(moff, moff);
+      float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float e[32];
+        float2 e[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(sr[32 * c + i]), f_row, moff));
+        for (int i = 0; i < 16; ++i) {
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(sr[32 * c + 2 * i]), __uint_as_float(sr[32 * c + 2 * i + 1])), fr2, mo2);
+          e[i] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        }
         uint32_t hv[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[2 * i], e[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[i].x, e[i].y);
         tmem_st16(tP + 16 * c, hv);
-        float s8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s8[i] = (e[4 * i] + e[4 * i + 1]) + (e[4 * i + 2] + e[4 * i + 3]);
-        ell += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) e[i] = __fadd2_rn(e[i], e[i + w]);
+        lsum = __fadd2_rn(lsum, e[0]);
       }
+      ell += lsum.x + lsum.y;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + g));
@@ -639,7 +700,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // from both accumulators.  Then the whole tile is stored, or merged
     // across splits, with coalesced 16-byte accesses.
     const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-    const float scale_v = r.scales[H + h];
     const bool single = prm.nsplit == 1;
     constexpr int SP = D + 4;                 // padded row stride (floats)
     constexpr int F4 = kTile * D / 4;         // float4 per tile
@@ -691,8 +751,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < PER; ++i) store_out(threadIdx.x + i * kSoftmaxThreads, staged(threadIdx.x + i * kSoftmaxThreads));
     } else if (prm.cluster_merge) {
-      // the staged partial and its log2-sum-exp stay here; the cluster
-      // merges them after the role branches
+      // the staged partial stays here; the row's log2-sum-exp goes to every
+      // CTA of the cluster now (a region nothing else uses), so the merge
+      // after the cluster barrier reads the weights locally
+      if (threadIdx.x < kTile) {
+        const float v = lse_row[threadIdx.x];
+        const uint32_t a = sbase + L::kLseAll + 4u * (uint32_t)(split * kTile + threadIdx.x);
+        for (int s2 = 0; s2 < prm.nsplit; ++s2) st_dsmem_f32(dsmem_addr(a, (uint32_t)s2), v);
+      }
+      fence_proxy_async_smem();   // the staged rows are read by bulk copies
     } else {
       // partial (normalised) tile and its per-row log2-sum-exp
       const size_t pbase = ((size_t)split * r.qtiles_max + qt) * H + h;
@@ -758,24 +825,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------ cluster merge
-  // The nsplit CTAs of this query tile form one cluster (rank = split).
-  // After the first cluster barrier every CTA's normalised partial and
-  // log2-sum-exp are staged in its shared memory; CTA `split` merges rows
-  // [split 128 / nsplit, (split + 1) 128 / nsplit) from all of them through
-  // distributed shared memory and stores the output rows.  The second
-  // barrier keeps every CTA's shared memory alive until its peers are done.
+  // The nsplit CTAs of this query tile form one cluster (rank = split); CTA
+  // `split` owns output rows [split 128 / nsplit, (split + 1) 128 / nsplit).
+  // After the cluster barrier every CTA's normalised partial is staged in
+  // its shared memory, every CTA holds all log2-sum-exps (pushed to it
+  // before the barrier), and no CTA needs its f16 V tiles any more: each CTA
+  // bulk-copies the rows every peer owns into that peer's f16 V space (one
+  // slot per sender), completing on the peer's merge barrier, then merges
+  // its own rows from its own shared memory and stores them.  A CTA leaves
+  // once its outgoing copies have read its rows and its incoming ones have
+  // landed, so no second cluster barrier is needed.
   if (prm.cluster_merge) {
     __syncwarp();
     cluster_sync_all();
+    constexpr int SP = D + 4;                      // staged row stride (floats)
+    constexpr uint32_t SPB = SP * 4;               // ... in bytes
+    const int ns = prm.nsplit;
+    const int maxr = (kTile + ns - 1) / ns;        // rows of one slot
+    const int r0 = split * kTile / ns, r1 = (split + 1) * kTile / ns, nr = r1 - r0;
+    if (threadIdx.x == kWarpTma * 32) {
+      mbar_arrive_expect_tx(bar(L::kBarMerge), (uint32_t)((ns - 1) * nr) * SPB);
+      for (int p = 0; p < ns; ++p) {
+        if (p == split) continue;
+        const int p0 = p * kTile / ns, p1 = (p + 1) * kTile / ns;
+        const int slot = split < p ? split : split - 1;
+        bulk_copy_to_cluster(dsmem_addr(sbase + L::kVh + (uint32_t)(slot * maxr) * SPB, (uint32_t)p),
+                             sbase + L::kK + (uint32_t)p0 * SPB, (uint32_t)(p1 - p0) * SPB,
+                             dsmem_addr(bar(L::kBarMerge), (uint32_t)p));
+      }
+      bulk_commit();
+    }
     if (warp < kSoftmaxThreads / 32) {
-      constexpr int SP = D + 4;
       constexpr int MT = (kTile / 2) * (D / 4) / kSoftmaxThreads;  // float4 tasks per thread (nsplit >= 2)
-      const int ns = prm.nsplit;
-      const int r0 = split * kTile / ns, r1 = (split + 1) * kTile / ns, nr = r1 - r0;
-      const uint32_t stage_a = sbase + L::kK;
-      const uint32_t lse_a = sbase + L::kEpi + 4 * kTile * 4;
+      const float* lse_all = reinterpret_cast<const float*>(sm + L::kLseAll);   // [nsplit][128]
       float* wts = reinterpret_cast<float*>(sm + L::kQ);   // [nsplit][128]
-      const float scale_v = r.scales[H + h];
+      const int ntask = nr * (D / 4);
       if ((int)threadIdx.x < nr) {
         const int row = r0 + threadIdx.x;
         float lv[8];
@@ -783,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s2 = 0; s2 < 8; ++s2)
           if (s2 < ns) {
-            lv[s2] = ld_dsmem_f32(dsmem_addr(lse_a + 4u * row, s2));
+            lv[s2] = lse_all[s2 * kTile + row];
             mx = fmaxf(mx, lv[s2]);
           }
         float sum = 0.f;
@@ -798,36 +882,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s2 = 0; s2 < 8; ++s2)
           if (s2 < ns) wts[s2 * kTile + threadIdx.x] = lv[s2] * gsc;
       }
+      const bool landed =
+          __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarMerge), 0, abort, kWaitLimitNs));
       sync_softmax();
-      const int ntask = nr * (D / 4);
       const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
       float4 acc[MT];
 #pragma unroll
       for (int i = 0; i < MT; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s2 = 0; s2 < ns; ++s2) {
-        float4 v[MT];
+      for (int s2 = 0; landed && s2 < ns; ++s2) {
+        // split s2's rows of this range: own staging, or the sender's slot
+        const uint8_t* src = s2 == split ? sm + L::kK + (size_t)r0 * SPB
+                                         : sm + L::kVh + (size_t)((s2 < split ? s2 : s2 - 1) * maxr) * SPB;
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
           const int idx = threadIdx.x + i * kSoftmaxThreads;
-          const int row = r0 + idx / (D / 4), c4 = idx % (D / 4);
-          v[i] = idx < ntask ? ld_dsmem_f4(dsmem_addr(stage_a + 4u * (row * SP + 4 * c4), s2))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-          const int idx = threadIdx.x + i * kSoftmaxThreads;
-          const float w = idx < ntask ? wts[s2 * kTile + idx / (D / 4)] : 0.f;
-          acc[i].x = fmaf(w, v[i].x, acc[i].x);
-          acc[i].y = fmaf(w, v[i].y, acc[i].y);
-          acc[i].z = fmaf(w, v[i].z, acc[i].z);
-          acc[i].w = fmaf(w, v[i].w, acc[i].w);
+          if (idx >= ntask) continue;
+          const int lr = idx / (D / 4), c4 = idx % (D / 4);
+          const float4 v = *reinterpret_cast<const float4*>(src + (size_t)lr * SPB + 16 * c4);
+          const float w = wts[s2 * kTile + lr];
+          acc[i].x = fmaf(w, v.x, acc[i].x);
+          acc[i].y = fmaf(w, v.y, acc[i].y);
+          acc[i].z = fmaf(w, v.z, acc[i].z);
+          acc[i].w = fmaf(w, v.w, acc[i].w);
         }
       }
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
         const int idx = threadIdx.x + i * kSoftmaxThreads;
         const int row = r0 + idx / (D / 4), c4 = idx % (D / 4);
-        if (idx >= ntask || row >= rows_live) continue;
+        if (!landed || idx >= ntask || row >= rows_live) continue;
         const size_t e = ((size_t)(qt * kTile + row) * H + h) * D + 4 * c4;
         if (prm.out_bf16) {
           const __nv_bfloat162 a0 = __floats2bfloat162_rn(acc[i].x, acc[i].y), a1 = __floats2bfloat162_rn(acc[i].z, acc[i].w);
@@ -838,8 +921,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    __syncwarp();
-    cluster_sync_all();
+    // the outgoing copies have read this CTA's rows before it may leave
+    if (threadIdx.x == kWarpTma * 32) bulk_wait_read();
   }
 
   // ------------------------------------------------------------ teardown
