@@ -21,7 +21,7 @@
 //               raised running maximum; probabilities carry 2^7 and are
 //               written into P_g as f16, and the thread sums its fp32
 //               probabilities into the row's normaliser.  O is rescaled in TMEM when the maximum
-//               rises by more than 1.5 (log2 units).  Epilogue: the two
+//               rises by more than 8 (log2 units).  Epilogue: the two
 //               groups' (m, l, O) merged, O / l, split partials and their merge.
 //   warp 8      Copy producer: K and V tiles [128 slots][d] by TMA into a
 //               3-stage ring (the third stage once the query prologue is done).
@@ -72,8 +72,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 // Probabilities carry a factor 2^kPShift relative to the running maximum,
 // which is raised only when a tile's maximum exceeds it by more than kTau:
-// the largest probability is 2^(kPShift + kTau) = 2^8.5, well inside f16.
-constexpr float kTau = 1.5f;
+// the largest probability is 2^(kPShift + kTau) = 2^15, inside f16 (whose
+// relative precision does not depend on the magnitude).  A raise costs a
+// rescale of O in TMEM by every warp holding an affected row; with a
+// threshold of 8 (a factor 256) rescales are rare after the first tiles.
+constexpr float kTau = 8.0f;
 constexpr float kPShift = 7.0f;
 // Level rule: with L = max|q| * max|k| over the tile (rotated query units
 // times 448 * scale_k) and V = 448 * scale_v (the largest value), level 1

@@ -40,7 +40,8 @@ def test_kernel_matches_its_mirror_tightly(level):
     ring, orc, frames = _tiny_loaded(6, max_kv_splits=1, attn_precision=level)
     q = frames[6][0]
     out = ring.attention(dev(q)).cpu().numpy()
-    mirror = attention_emulated(orc, f(q), None, level, "f16")
+    # the kernel's probability shift (2^7) and rescale threshold (8, log2 units)
+    mirror = attention_emulated(orc, f(q), None, level, "f16", p_shift=7.0, tau=8.0)
     mx, mn = attn_errors(out, mirror)
     scale = np.abs(mirror).max()
     assert mx <= 2e-3 * scale, (level, mx, scale)
