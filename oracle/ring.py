@@ -22,6 +22,16 @@ Readings of what the pages leave open (each listed in the design notes):
 * the reset's delta D defaults to the position of the oldest cached slot,
   so the window restarts at position 0; cached keys are rotated by -D in
   scaled (code) units, positions and the next position drop by D.
+
+Variant with a pinned prefix (the pages give 5,788 = 7 x 757 + 489 slots
+and say nothing of a part that is never evicted; this variant reads the 489
+as such a part): the first P slots take the first P tokens ever written and
+are never overwritten; later tokens cycle over the other C - P slots.  A
+reset rotates only those rolling slots, and its default delta puts the
+oldest rolling position right after the prefix (delta = oldest rolling
+position - (last prefix position + 1), at least 0); prefix keys and their
+positions never change, so their FP8 codes are not re-rounded at every
+reset.  P = 0 is the plain ring.
 """
 from __future__ import annotations
 
@@ -46,8 +56,12 @@ class Ring:
     """One layer's cache: K and V codes as [heads][capacity][head_dim] uint8."""
 
     def __init__(self, heads: int, head_dim: int, capacity: int,
-                 max_position: int, rope_base: float = 10000.0):
+                 max_position: int, rope_base: float = 10000.0, prefix: int = 0):
+        if not 0 <= prefix < capacity:
+            raise ValueError("prefix must be in [0, capacity)")
         self.H, self.d, self.C = heads, head_dim, capacity
+        self.P = int(prefix)
+        self.W = capacity - self.P            # rolling slots
         self.table = Table(head_dim, rope_base, max_position)
         self.K = np.zeros((heads, capacity, head_dim), dtype=np.uint8)
         self.V = np.zeros((heads, capacity, head_dim), dtype=np.uint8)
@@ -100,16 +114,21 @@ class Ring:
     def quantise_values(self, v: np.ndarray) -> np.ndarray:
         return e4m3.encode(np.asarray(v, dtype=np.float32) * self.inv_v[None, :, None])
 
+    def slot_of(self, g) -> np.ndarray:
+        """Slot of the g-th token ever written (g >= 0)."""
+        g = np.asarray(g, dtype=np.int64)
+        return np.where(g < self.P, g, self.P + (g - self.P) % self.W)
+
     def slots_for(self, n: int) -> np.ndarray:
-        return (self.head + np.arange(n, dtype=np.int64)) % self.C
+        return self.slot_of(self.total + np.arange(n, dtype=np.int64))
 
     def write(self, k: np.ndarray, v: np.ndarray, pos=None) -> np.ndarray:
         """Write one frame; returns the slots used."""
         if not self.calibrated:
             raise RuntimeError("write before calibration")
         n = np.asarray(k).shape[0]
-        if not 1 <= n <= self.C:
-            raise ValueError("frame must hold 1..capacity tokens")
+        if not 1 <= n <= (self.C if self.P == 0 else self.W):
+            raise ValueError("frame must hold 1..capacity tokens (1..capacity - prefix with a prefix)")
         positions = self._positions(n, pos)
         slots = self.slots_for(n)
         kc = self.quantise_keys(k, positions)                # [n, H, d]
@@ -117,29 +136,38 @@ class Ring:
         self.K[:, slots, :] = kc.transpose(1, 0, 2)
         self.V[:, slots, :] = vc.transpose(1, 0, 2)
         self.slot_pos[slots] = positions
-        self.head = int((self.head + n) % self.C)
-        self.n_valid = min(self.C, self.n_valid + n)
         self.total += n
+        self.head = int(self.slot_of(self.total))
+        self.n_valid = min(self.C, self.n_valid + n)
         self.next_pos += n
         return slots
 
     def oldest_slot(self) -> int:
-        return self.head if self.n_valid == self.C else 0
+        """The oldest rolling slot (the next to be overwritten once full)."""
+        return self.head if self.n_valid == self.C else self.P
+
+    def default_delta(self) -> int:
+        if self.n_valid <= self.P:
+            return 0                          # no rolling token yet
+        oldest = int(self.slot_pos[self.oldest_slot()])
+        if self.P == 0:
+            return oldest
+        return max(0, oldest - (int(self.slot_pos[self.P - 1]) + 1))
 
     def delta_rotate(self, delta: int = TO_OLDEST) -> int:
-        """Rotate every cached key by -delta in place; returns the delta used."""
+        """Rotate every rolling key by -delta in place; returns the delta used."""
         if delta == TO_OLDEST:
-            delta = int(self.slot_pos[self.oldest_slot()]) if self.n_valid else 0
+            delta = self.default_delta()
         delta = int(delta)
         if delta < 0:
             raise ValueError("delta must be >= 0")
-        nv = self.n_valid
-        if nv:
+        lo, nv = self.P, self.n_valid
+        if nv > lo:
             c, s = self.table.row(delta)
-            a = e4m3.decode(self.K[:, :nv, :]).astype(np.float32)   # exact
+            a = e4m3.decode(self.K[:, lo:nv, :]).astype(np.float32)   # exact
             y = unrotate_pinned_f32(a, c, s)
-            self.K[:, :nv, :] = e4m3.encode(y)
-            self.slot_pos[:nv] -= delta
+            self.K[:, lo:nv, :] = e4m3.encode(y)
+            self.slot_pos[lo:nv] -= delta
         self.next_pos -= delta
         return delta
 
