@@ -71,7 +71,11 @@ typedef struct {
   int32_t max_position;   /* RoPE table rows: positions lie in [0, max_position) */
   int32_t max_kv_splits;  /* most key/value partitions one attention call may use (1..32) */
   int32_t attn_precision; /* 0 = automatic per tile; 1..3 = fixed FP8 term level */
-  int32_t reserved;       /* must be 0 */
+  int32_t pinned_prefix;  /* P, 0 .. capacity - 1: slots [0, P) keep the first P tokens ever
+                             written and are never overwritten; later tokens cycle over the
+                             other capacity - P slots.  0 = the plain ring.  (The pages give
+                             5,788 = 7 x 757 + 489 slots and do not say whether a part is
+                             never evicted; P = 489 reads the remainder as such a part.) */
   double rope_base;       /* RoPE base, e.g. 10000 */
 } kvring_config;
 
@@ -122,15 +126,18 @@ kvring_status kvring_calibrate_scales(kvring_t* ring, const void* k_bf16, const 
                                       const int32_t* pos, int32_t n, void* stream);
 
 /* Write one frame of n new tokens ("Do It Once, at Write Time").
- * Token t goes to slot (head + t) mod capacity:
+ * Token t goes to slot (head + t) mod capacity (with a pinned prefix P:
+ * the g-th token ever written goes to slot g while g < P, else to slot
+ * P + (g - P) mod (capacity - P)):
  *   K[h][slot][:] = e4m3(rope(k[t,h,:], pos[t]) * inv_scale_k[h])
  *   V[h][slot][:] = e4m3(v[t,h,:] * inv_scale_v[h])
  *   slot_pos[slot] = pos[t]
- * then head += n (mod capacity), n_valid = min(capacity, n_valid + n),
+ * then head advances by n slots, n_valid = min(capacity, n_valid + n),
  * total += n, next_pos += n.  RoPE is computed in fp32 from the fp32
  * cos/sin table with every product and sum rounded separately.
  * pos: int32 [n] device positions, or NULL for next_pos + t.
- * Errors: NOT_CALIBRATED, CAPACITY (n > capacity or n > max_tokens), INVALID_ARG. */
+ * Errors: NOT_CALIBRATED, CAPACITY (n > capacity, n > capacity - P when
+ * P > 0, or n > max_tokens), INVALID_ARG. */
 kvring_status kvring_write_frame(kvring_t* ring, const void* k_bf16, const void* v_bf16,
                                  const int32_t* pos, int32_t n, void* stream);
 
@@ -143,6 +150,11 @@ kvring_status kvring_write_frame(kvring_t* ring, const void* k_bf16, const void*
  * touched.  delta = KVRING_DELTA_TO_OLDEST reads, on the device, the
  * position of the oldest slot (the next slot to be overwritten once the
  * ring is full, slot 0 before), so the window restarts at position 0.
+ * With a pinned prefix P only the rolling slots [P, n_valid) are rotated
+ * and have their positions lowered (prefix keys are never re-rounded), and
+ * KVRING_DELTA_TO_OLDEST takes delta = position of the oldest rolling slot -
+ * (position of slot P - 1 + 1), at least 0, so the window continues right
+ * after the prefix.
  * Errors: INVALID_ARG (delta < -1 or >= max_position). */
 kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
 
@@ -161,7 +173,8 @@ kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
  * and E4M3 conversion as kvring_write_frame.  Afterwards kvring_attention
  * reads the ring as usual.  Do not mix with kvring_write_frame on one ring.
  * Errors: INVALID_ARG (NULL, unaligned or aliased buffers), CAPACITY
- * (n > capacity or n > max_tokens). */
+ * (n > capacity or n > max_tokens), UNSUPPORTED (a ring with a pinned
+ * prefix: the original upkeep had none). */
 kvring_status kvring_legacy_upkeep(kvring_t* ring, const void* wk_in, const void* wv_in, void* wk_out,
                                    void* wv_out, const void* k_bf16, const void* v_bf16, int32_t n,
                                    void* stream);
@@ -172,7 +185,7 @@ kvring_status kvring_legacy_upkeep(kvring_t* ring, const void* wk_in, const void
 /* kvring_write_frame on num_rings rings at once, in one launch: ring i gets
  * k_bf16[i], v_bf16[i] and pos[i] (pos may be NULL, or any pos[i] NULL, for
  * next_pos + t of that ring).  Every ring must have the same num_heads,
- * head_dim and capacity; n applies to all.  The result on each ring is
+ * head_dim, capacity and pinned_prefix; n applies to all.  The result on each ring is
  * byte-for-byte that of kvring_write_frame.  The reset of the page
  * ("Do It Once, at Write Time") and the per-step upkeep touch every layer,
  * and one launch over all of them moves hundreds of megabytes instead of a
@@ -186,8 +199,8 @@ kvring_status kvring_write_frames_many(kvring_t* const* rings, int32_t num_rings
                                        const void* const* k_bf16, const void* const* v_bf16,
                                        const int32_t* const* pos, int32_t n, void* stream);
 
-/* kvring_delta_rotate on num_rings rings of the same num_heads, head_dim and
- * capacity in one launch (delta, or KVRING_DELTA_TO_OLDEST read per ring on
+/* kvring_delta_rotate on num_rings rings of the same num_heads, head_dim,
+ * capacity and pinned_prefix in one launch (delta, or KVRING_DELTA_TO_OLDEST read per ring on
  * the device).  Each ring ends byte-for-byte as after kvring_delta_rotate.
  * Errors: INVALID_ARG (as above, or delta < -1 or >= a ring's max_position);
  * nothing is launched on an error. */

@@ -49,7 +49,7 @@ class KvringConfig(ctypes.Structure):
         ("max_position", ctypes.c_int32),
         ("max_kv_splits", ctypes.c_int32),
         ("attn_precision", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("pinned_prefix", ctypes.c_int32),
         ("rope_base", ctypes.c_double),
     ]
 
@@ -152,10 +152,10 @@ def _positions(pos, n: int, name: str):
 # C-named functions (marshalling only)
 # ---------------------------------------------------------------------------
 def make_config(heads, head_dim, capacity, max_tokens, max_position, rope_base=10000.0,
-                max_kv_splits=16, attn_precision=0) -> KvringConfig:
+                max_kv_splits=16, attn_precision=0, pinned_prefix=0) -> KvringConfig:
     return KvringConfig(int(heads), int(head_dim), int(capacity), int(max_tokens),
-                        int(max_position), int(max_kv_splits), int(attn_precision), 0,
-                        float(rope_base))
+                        int(max_position), int(max_kv_splits), int(attn_precision),
+                        int(pinned_prefix), float(rope_base))
 
 
 def kvring_required_bytes(cfg: KvringConfig) -> int:
@@ -290,14 +290,15 @@ class KvRing:
 
     def __init__(self, heads: int, head_dim: int, capacity: int, max_tokens: int,
                  max_position: int, rope_base: float = 10000.0, max_kv_splits: int = 16,
-                 attn_precision: int = 0, device=None, stream=None):
+                 attn_precision: int = 0, device=None, stream=None, pinned_prefix: int = 0):
         if not torch.cuda.is_available():
             raise RuntimeError("KvRing needs a CUDA device")
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.H, self.d, self.C = int(heads), int(head_dim), int(capacity)
         self.max_tokens = int(max_tokens)
+        self.P = int(pinned_prefix)
         self.cfg = make_config(heads, head_dim, capacity, max_tokens, max_position, rope_base,
-                               max_kv_splits, attn_precision)
+                               max_kv_splits, attn_precision, pinned_prefix)
         n = kvring_required_bytes(self.cfg)
         if n == 0:
             raise ValueError("invalid kvring config")

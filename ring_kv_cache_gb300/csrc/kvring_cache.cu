@@ -150,6 +150,29 @@ __global__ void __launch_bounds__(kThreads) k_calibrate(RingDev r, const uint16_
 }
 
 // ---------------------------------------------------------------- write ---
+// Ring state after a write of n tokens that started at slot head0 with
+// default position next0; run by the one thread that completes the write.
+__device__ __forceinline__ void publish_write(const RingDev& r, int head0, int next0, int n) {
+  const int C = r.C, P = r.P;
+  int head = head0 + n;
+  if (head >= C) head -= C - P;   // the wrap skips the pinned prefix
+  int nv = r.state[ST_NVALID] + n;
+  nv = nv < C ? nv : C;
+  r.state[ST_HEAD] = head;
+  r.state[ST_NVALID] = nv;
+  const unsigned long long tot =
+      ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
+      (unsigned long long)n;
+  r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
+  r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
+  r.state[ST_NEXT_POS] = next0 + n;
+  // oldest rolling slot: the next one to be overwritten once full, else slot P
+  r.state[ST_OLDEST_POS] = nv > P ? __ldcg(r.slot_pos + (nv >= C ? head : P)) : kEmptyPos;
+  if (P > 0 && nv >= P) r.state[ST_PREFIX_END] = __ldcg(r.slot_pos + P - 1) + 1;
+  r.state[ST_TICKET_WRITE] = 0;
+  __threadfence();
+}
+
 // Each thread owns kWriteU chunks, (block * kWriteU + u) * 256 + tid, so a
 // warp's accesses stay contiguous; all input loads are issued before the
 // ring state is read, which hides one DRAM round trip.
@@ -216,8 +239,9 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
     const long long th = w / CH;
     const int h = (int)(th % H);
     const int t = (int)(th / H);
+    // head < C and t < n <= C - P: at most one wrap, which skips the prefix
     int slot = s_head + t;
-    if (slot >= C) slot -= C;  // head < C and t < n <= C
+    if (slot >= C) slot -= C - r.P;
     float x[16];
     unpack_bf16x16(in[u][0], in[u][1], x);
     bool ok = true;
@@ -245,21 +269,7 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
     const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
     if (tk == nblk - 1) {
       __threadfence();
-      int head = s_head + n;
-      if (head >= C) head -= C;
-      const int nv = r.state[ST_NVALID] + n;
-      r.state[ST_HEAD] = head;
-      r.state[ST_NVALID] = nv < C ? nv : C;
-      const unsigned long long tot =
-          ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
-          (unsigned long long)n;
-      r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
-      r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
-      r.state[ST_NEXT_POS] = s_next + n;
-      // oldest filled slot: the next one to be overwritten once full, else slot 0
-      r.state[ST_OLDEST_POS] = __ldcg(r.slot_pos + (nv >= C ? head : 0));
-      r.state[ST_TICKET_WRITE] = 0;
-      __threadfence();
+      publish_write(r, s_head, s_next, n);
     }
   }
 }
@@ -514,7 +524,7 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
     next = hdr[g.TU + 1];
     const bool act = dt < ntok && hl < nh;
     int slot = head + t0 + dt;
-    if (slot >= C) slot -= C;
+    if (slot >= C) slot -= C - r.P;   // at most one wrap, which skips the prefix
     const uint32_t eb = smem_u32(&empty[s]);
     if (isv)
       wm_place<D, false>(r, st, hdr, act, false, in_off, tab_off, dt, k, h, slot, 0, invv, eb, lane);
@@ -537,20 +547,7 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
         const int tk = atomicAdd(r.state + ST_TICKET_WRITE, done);
         if (tk + done == kWmConsumerWarps * (int)up) {
           __threadfence();
-          int nh2 = head + n;
-          if (nh2 >= C) nh2 -= C;
-          const int nv = r.state[ST_NVALID] + n;
-          r.state[ST_HEAD] = nh2;
-          r.state[ST_NVALID] = nv < C ? nv : C;
-          const unsigned long long tot =
-              ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
-              (unsigned long long)n;
-          r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
-          r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
-          r.state[ST_NEXT_POS] = next + n;
-          r.state[ST_OLDEST_POS] = __ldcg(r.slot_pos + (nv >= C ? nh2 : 0));
-          r.state[ST_TICKET_WRITE] = 0;
-          __threadfence();
+          publish_write(r, head, next, n);
         }
       }
       done = 0;
@@ -598,7 +595,8 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
   __shared__ int hdr[kDpStages][2];  // filled rows of the unit, its ring's delta (-1: none)
   __shared__ int s_abort;
   const int H = b.r[0].H, C = b.r[0].C;
-  const int runs = (C + RU - 1) / RU;
+  const int P = b.r[0].P;                  // pinned prefix: never rotated
+  const int runs = (C - P + RU - 1) / RU;  // runs of rolling slots per head
   const long long up = (long long)H * runs;  // units per ring
   const long long total = up * count;
   const long long u_begin = total * blockIdx.x / gridDim.x;
@@ -636,13 +634,24 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
         cur = ring;
         nv = __ldcg(r.state + ST_NVALID);
         d = delta_arg;
-        if (d == KVRING_DELTA_TO_OLDEST) d = nv > 0 ? __ldcg(r.state + ST_OLDEST_POS) : 0;
+        if (d == KVRING_DELTA_TO_OLDEST) {
+          // the oldest rolling position, less the prefix's end with a prefix
+          const int oldest = __ldcg(r.state + ST_OLDEST_POS);
+          if (nv <= P || oldest == kEmptyPos) {
+            d = 0;
+          } else if (P == 0) {
+            d = oldest;
+          } else {
+            const int gap = oldest - __ldcg(r.state + ST_PREFIX_END);
+            d = gap > 0 ? gap : 0;
+          }
+        }
         if (d < 0 || d >= r.max_pos) {
           atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_DELTA);
           d = -1;  // skip the rotation entirely
         }
       }
-      const int r0 = run * RU;
+      const int r0 = P + run * RU;
       int rows = d > 0 ? nv - r0 : 0;
       rows = rows < 0 ? 0 : (rows > RU ? RU : rows);
       hdr[s][0] = rows;
@@ -693,7 +702,7 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     const RingDev& r = b.r[ring];
-    const int r0 = run * RU;
+    const int r0 = P + run * RU;
     if (rows > 0) {
       if (d != cur_d) {
         cur_d = d;
@@ -744,7 +753,7 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
           __threadfence();
           if (d >= 0) {
             r.state[ST_NEXT_POS] -= d;
-            r.state[ST_OLDEST_POS] -= d;
+            if (r.state[ST_OLDEST_POS] != kEmptyPos) r.state[ST_OLDEST_POS] -= d;
             r.state[ST_LAST_DELTA] = d;
           }
           r.state[ST_TICKET_DELTA] = 0;
@@ -1005,7 +1014,7 @@ cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t
 cudaError_t launch_delta_pipe(const DeltaMany& b, int count, int delta, cudaStream_t s) {
   const RingDev& r = b.r[0];
   const int ru = kDpUnitBytes / r.D;
-  const long long units = (long long)count * r.H * ((r.C + ru - 1) / ru);
+  const long long units = (long long)count * r.H * ((r.C - r.P + ru - 1) / ru);
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   long long grid = sms;

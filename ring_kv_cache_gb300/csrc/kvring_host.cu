@@ -38,7 +38,7 @@ bool config_ok(const kvring_config* c) {
   if (c->max_position < 1 || c->max_position > (1 << 24)) return false;
   if (c->max_kv_splits < 1 || c->max_kv_splits > 32) return false;
   if (c->attn_precision < 0 || c->attn_precision > 3) return false;
-  if (c->reserved != 0) return false;
+  if (c->pinned_prefix < 0 || c->pinned_prefix >= c->capacity) return false;
   if (!(c->rope_base > 0.0) || !std::isfinite(c->rope_base)) return false;
   return true;
 }
@@ -195,6 +195,7 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   d.max_tokens = cfg->max_tokens;
   d.max_splits = cfg->max_kv_splits;
   d.qtiles_max = p.qtiles;
+  d.P = cfg->pinned_prefix;
 
   if (kvr::attention_prepare(d.D) != cudaSuccess || kvr::cache_prepare() != cudaSuccess) {
     delete r;
@@ -260,7 +261,7 @@ kvring_status kvring_write_frame(kvring_t* r, const void* k, const void* v, cons
   if (!r || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (pos && !aligned(pos, 4)) || n < 1)
     return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
-  if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+  if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   return cuda_status(kvr::launch_write(r->dev, k, v, pos, n, (cudaStream_t)stream));
 }
 
@@ -280,7 +281,7 @@ kvring_status check_batch(kvring_t* const* rings, int32_t count) {
     if (!r) return KVRING_ERR_INVALID_ARG;
     const kvring* r0 = rings[0];
     if (r->cfg.num_heads != r0->cfg.num_heads || r->cfg.head_dim != r0->cfg.head_dim ||
-        r->cfg.capacity != r0->cfg.capacity)
+        r->cfg.capacity != r0->cfg.capacity || r->cfg.pinned_prefix != r0->cfg.pinned_prefix)
       return KVRING_ERR_INVALID_ARG;
     for (int j = 0; j < i; ++j)
       if (rings[j] == r) return KVRING_ERR_INVALID_ARG;
@@ -302,7 +303,7 @@ kvring_status kvring_write_frames_many(kvring_t* const* rings, int32_t count, co
     if (!k[i] || !v[i] || !aligned(k[i], 16) || !aligned(v[i], 16) || (p && !aligned(p, 4)))
       return KVRING_ERR_INVALID_ARG;
     if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
-    if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+    if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
     b.r[i] = r->dev;
     b.k[i] = static_cast<const uint16_t*>(k[i]);
     b.v[i] = static_cast<const uint16_t*>(v[i]);
@@ -331,6 +332,7 @@ kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* w
   for (const void* p : ptrs)
     if (!aligned(p, 16)) return KVRING_ERR_INVALID_ARG;
   if (wk_in == wk_out || wv_in == wv_out || wk_out == wv_out) return KVRING_ERR_INVALID_ARG;
+  if (r->cfg.pinned_prefix != 0) return KVRING_ERR_UNSUPPORTED;   // the original upkeep had no prefix
   if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   const kvring_status st = cuda_status(
       kvr::launch_legacy_upkeep(r->dev, wk_in, wv_in, wk_out, wv_out, k, v, n, (cudaStream_t)stream));

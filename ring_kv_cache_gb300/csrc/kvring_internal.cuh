@@ -26,7 +26,8 @@ enum : int {
   ST_TICKET_WRITE = 8,
   ST_TICKET_CALIB = 9,
   ST_TICKET_DELTA = 10,
-  ST_OLDEST_POS = 11,   // position of the oldest filled slot (the default reset delta)
+  ST_OLDEST_POS = 11,   // position of the oldest rolling slot (the default reset delta)
+  ST_PREFIX_END = 12,   // with a pinned prefix: position of its last slot + 1
   ST_WORDS_ALLOC = 16,
 };
 
@@ -47,6 +48,7 @@ struct RingDev {
   int32_t* tickets;    // [qtiles][H] split completion counters (0 between calls)
   int32_t* levels;     // [qtiles][H] precision level of each query tile
   int H, D, C, max_pos, max_tokens, max_splits, qtiles_max;
+  int P;               // pinned prefix slots; tokens past it cycle over slots [P, C)
 };
 
 // ---------------------------------------------------------------- E4M3 ----

@@ -46,7 +46,8 @@ def test_required_bytes_matches_layout(L):
 
 @pytest.mark.parametrize("field,value", [
     ("num_heads", 0), ("head_dim", 96), ("capacity", 0), ("max_tokens", 0),
-    ("max_position", 0), ("max_kv_splits", 0), ("attn_precision", 4), ("reserved", 1),
+    ("max_position", 0), ("max_kv_splits", 0), ("attn_precision", 4),
+    ("pinned_prefix", -1), ("pinned_prefix", 48),
     ("rope_base", 0.0), ("rope_base", float("inf")),
 ])
 def test_bad_configs_are_rejected(L, field, value):
