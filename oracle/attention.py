@@ -51,13 +51,14 @@ def softmax_attention_f64(qt: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.nd
 def attention_exact(ring, q: np.ndarray, qpos=None) -> np.ndarray:
     """Reference attention of queries q (float32 [n, H, d]) over ``ring``.
 
-    qpos defaults to the n positions just before ``ring.next_pos``.
+    qpos defaults to the n positions just before ``ring.next_pos``; with the
+    3-D RoPE variant it is an explicit [n, 3] array of (t, y, x).
     """
     q = np.asarray(q, dtype=np.float64)
     n = q.shape[0]
     if qpos is None:
         qpos = ring.next_pos - n + np.arange(n)
-    qt = rotate_f64(q, np.asarray(qpos, dtype=np.int64), ring.table.theta)
+    qt = ring.rope_f64(q, qpos)
     k, v, _ = ring.dequantised()
     return softmax_attention_f64(qt, k, v)
 
@@ -129,7 +130,7 @@ def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
     n, H, d = q.shape
     if qpos is None:
         qpos = ring.next_pos - n + np.arange(n)
-    qt = rotate_f64(q, np.asarray(qpos, np.int64), ring.table.theta).astype(np.float32)
+    qt = ring.rope_f64(q, qpos).astype(np.float32)
     amax = np.abs(qt).max(axis=2)                                # [n, H]
     sq = (amax / np.float32(448.0)).astype(np.float32)
     sq = np.where(sq >= np.float32(2.0 ** -126), sq, np.float32(1.0)).astype(np.float32)

@@ -32,13 +32,21 @@ oldest rolling position right after the prefix (delta = oldest rolling
 position - (last prefix position + 1), at least 0); prefix keys and their
 positions never change, so their FP8 codes are not re-rounded at every
 reset.  P = 0 is the plain ring.
+
+Variant with 3-D RoPE (rope3d = (T, Y): T temporal pairs, Y pairs for the
+spatial row, the rest for the column; see ``oracle.rope``): every token
+carries an explicit (t, y, x) position, slot positions hold t, and a reset
+rotates only the T temporal pairs of the cached keys by -delta (a reset
+moves the frame index, not the place in the frame); the spatial pairs' codes
+are left as they are.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from . import e4m3
-from .rope import Table, rotate_pinned_f32, unrotate_pinned_f32
+from .rope import (Table, rotate_f64, rotate_f64_3d, rotate_pinned_f32, rows_3d, sections, theta_3d,
+                   unrotate_pinned_f32)
 
 INT32_MIN = -(2 ** 31)
 TO_OLDEST = -1
@@ -56,13 +64,20 @@ class Ring:
     """One layer's cache: K and V codes as [heads][capacity][head_dim] uint8."""
 
     def __init__(self, heads: int, head_dim: int, capacity: int,
-                 max_position: int, rope_base: float = 10000.0, prefix: int = 0):
+                 max_position: int, rope_base: float = 10000.0, prefix: int = 0, rope3d=None):
         if not 0 <= prefix < capacity:
             raise ValueError("prefix must be in [0, capacity)")
         self.H, self.d, self.C = heads, head_dim, capacity
         self.P = int(prefix)
         self.W = capacity - self.P            # rolling slots
-        self.table = Table(head_dim, rope_base, max_position)
+        self.rope3d = None if rope3d is None else (int(rope3d[0]), int(rope3d[1]))
+        if self.rope3d is None:
+            self.axis = None
+            self.table = Table(head_dim, rope_base, max_position)
+        else:
+            self.axis = sections(head_dim, *self.rope3d)
+            self.table = Table(head_dim, rope_base, max_position,
+                               theta_3d(head_dim, rope_base, *self.rope3d))
         self.K = np.zeros((heads, capacity, head_dim), dtype=np.uint8)
         self.V = np.zeros((heads, capacity, head_dim), dtype=np.uint8)
         self.slot_pos = np.full(capacity, INT32_MIN, dtype=np.int64)
@@ -78,6 +93,13 @@ class Ring:
 
     # -- helpers -----------------------------------------------------------
     def _positions(self, n: int, pos) -> np.ndarray:
+        if self.rope3d is not None:
+            if pos is None:
+                raise ValueError("3-D RoPE needs an explicit (t, y, x) position per token")
+            pos = np.asarray(pos, dtype=np.int64).reshape(-1, 3)
+            if pos.shape[0] != n:
+                raise ValueError("one (t, y, x) position per token")
+            return pos
         if pos is None:
             return self.next_pos + np.arange(n, dtype=np.int64)
         pos = np.asarray(pos, dtype=np.int64).reshape(-1)
@@ -86,8 +108,17 @@ class Ring:
         return pos
 
     def _rope(self, k: np.ndarray, positions: np.ndarray) -> np.ndarray:
-        c, s = self.table.rows(positions)                    # [n, d/2]
+        if self.rope3d is not None:
+            c, s = rows_3d(self.table, self.axis, positions)  # [n, d/2]
+        else:
+            c, s = self.table.rows(positions)                 # [n, d/2]
         return rotate_pinned_f32(k, c[:, None, :], s[:, None, :])
+
+    def rope_f64(self, x: np.ndarray, positions: np.ndarray) -> np.ndarray:
+        """Exact rotation of x [n, ..., d] at the ring's RoPE variant."""
+        if self.rope3d is not None:
+            return rotate_f64_3d(x, positions, self.table.theta, self.axis)
+        return rotate_f64(x, np.asarray(positions, np.int64), self.table.theta)
 
     # -- the four operations --------------------------------------------------
     def calibrate(self, k: np.ndarray, v: np.ndarray, pos=None) -> None:
@@ -135,7 +166,7 @@ class Ring:
         vc = self.quantise_values(v)
         self.K[:, slots, :] = kc.transpose(1, 0, 2)
         self.V[:, slots, :] = vc.transpose(1, 0, 2)
-        self.slot_pos[slots] = positions
+        self.slot_pos[slots] = positions if self.rope3d is None else positions[:, 0]
         self.total += n
         self.head = int(self.slot_of(self.total))
         self.n_valid = min(self.C, self.n_valid + n)
@@ -164,9 +195,10 @@ class Ring:
         lo, nv = self.P, self.n_valid
         if nv > lo:
             c, s = self.table.row(delta)
-            a = e4m3.decode(self.K[:, lo:nv, :]).astype(np.float32)   # exact
-            y = unrotate_pinned_f32(a, c, s)
-            self.K[:, lo:nv, :] = e4m3.encode(y)
+            dims = self.d if self.rope3d is None else 2 * self.rope3d[0]   # 3-D: temporal pairs only
+            a = e4m3.decode(self.K[:, lo:nv, :dims]).astype(np.float32)   # exact
+            y = unrotate_pinned_f32(a, c[:dims // 2], s[:dims // 2])
+            self.K[:, lo:nv, :dims] = e4m3.encode(y)
             self.slot_pos[lo:nv] -= delta
         self.next_pos -= delta
         return delta

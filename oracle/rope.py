@@ -20,6 +20,14 @@ Two arithmetic forms are kept:
   precision, each product and sum rounded separately (no fused multiply-add).
   The delta rotation by -D uses the same table row for D with the signs
   flipped: y0 = fl(fl(a*c) + fl(b*s)), y1 = fl(fl(b*c) - fl(a*s)).
+
+3-D variant (a video model's tokens carry a frame index t and a spatial row
+y and column x; the pages give only "RoPE" and one position per token, so
+this is a variant): the d/2 pairs are cut into a temporal section of T pairs,
+then Y pairs for y, then X = d/2 - T - Y pairs for x.  Each section is a
+RoPE of its own over its 2T (2Y, 2X) dimensions: local pair j of a section
+of 2m dimensions turns by position_axis * base^(-2j/(2m)).  A token's
+(t, y, x) position picks, for every pair, the coordinate of its section.
 """
 from __future__ import annotations
 
@@ -34,14 +42,38 @@ def theta(head_dim: int, base: float) -> np.ndarray:
                      for i in range(head_dim // 2)], dtype=np.float64)
 
 
-class Table:
-    """fp32 cos/sin rows, built lazily from float64 libm cos/sin per element."""
+def sections(head_dim: int, pairs_t: int, pairs_y: int) -> np.ndarray:
+    """Axis (0 = t, 1 = y, 2 = x) of every pair of the 3-D variant."""
+    h = head_dim // 2
+    if not (pairs_t >= 1 and pairs_y >= 0 and pairs_t + pairs_y <= h):
+        raise ValueError("sections must fit the head")
+    return np.r_[np.zeros(pairs_t, np.int64), np.ones(pairs_y, np.int64),
+                 np.full(h - pairs_t - pairs_y, 2, np.int64)]
 
-    def __init__(self, head_dim: int, base: float, max_position: int):
+
+def theta_3d(head_dim: int, base: float, pairs_t: int, pairs_y: int) -> np.ndarray:
+    """Per-pair angles of the 3-D variant: each section its own ladder
+    base^(-2j/(2m)) over its m pairs (libm pow per element)."""
+    ax = sections(head_dim, pairs_t, pairs_y)
+    out = np.empty(head_dim // 2, dtype=np.float64)
+    for a in range(3):
+        idx = np.nonzero(ax == a)[0]
+        m = len(idx)
+        for j, i in enumerate(idx):
+            out[i] = math.pow(base, (-2.0 * j) / (2 * m))
+    return out
+
+
+class Table:
+    """fp32 cos/sin rows, built lazily from float64 libm cos/sin per element.
+
+    ``th`` gives the per-pair angles (default: the 1-D ladder)."""
+
+    def __init__(self, head_dim: int, base: float, max_position: int, th=None):
         self.head_dim = head_dim
         self.base = base
         self.max_position = max_position
-        self.theta = theta(head_dim, base)
+        self.theta = theta(head_dim, base) if th is None else np.asarray(th, dtype=np.float64)
         self._rows: dict[int, tuple[np.ndarray, np.ndarray]] = {}
 
     def row(self, p: int):
@@ -92,6 +124,40 @@ def unrotate_pinned_f32(x: np.ndarray, c: np.ndarray, s: np.ndarray) -> np.ndarr
     y = np.empty_like(x)
     y[..., 0::2] = (a * c) + (b * s)
     y[..., 1::2] = (b * c) - (a * s)
+    return y
+
+
+def rows_3d(table: Table, axis: np.ndarray, positions3: np.ndarray):
+    """(c, s) [n, d/2] float32: pair i of token t takes the table row of its
+    section's coordinate positions3[t, axis[i]]."""
+    p3 = np.asarray(positions3, dtype=np.int64).reshape(-1, 3)
+    n, h = p3.shape[0], len(axis)
+    c = np.empty((n, h), np.float32)
+    s = np.empty((n, h), np.float32)
+    for t in range(n):
+        for a in range(3):
+            sel = axis == a
+            if sel.any():
+                cr, sr = table.row(int(p3[t, a]))
+                c[t, sel] = cr[sel]
+                s[t, sel] = sr[sel]
+    return c, s
+
+
+def rotate_f64_3d(x: np.ndarray, positions3: np.ndarray, th: np.ndarray, axis: np.ndarray) -> np.ndarray:
+    """Exact-arithmetic 3-D rotation in float64: token t's pair i turns by
+    positions3[t, axis[i]] * th[i] (token axis first in ``x``)."""
+    x = np.asarray(x, dtype=np.float64)
+    p3 = np.asarray(positions3, dtype=np.float64).reshape(-1, 3)
+    ang = p3[:, axis] * th                                   # [n, d/2]
+    ang = ang.reshape((ang.shape[0],) + (1,) * (x.ndim - 2) + (ang.shape[1],))
+    c = np.cos(ang)
+    s = np.sin(ang)
+    x0 = x[..., 0::2]
+    x1 = x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2] = x0 * c - x1 * s
+    y[..., 1::2] = x0 * s + x1 * c
     return y
 
 
