@@ -76,6 +76,17 @@ typedef struct {
                              other capacity - P slots.  0 = the plain ring.  (The pages give
                              5,788 = 7 x 757 + 489 slots and do not say whether a part is
                              never evicted; P = 489 reads the remainder as such a part.) */
+  int32_t rope_pairs_t;   /* 0 = 1-D RoPE (one position per token).  Else the 3-D variant: of
+                             the head_dim/2 rotation pairs, [0, T) turn with the frame index t,
+                             [T, T + Y) with the row y and the rest with the column x, each
+                             section a RoPE of its own (local pair j of a section of 2m dims
+                             turns by coordinate * base^(-2j/(2m))).  T >= 8; T, Y and the
+                             column pairs are multiples of 8.  Positions are then int32
+                             [n][3] = (t, y, x), required by every call that takes them;
+                             slot positions hold t, and a reset turns only the temporal
+                             pairs.  (The pages give one position per token; a video model's
+                             tokens have three coordinates.) */
+  int32_t rope_pairs_y;   /* Y, the row pairs of the 3-D variant (0 with 1-D RoPE) */
   double rope_base;       /* RoPE base, e.g. 10000 */
 } kvring_config;
 
@@ -116,7 +127,7 @@ kvring_status kvring_destroy(kvring_t* ring);
 
 /* Once per session ("Do It Once, at Write Time": per-head scales calibrated
  * once per session).  k, v: bf16 [n][H][d]; pos: int32 [n] device positions
- * of the keys, or NULL for next_pos + i.  For each head h:
+ * of the keys, or NULL for next_pos + i (3-D RoPE: int32 [n][3], required).  For each head h:
  *   scale_k[h] = max |rope(k)[., h, .]| / 448, scale_v[h] = max |v[., h, .]| / 448
  * (IEEE single division; a result below 2^-126, e.g. an all-zero head,
  * becomes 1), and the reciprocals used for quantisation.  Writes nothing
@@ -135,7 +146,8 @@ kvring_status kvring_calibrate_scales(kvring_t* ring, const void* k_bf16, const 
  * then head advances by n slots, n_valid = min(capacity, n_valid + n),
  * total += n, next_pos += n.  RoPE is computed in fp32 from the fp32
  * cos/sin table with every product and sum rounded separately.
- * pos: int32 [n] device positions, or NULL for next_pos + t.
+ * pos: int32 [n] device positions, or NULL for next_pos + t (3-D RoPE:
+ * int32 [n][3] = (t, y, x), required; slot_pos[slot] = t).
  * Errors: NOT_CALIBRATED, CAPACITY (n > capacity, n > capacity - P when
  * P > 0, or n > max_tokens), INVALID_ARG. */
 kvring_status kvring_write_frame(kvring_t* ring, const void* k_bf16, const void* v_bf16,
@@ -174,7 +186,7 @@ kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
  * reads the ring as usual.  Do not mix with kvring_write_frame on one ring.
  * Errors: INVALID_ARG (NULL, unaligned or aliased buffers), CAPACITY
  * (n > capacity or n > max_tokens), UNSUPPORTED (a ring with a pinned
- * prefix: the original upkeep had none). */
+ * prefix or 3-D RoPE: the original upkeep had neither). */
 kvring_status kvring_legacy_upkeep(kvring_t* ring, const void* wk_in, const void* wv_in, void* wk_out,
                                    void* wv_out, const void* k_bf16, const void* v_bf16, int32_t n,
                                    void* stream);
@@ -217,7 +229,8 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t num_rings
  * attn_precision fixes it); the probabilities multiply V in half precision
  * (V widened exactly from its E4M3 codes); products accumulate in fp32 on
  * the tensor cores.
- * q: bf16 [n_q][H][d]; qpos: int32 [n_q] device positions, or NULL for
+ * q: bf16 [n_q][H][d]; qpos: int32 [n_q] device positions (3-D RoPE:
+ * int32 [n_q][3], required), or NULL for
  * next_pos - n_q + t (the positions of the last n_q tokens written with
  * default positions).  out: [n_q][H][d], fp32 (KVRING_OUT_F32) or bf16
  * (KVRING_OUT_BF16).  An empty ring gives zeros.

@@ -50,6 +50,8 @@ class KvringConfig(ctypes.Structure):
         ("max_kv_splits", ctypes.c_int32),
         ("attn_precision", ctypes.c_int32),
         ("pinned_prefix", ctypes.c_int32),
+        ("rope_pairs_t", ctypes.c_int32),
+        ("rope_pairs_y", ctypes.c_int32),
         ("rope_base", ctypes.c_double),
     ]
 
@@ -139,12 +141,16 @@ def _tokens(x: torch.Tensor, heads: int, dim: int, name: str) -> int:
     return x.shape[0]
 
 
-def _positions(pos, n: int, name: str):
+def _positions(pos, n: int, name: str, three_d: bool = False):
+    """Check a position tensor: int32 [n] (1-D RoPE) or [n, 3] = (t, y, x)."""
     if pos is None:
+        if three_d:
+            raise ValueError(f"{name}: 3-D RoPE needs explicit (t, y, x) positions")
         return None
+    shape = (n, 3) if three_d else (n,)
     if not isinstance(pos, torch.Tensor) or not pos.is_cuda or pos.dtype != torch.int32 \
-            or pos.dim() != 1 or pos.shape[0] != n or not pos.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor of {n} positions")
+            or tuple(pos.shape) != shape or not pos.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor of shape {shape}")
     return pos
 
 
@@ -152,10 +158,11 @@ def _positions(pos, n: int, name: str):
 # C-named functions (marshalling only)
 # ---------------------------------------------------------------------------
 def make_config(heads, head_dim, capacity, max_tokens, max_position, rope_base=10000.0,
-                max_kv_splits=16, attn_precision=0, pinned_prefix=0) -> KvringConfig:
+                max_kv_splits=16, attn_precision=0, pinned_prefix=0, rope3d=None) -> KvringConfig:
+    pt, py = (0, 0) if rope3d is None else (int(rope3d[0]), int(rope3d[1]))
     return KvringConfig(int(heads), int(head_dim), int(capacity), int(max_tokens),
                         int(max_position), int(max_kv_splits), int(attn_precision),
-                        int(pinned_prefix), float(rope_base))
+                        int(pinned_prefix), pt, py, float(rope_base))
 
 
 def kvring_required_bytes(cfg: KvringConfig) -> int:
@@ -218,7 +225,9 @@ def write_frames_many(rings, ks, vs, poss=None, stream=None) -> None:
         if _tokens(ks[i], r.H, r.d, "k") != n or _tokens(vs[i], r.H, r.d, "v") != n:
             raise ValueError("every k and v must hold the same number of tokens")
         if poss is not None:
-            _positions(poss[i], n, "pos")
+            _positions(poss[i], n, "pos", r.three_d)
+        elif r.three_d:
+            raise ValueError("3-D RoPE needs explicit (t, y, x) positions")
     kvring_write_frames_many([r.handle for r in rings], ks, vs, poss, n, r0._s(stream))
 
 
@@ -290,15 +299,17 @@ class KvRing:
 
     def __init__(self, heads: int, head_dim: int, capacity: int, max_tokens: int,
                  max_position: int, rope_base: float = 10000.0, max_kv_splits: int = 16,
-                 attn_precision: int = 0, device=None, stream=None, pinned_prefix: int = 0):
+                 attn_precision: int = 0, device=None, stream=None, pinned_prefix: int = 0,
+                 rope3d=None):
         if not torch.cuda.is_available():
             raise RuntimeError("KvRing needs a CUDA device")
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.H, self.d, self.C = int(heads), int(head_dim), int(capacity)
         self.max_tokens = int(max_tokens)
         self.P = int(pinned_prefix)
+        self.three_d = rope3d is not None
         self.cfg = make_config(heads, head_dim, capacity, max_tokens, max_position, rope_base,
-                               max_kv_splits, attn_precision, pinned_prefix)
+                               max_kv_splits, attn_precision, pinned_prefix, rope3d)
         n = kvring_required_bytes(self.cfg)
         if n == 0:
             raise ValueError("invalid kvring config")
@@ -314,13 +325,13 @@ class KvRing:
         n = _tokens(k, self.H, self.d, "k")
         if _tokens(v, self.H, self.d, "v") != n:
             raise ValueError("k and v must hold the same number of tokens")
-        kvring_calibrate_scales(self.handle, k, v, _positions(pos, n, "pos"), n, self._s(stream))
+        kvring_calibrate_scales(self.handle, k, v, _positions(pos, n, "pos", self.three_d), n, self._s(stream))
 
     def write(self, k, v, pos=None, stream=None) -> None:
         n = _tokens(k, self.H, self.d, "k")
         if _tokens(v, self.H, self.d, "v") != n:
             raise ValueError("k and v must hold the same number of tokens")
-        kvring_write_frame(self.handle, k, v, _positions(pos, n, "pos"), n, self._s(stream))
+        kvring_write_frame(self.handle, k, v, _positions(pos, n, "pos", self.three_d), n, self._s(stream))
 
     def delta_rotate(self, delta: int = TO_OLDEST, stream=None) -> None:
         kvring_delta_rotate(self.handle, delta, self._s(stream))
@@ -332,7 +343,7 @@ class KvRing:
         if out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (n, self.H, self.d) \
                 or not out.is_contiguous() or not out.is_cuda:
             raise ValueError("out must be a contiguous CUDA float32/bfloat16 tensor [n_q, H, d]")
-        kvring_attention(self.handle, q, _positions(qpos, n, "qpos"), n, out,
+        kvring_attention(self.handle, q, _positions(qpos, n, "qpos", self.three_d), n, out,
                          OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32, self._s(stream))
         return out
 

@@ -146,10 +146,38 @@ struct AttnParams {
   int cluster_merge;   // the splits of a query tile form one cluster (2..8 CTAs)
 };
 
+// 3-D RoPE: the (t, y, x) positions of a query tile's rows into qpos_s
+// [128][3], a CTA barrier, then each row's table words into `dst` with
+// cp.async, every 16-byte table chunk (2 pairs, one section: sections are
+// whole chunks of 8 pairs) from the row of its section's coordinate.  Only
+// the 3-D instantiation of the kernel contains it.
+template <int D>
+__device__ __forceinline__ void stage_rows_3d(const RingDev& r, const int32_t* qpos, int n_q, int qt, int rows_in,
+                                           int* qpos_s, uint32_t dst) {
+  constexpr int TPR = D / 4;
+  if (threadIdx.x < 3 * kTile) {
+    int p = 0;
+    if (qt * kTile + (int)threadIdx.x / 3 < n_q) {
+      p = __ldg(qpos + 3 * qt * kTile + threadIdx.x);
+      if (p < 0 || p >= r.max_pos) {
+        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+        p = 0;
+      }
+    }
+    qpos_s[threadIdx.x] = p;
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < rows_in * TPR; k += blockDim.x) {
+    const int rr = k / TPR, c = k % TPR;
+    const int p = qpos_s[3 * rr + rope_axis(r, 2 * c)];
+    cp_async16(dst + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)p * D + 4 * c);
+  }
+}
+
 // Named barriers: 0 = __syncthreads, 1 = the 256 softmax threads.
 __device__ __forceinline__ void sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <int D>
+template <int D, bool R3>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const AttnParams prm) {
@@ -276,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int CPR = D / 8;                           // 16-byte q chunks per row
       constexpr int TPR = D / 4;                           // 16-byte table chunks per row
       constexpr int PQ = (kTile * CPR + kThreads - 1) / kThreads;   // chunk tasks per thread
-      int* qpos_s = reinterpret_cast<int*>(epi + 2 * kTile);   // [128]
-      if (threadIdx.x < kTile) {
+      int* qpos_s = reinterpret_cast<int*>(epi + 2 * kTile);   // [128] (1-D) or [128][3] (3-D)
+      if (!R3 && threadIdx.x < kTile) {
         const int tq = qt * kTile + threadIdx.x;
         int p = 0;
         if (tq < prm.n_q) {
@@ -289,10 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         qpos_s[threadIdx.x] = p;
       }
+      if constexpr (R3) stage_rows_3d<D>(r, prm.qpos, prm.n_q, qt, rows_in, qpos_s, sbase + L::kVh);
       __syncthreads();
-      for (int k = threadIdx.x; k < rows_in * TPR; k += kThreads) {
-        const int rr = k / TPR, c = k % TPR;
-        cp_async16(sbase + L::kVh + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)qpos_s[rr] * D + 4 * c);
+      if constexpr (!R3) {
+        for (int k = threadIdx.x; k < rows_in * TPR; k += kThreads) {
+          const int rr = k / TPR, c = k % TPR;
+          cp_async16(sbase + L::kVh + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)qpos_s[rr] * D + 4 * c);
+        }
       }
       cp_async_commit();
       cp_async_wait_all();
@@ -943,8 +974,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t attention_prepare(int D) {
   const int smem = (int)attention_smem_bytes(D);
-  return D == 128 ? cudaFuncSetAttribute(k_attention<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                  : cudaFuncSetAttribute(k_attention<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e;
+  if (D == 128) {
+    e = cudaFuncSetAttribute(k_attention<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_attention<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  } else {
+    e = cudaFuncSetAttribute(k_attention<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_attention<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  }
+  return e;
 }
 
 size_t attention_smem_bytes(int D) {
@@ -985,8 +1025,12 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
     attr[1].val.clusterDim.z = (unsigned)a.nsplit;
     cfg.numAttrs = 2;
   }
-  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_attention<128>, *tmK, *tmV, p);
-  return cudaLaunchKernelEx(&cfg, k_attention<64>, *tmK, *tmV, p);
+  // 3-D RoPE has its own instantiation (query positions from three rows)
+  if (r.D == 128)
+    return r.pt ? cudaLaunchKernelEx(&cfg, k_attention<128, true>, *tmK, *tmV, p)
+                : cudaLaunchKernelEx(&cfg, k_attention<128, false>, *tmK, *tmV, p);
+  return r.pt ? cudaLaunchKernelEx(&cfg, k_attention<64, true>, *tmK, *tmV, p)
+              : cudaLaunchKernelEx(&cfg, k_attention<64, false>, *tmK, *tmV, p);
 }
 
 // ---------------------------------------------------------------------------

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads) k_calibrate(RingDev r, const uint16_
     unpack_bf16x16(__ldcs(src), __ldcs(src + 1), x);
     bool ok = true;
     if (!isv) {
-      const int p = pos ? __ldg(pos + t) : s_next + t;
+      const int p = pos ? rope_pos(r, pos, t, 8 * chunk) : s_next + t;   // 3-D: the chunk's coordinate
       if (p < 0 || p >= r.max_pos) {
         ok = false;
         atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
@@ -224,7 +224,7 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
     if (gid < per) {  // keys only
       const int chunk = (int)(gid % CH);
       const int t = (int)(gid / CH / H);
-      const int p = pos ? __ldg(pos + t) : s_next + t;
+      const int p = pos ? rope_pos(r, pos, t, 8 * chunk) : s_next + t;   // chunk 0: t (3-D)
       pp[u] = p;
       if (p >= 0 && p < r.max_pos) load_table16(r.table, D, p, chunk, cs[u]);
     }
@@ -453,7 +453,15 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
           bytes += (uint32_t)ntok * D * 4;
         } else {
           for (int t = 0; t < ntok; ++t) {
-            const int p = pos ? __ldg(pos + t0 + t) : p0 + t;
+            int p;
+            if (r.pt) {   // 3-D: a token is valid when all three coordinates are
+              const int32_t* q3 = pos + 3 * (t0 + t);
+              const int a0 = __ldg(q3), a1 = __ldg(q3 + 1), a2 = __ldg(q3 + 2);
+              const bool ok3 = a0 >= 0 && a0 < r.max_pos && a1 >= 0 && a1 < r.max_pos && a2 >= 0 && a2 < r.max_pos;
+              p = ok3 ? a0 : -1;
+            } else {
+              p = pos ? __ldg(pos + t0 + t) : p0 + t;
+            }
             hdr[t] = p;
             if (p >= 0 && p < r.max_pos) bytes += D * 4;
           }
@@ -468,7 +476,17 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
       } else if (!isv) {
         for (int t = 0; t < ntok; ++t) {
           const int p = hdr[t];
-          if (p >= 0 && p < r.max_pos) bulk_load(sa + g.tab_off + t * D * 4, r.table + (size_t)p * D, D * 4, fb);
+          if (!(p >= 0 && p < r.max_pos)) continue;
+          const uint32_t dst = sa + g.tab_off + t * D * 4;
+          if (r.pt) {   // 3-D: each section's cos/sin from its own coordinate's row
+            const int32_t* q3 = pos + 3 * (t0 + t);
+            const int lo[3] = {0, r.pt, r.pt + r.py}, m[3] = {r.pt, r.py, D / 2 - r.pt - r.py};
+            for (int a = 0; a < 3; ++a)
+              if (m[a] > 0)
+                bulk_load(dst + 8 * lo[a], r.table + (size_t)__ldg(q3 + a) * D + 2 * lo[a], (uint32_t)(8 * m[a]), fb);
+          } else {
+            bulk_load(dst, r.table + (size_t)p * D, D * 4, fb);
+          }
         }
       }
       if (++s == S) {
@@ -685,6 +703,9 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
 
   // ------------------------------------------------------------ consumers
   const int k = threadIdx.x % CH, row0 = threadIdx.x / CH;
+  // with 3-D RoPE only the temporal pairs turn: this thread's 8 pairs are
+  // temporal or not for every row (sections are whole chunks of 8 pairs)
+  const bool turns = b.r[0].pt == 0 || 8 * k < b.r[0].pt;
   float c[8], sn[8];  // cos / sin of this thread's 8 pairs at the ring's delta
   int cur_d = 0, done = 0, d = -1;
   for (long long u = u_begin; u < u_end; ++u) {
@@ -703,7 +724,7 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     const RingDev& r = b.r[ring];
     const int r0 = P + run * RU;
-    if (rows > 0) {
+    if (rows > 0 && turns) {
       if (d != cur_d) {
         cur_d = d;
         const float4* t = reinterpret_cast<const float4*>(r.table + (size_t)d * D + 16 * k);
@@ -733,8 +754,8 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
         }
         *reinterpret_cast<uint4*>(r.k + ((size_t)h * C + r0 + row) * D + 16 * k) = pack_e4m3x16(y);
       }
-      if (h == 0 && (int)threadIdx.x < rows) r.slot_pos[r0 + threadIdx.x] -= d;
     }
+    if (rows > 0 && h == 0 && (int)threadIdx.x < rows) r.slot_pos[r0 + threadIdx.x] -= d;
     ++done;
     if (++s == kDpStages) {
       s = 0;

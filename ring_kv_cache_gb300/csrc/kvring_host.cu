@@ -39,6 +39,10 @@ bool config_ok(const kvring_config* c) {
   if (c->max_kv_splits < 1 || c->max_kv_splits > 32) return false;
   if (c->attn_precision < 0 || c->attn_precision > 3) return false;
   if (c->pinned_prefix < 0 || c->pinned_prefix >= c->capacity) return false;
+  if (c->rope_pairs_t != 0 || c->rope_pairs_y != 0) {   // 3-D RoPE sections, in whole chunks of 8 pairs
+    const int half = c->head_dim / 2, t = c->rope_pairs_t, y = c->rope_pairs_y;
+    if (t < 8 || y < 0 || t % 8 != 0 || y % 8 != 0 || t + y > half || (half - t - y) % 8 != 0) return false;
+  }
   if (!(c->rope_base > 0.0) || !std::isfinite(c->rope_base)) return false;
   return true;
 }
@@ -196,6 +200,8 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   d.max_splits = cfg->max_kv_splits;
   d.qtiles_max = p.qtiles;
   d.P = cfg->pinned_prefix;
+  d.pt = cfg->rope_pairs_t;
+  d.py = cfg->rope_pairs_y;
 
   if (kvr::attention_prepare(d.D) != cudaSuccess || kvr::cache_prepare() != cudaSuccess) {
     delete r;
@@ -208,13 +214,20 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
 
   // Host-built contents: empty positions, unit scales, the RoPE table
   // (theta_i = base^(-2i/d) and cos/sin of p*theta_i in double libm,
-  // rounded to fp32).
+  // rounded to fp32; with 3-D RoPE each section has its own ladder:
+  // local pair j of a section of m pairs gets base^(-2j/(2m))).
   const int H = d.H, D = d.D, C = d.C;
   std::vector<int32_t> slot_pos(C, kvr::kEmptyPos);
   std::vector<float> scales(4 * H, 1.0f);
   std::vector<float> table((size_t)cfg->max_position * D);
   std::vector<double> theta(D / 2);
-  for (int i = 0; i < D / 2; ++i) theta[i] = std::pow(cfg->rope_base, (-2.0 * i) / (double)D);
+  if (d.pt == 0) {
+    for (int i = 0; i < D / 2; ++i) theta[i] = std::pow(cfg->rope_base, (-2.0 * i) / (double)D);
+  } else {
+    const int lo[3] = {0, d.pt, d.pt + d.py}, m[3] = {d.pt, d.py, D / 2 - d.pt - d.py};
+    for (int a = 0; a < 3; ++a)
+      for (int j = 0; j < m[a]; ++j) theta[lo[a] + j] = std::pow(cfg->rope_base, (-2.0 * j) / (double)(2 * m[a]));
+  }
   for (int pos = 0; pos < cfg->max_position; ++pos) {
     float* row = table.data() + (size_t)pos * D;
     for (int i = 0; i < D / 2; ++i) {
@@ -250,6 +263,7 @@ kvring_status kvring_calibrate_scales(kvring_t* r, const void* k, const void* v,
                                       int32_t n, void* stream) {
   if (!r || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (pos && !aligned(pos, 4)) || n < 1)
     return KVRING_ERR_INVALID_ARG;
+  if (r->dev.pt && !pos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
   if (n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   const kvring_status st = cuda_status(kvr::launch_calibrate(r->dev, k, v, pos, n, (cudaStream_t)stream));
   if (st == KVRING_OK) r->calibrated = true;
@@ -260,6 +274,7 @@ kvring_status kvring_write_frame(kvring_t* r, const void* k, const void* v, cons
                                  void* stream) {
   if (!r || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (pos && !aligned(pos, 4)) || n < 1)
     return KVRING_ERR_INVALID_ARG;
+  if (r->dev.pt && !pos) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   return cuda_status(kvr::launch_write(r->dev, k, v, pos, n, (cudaStream_t)stream));
@@ -281,7 +296,8 @@ kvring_status check_batch(kvring_t* const* rings, int32_t count) {
     if (!r) return KVRING_ERR_INVALID_ARG;
     const kvring* r0 = rings[0];
     if (r->cfg.num_heads != r0->cfg.num_heads || r->cfg.head_dim != r0->cfg.head_dim ||
-        r->cfg.capacity != r0->cfg.capacity || r->cfg.pinned_prefix != r0->cfg.pinned_prefix)
+        r->cfg.capacity != r0->cfg.capacity || r->cfg.pinned_prefix != r0->cfg.pinned_prefix ||
+        r->cfg.rope_pairs_t != r0->cfg.rope_pairs_t || r->cfg.rope_pairs_y != r0->cfg.rope_pairs_y)
       return KVRING_ERR_INVALID_ARG;
     for (int j = 0; j < i; ++j)
       if (rings[j] == r) return KVRING_ERR_INVALID_ARG;
@@ -302,6 +318,7 @@ kvring_status kvring_write_frames_many(kvring_t* const* rings, int32_t count, co
     const int32_t* p = pos ? pos[i] : nullptr;
     if (!k[i] || !v[i] || !aligned(k[i], 16) || !aligned(v[i], 16) || (p && !aligned(p, 4)))
       return KVRING_ERR_INVALID_ARG;
+    if (r->dev.pt && !p) return KVRING_ERR_INVALID_ARG;
     if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
     if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
     b.r[i] = r->dev;
@@ -332,7 +349,8 @@ kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* w
   for (const void* p : ptrs)
     if (!aligned(p, 16)) return KVRING_ERR_INVALID_ARG;
   if (wk_in == wk_out || wv_in == wv_out || wk_out == wv_out) return KVRING_ERR_INVALID_ARG;
-  if (r->cfg.pinned_prefix != 0) return KVRING_ERR_UNSUPPORTED;   // the original upkeep had no prefix
+  // the original upkeep had neither a prefix nor 3-D RoPE
+  if (r->cfg.pinned_prefix != 0 || r->dev.pt != 0) return KVRING_ERR_UNSUPPORTED;
   if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   const kvring_status st = cuda_status(
       kvr::launch_legacy_upkeep(r->dev, wk_in, wv_in, wk_out, wv_out, k, v, n, (cudaStream_t)stream));
@@ -344,6 +362,7 @@ kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, 
                                int32_t out_dtype, void* stream) {
   if (!r || !q || !out || !aligned(q, 16) || !aligned(out, 16) || (qpos && !aligned(qpos, 4)) || n_q < 1)
     return KVRING_ERR_INVALID_ARG;
+  if (r->dev.pt && !qpos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
   if (out_dtype != KVRING_OUT_F32 && out_dtype != KVRING_OUT_BF16) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n_q > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
@@ -362,6 +381,7 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
                                        void* out, int32_t out_dtype, void* stream) {
   if (!r || !q || !out || !aligned(q, 16) || !aligned(out, 16) || (qpos && !aligned(qpos, 4)) || n_q < 1)
     return KVRING_ERR_INVALID_ARG;
+  if (r->dev.pt && !qpos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
   if (out_dtype != KVRING_OUT_F32 && out_dtype != KVRING_OUT_BF16) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n_q > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;

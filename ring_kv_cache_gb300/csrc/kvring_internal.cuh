@@ -49,7 +49,18 @@ struct RingDev {
   int32_t* levels;     // [qtiles][H] precision level of each query tile
   int H, D, C, max_pos, max_tokens, max_splits, qtiles_max;
   int P;               // pinned prefix slots; tokens past it cycle over slots [P, C)
+  int pt, py;          // 3-D RoPE: temporal and row pairs (pt = 0: 1-D RoPE)
 };
+
+// Coordinate (0 = t, 1 = y, 2 = x) a rotation pair takes its position from;
+// 0 with 1-D RoPE, whose positions are one int32 per token.
+__host__ __device__ inline int rope_axis(const RingDev& r, int pair) {
+  return pair < r.pt || r.pt == 0 ? 0 : (pair < r.pt + r.py ? 1 : 2);
+}
+// Position of token t for pair `pair`: pos is [n] (1-D) or [n][3] (3-D).
+__device__ __forceinline__ int rope_pos(const RingDev& r, const int32_t* pos, int t, int pair) {
+  return r.pt == 0 ? __ldg(pos + t) : __ldg(pos + 3 * t + rope_axis(r, pair));
+}
 
 // ---------------------------------------------------------------- E4M3 ----
 // Two fp32 values to two E4M3 codes (round to nearest even, saturating to

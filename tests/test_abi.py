@@ -48,6 +48,7 @@ def test_required_bytes_matches_layout(L):
     ("num_heads", 0), ("head_dim", 96), ("capacity", 0), ("max_tokens", 0),
     ("max_position", 0), ("max_kv_splits", 0), ("attn_precision", 4),
     ("pinned_prefix", -1), ("pinned_prefix", 48),
+    ("rope_pairs_t", 4), ("rope_pairs_t", 40), ("rope_pairs_y", 8), ("rope_pairs_t", 12),
     ("rope_base", 0.0), ("rope_base", float("inf")),
 ])
 def test_bad_configs_are_rejected(L, field, value):
@@ -55,6 +56,13 @@ def test_bad_configs_are_rejected(L, field, value):
     assert kv.kvring_required_bytes(cfg) > 0
     setattr(cfg, field, value)
     assert kv.kvring_required_bytes(cfg) == 0
+
+
+def test_3d_rope_sections_are_accepted_in_whole_chunks(L):
+    for sec in [(8, 8), (16, 0), (8, 16), (32, 0)]:
+        assert kv.kvring_required_bytes(kv.make_config(2, 64, 48, 12, 256, rope3d=sec)) > 0
+    assert kv.kvring_required_bytes(kv.make_config(2, 128, 48, 12, 256, rope3d=(16, 24))) > 0
+    assert kv.kvring_required_bytes(kv.make_config(2, 64, 48, 12, 256, rope3d=(8, 12))) == 0
 
 
 def test_status_strings(L):
