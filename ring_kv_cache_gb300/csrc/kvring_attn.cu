@@ -398,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // place in the query images
         float sq = rm[i] / 448.0f;
         if (!(sq >= 0x1p-126f)) sq = 1.0f;
-        const float invq = 1.0f / sq;
+        // only invq * sq matters (the logit factor uses sq): a fast
+        // reciprocal (a couple of ulp) leaves it 1 within 2^-21
+        const float invq = __fdividef(1.0f, sq);
         float* v = u[i];
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] *= invq;
@@ -923,21 +925,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4 acc[MT];
 #pragma unroll
       for (int i = 0; i < MT; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s2 = 0; landed && s2 < ns; ++s2) {
-        // split s2's rows of this range: own staging, or the sender's slot
-        const uint8_t* src = s2 == split ? sm + L::kK + (size_t)r0 * SPB
-                                         : sm + L::kVh + (size_t)((s2 < split ? s2 : s2 - 1) * maxr) * SPB;
+      // split s2's rows of this range: own staging, or the sender's slot;
+      // two splits at a time with all their loads issued before any use
+      auto rows_of = [&](int s2) -> const uint8_t* {
+        return s2 == split ? sm + L::kK + (size_t)r0 * SPB
+                           : sm + L::kVh + (size_t)((s2 < split ? s2 : s2 - 1) * maxr) * SPB;
+      };
+      for (int s0 = 0; landed && s0 < ns; s0 += 2) {
+        float4 v[2][MT];
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-          const int idx = threadIdx.x + i * kSoftmaxThreads;
-          if (idx >= ntask) continue;
-          const int lr = idx / (D / 4), c4 = idx % (D / 4);
-          const float4 v = *reinterpret_cast<const float4*>(src + (size_t)lr * SPB + 16 * c4);
-          const float w = wts[s2 * kTile + lr];
-          acc[i].x = fmaf(w, v.x, acc[i].x);
-          acc[i].y = fmaf(w, v.y, acc[i].y);
-          acc[i].z = fmaf(w, v.z, acc[i].z);
-          acc[i].w = fmaf(w, v.w, acc[i].w);
+        for (int q = 0; q < 2; ++q) {
+          const uint8_t* src = rows_of(s0 + q < ns ? s0 + q : s0);
+#pragma unroll
+          for (int i = 0; i < MT; ++i) {
+            const int idx = threadIdx.x + i * kSoftmaxThreads;
+            const int lr = idx / (D / 4), c4 = idx % (D / 4);
+            v[q][i] = idx < ntask ? *reinterpret_cast<const float4*>(src + (size_t)lr * SPB + 16 * c4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (s0 + q >= ns) break;
+#pragma unroll
+          for (int i = 0; i < MT; ++i) {
+            const int idx = threadIdx.x + i * kSoftmaxThreads;
+            const float w = idx < ntask ? wts[(s0 + q) * kTile + idx / (D / 4)] : 0.f;
+            acc[i].x = fmaf(w, v[q][i].x, acc[i].x);
+            acc[i].y = fmaf(w, v[q][i].y, acc[i].y);
+            acc[i].z = fmaf(w, v[q][i].z, acc[i].z);
+            acc[i].w = fmaf(w, v[q][i].w, acc[i].w);
+          }
         }
       }
 #pragma unroll
