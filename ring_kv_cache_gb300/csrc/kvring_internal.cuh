@@ -172,6 +172,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// A relaxed load at device scope: a read of a word that a preceding kernel
+// may still be writing, used only as a guess that is checked later.
+__device__ __forceinline__ int ld_relaxed_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Non-blocking probe of the phase with the given parity.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
