@@ -81,6 +81,41 @@ def test_single_filled_slot_returns_its_value():
     assert np.allclose(out, want, atol=1e-5 * np.abs(want).max())
 
 
+def test_default_positions_up_to_the_table_end_and_before_enough_tokens():
+    """Default query positions are the last n_q positions written.  When all
+    of them lie in the RoPE table (here up to its last row, in both query
+    tiles) the output matches the reference and no error is recorded.  When
+    fewer than n_q tokens were ever written, the first rows' positions are
+    negative: the device error word records it, and the rows whose positions
+    are valid still match."""
+    rng = np.random.default_rng(7)
+    shape = RingShape(heads=2, head_dim=128, capacity=300, tokens=150, queries=150, max_position=450)
+    ring, orc = make_pair(shape, Ring)
+    for i in range(3):                        # positions 0..449: the table's last row is used
+        q, k, v = frame(rng, shape, 150)
+        if i == 0:
+            ring.calibrate(dev(k), dev(v))
+            orc.calibrate(f(k), f(v))
+        ring.write(dev(k), dev(v))
+        orc.write(f(k), f(v))
+    out = ring.attention(dev(q)).cpu().numpy()
+    mx, mn = attn_errors(out, attention_exact(orc, f(q)))
+    assert mx <= MAX_ABS and mn <= MEAN_ABS, (mx, mn)
+    assert ring.export()["state"][kv.STATE["error"]].item() == 0
+
+    ring, orc = make_pair(shape, Ring)
+    q, k, v = frame(rng, shape, 150)
+    ring.calibrate(dev(k), dev(v))
+    orc.calibrate(f(k), f(v))
+    ring.write(dev(k[:100]), dev(v[:100]))
+    orc.write(f(k[:100]), f(v[:100]))
+    out = ring.attention(dev(q)).cpu().numpy()      # default positions -50 .. 99
+    assert ring.export()["state"][kv.STATE["error"]].item() & kv.DEVERR_POSITION
+    rows = np.arange(50, 150)
+    mx, mn = attn_errors(out[rows], attention_exact(orc, f(q[rows]), rows - 50))
+    assert mx <= MAX_ABS and mn <= MEAN_ABS, (mx, mn)
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 5, 8, 16])
 def test_split_merge_consistent(splits):
     """2..8 splits merge inside a thread-block cluster, more through global
