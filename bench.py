@@ -327,6 +327,42 @@ def gpu_arm(args, rank, world):
         barrier()
     e2e_ms = e0.elapsed_time(e1)
 
+    # The same step's copies alone (no kernels), each direction on its own
+    # stream and buffers as above, K steps as one graph replay: what the
+    # host link alone allows per step.
+    def copies_alone(s_cp, body):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s_cp):
+            for i in range(args.steps):
+                body(i)
+        gr.replay()
+        torch.cuda.synchronize(dev)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(s_cp)
+        gr.replay()
+        c1.record(s_cp)
+        torch.cuda.synchronize(dev)
+        return c0.elapsed_time(c1) * 1e3 / args.steps
+
+    def h2d(i):
+        for j in range(3):
+            din[i % NB][j].copy_(hin[i % NB][j], non_blocking=True)
+
+    def d2h(i):
+        hout[i % NB].copy_(outs[i % RINGS], non_blocking=True)
+
+    def both(i):          # both directions at once: H2D here, D2H forked to its stream
+        if i == 0:
+            s_out.wait_stream(s_in)
+            with torch.cuda.stream(s_out):
+                for j in range(args.steps):
+                    d2h(j)
+        h2d(i)
+        if i == args.steps - 1:
+            s_in.wait_stream(s_out)
+
+    copy_us = {"h2d": copies_alone(s_in, h2d), "d2h": copies_alone(s_out, d2h), "both": copies_alone(s_in, both)}
+
     # precision levels used on the timed workload (for the issued-FLOP count)
     levels = []
     for r in rings:
@@ -336,7 +372,8 @@ def gpu_arm(args, rank, world):
     errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
     batched = batched_upkeep(args, dev, stream) if not args.no_batched else None
     legacy_us = legacy_upkeep_us(dev, stream) if not args.no_batched else None
-    return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, e2e_ms=e2e_ms, clocks=clk.summary(),
+    return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, e2e_ms=e2e_ms, copy_us=copy_us,
+                clocks=clk.summary(),
                 batched=batched, legacy_us=legacy_us,
                 resets=timed_resets,
                 levels=levels, device_errors=int(np.bitwise_or.reduce(errs)))
@@ -630,7 +667,9 @@ def main():
             }),
         },
         "e2e": {"value": e2e_ms * 1e3 / units, "unit": "µs",
-                "h2d_bytes_per_step": H2D_BYTES, "d2h_bytes_per_step": D2H_BYTES},
+                "h2d_bytes_per_step": H2D_BYTES, "d2h_bytes_per_step": D2H_BYTES,
+                "copies_alone_us_per_step": res["copy_us"],
+                "note": "the step's pinned-memory copies timed alone (no kernels): each direction, and both at once"},
         "gpu_launches": 2 * K + res["resets"],   # per step: write + attention; a delta rotation per reset
         "clocks": res["clocks"],
         "device_errors": res["device_errors"],
