@@ -32,6 +32,11 @@
  *     call only enqueues work on that stream; none synchronises with the
  *     host, none allocates memory.  Calls on one ring must be ordered (one
  *     stream, or the caller's events); two rings are independent.
+ *   - A ring belongs to the device that was current at kvring_create; every
+ *     call that takes a ring returns KVRING_ERR_INVALID_ARG unless that
+ *     device is current (the kernels would otherwise run on another GPU
+ *     against this one's memory).  Its tensors and stream must be on that
+ *     device too, which the library cannot check.
  *   - Arguments are checked on the host before anything is enqueued; a
  *     failed check enqueues nothing and returns an error status.  CUDA
  *     launch failures return KVRING_ERR_CUDA.  Problems only the device can

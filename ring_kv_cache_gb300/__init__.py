@@ -129,9 +129,11 @@ def _stream_ptr(stream, device) -> int:
     return s.cuda_stream
 
 
-def _tokens(x: torch.Tensor, heads: int, dim: int, name: str) -> int:
+def _tokens(x: torch.Tensor, heads: int, dim: int, name: str, device=None) -> int:
     if not isinstance(x, torch.Tensor) or not x.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and x.device != device:
+        raise ValueError(f"{name} is on {x.device}, the ring on {device}")
     if x.dtype != torch.bfloat16:
         raise ValueError(f"{name} must be bfloat16")
     if x.dim() != 3 or x.shape[1] != heads or x.shape[2] != dim:
@@ -141,7 +143,7 @@ def _tokens(x: torch.Tensor, heads: int, dim: int, name: str) -> int:
     return x.shape[0]
 
 
-def _positions(pos, n: int, name: str, three_d: bool = False):
+def _positions(pos, n: int, name: str, three_d: bool = False, device=None):
     """Check a position tensor: int32 [n] (1-D RoPE) or [n, 3] = (t, y, x)."""
     if pos is None:
         if three_d:
@@ -151,6 +153,8 @@ def _positions(pos, n: int, name: str, three_d: bool = False):
     if not isinstance(pos, torch.Tensor) or not pos.is_cuda or pos.dtype != torch.int32 \
             or tuple(pos.shape) != shape or not pos.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA int32 tensor of shape {shape}")
+    if device is not None and pos.device != device:
+        raise ValueError(f"{name} is on {pos.device}, the ring on {device}")
     return pos
 
 
@@ -220,22 +224,28 @@ def write_frames_many(rings, ks, vs, poss=None, stream=None) -> None:
     if not rings or len(ks) != len(rings) or len(vs) != len(rings) or (poss is not None and len(poss) != len(rings)):
         raise ValueError("one k, v (and pos) per ring")
     r0 = rings[0]
-    n = _tokens(ks[0], r0.H, r0.d, "k")
+    n = _tokens(ks[0], r0.H, r0.d, "k", r0.device)
     for i, r in enumerate(rings):
-        if _tokens(ks[i], r.H, r.d, "k") != n or _tokens(vs[i], r.H, r.d, "v") != n:
+        if r.device != r0.device:
+            raise ValueError("every ring must be on one device")
+        if _tokens(ks[i], r.H, r.d, "k", r.device) != n or _tokens(vs[i], r.H, r.d, "v", r.device) != n:
             raise ValueError("every k and v must hold the same number of tokens")
         if poss is not None:
-            _positions(poss[i], n, "pos", r.three_d)
+            _positions(poss[i], n, "pos", r.three_d, r.device)
         elif r.three_d:
             raise ValueError("3-D RoPE needs explicit (t, y, x) positions")
-    kvring_write_frames_many([r.handle for r in rings], ks, vs, poss, n, r0._s(stream))
+    with torch.cuda.device(r0.device):
+        kvring_write_frames_many([r.handle for r in rings], ks, vs, poss, n, r0._s(stream))
 
 
 def delta_rotate_many(rings, delta: int = TO_OLDEST, stream=None) -> None:
     """kvring_delta_rotate on several rings of one shape in one launch."""
     if not rings:
         raise ValueError("no rings")
-    kvring_delta_rotate_many([r.handle for r in rings], delta, rings[0]._s(stream))
+    if any(r.device != rings[0].device for r in rings):
+        raise ValueError("every ring must be on one device")
+    with torch.cuda.device(rings[0].device):
+        kvring_delta_rotate_many([r.handle for r in rings], delta, rings[0]._s(stream))
 
 
 def kvring_legacy_upkeep(handle, wk_in, wv_in, wk_out, wv_out, k, v, n, stream_ptr) -> None:
@@ -256,11 +266,12 @@ class LegacyWindows:
     def upkeep(self, k, v, stream=None) -> None:
         """One call of the original upkeep on `ring` with the frame (k, v)."""
         r = self.ring
-        n = _tokens(k, r.H, r.d, "k")
-        if _tokens(v, r.H, r.d, "v") != n:
+        n = _tokens(k, r.H, r.d, "k", r.device)
+        if _tokens(v, r.H, r.d, "v", r.device) != n:
             raise ValueError("k and v must hold the same number of tokens")
         a, b = self.cur, 1 - self.cur
-        kvring_legacy_upkeep(r.handle, self.k[a], self.v[a], self.k[b], self.v[b], k, v, n, r._s(stream))
+        with torch.cuda.device(r.device):
+            kvring_legacy_upkeep(r.handle, self.k[a], self.v[a], self.k[b], self.v[b], k, v, n, r._s(stream))
         self.cur = b
 
     def window(self):
@@ -295,7 +306,10 @@ def encode_e4m3(x: torch.Tensor, stream=None) -> torch.Tensor:
 
 # ---------------------------------------------------------------------------
 class KvRing:
-    """One layer's rolling FP8 attention cache on the current CUDA device."""
+    """One layer's rolling FP8 attention cache on one CUDA device (the
+    current one unless ``device`` names another).  Every call runs with that
+    device current and takes tensors on it.  The ring's buffer is freed with
+    the object: keep it alive until the work enqueued on it has completed."""
 
     def __init__(self, heads: int, head_dim: int, capacity: int, max_tokens: int,
                  max_position: int, rope_base: float = 10000.0, max_kv_splits: int = 16,
@@ -303,7 +317,10 @@ class KvRing:
                  rope3d=None):
         if not torch.cuda.is_available():
             raise RuntimeError("KvRing needs a CUDA device")
-        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        d = torch.device(device) if device is not None else torch.device("cuda")
+        if d.type != "cuda":
+            raise ValueError("KvRing needs a CUDA device")
+        self.device = d if d.index is not None else torch.device("cuda", torch.cuda.current_device())
         self.H, self.d, self.C = int(heads), int(head_dim), int(capacity)
         self.max_tokens = int(max_tokens)
         self.P = int(pinned_prefix)
@@ -322,29 +339,36 @@ class KvRing:
         return _stream_ptr(stream, self.device)
 
     def calibrate(self, k, v, pos=None, stream=None) -> None:
-        n = _tokens(k, self.H, self.d, "k")
-        if _tokens(v, self.H, self.d, "v") != n:
+        n = _tokens(k, self.H, self.d, "k", self.device)
+        if _tokens(v, self.H, self.d, "v", self.device) != n:
             raise ValueError("k and v must hold the same number of tokens")
-        kvring_calibrate_scales(self.handle, k, v, _positions(pos, n, "pos", self.three_d), n, self._s(stream))
+        pos = _positions(pos, n, "pos", self.three_d, self.device)
+        with torch.cuda.device(self.device):
+            kvring_calibrate_scales(self.handle, k, v, pos, n, self._s(stream))
 
     def write(self, k, v, pos=None, stream=None) -> None:
-        n = _tokens(k, self.H, self.d, "k")
-        if _tokens(v, self.H, self.d, "v") != n:
+        n = _tokens(k, self.H, self.d, "k", self.device)
+        if _tokens(v, self.H, self.d, "v", self.device) != n:
             raise ValueError("k and v must hold the same number of tokens")
-        kvring_write_frame(self.handle, k, v, _positions(pos, n, "pos", self.three_d), n, self._s(stream))
+        pos = _positions(pos, n, "pos", self.three_d, self.device)
+        with torch.cuda.device(self.device):
+            kvring_write_frame(self.handle, k, v, pos, n, self._s(stream))
 
     def delta_rotate(self, delta: int = TO_OLDEST, stream=None) -> None:
-        kvring_delta_rotate(self.handle, delta, self._s(stream))
+        with torch.cuda.device(self.device):
+            kvring_delta_rotate(self.handle, delta, self._s(stream))
 
     def attention(self, q, qpos=None, out=None, out_dtype=torch.float32, stream=None) -> torch.Tensor:
-        n = _tokens(q, self.H, self.d, "q")
+        n = _tokens(q, self.H, self.d, "q", self.device)
         if out is None:
-            out = torch.empty((n, self.H, self.d), dtype=out_dtype, device=q.device)
+            out = torch.empty((n, self.H, self.d), dtype=out_dtype, device=self.device)
         if out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (n, self.H, self.d) \
-                or not out.is_contiguous() or not out.is_cuda:
-            raise ValueError("out must be a contiguous CUDA float32/bfloat16 tensor [n_q, H, d]")
-        kvring_attention(self.handle, q, _positions(qpos, n, "qpos", self.three_d), n, out,
-                         OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32, self._s(stream))
+                or not out.is_contiguous() or not out.is_cuda or out.device != self.device:
+            raise ValueError("out must be a contiguous float32/bfloat16 tensor [n_q, H, d] on the ring's device")
+        qpos = _positions(qpos, n, "qpos", self.three_d, self.device)
+        with torch.cuda.device(self.device):
+            kvring_attention(self.handle, q, qpos, n, out,
+                             OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32, self._s(stream))
         return out
 
     def export(self, stream=None) -> dict:
@@ -355,14 +379,16 @@ class KvRing:
         scales = torch.empty(4 * self.H, dtype=torch.float32, device=dev)
         slot_pos = torch.empty(self.C, dtype=torch.int32, device=dev)
         state = torch.empty(STATE_WORDS, dtype=torch.int32, device=dev)
-        kvring_export(self.handle, k, v, scales, slot_pos, state, self._s(stream))
+        with torch.cuda.device(dev):
+            kvring_export(self.handle, k, v, scales, slot_pos, state, self._s(stream))
         return dict(k=k, v=v, scales=scales, slot_pos=slot_pos, state=state)
 
     def levels(self, stream=None) -> torch.Tensor:
         qt = (self.max_tokens + 127) // 128
         out = torch.empty((qt, self.H), dtype=torch.int32, device=self.device)
-        _check(lib().kvring_debug_attention_levels(self.handle, out.data_ptr(), self._s(stream)),
-               "kvring_debug_attention_levels")
+        with torch.cuda.device(self.device):
+            _check(lib().kvring_debug_attention_levels(self.handle, out.data_ptr(), self._s(stream)),
+                   "kvring_debug_attention_levels")
         return out
 
     def close(self) -> None:

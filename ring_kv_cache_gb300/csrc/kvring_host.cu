@@ -18,6 +18,7 @@ struct kvring {
   CUtensorMap tmV;
   int sm_count;
   int qtiles_max;
+  int device;        // current at create; every call must run with it current
   bool calibrated;   // host mirror: a calibration has been enqueued
 };
 
@@ -81,6 +82,13 @@ Plan plan_for(const kvring_config* c) {
 }
 
 kvring_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVRING_OK : KVRING_ERR_CUDA; }
+
+// The ring's device is the current one (its kernels run on the current
+// device, against the ring's memory).
+bool on_device(const kvring* r) {
+  int cur = -1;
+  return cudaGetDevice(&cur) == cudaSuccess && cur == r->device;
+}
 
 // Split-KV count for one attention call: the grid has qtiles * H * nsplit
 // CTAs of which one fits per SM; pick the split count with the fewest
@@ -177,6 +185,7 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   if (!r) return KVRING_ERR_INVALID_ARG;
   r->cfg = *cfg;
   r->sm_count = sms > 0 ? sms : 1;
+  r->device = dev;
   r->qtiles_max = p.qtiles;
   r->calibrated = false;
   uint8_t* b = static_cast<uint8_t*>(dev_buf);
@@ -264,6 +273,7 @@ kvring_status kvring_calibrate_scales(kvring_t* r, const void* k, const void* v,
   if (!r || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (pos && !aligned(pos, 4)) || n < 1)
     return KVRING_ERR_INVALID_ARG;
   if (r->dev.pt && !pos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
+  if (!on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   const kvring_status st = cuda_status(kvr::launch_calibrate(r->dev, k, v, pos, n, (cudaStream_t)stream));
   if (st == KVRING_OK) r->calibrated = true;
@@ -275,13 +285,14 @@ kvring_status kvring_write_frame(kvring_t* r, const void* k, const void* v, cons
   if (!r || !k || !v || !aligned(k, 16) || !aligned(v, 16) || (pos && !aligned(pos, 4)) || n < 1)
     return KVRING_ERR_INVALID_ARG;
   if (r->dev.pt && !pos) return KVRING_ERR_INVALID_ARG;
+  if (!on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   return cuda_status(kvr::launch_write(r->dev, k, v, pos, n, (cudaStream_t)stream));
 }
 
 kvring_status kvring_delta_rotate(kvring_t* r, int32_t delta, void* stream) {
-  if (!r) return KVRING_ERR_INVALID_ARG;
+  if (!r || !on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (delta != KVRING_DELTA_TO_OLDEST && (delta < 0 || delta >= r->cfg.max_position))
     return KVRING_ERR_INVALID_ARG;
   return cuda_status(kvr::launch_delta(r->dev, delta, (cudaStream_t)stream));
@@ -293,7 +304,7 @@ kvring_status check_batch(kvring_t* const* rings, int32_t count) {
   if (!rings || count < 1 || count > KVRING_MAX_BATCH || count > kvr::kMaxBatch) return KVRING_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     const kvring* r = rings[i];
-    if (!r) return KVRING_ERR_INVALID_ARG;
+    if (!r || !on_device(r)) return KVRING_ERR_INVALID_ARG;
     const kvring* r0 = rings[0];
     if (r->cfg.num_heads != r0->cfg.num_heads || r->cfg.head_dim != r0->cfg.head_dim ||
         r->cfg.capacity != r0->cfg.capacity || r->cfg.pinned_prefix != r0->cfg.pinned_prefix ||
@@ -344,7 +355,8 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, in
 
 kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* wv_in, void* wk_out, void* wv_out,
                                    const void* k, const void* v, int32_t n, void* stream) {
-  if (!r || !wk_in || !wv_in || !wk_out || !wv_out || !k || !v || n < 1) return KVRING_ERR_INVALID_ARG;
+  if (!r || !wk_in || !wv_in || !wk_out || !wv_out || !k || !v || n < 1 || !on_device(r))
+    return KVRING_ERR_INVALID_ARG;
   const void* ptrs[6] = {wk_in, wv_in, wk_out, wv_out, k, v};
   for (const void* p : ptrs)
     if (!aligned(p, 16)) return KVRING_ERR_INVALID_ARG;
@@ -364,6 +376,7 @@ kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, 
     return KVRING_ERR_INVALID_ARG;
   if (r->dev.pt && !qpos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
   if (out_dtype != KVRING_OUT_F32 && out_dtype != KVRING_OUT_BF16) return KVRING_ERR_INVALID_ARG;
+  if (!on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n_q > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   kvr::AttnLaunch a;
@@ -383,6 +396,7 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
     return KVRING_ERR_INVALID_ARG;
   if (r->dev.pt && !qpos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
   if (out_dtype != KVRING_OUT_F32 && out_dtype != KVRING_OUT_BF16) return KVRING_ERR_INVALID_ARG;
+  if (!on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n_q > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   // Scratch for this call inside the static array: the precision level of
@@ -420,7 +434,7 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
 
 kvring_status kvring_export(kvring_t* r, void* k_out, void* v_out, float* scales, int32_t* slot_pos,
                             int32_t* state, void* stream) {
-  if (!r) return KVRING_ERR_INVALID_ARG;
+  if (!r || !on_device(r)) return KVRING_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t cache = (size_t)r->dev.H * r->dev.C * r->dev.D;
   cudaError_t e = cudaSuccess;
@@ -442,7 +456,7 @@ kvring_status kvring_debug_encode_e4m3(const float* in, uint8_t* out, int64_t n,
 }
 
 kvring_status kvring_debug_attention_levels(kvring_t* r, int32_t* levels, void* stream) {
-  if (!r || !levels) return KVRING_ERR_INVALID_ARG;
+  if (!r || !levels || !on_device(r)) return KVRING_ERR_INVALID_ARG;
   const size_t bytes = (size_t)r->qtiles_max * r->dev.H * sizeof(int32_t);
   return cuda_status(cudaMemcpyAsync(levels, r->dev.levels, bytes, cudaMemcpyDefault, (cudaStream_t)stream));
 }
