@@ -18,10 +18,12 @@ Modules:
              diagnostic that mirrors the kernel's FP8 operand choices.
   legacy     the original upkeep the ring replaced (window copy, RoPE of
              every cached key and re-quantisation at every call).
+  projection the QKV projection in front of the cache (bf16 x bf16, summed,
+             rounded once to bf16), split into queries, keys and values.
 
 Parity pins: every function here is checked in tests/test_oracle_*.py
 against closed forms, invariants, library routines or brute force.  Nothing
 in this package is "parity unpinned".
 """
-from . import e4m3, rope, ring, attention, legacy  # noqa: F401
+from . import e4m3, rope, ring, attention, legacy, projection  # noqa: F401
 from .ring import Ring, INT32_MIN, TO_OLDEST  # noqa: F401
