@@ -37,6 +37,16 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2
     assert d["higher_is_better"] is False and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    # every key of the bench line's contract, with the reference arm's values
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    # at least 3 warm-up steps always run (asked for 1), and the line reports what ran
+    assert d["warmup"] == 3 and d["scaling"] == "weak" and d["data"] == "synthetic"
+    assert "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
 def _rank(rank, world, port, q):
