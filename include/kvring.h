@@ -75,7 +75,7 @@ typedef struct {
   int32_t max_tokens;     /* most tokens per write / calibration / attention call */
   int32_t max_position;   /* RoPE table rows: positions lie in [0, max_position) */
   int32_t max_kv_splits;  /* most key/value partitions one attention call may use (1..32) */
-  int32_t attn_precision; /* 0 = automatic per tile; 1..3 = fixed FP8 term level */
+  int32_t attn_precision; /* 0 = automatic per tile; 1..4 = fixed precision level */
   int32_t pinned_prefix;  /* P, 0 .. capacity - 1: slots [0, P) keep the first P tokens ever
                              written and are never overwritten; later tokens cycle over the
                              other capacity - P slots.  0 = the plain ring.  (The pages give
@@ -229,11 +229,14 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t num_rings
  *   out[t,h,:] = sum_j softmax_j(rope(q[t,h,:], qpos[t]) . Kdeq[h,j,:] / sqrt(d)) Vdeq[h,j,:]
  * over the filled slots j, with Kdeq = code * scale_k[h], Vdeq = code *
  * scale_v[h].  Slot order does not matter: keys carry their rotation.
- * Queries are split into 1 to 3 FP8 terms with a per-row scale (the level
- * is chosen per 128-query tile from the query and key ranges unless
- * attn_precision fixes it); the probabilities multiply V in half precision
- * (V widened exactly from its E4M3 codes); products accumulate in fp32 on
- * the tensor cores.
+ * Queries are split into 1 to 4 FP8 terms with a per-row scale; the
+ * probabilities multiply V in half precision (V widened exactly from its
+ * E4M3 codes), as one f16 term at levels 1-3 and as two (the f16 value and
+ * the f16 rounding of what it left) at level 4; products accumulate in fp32
+ * on the tensor cores.  The level (1-4 query terms) is chosen per 128-query
+ * tile from L = max|rotated q| * max|k| and V = max|v| of the head, unless
+ * attn_precision fixes it: 4 when V > 128 or L*V > 4800, else 1 when L <= 4
+ * and V <= 0.5, else 2 while L*V <= 435, else 3.
  * q: bf16 [n_q][H][d]; qpos: int32 [n_q] device positions (3-D RoPE:
  * int32 [n_q][3], required), or NULL for
  * next_pos - n_q + t (the positions of the last n_q tokens written with
@@ -282,7 +285,29 @@ kvring_status kvring_export(kvring_t* ring, void* k_out, void* v_out, float* sca
  * with the same conversion the kernels use (device pointers). */
 kvring_status kvring_debug_encode_e4m3(const float* in, uint8_t* out, int64_t n, void* stream);
 
-/* Test support: the precision level (1..3) each attention tile used in the
+/* Measurement support: the fixed cost of kvring_write_frame for n tokens.
+ * Launches a kernel with the write's grid, launch mode (a programmatic
+ * dependent of the preceding kernel), wait, ring-state read, completion
+ * ticket and state publication, but no data: nothing is read from the
+ * frame, nothing written to the cache, and the ring state is rewritten with
+ * its current values.  (The delta rotation's counterpart is
+ * kvring_delta_rotate with delta 0, which moves no rows.)
+ * Errors: INVALID_ARG, CAPACITY (as kvring_write_frame). */
+kvring_status kvring_debug_write_floor(kvring_t* ring, int32_t n, void* stream);
+
+/* Test support for the attention kernel's bounded waits.  Every wait in the
+ * kernel gives up after limit_ns of wall time (default one second); a wait
+ * that gives up sets KVRING_DEVERR_TIMEOUT in the ring's error word and the
+ * kernel drains its copies and MMAs, frees its tensor memory and returns, so
+ * the context stays usable.  With stall = 1 the kernel's first QK waits on a
+ * barrier that nothing ever completes, so every following attention call on
+ * this ring takes that path on purpose (its output is not the attention);
+ * stall = 0 restores normal calls.  Host-side setting only: takes effect on
+ * calls enqueued afterwards.
+ * Errors: INVALID_ARG (limit_ns outside [1000, 6e10], stall not 0 or 1). */
+kvring_status kvring_debug_set_attention_wait(kvring_t* ring, int64_t limit_ns, int32_t stall);
+
+/* Test support: the precision level (1..4) each attention tile used in the
  * last kvring_attention call, int32 [ceil(n_q/128)][H], copied to `levels`
  * (device or pinned host) on `stream`. */
 kvring_status kvring_debug_attention_levels(kvring_t* ring, int32_t* levels, void* stream);

@@ -17,9 +17,9 @@ and a float64 softmax with the row maximum subtracted.
 
 ``attention_emulated`` is a diagnostic that repeats the CUDA kernel's
 choices (queries split into FP8 terms with a per-row scale, probabilities
-scaled by 2^7 relative to a lazily raised running maximum and carried either
-as FP8 terms or in half precision) in float64, so that format error and
-kernel bugs can be told apart.
+scaled by 2^7 relative to a lazily raised running maximum and carried as FP8
+terms, in half precision, or as two half-precision terms) in float64, so
+that format error and kernel bugs can be told apart.
 """
 from __future__ import annotations
 
@@ -124,7 +124,9 @@ def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
     q_terms may be an int or a per-head sequence.  p_terms is the number of
     E4M3 terms of the probabilities (1 or 2; the normaliser then sums the
     same FP8 values), or "f16": probabilities rounded to IEEE half precision
-    for the value product while the normaliser sums the unrounded values.
+    for the value product while the normaliser sums the unrounded values, or
+    "f16x2": the same with two half-precision terms, the rounded value and
+    the rounding of what it left (p - hi taken in float32, where it is exact).
     """
     q = np.asarray(q, dtype=np.float64)
     n, H, d = q.shape
@@ -138,7 +140,7 @@ def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
     u = (qt * invq[:, :, None]).astype(np.float32)
     qt_terms = np.broadcast_to(np.asarray(q_terms), (H,))
     p_f16 = isinstance(p_terms, str)
-    if p_f16 and p_terms != "f16":
+    if p_f16 and p_terms not in ("f16", "f16x2"):
         raise ValueError(p_terms)
     pt_terms = None if p_f16 else np.broadcast_to(np.asarray(p_terms), (H,))
     out = np.zeros((n, H, d), dtype=np.float64)
@@ -163,7 +165,12 @@ def attention_emulated(ring, q, qpos=None, q_terms=1, p_terms=1, tile=128,
             ell *= alpha
             p = np.exp2(x - m[:, None] + p_shift).astype(np.float32)
             if p_f16:
-                O += p.astype(np.float16).astype(np.float64) @ vc[j0:j0 + tile]
+                hi = p.astype(np.float16)
+                pv = hi.astype(np.float64)
+                if p_terms == "f16x2":
+                    lo = (p - hi.astype(np.float32)).astype(np.float16)
+                    pv = pv + lo.astype(np.float64)
+                O += pv @ vc[j0:j0 + tile]
                 ell += p.astype(np.float64).sum(axis=1)
             else:
                 ps = sum(_split_terms(p, int(pt_terms[h])))

@@ -95,6 +95,8 @@ def lib():
         "kvring_export": (i32, [vp, vp, vp, vp, vp, vp, vp]),
         "kvring_debug_encode_e4m3": (i32, [vp, vp, i64, vp]),
         "kvring_debug_attention_levels": (i32, [vp, vp, vp]),
+        "kvring_debug_set_attention_wait": (i32, [vp, i64, i32]),
+        "kvring_debug_write_floor": (i32, [vp, i32, vp]),
         "kvring_status_string": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -390,6 +392,19 @@ class KvRing:
             _check(lib().kvring_debug_attention_levels(self.handle, out.data_ptr(), self._s(stream)),
                    "kvring_debug_attention_levels")
         return out
+
+    def write_floor(self, n: int, stream=None) -> None:
+        """Measurement support: the write's fixed cost for n tokens, no data
+        (see the C header); the ring is left unchanged."""
+        with torch.cuda.device(self.device):
+            _check(lib().kvring_debug_write_floor(self.handle, int(n), self._s(stream)),
+                   "kvring_debug_write_floor")
+
+    def set_attention_wait(self, limit_ns: int = 1_000_000_000, stall: bool = False) -> None:
+        """Test support: the attention kernel's wait limit, and a stall that
+        makes its first wait give up on purpose (see the C header)."""
+        _check(lib().kvring_debug_set_attention_wait(self.handle, int(limit_ns), int(bool(stall))),
+               "kvring_debug_set_attention_wait")
 
     def close(self) -> None:
         if getattr(self, "handle", None):

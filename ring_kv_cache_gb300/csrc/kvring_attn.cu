@@ -47,13 +47,22 @@
 //
 // Precision level per query tile (from the tile's amax and the head's key
 // range 448*scale_k and value range 448*scale_v): the number of E4M3 terms of
-// the queries, 1, 2 or 3.  Extra terms are residuals at the same scale,
-// accumulated into the same TMEM accumulator.  Probabilities are always f16.
+// the queries, 1 to 4.  Extra terms are residuals at the same scale,
+// accumulated into the same TMEM accumulator.  Probabilities are f16; at
+// level 4 they are carried as two f16 terms (p = hi + lo, lo = f16(p - hi)),
+// each multiplied into O by its own PV MMA.  Level 4 has its own TMEM and
+// shared-memory plan: each softmax group owns a 128-column S/P region (the
+// group's scores, then its hi and lo probabilities in the same columns), so
+// QK of a group's next tile waits for PV of its previous one instead of the
+// shared S buffer's hand-over; the fourth query term lives in the third K
+// stage, so the K tiles cycle through two stages.
 //
-// Every wait is bounded (about a second of wall time); a wait that gives up
-// sets KVRING_DEVERR_TIMEOUT in the ring's error word, the CTA drains its
-// in-flight copies and MMAs, frees TMEM and returns.
+// Every wait is bounded (one second of wall time unless the ring's debug
+// setting shortens it); a wait that gives up sets KVRING_DEVERR_TIMEOUT in the
+// ring's error word, the CTA drains its in-flight copies and MMAs, frees TMEM
+// and returns.
 #include <mutex>
+#include <type_traits>
 
 #include "kvring_internal.cuh"
 
@@ -69,7 +78,6 @@ constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpCvt = 10;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 // Probabilities carry a factor 2^kPShift relative to the running maximum,
 // which is raised only when a tile's maximum exceeds it by more than kTau:
 // the largest probability is 2^(kPShift + kTau) = 2^15, inside f16 (whose
@@ -88,6 +96,15 @@ constexpr float kPShift = 7.0f;
 constexpr float kLevel1MaxL = 4.0f;
 constexpr float kLevel1MaxV = 0.5f;
 constexpr float kLevel2MaxLV = 435.0f;
+// Level 4 (four query terms, probabilities as two f16 terms) once level 3
+// would leave too much: its error grows about as 9e-7 * L * V on Gaussian
+// heads (so L * V <= 4800 keeps it within 4.4e-3), and single f16
+// probabilities err by up to about 1e-4 * V on heavy-tailed heads (so V <= 128
+// keeps that near 1e-2 at worst).  Measured with the float64 emulation of the
+// kernel on 40 Student-t heads with scales up to 10: level 3 + f16 reaches
+// 7e-2 max-abs, level 4 stays within 3.7e-3.
+constexpr float kLevel3MaxLV = 4800.0f;
+constexpr float kLevel3MaxV = 128.0f;
 
 template <int D>
 struct Layout {
@@ -114,16 +131,23 @@ struct Layout {
   static constexpr int kBarPvIssuerDone = 2 * kStages + 11;  // every PV of the PV issuer has finished
   static constexpr int kBarVFull = 2 * kStages + 12;    // V tile of a stage landed
   static constexpr int kBarVEmpty = 3 * kStages + 12;   // ... widened to f16 by the converters
-  static constexpr int kNumBars = 4 * kStages + 12;
+  static constexpr int kBarNever = 4 * kStages + 12;    // never arrived on: the debug stall waits here
+  static constexpr int kNumBars = 4 * kStages + 13;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kLseAll = kMisc + 64;             // float [8 splits][128]: the cluster's log2-sum-exps
   static constexpr int kBytes = kLseAll + 8 * kTile * 4;
   static constexpr uint32_t kSwz = D == 128 ? 2u : 4u;  // UMMA swizzle code of the E4M3 tiles
   static_assert(kVh % 1024 == 0, "128B-swizzled atoms need 1024-byte alignment");
-  // TMEM columns
+  // TMEM columns (levels 1-3)
   static constexpr uint32_t kColS = 0;        // the S buffer (128 columns, one tile's scores)
   static constexpr uint32_t kColP = 128;      // f16 probabilities of group g at 128 + 64 g
   static constexpr uint32_t kColO = 256;      // O accumulator of group g at 256 + 128 g (D columns)
+  // Level 4: group g's S/P region at 128 g (scores, then hi probabilities in
+  // its first 64 columns and lo in the next 64); O as above.
+  static constexpr uint32_t kColSP4 = 128;
+  // Shared-memory byte offset of query term t (0..3): terms 0-2 in the Q
+  // images, term 3 (level 4 only) in the third K stage.
+  static constexpr int q_term(int t) { return t < 3 ? kQ + t * kQTile : kK + 2 * kKVTile; }
 };
 
 struct Misc {
@@ -144,6 +168,8 @@ struct AttnParams {
   int tiles_per_split;
   int forced_level;
   int cluster_merge;   // the splits of a query tile form one cluster (2..8 CTAs)
+  int debug_stall;     // 1: the QK issuer first waits on a barrier nothing arrives on
+  unsigned long long wait_ns;   // limit of every bounded wait
 };
 
 // 3-D RoPE: the (t, y, x) positions of a query tile's rows into qpos_s
@@ -194,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBars + 8u * (uint32_t)i; };
 
   const RingDev& r = prm.r;
+  const uint64_t wait_ns = prm.wait_ns;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
   const int H = r.H;
@@ -236,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::kBarSFree), kGroupThreads / 32);  // a tile's S is in its group's registers
     mbar_init(bar(L::kBarMerge), 1);
     mbar_init(bar(L::kBarPvIssuerDone), 1);
+    mbar_init(bar(L::kBarNever), 1);
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
@@ -386,7 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (level == 0) {
         const float lg = qm * 448.0f * scale_k;
         const float vmax = 448.0f * scale_v;
-        level = (lg <= kLevel1MaxL && vmax <= kLevel1MaxV) ? 1 : (lg * vmax <= kLevel2MaxLV ? 2 : 3);
+        level = (vmax > kLevel3MaxV || lg * vmax > kLevel3MaxLV) ? 4
+                : (lg <= kLevel1MaxL && vmax <= kLevel1MaxV)     ? 1
+                : (lg * vmax <= kLevel2MaxLV)                   ? 2
+                                                                : 3;
       }
 #pragma unroll
       for (int i = 0; i < PQ; ++i) {
@@ -406,12 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 8; ++e) v[e] *= invq;
         const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
 #pragma unroll
-        for (int term = 0; term < 3; ++term) {
+        for (int term = 0; term < 4; ++term) {
           if (term < level) {
             uint16_t c4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(v[2 * e], v[2 * e + 1]);
-            *reinterpret_cast<uint2*>(sm + L::kQ + term * L::kQTile + off) =
+            // (term 3 overwrites the third K stage, whose staged query rows
+            // pass 1 read before the CTA barrier)
+            *reinterpret_cast<uint2*>(sm + L::q_term(term) + off) =
                 make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
             if (term + 1 < level) {
 #pragma unroll
@@ -441,6 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // needs longer to issue an M = 128, N = 128 MMA than the tensor core
     // needs to run it).
     if (lane == 0) {
+      // Level 4 cycles the K tiles through two stages (the third holds the
+      // fourth query term) and issues two PV MMAs per tile (hi, then lo
+      // probabilities, from the group's S/P region).
+      const bool l4 = misc->level == 4;   // the prologue ended with a CTA barrier
+      auto kst = [&](int j) { return l4 ? (j & 1) : (j % kStages); };
+      auto kph = [&](int j) { return l4 ? ((j >> 1) & 1) : ((j / kStages) & 1); };
+      const int nks = l4 ? 2 : kStages;
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
       // f16 V: 128B-swizzled MN-major atoms of 64 columns x 8 rows (1024 B
       // apart along the slots); the second 64 columns one atom column further
@@ -451,11 +491,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1;
         tc_fence_after();
         const uint32_t vl = v_lo + (uint32_t)b * kVhStep;
-        const uint32_t pa = tmem + L::kColP + 64u * b;
+        if (!l4) {
+          const uint32_t pa = tmem + L::kColP + 64u * b;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
-                       (j > 1 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
+                         (j > 1 || kk > 0) ? 1u : 0u);
+        } else {
+          // level 4: the block of slots 16 kk + [0, 16) has its f16 values at
+          // columns 16 kk + [0, 8) of the group's region and the second terms
+          // at 16 kk + [8, 16)
+          const uint32_t pa = tmem + L::kColSP4 * b;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 16, vl + kk * (16 * 128 / 16), v_hi, idesc_pv,
+                         (j > 1 || kk > 0) ? 1u : 0u);
+            mma_f16_ts_w(tmem + L::kColO + b * 128, pa + kk * 16 + 8, vl + kk * (16 * 128 / 16), v_hi, idesc_pv, 1u);
+          }
+        }
         mma_commit(bar(L::kBarPvDone + b));
       };
       const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
@@ -469,9 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(np++);
           prog = true;
         }
-        if (k_issued < ntiles &&
-            mbar_test_wait(bar(L::kBarKEmpty + k_issued % kStages), ((k_issued / kStages) & 1) ^ 1)) {
-          const int s = k_issued % kStages;
+        if (k_issued < ntiles && mbar_test_wait(bar(L::kBarKEmpty + kst(k_issued)), kph(k_issued) ^ 1)) {
+          const int s = kst(k_issued);
           mbar_arrive_expect_tx(bar(L::kBarKFull + s), (uint32_t)(kTile * D));
           tma_load_3d(sbase + L::kK + s * L::kKVTile, &tmK, 0, (tile0 + k_issued) * kTile, h, bar(L::kBarKFull + s));
           ++k_issued;
@@ -493,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           t_idle = globaltimer_ns();
         } else if ((idle & 15u) == 0) {
           if (*abort) break;
-          if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+          if (globaltimer_ns() - t_idle > wait_ns) {
             *abort = 1;
             break;
           }
@@ -501,13 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Drain: every issued copy must land before the CTA may exit.
       volatile int no_abort = 0;
-      for (int j = k_issued - kStages < 0 ? 0 : k_issued - kStages; j < k_issued; ++j)
-        mbar_wait_bounded(bar(L::kBarKFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
+      for (int j = k_issued - nks < 0 ? 0 : k_issued - nks; j < k_issued; ++j)
+        mbar_wait_bounded(bar(L::kBarKFull + kst(j)), kph(j), &no_abort, wait_ns);
       for (int j = v_issued - kStages < 0 ? 0 : v_issued - kStages; j < v_issued; ++j)
-        mbar_wait_bounded(bar(L::kBarVFull + j % kStages), (j / kStages) & 1, &no_abort, kWaitLimitNs);
+        mbar_wait_bounded(bar(L::kBarVFull + j % kStages), (j / kStages) & 1, &no_abort, wait_ns);
       // and every PV this thread issued has finished before TMEM is freed
       mma_commit(bar(L::kBarPvIssuerDone));
-      mbar_wait_bounded(bar(L::kBarPvIssuerDone), 0, &no_abort, kWaitLimitNs);
+      mbar_wait_bounded(bar(L::kBarPvIssuerDone), 0, &no_abort, wait_ns);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -519,23 +571,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq = smem_desc(sbase + L::kQ, 16, 8 * D, L::kSwz);
       const uint64_t dk = smem_desc(sbase + L::kK, 16, 8 * D, L::kSwz);
       const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, kq_hi = (uint32_t)(dq >> 32);
-      constexpr uint32_t kQStep = L::kQTile >> 4, kKVStep = L::kKVTile >> 4;
+      constexpr uint32_t kKVStep = L::kKVTile >> 4;
       const int n_qterms = misc->level;   // the prologue ended with a CTA barrier
-      // S(j) into the S buffer once its group has S(j - 1) in registers and
-      // the K/V stage has landed; the K stage is freed by the commit.
-      for (int j = 0; j < ntiles; ++j) {
-        const int s = j % kStages;
-        if (j > 0 && !mbar_wait_bounded(bar(L::kBarSFree), (j - 1) & 1, abort, kWaitLimitNs)) break;
-        if (!mbar_wait_bounded(bar(L::kBarKFull + s), (j / kStages) & 1, abort, kWaitLimitNs)) break;
+      const bool l4 = n_qterms == 4;
+      // The debug stall: a wait that nothing ends, so that the bounded wait
+      // gives up and the whole CTA takes its abort path.
+      const bool go = !prm.debug_stall || mbar_wait_bounded(bar(L::kBarNever), 0, abort, wait_ns);
+      // Levels 1-3: S(j) into the one S buffer once its group has S(j - 1) in
+      // registers and the K stage has landed.  Level 4: S(j) into group
+      // (j & 1)'s S/P region once PV(j - 2) has read that group's previous
+      // probabilities from it.  The K stage is freed by the commit.
+      for (int j = 0; go && j < ntiles; ++j) {
+        const int s = l4 ? (j & 1) : j % kStages;
+        if (l4) {
+          if (j > 1 && !mbar_wait_bounded(bar(L::kBarPvDone + (j & 1)), ((j - 2) >> 1) & 1, abort, wait_ns)) break;
+        } else {
+          if (j > 0 && !mbar_wait_bounded(bar(L::kBarSFree), (j - 1) & 1, abort, wait_ns)) break;
+        }
+        if (!mbar_wait_bounded(bar(L::kBarKFull + s), l4 ? (j >> 1) & 1 : (j / kStages) & 1, abort, wait_ns))
+          break;
         tc_fence_after();
         const uint32_t kl = k_lo + s * kKVStep;
-        const uint32_t dst = tmem + L::kColS;
+        const uint32_t dst = l4 ? tmem + L::kColSP4 * (j & 1) : tmem + L::kColS;
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
+        for (int t = 0; t < 4; ++t) {
           if (t < n_qterms) {
+            const uint32_t qt_lo = q_lo + (uint32_t)((L::q_term(t) - L::kQ) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk)
-              mma_e4m3_w(dst, q_lo + t * kQStep + 2 * kk, kq_hi, kl + 2 * kk, kq_hi, idesc_qk, (t | kk) != 0);
+              mma_e4m3_w(dst, qt_lo + 2 * kk, kq_hi, kl + 2 * kk, kq_hi, idesc_qk, (t | kk) != 0);
           }
         }
         mma_commit(bar(L::kBarSFull + (j & 1)));
@@ -545,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
       mma_commit(bar(L::kBarMmaDone));
       volatile int no_abort = 0;
-      mbar_wait_bounded(bar(L::kBarMmaDone), 0, &no_abort, kWaitLimitNs);
+      mbar_wait_bounded(bar(L::kBarMmaDone), 0, &no_abort, wait_ns);
     }
     __syncwarp();
   } else if (warp >= kWarpCvt) {
@@ -560,8 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ct = threadIdx.x - kWarpCvt * 32;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages, b = j & 1;
-      bool ok = mbar_wait_bounded(bar(L::kBarVFull + s), (j / kStages) & 1, abort, kWaitLimitNs);
-      if (ok && j >= 2) ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, kWaitLimitNs);
+      bool ok = mbar_wait_bounded(bar(L::kBarVFull + s), (j / kStages) & 1, abort, wait_ns);
+      if (ok && j >= 2) ok = mbar_wait_bounded(bar(L::kBarPvDone + b), ((j >> 1) & 1) ^ 1, abort, wait_ns);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       const uint8_t* src = sm + L::kV + s * L::kKVTile;
       uint8_t* dst = sm + L::kVh + b * L::kVhTile;
@@ -608,40 +672,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       f_row = fmaxf(sq * scale_k * (1.4426950408889634f / sqrtf((float)D)), 1e-30f);
     }
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tS = trow + L::kColS, tP = trow + L::kColP + 64 * g, tO = trow + L::kColO + g * 128;
+    const uint32_t tO = trow + L::kColO + g * 128;
     float m_run = -INFINITY;
     float ell = 0.f;
     bool ok = true;
+    // The tile loop, instantiated for levels 1-3 and for level 4.  Levels
+    // 1-3 load a tile's 128 scores into registers at once and hand the S
+    // buffer back.  Level 4 keeps its scores in the group's own S/P region
+    // and streams them in 32-column chunks, twice (row maximum, then
+    // probabilities): its probabilities go in place over the scores they
+    // come from, each 16-slot block's 16 columns taking the block's f16
+    // values (8 columns) and then the f16 roundings of what those left (8
+    // columns), so no chunk overwrites a score not yet read.
+    auto tile_loop = [&](auto level4) {
+    constexpr bool l4 = decltype(level4)::value;
+    const uint32_t tS = l4 ? trow + L::kColSP4 * g : trow + L::kColS;
+    const uint32_t tP = l4 ? trow + L::kColSP4 * g : trow + L::kColP + 64 * g;
     for (int j = g; j < ntiles; j += 2) {
       const int n = j >> 1;
-      ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait_bounded(bar(L::kBarSFull + g), n & 1, abort, kWaitLimitNs));
+      ok = __all_sync(0xFFFFFFFFu, ok && mbar_wait_bounded(bar(L::kBarSFull + g), n & 1, abort, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-      tmem_wait_ld();
-      // the scores are in registers: the S buffer may take the next tile
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::kBarSFree));
-      // mask slots past the fill level (only the ring's last tile)
+      // slots past the fill level are masked (only the ring's last tile)
       const int valid = nvalid - (tile0 + j) * kTile;
-      if (valid < kTile) {
+      uint32_t sr[l4 ? 1 : 128];
+      float smax;
+      if constexpr (!l4) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+        tmem_wait_ld();
+        // the scores are in registers: the S buffer may take the next tile
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kBarSFree));
+        if (valid < kTile) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // row maximum: eight running three-way maxima, then a small tree
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mx[k] = fmax3(mx[k], __uint_as_float(sr[16 * i + 2 * k]), __uint_as_float(sr[16 * i + 2 * k + 1]));
+        smax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
+      } else {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r32[32];
+          tmem_ld32(tS + 32 * c, r32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = 32 * c + i < valid ? __uint_as_float(r32[i]) : -INFINITY;
+            mx[i & 3] = fmaxf(mx[i & 3], x);
+          }
+        }
+        smax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
-      // row maximum: eight running three-way maxima, then a small tree
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(__uint_as_float(sr[2 * k]), __uint_as_float(sr[2 * k + 1]));
-#pragma unroll
-      for (int i = 1; i < 8; ++i)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mx[k] = fmax3(mx[k], __uint_as_float(sr[16 * i + 2 * k]), __uint_as_float(sr[16 * i + 2 * k + 1]));
-      const float smax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
       const float tmax = smax * f_row;          // f_row > 0
       const bool need = tmax > m_run + kTau;
       const float m_new = need ? tmax : m_run;
@@ -649,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile, has completed
       if (j > 1) {
         ok = __all_sync(0xFFFFFFFFu,
-                        mbar_wait_bounded(bar(L::kBarPvDone + g), ((j - 2) >> 1) & 1, abort, kWaitLimitNs));
+                        mbar_wait_bounded(bar(L::kBarPvDone + g), ((j - 2) >> 1) & 1, abort, wait_ns));
         if (!ok) break;
         tc_fence_after();
       }
@@ -674,37 +767,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         ell *= alpha;
       }
       m_run = m_new;
-      // probabilities 2^(x - m + 7): f16 pairs into P_g, slots 32 c + [0, 32)
-      // -> columns 16 c + [0, 16), the lower slot in the low half; the
-      // normaliser takes the fp32 values
-      // (pairs of scores through the packed two-lane fp32 FMA and add)
+      // probabilities 2^(x - m + 7) as f16 pairs, the lower slot in the low
+      // half; the normaliser takes the fp32 values (pairs of scores through
+      // the packed two-lane fp32 FMA and add)
       const float moff = kPShift - m_run;
       const float2 fr2 = make_float2(f_row, f_row), mo2 = make_float2(moff, moff);
       float2 lsum = make_float2(0.f, 0.f);
+      if constexpr (l4) {
+        // slots 16 b + [0, 16) -> columns 16 b + [0, 8) (f16 values) and
+        // 16 b + [8, 16) (f16 roundings of what the values left; the fp32
+        // difference is exact, both lying within 2^-11 of each other)
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r32[32];
+          tmem_ld32(tS + 32 * c, r32);
+          tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float2 e[16];
+          for (int hb = 0; hb < 2; ++hb) {
+            float2 e[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = __ffma2_rn(
-              make_float2(__uint_as_float(sr[32 * c + 2 * i]), __uint_as_float(sr[32 * c + 2 * i + 1])), fr2, mo2);
-          e[i] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            for (int i = 0; i < 8; ++i) {
+              const int k = 16 * hb + 2 * i;
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(r32[k]), __uint_as_float(r32[k + 1])), fr2, mo2);
+              e[i] = make_float2(32 * c + k < valid ? ex2_approx(x.x) : 0.f,
+                                 32 * c + k + 1 < valid ? ex2_approx(x.y) : 0.f);
+            }
+            uint32_t hv[8], lv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              hv[i] = f32x2_to_f16x2(e[i].x, e[i].y);
+              const float2 hf = f16x2_to_f32x2(hv[i]);
+              lv[i] = f32x2_to_f16x2(e[i].x - hf.x, e[i].y - hf.y);
+            }
+            tmem_st_n<8>(tP + 32 * c + 16 * hb, hv);
+            tmem_st_n<8>(tP + 32 * c + 16 * hb + 8, lv);
+#pragma unroll
+            for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+              for (int i = 0; i < w; ++i) e[i] = __fadd2_rn(e[i], e[i + w]);
+            lsum = __fadd2_rn(lsum, e[0]);
+          }
         }
-        uint32_t hv[16];
+      } else {
+        // slots 32 c + [0, 32) -> columns 16 c + [0, 16) of P_g
 #pragma unroll
-        for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[i].x, e[i].y);
-        tmem_st16(tP + 16 * c, hv);
+        for (int c = 0; c < 4; ++c) {
+          float2 e[16];
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(sr[32 * c + 2 * i]), __uint_as_float(sr[32 * c + 2 * i + 1])), fr2, mo2);
+            e[i] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          }
+          uint32_t hv[16];
 #pragma unroll
-          for (int i = 0; i < w; ++i) e[i] = __fadd2_rn(e[i], e[i + w]);
-        lsum = __fadd2_rn(lsum, e[0]);
+          for (int i = 0; i < 16; ++i) hv[i] = f32x2_to_f16x2(e[i].x, e[i].y);
+          tmem_st16(tP + 16 * c, hv);
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) e[i] = __fadd2_rn(e[i], e[i + w]);
+          lsum = __fadd2_rn(lsum, e[0]);
+        }
       }
       ell += lsum.x + lsum.y;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::kBarPFull + g));
     }
+    };
+    if (misc->level == 4) tile_loop(std::true_type{});
+    else tile_loop(std::false_type{});
 
     // ---------------------------------------------------------- epilogue
     // merge the two groups: m = max(m_0, m_1), w_g = 2^(m_g - m),
@@ -727,9 +860,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int jl0 = ntiles > 0 ? ((ntiles - 1) & ~1) : -1;
     const int jl1 = ntiles > 1 ? (((ntiles - 2) & ~1) + 1) : -1;
     if (ok && jl0 >= 0)
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + 0), (jl0 >> 1) & 1, abort, kWaitLimitNs));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + 0), (jl0 >> 1) & 1, abort, wait_ns));
     if (ok && jl1 >= 0)
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + 1), (jl1 >> 1) & 1, abort, kWaitLimitNs));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarPvDone + 1), (jl1 >> 1) & 1, abort, wait_ns));
     // Normalised rows go to shared memory (the key/value stages are free:
     // every copy landed, was converted and read by its MMAs), fp32
     // [128][d + 4]: group g's thread of the row writes columns [g d/2, (g+1) d/2)
@@ -918,8 +1051,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s2 = 0; s2 < 8; ++s2)
           if (s2 < ns) wts[s2 * kTile + threadIdx.x] = lv[s2] * gsc;
       }
+      // The peers' copies were issued unconditionally after the cluster
+      // barrier, so they land even on an aborted call: wait for them
+      // whatever the abort flag says (a CTA must not exit while copies into
+      // its shared memory are in flight).
+      volatile int no_abort = 0;
       const bool landed =
-          __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarMerge), 0, abort, kWaitLimitNs));
+          __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarMerge), 0, &no_abort, wait_ns));
       sync_softmax();
       const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
       float4 acc[MT];
@@ -1022,6 +1160,8 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   p.tiles_per_split = a.tiles_per_split;
   p.forced_level = a.forced_level;
   p.cluster_merge = (a.nsplit >= 2 && a.nsplit <= 8) ? 1 : 0;
+  p.debug_stall = a.debug_stall;
+  p.wait_ns = a.wait_ns;
   const unsigned qtiles = (unsigned)((a.n_q + kTile - 1) / kTile);
   // A programmatic dependent of the preceding kernel: it may start while
   // that kernel still runs, copies its query rows, and waits

@@ -294,6 +294,15 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
   write_body<D, kWriteU>(r, k, v, pos, n, blockIdx.x, gridDim.x);
 }
 
+// The write's fixed cost alone: the grid of an n-token write, the same
+// programmatic-dependent launch, wait, ring-state read, completion ticket
+// and state publication by the last block, with no data (zero tokens, so the
+// published state equals the state read and the ring is unchanged).
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_write_floor(RingDev r) {
+  write_body<D, kWriteU>(r, nullptr, nullptr, nullptr, 0, blockIdx.x, gridDim.x);
+}
+
 // Many rings of one shape in one launch, as a bulk-copy pipeline.  The work
 // is cut into units of whole tokens (TU = RU / H tokens of all H heads, RU =
 // 8192 / D rows, 16 KB of bf16) -- or, when one token's heads exceed RU rows,
@@ -1023,6 +1032,14 @@ cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const i
   const uint16_t* vv = static_cast<const uint16_t*>(v);
   if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write<128>, r, kk, vv, pos, n);
   return cudaLaunchKernelEx(&cfg, k_write<64>, r, kk, vv, pos, n);
+}
+
+cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s) {
+  const long long items = 2LL * n * r.H * (r.D / 16);   // the grid of an n-token write
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteU - 1) / kWriteU)), s, attr);
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write_floor<128>, r);
+  return cudaLaunchKernelEx(&cfg, k_write_floor<64>, r);
 }
 
 cudaError_t launch_write_many(const WriteMany& b, int count, int n, cudaStream_t s) {

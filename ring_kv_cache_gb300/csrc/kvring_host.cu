@@ -20,11 +20,14 @@ struct kvring {
   int qtiles_max;
   int device;        // current at create; every call must run with it current
   bool calibrated;   // host mirror: a calibration has been enqueued
+  unsigned long long attn_wait_ns;   // limit of the attention kernel's bounded waits
+  int attn_debug_stall;              // test support: the next attention calls time out on purpose
 };
 
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;   // one second
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -38,7 +41,7 @@ bool config_ok(const kvring_config* c) {
   if (c->max_tokens < 1 || c->max_tokens > (1 << 24)) return false;
   if (c->max_position < 1 || c->max_position > (1 << 24)) return false;
   if (c->max_kv_splits < 1 || c->max_kv_splits > 32) return false;
-  if (c->attn_precision < 0 || c->attn_precision > 3) return false;
+  if (c->attn_precision < 0 || c->attn_precision > 4) return false;
   if (c->pinned_prefix < 0 || c->pinned_prefix >= c->capacity) return false;
   if (c->rope_pairs_t != 0 || c->rope_pairs_y != 0) {   // 3-D RoPE sections, in whole chunks of 8 pairs
     const int half = c->head_dim / 2, t = c->rope_pairs_t, y = c->rope_pairs_y;
@@ -188,6 +191,8 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   r->device = dev;
   r->qtiles_max = p.qtiles;
   r->calibrated = false;
+  r->attn_wait_ns = kDefaultWaitNs;
+  r->attn_debug_stall = 0;
   uint8_t* b = static_cast<uint8_t*>(dev_buf);
   kvr::RingDev& d = r->dev;
   d.k = b + p.k;
@@ -386,6 +391,8 @@ kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, 
   a.n_q = n_q;
   a.out_bf16 = out_dtype == KVRING_OUT_BF16;
   a.forced_level = r->cfg.attn_precision;
+  a.debug_stall = r->attn_debug_stall;
+  a.wait_ns = r->attn_wait_ns;
   choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
   return cuda_status(kvr::launch_attention(r->dev, &r->tmK, &r->tmV, a, (cudaStream_t)stream));
 }
@@ -413,6 +420,8 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
   a.n_q = n_q;
   a.out_bf16 = out_dtype == KVRING_OUT_BF16;
   a.forced_level = r->cfg.attn_precision;
+  a.debug_stall = r->attn_debug_stall;
+  a.wait_ns = r->attn_wait_ns;
   choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
   const int ctiles = (r->cfg.capacity + kvr::kTile - 1) / kvr::kTile;
   if (a.nsplit > 8) {
@@ -453,6 +462,20 @@ kvring_status kvring_debug_encode_e4m3(const float* in, uint8_t* out, int64_t n,
   if ((!in || !out) && n > 0) return KVRING_ERR_INVALID_ARG;
   if (n < 0) return KVRING_ERR_INVALID_ARG;
   return cuda_status(kvr::launch_encode_e4m3(in, out, n, (cudaStream_t)stream));
+}
+
+kvring_status kvring_debug_write_floor(kvring_t* r, int32_t n, void* stream) {
+  if (!r || n < 1 || !on_device(r)) return KVRING_ERR_INVALID_ARG;
+  if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
+  return cuda_status(kvr::launch_write_floor(r->dev, n, (cudaStream_t)stream));
+}
+
+kvring_status kvring_debug_set_attention_wait(kvring_t* r, int64_t limit_ns, int32_t stall) {
+  if (!r || limit_ns < 1000 || limit_ns > 60000000000ll || (stall != 0 && stall != 1))
+    return KVRING_ERR_INVALID_ARG;
+  r->attn_wait_ns = (unsigned long long)limit_ns;
+  r->attn_debug_stall = stall;
+  return KVRING_OK;
 }
 
 kvring_status kvring_debug_attention_levels(kvring_t* r, int32_t* levels, void* stream) {

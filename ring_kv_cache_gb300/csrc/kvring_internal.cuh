@@ -86,6 +86,14 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// The two halves of an f16 pair (low half first) as fp32, exactly.
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
+  float2 r;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(h2));
+  return r;
+}
 __device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t h2) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
@@ -536,6 +544,7 @@ cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, con
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
                          cudaStream_t s);
 cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s);
+cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s);
 cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
 
 struct AttnLaunch {
@@ -547,6 +556,8 @@ struct AttnLaunch {
   int nsplit;
   int tiles_per_split;
   int forced_level;
+  int debug_stall;                 // test support: make the first QK wait time out
+  unsigned long long wait_ns;      // limit of every bounded wait in the kernel
 };
 // Batched write / delta over rings of one shape (kernel parameters: no
 // device memory is needed to describe the batch).

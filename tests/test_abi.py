@@ -46,7 +46,7 @@ def test_required_bytes_matches_layout(L):
 
 @pytest.mark.parametrize("field,value", [
     ("num_heads", 0), ("head_dim", 96), ("capacity", 0), ("max_tokens", 0),
-    ("max_position", 0), ("max_kv_splits", 0), ("attn_precision", 4),
+    ("max_position", 0), ("max_kv_splits", 0), ("attn_precision", 5),
     ("pinned_prefix", -1), ("pinned_prefix", 48),
     ("rope_pairs_t", 4), ("rope_pairs_t", 40), ("rope_pairs_y", 8), ("rope_pairs_t", 12),
     ("rope_base", 0.0), ("rope_base", float("inf")),

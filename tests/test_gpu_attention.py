@@ -33,15 +33,17 @@ def _tiny_loaded(frames_written, **kw):
     return ring, orc, frames
 
 
-@pytest.mark.parametrize("level", [1, 2, 3])
+@pytest.mark.parametrize("level", [1, 2, 3, 4])
 def test_kernel_matches_its_mirror_tightly(level):
     """Level 1 is only chosen automatically for tiny-magnitude heads; forced
-    here, its output must still match its mirror (format error aside)."""
+    here, its output must still match its mirror (format error aside).
+    Level 4 carries the probabilities as two f16 terms."""
     ring, orc, frames = _tiny_loaded(6, max_kv_splits=1, attn_precision=level)
     q = frames[6][0]
     out = ring.attention(dev(q)).cpu().numpy()
     # the kernel's probability shift (2^7) and rescale threshold (8, log2 units)
-    mirror = attention_emulated(orc, f(q), None, level, "f16", p_shift=7.0, tau=8.0)
+    mirror = attention_emulated(orc, f(q), None, level, "f16x2" if level == 4 else "f16",
+                                p_shift=7.0, tau=8.0)
     mx, mn = attn_errors(out, mirror)
     scale = np.abs(mirror).max()
     assert mx <= 2e-3 * scale, (level, mx, scale)
@@ -55,7 +57,53 @@ def test_levels_reported_and_automatic_choice_is_in_range():
     ring, orc, frames = _tiny_loaded(3)
     ring.attention(dev(frames[3][0]))
     lv = ring.levels().cpu().numpy()
-    assert lv.shape[1] == TINY.heads and np.all((lv[0] >= 1) & (lv[0] <= 3))
+    assert lv.shape[1] == TINY.heads and np.all((lv[0] >= 1) & (lv[0] <= 4))
+
+
+def _loaded(shape, frames, **kw):
+    ring, orc = make_pair(shape, Ring, **kw)
+    ring.calibrate(dev(frames[0][1]), dev(frames[0][2]))
+    orc.calibrate(f(frames[0][1]), f(frames[0][2]))
+    for _, k, v in frames:
+        ring.write(dev(k), dev(v))
+        orc.write(f(k), f(v))
+    return ring, orc
+
+
+def test_automatic_level_1_on_small_heads_meets_the_bar():
+    """Heads whose keys and values are small (sigma 0.08: L = max|q| max|k|
+    about 2, V = max|v| about 0.35) are given one query term by the automatic
+    rule; the output still meets the float64 reference's bar."""
+    rng = np.random.default_rng(12)
+    shape = RingShape(heads=2, head_dim=128, capacity=700, tokens=300, queries=256, max_position=2000)
+    sig = np.array([0.08, 0.06])
+    frames = [frame(rng, shape, 300, sig, sig) for _ in range(3)]
+    ring, orc = _loaded(shape, frames)
+    q, _, _ = frame(rng, shape, 256)
+    out = ring.attention(dev(q)).cpu().numpy()
+    lv = ring.levels().cpu().numpy()[:2]
+    assert np.all(lv == 1), lv
+    mx, mn = attn_errors(out, attention_exact(orc, f(q)))
+    assert mx <= MAX_ABS and mn <= MEAN_ABS, (mx, mn)
+
+
+def test_automatic_level_4_on_heavy_tailed_heads_meets_the_bar():
+    """Heavy-tailed heads with large values (Student-t keys and values, 3
+    degrees of freedom, scales up to 10: V = max|v| in the hundreds) are given
+    four query terms and two-term f16 probabilities by the automatic rule, and
+    meet the float64 reference's absolute bar."""
+    rng = np.random.default_rng(13)
+    shape = RingShape(heads=2, head_dim=128, capacity=1500, tokens=700, queries=256, max_position=4000)
+    sk, sv = np.array([6.0, 2.5]), np.array([10.0, 4.0])
+    frames = [frame(rng, shape, 700, sk, sv, dist="student_t") for _ in range(3)]
+    ring, orc = _loaded(shape, frames, max_tokens=700)
+    q, _, _ = frame(rng, shape, 256)
+    out = ring.attention(dev(q)).cpu().numpy()
+    lv = ring.levels().cpu().numpy()[:2]
+    assert np.all(lv == 4), lv
+    want = attention_exact(orc, f(q))
+    mx, mn = attn_errors(out, want)
+    assert mx <= MAX_ABS and mn <= MEAN_ABS, (mx, mn, np.abs(want).max())
 
 
 def test_empty_ring_gives_zeros():

@@ -193,13 +193,10 @@ def test_stress_40_heads_heavy_tails():
         assert r.export()["state"][kv.STATE["error"]].item() == 0
     print("stress attention errors (step, max-abs, mean-abs, max|o|, rms o):", worst)
     for st, mx, mn, omax, orms in worst:
-        # The mean-abs bar holds as stated.  The max-abs bar of 2e-2 cannot
-        # hold with FP8 operands once outputs reach the hundreds (heavy tails
-        # put single values near 448 * scale): the probabilities' two E4M3
-        # terms carry about 8 significant bits, so the worst element errs by
-        # a few 1e-3 of the largest output.  Checked against that, stated
-        # relative bound instead (measured: about 2.6e-3).
+        # The stated bar, as for every other workload: the heads whose value
+        # or logit range would push three query terms and f16 probabilities
+        # past it take four query terms and two-term f16 probabilities.
         assert mn <= MEAN_ABS, (st, mn)
-        assert mx <= max(MAX_ABS, 4e-3 * omax), (st, mx, omax)
+        assert mx <= MAX_ABS, (st, mx, omax)
     del rings
     _free()

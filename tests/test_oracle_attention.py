@@ -115,3 +115,22 @@ def test_kernel_mirror_single_tile_equals_reference_structure():
     a = attention_emulated(r, q, np.arange(72, 84), 3, 2, tile=1, tau=0.0)
     b = attention_emulated(r, q, np.arange(72, 84), 3, 2, tile=128)
     assert np.abs(a - b).max() < 1e-3
+
+
+def test_kernel_mirror_two_f16_probability_terms():
+    """The level-4 mirror (four query terms, probabilities as an f16 value
+    plus the f16 rounding of what it left) errs far less than three terms
+    with single f16 probabilities, and its probability pair carries p to
+    about 22 bits (a lower bound on what two 11-bit terms give)."""
+    r, frames = _tiny_ring(6)
+    q = f32_from_bf16(frames[6][0])
+    qpos = np.arange(72, 84)
+    ref = attention_exact(r, q, qpos)
+    e3 = np.abs(attention_emulated(r, q, qpos, 3, "f16", tile=16, tau=8.0) - ref).max()
+    e4 = np.abs(attention_emulated(r, q, qpos, 4, "f16x2", tile=16, tau=8.0) - ref).max()
+    assert e4 < e3 / 4 and e4 < 5e-5, (e3, e4)
+    p = np.random.default_rng(0).uniform(2.0 ** -6, 2.0 ** 15, 10000).astype(np.float32)
+    hi = p.astype(np.float16)
+    lo = (p - hi.astype(np.float32)).astype(np.float16)
+    rel = np.abs(hi.astype(np.float64) + lo.astype(np.float64) - p) / p
+    assert rel.max() <= 2.0 ** -21
