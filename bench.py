@@ -20,7 +20,7 @@ durations come from graphs of 16 back-to-back calls (one per ring).
 The metric is time-like (microseconds per write + attention).
 
 ``--impl reference`` times the CPU oracle (float64 NumPy, the test oracle)
-on this host's cores on a bounded sample of each step (see ``cpu_step``).
+on this host's cores on a bounded sample of each step (see ``cpu_sample``).
 Replicas only across GPUs: each rank runs its own rings; no collective is
 on the data path.
 """
@@ -41,6 +41,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "µs per 757-token cache write + 5788-slot FP8 attn; GB/s & TFLOP/s vs GB300 peak"
+WORKLOAD = ("production-shaped call: 757-token write + 757-query attention over a wrapped 5,788-slot "
+            "ring, 10 heads x 128 (E4M3 cache, bf16 in, fp32 out)")
 H, D, C, N_NEW, N_Q, MAX_POS = 10, 128, 5788, 757, 757, 40960
 RINGS = 16
 RESET_PERIOD = 42   # the pages reset positions once per 42 steps (Do It Once, at Write Time)
@@ -253,6 +255,15 @@ def gpu_arm(args, rank, world):
     w_us = timed(g_write, w_reps) * 1e3 / (w_reps * RINGS)
     d_ms += timed(g_delta, 1)                     # delta = 41 frames of positions
     d_us = d_ms * 1e3 / (2 * RINGS)
+    # The fixed cost of each, with no data: the write's grid, launch mode,
+    # wait, state read, completion ticket and state publication
+    # (kvring_debug_write_floor), and the delta rotation's full grid with a
+    # delta of 0 (no rows move).  Same graphs of 16 back-to-back calls.
+    g_wfloor = capture(lambda: [rings[r].write_floor(N_NEW, stream=stream) for r in range(RINGS)])
+    g_dfloor = capture(lambda: [rings[r].delta_rotate(0, stream=stream) for r in range(RINGS)])
+    timed(g_wfloor, 1)
+    wf_us = timed(g_wfloor, 8) * 1e3 / (8 * RINGS)
+    df_us = timed(g_dfloor, 4) * 1e3 / (4 * RINGS)
     for r in range(RINGS):
         writes[r] = 1   # every window was just reset: the next reset is 41 writes away
 
@@ -335,12 +346,16 @@ def gpu_arm(args, rank, world):
         with torch.cuda.graph(gr, stream=s_cp):
             for i in range(args.steps):
                 body(i)
-        gr.replay()
+        with torch.cuda.stream(s_cp):
+            gr.replay()
         torch.cuda.synchronize(dev)
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(s_cp)
-        gr.replay()
-        c1.record(s_cp)
+        # a graph replays on the current stream: make it the one the events
+        # are recorded on, so they bracket the copies
+        with torch.cuda.stream(s_cp):
+            c0.record(s_cp)
+            gr.replay()
+            c1.record(s_cp)
         torch.cuda.synchronize(dev)
         return c0.elapsed_time(c1) * 1e3 / args.steps
 
@@ -372,9 +387,14 @@ def gpu_arm(args, rank, world):
     errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
     batched = batched_upkeep(args, dev, stream) if not args.no_batched else None
     legacy_us = legacy_upkeep_us(dev, stream) if not args.no_batched else None
-    return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, e2e_ms=e2e_ms, copy_us=copy_us,
+    proj = project_write_us(dev, stream) if not args.no_batched else None
+    del g_warm, g_timed, g_attn, g_write, g_delta, g_wfloor, g_dfloor, g_e2e
+    full_step = full_step_60_layers(dev, stream) if not args.no_batched else None
+    stress = stress_40_heads(dev, stream) if not args.no_batched else None
+    return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, wf_us=wf_us, df_us=df_us,
+                full_step=full_step, stress=stress, e2e_ms=e2e_ms, copy_us=copy_us,
                 clocks=clk.summary(),
-                batched=batched, legacy_us=legacy_us,
+                batched=batched, legacy_us=legacy_us, proj=proj,
                 resets=timed_resets,
                 levels=levels, device_errors=int(np.bitwise_or.reduce(errs)))
 
@@ -425,6 +445,176 @@ def batched_upkeep(args, dev, stream):
     return dict(write_us=w_us, delta_us=d_us)
 
 
+def full_step_60_layers(dev, stream):
+    """The full denoising step on one GPU: 60 layer rings of the production
+    shape, per step one 757-token write per layer (the cache upkeep) and 4
+    passes x 60 attention calls of 757 queries ("Where the Time Went": 4
+    passes through 60 blocks, 240 attention calls per step).  Upkeep,
+    attention and the whole step are each one CUDA graph, replayed; the 60
+    writes are also timed as one batched launch.  Inputs: per layer sigma_k,
+    sigma_v log-uniform in [0.25, 4] (seed 3), N(0,1) draws of a seeded CUDA
+    generator; 14.8 MB of cache per layer, so every call is L2-cold."""
+    import torch
+    import ring_kv_cache_gb300 as kv
+    from workloads import cuda_frame, cuda_generator, log_uniform
+    rng = np.random.default_rng(3)
+    with torch.cuda.stream(stream):
+        gen = cuda_generator(3, device=dev)
+        rings, frames = [], []
+        for _ in range(LAYERS):
+            sk, sv = log_uniform(rng, H, 0.25, 4.0), log_uniform(rng, H, 0.25, 4.0)
+            fr = [cuda_frame(gen, H, D, N_NEW, sk, sv, device=dev) for _ in range(2)]
+            ring = kv.KvRing(H, D, C, N_NEW, MAX_POS, 10000.0, max_kv_splits=8, stream=stream)
+            ring.calibrate(fr[0][1], fr[0][2], stream=stream)
+            for i in range(8):                     # 6,056 tokens: wrapped
+                ring.write(fr[i % 2][1], fr[i % 2][2], stream=stream)
+            rings.append(ring)
+            frames.append(fr)
+        outs = [torch.empty((N_Q, H, D), dtype=torch.float32, device=dev) for _ in range(4 * LAYERS)]
+    torch.cuda.synchronize(dev)
+
+    def upkeep():
+        for l in range(LAYERS):
+            rings[l].write(frames[l][0][1], frames[l][0][2], stream=stream)
+
+    def upkeep_batched():
+        kv.write_frames_many(rings, [f[0][1] for f in frames], [f[0][2] for f in frames], stream=stream)
+
+    def attention():
+        for p in range(4):
+            for l in range(LAYERS):
+                rings[l].attention(frames[l][p % 2][0], out=outs[4 * l + p], stream=stream)
+
+    def graph(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def timed(g, reps):
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    g_up, g_upb, g_at = graph(upkeep), graph(upkeep_batched), graph(attention)
+    g_step = graph(lambda: (upkeep(), attention()))
+    res = dict(upkeep_us=timed(g_up, 5), upkeep_batched_us=timed(g_upb, 5),
+               attention_us=timed(g_at, 3), step_us=timed(g_step, 3))
+    del g_up, g_upb, g_at, g_step, rings, frames, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def stress_40_heads(dev, stream):
+    """The stress workload's call: the whole unsharded head set (40 heads x
+    128) over a wrapped 5,788-slot ring, keys and values Student-t (3 degrees
+    of freedom) with per-head scales log-uniform in [0.1, 10] (seed 5), a
+    first frame of the seeded prompt length, then 757-token frames.  Four
+    rings round-robin (59 MB of cache each), one attention call of 757
+    queries (89.7 GFLOP) or one write (23.3 MB) per ring, as graphs of four
+    calls; the precision levels the rule chose are reported."""
+    import torch
+    import ring_kv_cache_gb300 as kv
+    from workloads import cuda_frame, cuda_generator, log_uniform, stress_prompt_length
+    HS, NR = 40, 4
+    rng = np.random.default_rng(5)
+    n0 = stress_prompt_length(5)
+    with torch.cuda.stream(stream):
+        gen = cuda_generator(5, device=dev)
+        rings, frames = [], []
+        for _ in range(NR):
+            sk, sv = log_uniform(rng, HS, 0.1, 10.0), log_uniform(rng, HS, 0.1, 10.0)
+            q0, k0, v0 = cuda_frame(gen, HS, D, n0, sk, sv, dist="student_t3", device=dev)
+            ring = kv.KvRing(HS, D, C, 2000, MAX_POS, 10000.0, max_kv_splits=8, stream=stream)
+            ring.calibrate(k0, v0, stream=stream)
+            ring.write(k0, v0, stream=stream)
+            fr = [cuda_frame(gen, HS, D, N_NEW, sk, sv, dist="student_t3", device=dev) for _ in range(2)]
+            for i in range(8):
+                ring.write(fr[i % 2][1], fr[i % 2][2], stream=stream)
+            rings.append(ring)
+            frames.append(fr)
+        outs = [torch.empty((N_Q, HS, D), dtype=torch.float32, device=dev) for _ in range(NR)]
+    torch.cuda.synchronize(dev)
+
+    def graph(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def timed(g, reps):
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / (reps * NR)
+
+    g_at = graph(lambda: [rings[i].attention(frames[i][0][0], out=outs[i], stream=stream) for i in range(NR)])
+    g_wr = graph(lambda: [rings[i].write(frames[i][1][1], frames[i][1][2], stream=stream) for i in range(NR)])
+    a_us, w_us = timed(g_at, 4), timed(g_wr, 8)
+    lv = np.concatenate([r.levels().cpu().numpy()[: (N_Q + 127) // 128].ravel() for r in rings])
+    flops = 4.0 * HS * N_Q * C * D
+    wbytes = 2 * N_NEW * HS * D * 2 + 2 * N_NEW * HS * D + N_NEW * 4
+    q_terms = lv.astype(np.float64)
+    pv = np.where(lv >= 4, 2.0, 1.0)            # PV MMAs per tile in f16 (two at level 4)
+    issued = float(np.mean(q_terms + 2.0 * pv)) / 2.0
+    del g_at, g_wr, rings, frames, outs
+    torch.cuda.empty_cache()
+    return dict(attention_us=a_us, attention_tflops=flops / (a_us * 1e-6) / 1e12, flops_per_call=flops,
+                write_us=w_us, write_gbs=wbytes / (w_us * 1e-6) / 1e9, write_bytes=wbytes,
+                levels={str(k): int((lv == k).sum()) for k in (1, 2, 3, 4)},
+                issued_mma_over_algorithmic=issued, prompt_tokens=n0)
+
+
+D_MODEL = 5120                       # 40 heads x 128 (the model's width; 10 heads per GPU)
+
+
+def project_write_us(dev, stream):
+    """kvring_project_write at the production shape: a 757-token frame's
+    x [757, 5,120] times W [3,840, 5,120] (29.8 GFLOP), keys and values
+    written into the ring in the epilogue, queries stored.  Four rings with
+    their own weights round-robin (4 x 39 MB of weights), so each call's
+    weights are L2-cold; a CUDA graph of the four calls, replayed."""
+    import torch
+    import ring_kv_cache_gb300 as kv
+    with torch.cuda.stream(stream):
+        g = torch.Generator(device=dev)
+        g.manual_seed(13)
+        rings = [kv.KvRing(H, D, C, N_NEW, MAX_POS, 10000.0, max_kv_splits=1, stream=stream) for _ in range(4)]
+        ws = [(torch.randn((3 * H * D, D_MODEL), generator=g, device=dev) * 0.015).bfloat16() for _ in range(4)]
+        xs = [torch.randn((N_NEW, D_MODEL), generator=g, device=dev).bfloat16() for _ in range(4)]
+        for r, x, w in zip(rings, xs, ws):
+            _, kvo = r.project_write(x, w, write=False, store_kv=True, stream=stream)
+            r.calibrate(kvo[0], kvo[1], stream=stream)
+        torch.cuda.synchronize(dev)
+        qs = [torch.empty((N_NEW, H, D), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for r, x, w, q in zip(rings, xs, ws, qs):
+                r.project_write(x, w, q_out=q, stream=stream)
+        gr.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 8
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / (reps * 4)
+    flops = 2.0 * N_NEW * 3 * H * D * D_MODEL
+    return us, flops
+
+
 def legacy_upkeep_us(dev, stream):
     """The upkeep the ring replaced, per call with a full 5,788-slot window:
     window copy, RoPE of every cached key, window scales, re-quantisation of
@@ -473,19 +663,15 @@ def reduce_max(x: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------------------
-def cpu_step(ring_state, tokens: int, queries: int):
-    """One bounded sample of a step on the CPU oracle: write `tokens` of the
-    frame and attend `queries` of the queries; returns seconds scaled to the
-    full 757-token write + 757-query attention."""
-    from oracle.attention import attention_exact
-    orc, fr = ring_state
-    q, k, v = fr
-    t0 = time.perf_counter()
-    orc.write(k[:tokens], v[:tokens])
-    t1 = time.perf_counter()
-    attention_exact(orc, q[:queries], np.arange(orc.next_pos - queries, orc.next_pos))
-    t2 = time.perf_counter()
-    return (t1 - t0) * N_NEW / tokens + (t2 - t1) * N_Q / queries
+# The CPU oracle (float64 NumPy, the test oracle) timed on this host, one
+# sample recipe for both the default run's cpu_baseline and the reference
+# arm.  A full step on the oracle takes seconds, so each sample is bounded
+# and extrapolated: a write of SAMPLE_TOKENS tokens scaled to 757 (its cost
+# is linear in the tokens), and attention of SAMPLE_Q[0] and SAMPLE_Q[1]
+# queries, fitted as a fixed part (dequantising the whole cache, paid once
+# per call) plus a per-query part, then evaluated at 757 queries.
+SAMPLE_TOKENS = 64
+SAMPLE_Q = (8, 64)
 
 
 def cpu_setup():
@@ -497,7 +683,32 @@ def cpu_setup():
     for q, k, v in fr[:8]:
         orc.write(f32_from_bf16(k), f32_from_bf16(v))
     q, k, v = fr[8]
-    return orc, (f32_from_bf16(q), f32_from_bf16(k), f32_from_bf16(v))
+    st = orc, (f32_from_bf16(q), f32_from_bf16(k), f32_from_bf16(v))
+    cpu_sample(st)          # untimed: the first attention call pays one-time costs
+    return st
+
+
+def cpu_sample(st):
+    """One bounded sample of a step on the oracle; returns the extrapolated
+    seconds of the full 757-token write, of the full 757-query attention, and
+    the process CPU seconds and wall seconds the sample took."""
+    from oracle.attention import attention_exact
+    orc, (q, k, v) = st
+    c0, w0 = os.times(), time.perf_counter()
+    t0 = time.perf_counter()
+    orc.write(k[:SAMPLE_TOKENS], v[:SAMPLE_TOKENS])
+    t1 = time.perf_counter()
+    ta = []
+    for nq in SAMPLE_Q:
+        ts = time.perf_counter()
+        attention_exact(orc, q[:nq], np.arange(orc.next_pos - nq, orc.next_pos))
+        ta.append(time.perf_counter() - ts)
+    per_q = max((ta[1] - ta[0]) / (SAMPLE_Q[1] - SAMPLE_Q[0]), 0.0)
+    fixed = max(ta[0] - per_q * SAMPLE_Q[0], 0.0)
+    c1, w1 = os.times(), time.perf_counter()
+    cpu = (c1.user - c0.user) + (c1.system - c0.system)
+    return dict(write_s=(t1 - t0) * N_NEW / SAMPLE_TOKENS, attn_s=fixed + per_q * N_Q, attn_fixed_s=fixed,
+                cpu_s=cpu, wall_s=w1 - w0)
 
 
 def cpu_cores() -> int:
@@ -507,38 +718,87 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(budget_s: float = 15.0):
+def blas_threads():
+    """The BLAS thread count NumPy would use (the oracle's einsum and
+    elementwise work do not go through BLAS, so it runs on one core)."""
+    try:
+        import threadpoolctl
+        info = [x for x in threadpoolctl.threadpool_info() if x.get("user_api") == "blas"]
+        if info:
+            return int(info[0]["num_threads"])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return None
+
+
+def sample_text(n):
+    return (f"{n} samples; each writes {SAMPLE_TOKENS} tokens into the wrapped 5,788-slot ring "
+            f"(10 heads x 128), scaled x757/{SAMPLE_TOKENS}, and attends {SAMPLE_Q[0]} and {SAMPLE_Q[1]} "
+            f"queries, fitted as fixed + per-query cost and evaluated at 757 queries; mean")
+
+
+def summarise_samples(xs):
+    step = [x["write_s"] + x["attn_s"] for x in xs]
+    cpu, wall = sum(x["cpu_s"] for x in xs), sum(x["wall_s"] for x in xs)
+    return dict(step_us=float(np.mean(step)) * 1e6, write_us=float(np.mean([x["write_s"] for x in xs])) * 1e6,
+                attention_us=float(np.mean([x["attn_s"] for x in xs])) * 1e6,
+                attention_fixed_us=float(np.mean([x["attn_fixed_s"] for x in xs])) * 1e6,
+                threads_used=max(1, int(round(cpu / wall))) if wall > 0 else 1)
+
+
+def cpu_single_threaded_parts(st):
+    """Measured whole, on one core: the full 757-token write, and the delta
+    rotation of the full window (after an untimed rotation by 0, which leaves
+    the codes as they are, so one-time set-up is not counted)."""
+    orc, (q, k, v) = st
+    t0 = time.perf_counter()
+    orc.write(k, v)
+    t1 = time.perf_counter()
+    orc.delta_rotate(0)
+    t2 = time.perf_counter()
+    orc.delta_rotate()
+    t3 = time.perf_counter()
+    return dict(write_757_us=(t1 - t0) * 1e6, delta_full_window_us=(t3 - t2) * 1e6)
+
+
+def cpu_baseline(budget_s: float = 12.0):
     st = cpu_setup()
-    secs = []
+    xs = []
     t_end = time.perf_counter() + budget_s
-    while time.perf_counter() < t_end or not secs:
-        secs.append(cpu_step(st, 64, 16))
-    us = float(np.median(secs)) * 1e6
-    return {"value": us, "unit": "µs", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{len(secs)} samples of a 64-token write + 16-query attention over the "
-                      f"wrapped 5,788-slot ring (10 heads x 128), scaled x757/64 and x757/16; median"}
+    while time.perf_counter() < t_end or not xs:
+        xs.append(cpu_sample(st))
+    sm = summarise_samples(xs)
+    return {"value": sm["step_us"], "unit": "µs", "cores": sm["threads_used"], "kind": "oracle",
+            "extrapolated": True, "sample": sample_text(len(xs)),
+            "affinity_cores": cpu_cores(), "blas_threads": blas_threads(),
+            "parts_us": {"write": sm["write_us"], "attention": sm["attention_us"],
+                         "attention_fixed": sm["attention_fixed_us"]},
+            "single_threaded": cpu_single_threaded_parts(st)}
 
 
 def reference_arm(args, rank, world):
     if rank != 0:
         return
     st = cpu_setup()
-    tokens, queries = (8, 1) if args.steps > 50 else (64, 8)
     for _ in range(args.warmup):
-        cpu_step(st, tokens, queries)
-    secs = [cpu_step(st, tokens, queries) for _ in range(args.steps)]
-    us = float(np.mean(secs)) * 1e6
+        cpu_sample(st)
+    xs = [cpu_sample(st) for _ in range(args.steps)]
+    sm = summarise_samples(xs)
+    us = sm["step_us"]
     line = {
         "metric": METRIC, "value": us, "unit": "µs", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "impl": "reference",
-        "config": {"workload": "production-shaped call: 757-token write + 757-query attention over a "
-                               "wrapped 5,788-slot ring, 10 heads x 128",
-                   "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": us, "unit": "µs", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"each step writes {tokens} tokens and attends {queries} queries, "
-                                   f"scaled to 757 and 757"},
+        "impl": "reference", "extrapolated": True,
+        "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": us, "unit": "µs", "cores": sm["threads_used"], "kind": "oracle",
+                         "extrapolated": True, "sample": sample_text(len(xs)) + " (one sample per step)",
+                         "affinity_cores": cpu_cores(), "blas_threads": blas_threads(),
+                         "parts_us": {"write": sm["write_us"], "attention": sm["attention_us"],
+                                      "attention_fixed": sm["attention_fixed_us"]}},
         "e2e": {"value": us, "unit": "µs", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -584,10 +844,10 @@ def main():
     w_us, a_us, d_us = res["w_us"], res["a_us"], res["d_us"]
     fp8_peak = 2.0 * peaks["bf16"]            # FP8 dense = 2 x bf16 (nominal 4.5 / 2.25 PF)
     lv = res["levels"]
-    q_terms = np.where(lv >= 3, 3, np.where(lv >= 2, 2, 1))
     # issued tensor work relative to the algorithmic 2 FP8 units (QK, PV) per
-    # tile: one FP8 QK per query term, and PV in f16 at half the FP8 rate
-    issued = float(np.mean(q_terms + 2.0)) / 2.0
+    # tile: one FP8 QK per query term (the level), and PV in f16 at half the
+    # FP8 rate (two PV MMAs at level 4)
+    issued = float(np.mean(lv + 2.0 * np.where(lv >= 4, 2.0, 1.0))) / 2.0
     attn_tflops = ATTN_FLOPS / (a_us * 1e-6) / 1e12
     write_gbs = WRITE_BYTES / (w_us * 1e-6) / 1e9
     traffic = attention_traffic()
@@ -605,8 +865,7 @@ def main():
         "dtype": "e4m3",
         "data": "synthetic",
         "config": {
-            "workload": "production-shaped call: 757-token write + 757-query attention over a "
-                        "wrapped 5,788-slot ring, 10 heads x 128 (E4M3 cache, bf16 in, fp32 out)",
+            "workload": WORKLOAD,
             "heads": H, "head_dim": D, "capacity": C, "tokens_per_write": N_NEW, "queries": N_Q,
             "l2": f"cold: {RINGS} rings and input frames round-robin, >126 MB between reuses",
             "launch": "the K timed steps (write + attention of one ring each) as one CUDA graph, one replay",
@@ -627,18 +886,41 @@ def main():
             "issued_frac": attn_tflops * issued / fp8_peak,
             "algorithmic_flops_per_launch": ATTN_FLOPS,
             "avg_launch_us": a_us,
-            "precision_levels": {str(k): int((lv == k).sum()) for k in (1, 2, 3)},
+            "precision_levels": {str(k): int((lv == k).sum()) for k in (1, 2, 3, 4)},
         },
         "kernels": {
             "write": {"avg_launch_us": w_us, "algorithmic_bytes": WRITE_BYTES, "GB/s": write_gbs,
-                      "frac_hbm": write_gbs / peaks["hbm"], "peak_gbs": peaks["hbm"]},
+                      "frac_hbm": write_gbs / peaks["hbm"], "peak_gbs": peaks["hbm"],
+                      "floor_us": res["wf_us"],
+                      "floor_note": "same grid, launch, wait, state read, ticket and publication, no data "
+                                    "(kvring_debug_write_floor)"},
             "attention": {"avg_launch_us": a_us, "TFLOP/s": attn_tflops,
                           "cache_GB/s": ATTN_BYTES / (a_us * 1e-6) / 1e9,
                           "note": "one call = one attention kernel (query prologue fused)"},
             "delta_rotate": {"avg_launch_us": d_us, "algorithmic_bytes": DELTA_BYTES,
                              "GB/s": DELTA_BYTES / (d_us * 1e-6) / 1e9,
-                             "frac_hbm": DELTA_BYTES / (d_us * 1e-6) / 1e9 / peaks["hbm"]},
+                             "frac_hbm": DELTA_BYTES / (d_us * 1e-6) / 1e9 / peaks["hbm"],
+                             "floor_us": res["df_us"],
+                             "floor_note": "the same launch with delta 0 (no rows move)"},
+            **({} if res["full_step"] is None else {"full_step_60_layers": {
+                **res["full_step"],
+                "upkeep_GB/s": LAYERS * WRITE_BYTES / (res["full_step"]["upkeep_us"] * 1e-6) / 1e9,
+                "attention_TFLOP/s": CALLS_PER_STEP * ATTN_FLOPS / (res["full_step"]["attention_us"] * 1e-6) / 1e12,
+                "note": "60 layer rings; per step 60 writes (upkeep; also as one batched launch) and 4 x 60 "
+                        "attention calls, each set one CUDA graph; step = both in one graph"}}),
+            **({} if res["stress"] is None else {"stress_40_heads": {
+                **res["stress"],
+                "attention_frac_fp8": res["stress"]["attention_tflops"] / fp8_peak,
+                "note": "40 heads x 128, Student-t (3 dof) keys and values, scales log-uniform in [0.1, 10]; "
+                        "per call over a wrapped 5,788-slot ring, four rings round-robin"}}),
             "timing": "per-kernel: CUDA graphs of 16 back-to-back calls on 16 rings, events around replays",
+            **({} if res["proj"] is None else {
+                "project_write": {
+                    "avg_launch_us": res["proj"][0], "algorithmic_flops": res["proj"][1],
+                    "TFLOP/s": res["proj"][1] / (res["proj"][0] * 1e-6) / 1e12,
+                    "frac_bf16": res["proj"][1] / (res["proj"][0] * 1e-6) / 1e12 / peaks["bf16"],
+                    "note": "kvring_project_write: 757 x 5,120 x 3,840 bf16 projection (fp32 sums) "
+                            "with the ring write in its epilogue"}}),
             **({} if res["legacy_us"] is None else {
                 "legacy_upkeep": {
                     "avg_call_us": res["legacy_us"], "algorithmic_bytes": LEGACY_BYTES,

@@ -175,6 +175,35 @@ kvring_status kvring_write_frame(kvring_t* ring, const void* k_bf16, const void*
  * Errors: INVALID_ARG (delta < -1 or >= max_position). */
 kvring_status kvring_delta_rotate(kvring_t* ring, int32_t delta, void* stream);
 
+/* ------------------------------------------------------------------------
+ * QKV projection with the cache write in its epilogue ("fused pre-attention
+ * kernels", section "Judging Quality When Pixels Can't": the projection,
+ * RoPE and FP8 quantisation in front of the attention, fused).
+ *
+ * y = x W^T for one frame: x bf16 [n][d_model] (the block's input rows), W
+ * bf16 [3 * num_heads * head_dim][d_model] (a linear layer's weight: output
+ * rows by input columns; rows [0, H*d) make the queries, [H*d, 2*H*d) the
+ * keys, [2*H*d, 3*H*d) the values).  Summed in fp32 on the tensor cores and
+ * rounded once to bf16 (the projection's output format); then
+ *   - queries: stored to q_out bf16 [n][num_heads][head_dim] (NULL = not
+ *     stored), what kvring_attention takes;
+ *   - with KVRING_PROJECT_WRITE: keys and values written into the ring
+ *     exactly as kvring_write_frame(k, v, pos, n) writes those bf16 values
+ *     (same positions, slots, state advance, error word); needs a
+ *     calibrated ring and n <= capacity - pinned_prefix;
+ *   - with KVRING_PROJECT_STORE_KV: keys and values also stored to kv_out
+ *     bf16 [2][n][num_heads][head_dim] (keys first), e.g. to calibrate a new
+ *     session's scales from its first frame.
+ * d_model is a multiple of 64 (at least 64); n <= max_tokens.  An fp32
+ * tensor-core sum may round to a bf16 one step away from the exactly rounded
+ * sum when that sum lies that close to a rounding midpoint.
+ * ------------------------------------------------------------------------ */
+#define KVRING_PROJECT_WRITE 1
+#define KVRING_PROJECT_STORE_KV 2
+kvring_status kvring_project_write(kvring_t* ring, const void* x, const void* w, int32_t d_model,
+                                   const int32_t* pos, int32_t n, void* q_out, void* kv_out,
+                                   int32_t flags, void* stream);
+
 /* The cache upkeep the ring replaced, kept as the comparison path ("Where
  * the Time Went": before the ring, every attention call re-applied RoPE to
  * every cached key, re-quantised the cache to FP8 and shifted the window by

@@ -23,7 +23,7 @@ __all__ = [
     "kvring_required_bytes", "kvring_create", "kvring_destroy", "kvring_calibrate_scales",
     "kvring_write_frame", "kvring_delta_rotate", "kvring_attention", "kvring_attention_noalloc",
     "kvring_write_frames_many", "kvring_delta_rotate_many", "write_frames_many", "delta_rotate_many",
-    "kvring_legacy_upkeep", "LegacyWindows",
+    "kvring_legacy_upkeep", "LegacyWindows", "kvring_project_write",
     "kvring_export",
     "kvring_status_string", "encode_e4m3", "STATE",
 ]
@@ -38,6 +38,7 @@ STATE = dict(head=0, n_valid=1, total_lo=2, total_hi=3, next_pos=4, calibrated=5
              last_delta=7)
 STATE_WORDS = 8
 DEVERR_POSITION, DEVERR_TIMEOUT, DEVERR_DELTA = 1, 2, 4
+PROJECT_WRITE, PROJECT_STORE_KV = 1, 2
 
 
 class KvringConfig(ctypes.Structure):
@@ -92,6 +93,7 @@ def lib():
         "kvring_delta_rotate_many": (i32, [vp, i32, i32, vp]),
         "kvring_attention": (i32, [vp, vp, vp, i32, vp, i32, vp]),
         "kvring_attention_noalloc": (i32, [vp, vp, vp, i32, vp, i32, vp]),
+        "kvring_project_write": (i32, [vp, vp, vp, i32, vp, i32, vp, vp, i32, vp]),
         "kvring_export": (i32, [vp, vp, vp, vp, vp, vp, vp]),
         "kvring_debug_encode_e4m3": (i32, [vp, vp, i64, vp]),
         "kvring_debug_attention_levels": (i32, [vp, vp, vp]),
@@ -291,6 +293,11 @@ def kvring_attention_noalloc(handle, q, qpos, n_q, out, out_dtype, stream_ptr) -
                                           int(out_dtype), stream_ptr), "kvring_attention_noalloc")
 
 
+def kvring_project_write(handle, x, w, d_model, pos, n, q_out, kv_out, flags, stream_ptr) -> None:
+    _check(lib().kvring_project_write(handle, _ptr(x), _ptr(w), int(d_model), _ptr(pos), int(n), _ptr(q_out),
+                                      _ptr(kv_out), int(flags), stream_ptr), "kvring_project_write")
+
+
 def kvring_export(handle, k_out, v_out, scales, slot_pos, state, stream_ptr) -> None:
     _check(lib().kvring_export(handle, _ptr(k_out), _ptr(v_out), _ptr(scales), _ptr(slot_pos),
                                _ptr(state), stream_ptr), "kvring_export")
@@ -372,6 +379,40 @@ class KvRing:
             kvring_attention(self.handle, q, qpos, n, out,
                              OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32, self._s(stream))
         return out
+
+    def project_write(self, x, w, pos=None, write=True, store_kv=False, q_out=None, kv_out=None,
+                      stream=None):
+        """QKV projection of one frame with the cache write fused in
+        (kvring_project_write): x bf16 [n, d_model], w bf16 [3 H d, d_model]
+        (a linear layer's weight); returns (q_out bf16 [n, H, d], kv_out bf16
+        [2, n, H, d] or None).  With ``write`` the keys and values enter the
+        ring as kvring_write_frame would write them; ``store_kv`` also returns
+        them (e.g. to calibrate a session from its first frame)."""
+        for t, name in ((x, "x"), (w, "w")):
+            if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 2 \
+                    or not t.is_contiguous() or t.device != self.device:
+                raise ValueError(f"{name} must be a contiguous 2-D bfloat16 tensor on {self.device}")
+        n, dm = x.shape
+        if dm < 64 or dm % 64:
+            raise ValueError("d_model must be a positive multiple of 64")
+        if tuple(w.shape) != (3 * self.H * self.d, dm):
+            raise ValueError(f"w must have shape [{3 * self.H * self.d}, {dm}], got {tuple(w.shape)}")
+        if pos is not None or (write and self.three_d):
+            pos = _positions(pos, n, "pos", self.three_d, self.device)
+        if q_out is None:
+            q_out = torch.empty((n, self.H, self.d), dtype=torch.bfloat16, device=self.device)
+        _tokens(q_out, self.H, self.d, "q_out", self.device)
+        if store_kv:
+            if kv_out is None:
+                kv_out = torch.empty((2, n, self.H, self.d), dtype=torch.bfloat16, device=self.device)
+            if kv_out.dtype != torch.bfloat16 or tuple(kv_out.shape) != (2, n, self.H, self.d) \
+                    or not kv_out.is_contiguous() or kv_out.device != self.device:
+                raise ValueError("kv_out must be a contiguous bfloat16 tensor [2, n, H, d] on the ring's device")
+        flags = (PROJECT_WRITE if write else 0) | (PROJECT_STORE_KV if store_kv else 0)
+        with torch.cuda.device(self.device):
+            kvring_project_write(self.handle, x, w, dm, pos, n, q_out, kv_out if store_kv else None, flags,
+                                 self._s(stream))
+        return q_out, (kv_out if store_kv else None)
 
     def export(self, stream=None) -> dict:
         """Device copies of the cache, scales, positions and state (stream-ordered)."""

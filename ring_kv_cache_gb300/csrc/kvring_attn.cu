@@ -473,14 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two warps and neither waits behind the other's issue (a single thread
     // needs longer to issue an M = 128, N = 128 MMA than the tensor core
     // needs to run it).
-    if (lane == 0) {
-      // Level 4 cycles the K tiles through two stages (the third holds the
-      // fourth query term) and issues two PV MMAs per tile (hi, then lo
-      // probabilities, from the group's S/P region).
-      const bool l4 = misc->level == 4;   // the prologue ended with a CTA barrier
-      auto kst = [&](int j) { return l4 ? (j & 1) : (j % kStages); };
-      auto kph = [&](int j) { return l4 ? ((j >> 1) & 1) : ((j / kStages) & 1); };
-      const int nks = l4 ? 2 : kStages;
+    // Level 4 cycles the K tiles through two stages (the third holds the
+    // fourth query term) and issues two PV MMAs per tile (hi, then lo
+    // probabilities, from the group's S/P region); the loop is instantiated
+    // for levels 1-3 and for level 4 so that both keep constant stage math.
+    auto producer = [&](auto level4) {
+      constexpr bool l4 = decltype(level4)::value;
+      constexpr int nks = l4 ? 2 : kStages;   // K stages in use
+      auto kst = [](int j) { return j % nks; };
+      auto kph = [](int j) { return (j / nks) & 1; };
       constexpr uint32_t idesc_pv = idesc_f16(128, D, true);
       // f16 V: 128B-swizzled MN-major atoms of 64 columns x 8 rows (1024 B
       // apart along the slots); the second 64 columns one atom column further
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1;
         tc_fence_after();
         const uint32_t vl = v_lo + (uint32_t)b * kVhStep;
-        if (!l4) {
+        if constexpr (!l4) {
           const uint32_t pa = tmem + L::kColP + 64u * b;
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
@@ -560,11 +561,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and every PV this thread issued has finished before TMEM is freed
       mma_commit(bar(L::kBarPvIssuerDone));
       mbar_wait_bounded(bar(L::kBarPvIssuerDone), 0, &no_abort, wait_ns);
+    };
+    if (lane == 0) {   // the prologue ended with a CTA barrier: the level is known
+      if (misc->level == 4) producer(std::true_type{});
+      else producer(std::false_type{});
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- QK issuer
-    if (lane == 0 && ntiles > 0) {
+    auto qk_issuer = [&](auto level4) {
+      constexpr bool l4 = decltype(level4)::value;
       constexpr uint32_t idesc_qk = idesc_e4m3(128, 128, false);
       // Descriptors are built once; per MMA only the low word (start address
       // in 16-byte units) moves: +2 per 32-byte k-step of a K-major tile.
@@ -573,7 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, kq_hi = (uint32_t)(dq >> 32);
       constexpr uint32_t kKVStep = L::kKVTile >> 4;
       const int n_qterms = misc->level;   // the prologue ended with a CTA barrier
-      const bool l4 = n_qterms == 4;
       // The debug stall: a wait that nothing ends, so that the bounded wait
       // gives up and the whole CTA takes its abort path.
       const bool go = !prm.debug_stall || mbar_wait_bounded(bar(L::kBarNever), 0, abort, wait_ns);
@@ -583,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // probabilities from it.  The K stage is freed by the commit.
       for (int j = 0; go && j < ntiles; ++j) {
         const int s = l4 ? (j & 1) : j % kStages;
-        if (l4) {
+        if constexpr (l4) {
           if (j > 1 && !mbar_wait_bounded(bar(L::kBarPvDone + (j & 1)), ((j - 2) >> 1) & 1, abort, wait_ns)) break;
         } else {
           if (j > 0 && !mbar_wait_bounded(bar(L::kBarSFree), (j - 1) & 1, abort, wait_ns)) break;
@@ -594,8 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kl = k_lo + s * kKVStep;
         const uint32_t dst = l4 ? tmem + L::kColSP4 * (j & 1) : tmem + L::kColS;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (t < n_qterms) {
+        for (int t = 0; t < (l4 ? 4 : 3); ++t) {
+          if (l4 || t < n_qterms) {
             const uint32_t qt_lo = q_lo + (uint32_t)((L::q_term(t) - L::kQ) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk)
@@ -605,6 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(L::kBarSFull + (j & 1)));
         mma_commit(bar(L::kBarKEmpty + s));   // the K stage is read
       }
+    };
+    if (lane == 0 && ntiles > 0) {
+      if (misc->level == 4) qk_issuer(std::true_type{});
+      else qk_issuer(std::false_type{});
     }
     if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
       mma_commit(bar(L::kBarMmaDone));

@@ -21,6 +21,7 @@
 // fused multiply-add), the cos/sin table is fp32 built on the host, and the
 // E4M3 conversion is the hardware round-to-nearest-even saturating cvt.
 #include "kvring_internal.cuh"
+#include <cuda_bf16.h>
 
 namespace kvr {
 namespace {
@@ -993,6 +994,270 @@ __global__ void k_encode(const float* __restrict__ in, uint8_t* __restrict__ out
   }
 }
 
+// ------------------------------------------------------------ projection ---
+// The QKV projection y = x W^T of one frame (bf16 activations [n][dm], bf16
+// weights [3 H D][dm] in a linear layer's output-by-input layout), summed in
+// fp32 on the tensor cores and rounded once to bf16, with the rest of the
+// "fused pre-attention" work in its epilogue: query rows stored as bf16 for
+// the attention call, key rows rotated (the write's pinned RoPE), scaled and
+// quantised into their ring slots, value rows scaled and quantised, the slot
+// positions set and the ring state advanced by the last CTA -- byte for byte
+// what kvring_write_frame does with the same bf16 keys and values.
+//
+// One CTA per 128 tokens x 256 output columns (two heads of 128 of one kind,
+// or four of 64): a 4-stage TMA pipeline of 64-wide reduction slices (A 16 KB
+// + B 32 KB), one thread loading, one thread issuing M128 N256 K16 bf16 MMAs
+// (66 ns each, longer than one thread's issue cost), the accumulator in 256
+// TMEM columns, and all four warps in the epilogue with one token row per
+// thread.
+constexpr int kPjThreads = 128;
+constexpr int kPjBM = 128, kPjBN = 256, kPjBK = 64;
+constexpr int kPjStages = 4;
+constexpr int kPjABytes = kPjBM * kPjBK * 2;
+constexpr int kPjBBytes = kPjBN * kPjBK * 2;
+constexpr int kPjStageBytes = kPjABytes + kPjBBytes;
+constexpr int kPjMiscBytes = 256;
+constexpr int kPjSmem = kPjStages * kPjStageBytes + kPjMiscBytes + 1024;   // + alignment slack
+constexpr uint64_t kPjWaitNs = 1000000000ull;
+static_assert(kPjSmem <= 227 * 1024, "shared memory per CTA");
+
+enum : int { PJ_WRITE = 1, PJ_STORE_KV = 2 };
+
+struct ProjParams {
+  RingDev r;
+  const int32_t* pos;   // [n] or [n][3], or null (next position + t)
+  uint16_t* q_out;      // [n][H][D] bf16, or null
+  uint16_t* kv_out;     // [2][n][H][D] bf16 (keys, values), or null
+  int n, dm, flags;
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(mbar)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], bf16 x bf16 -> fp32.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// kind::f16 instruction descriptor with bf16 A and B (type code 1), both
+// K-major, and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float f) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return (uint32_t)(*reinterpret_cast<const uint16_t*>(&b));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPjThreads, 1)
+    k_project(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+              const ProjParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bars = sbase + kPjStages * kPjStageBytes;   // full[S], empty[S], accumulator
+  auto full = [&](int s) -> uint32_t { return bars + 8u * (uint32_t)s; };
+  auto empty = [&](int s) -> uint32_t { return bars + 8u * (uint32_t)(kPjStages + s); };
+  const uint32_t acc_bar = bars + 8u * (2 * kPjStages);
+  int* misc = reinterpret_cast<int*>(sm + kPjStages * kPjStageBytes + 8 * (2 * kPjStages + 1));
+  // misc: [0] TMEM base, [1] abort, [2] head, [3] next position, [4] slices issued, [5] slices consumed
+  volatile int* abort = misc + 1;
+
+  const RingDev& r = prm.r;
+  const int warp = threadIdx.x >> 5;
+  const int m0 = blockIdx.x * kPjBM, n0 = blockIdx.y * kPjBN;
+  const int KB = prm.dm / kPjBK;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmW);
+    for (int s = 0; s < kPjStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_bar, 1);
+    misc[1] = 0;
+    misc[4] = 0;
+    misc[5] = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    __syncwarp();                                  // warp-collective allocation
+    tmem_alloc(smem_u32(misc), kPjBN);
+    tmem_relinquish();
+  }
+  // The activations come from the preceding kernel; the ring as well.
+  griddep_wait();
+  if (threadIdx.x == 0) {
+    misc[2] = __ldcg(r.state + ST_HEAD);
+    misc[3] = __ldcg(r.state + ST_NEXT_POS);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_launch_dependents();
+  const uint32_t tmem = (uint32_t)misc[0];
+
+  if (threadIdx.x == 0) {
+    // ------------------------------------------------------ TMA producer
+    int kb = 0;
+    for (; kb < KB; ++kb) {
+      const int s = kb % kPjStages;
+      if (kb >= kPjStages && !mbar_wait_bounded(empty(s), (uint32_t)((kb / kPjStages) - 1) & 1u, abort, kPjWaitNs))
+        break;
+      const uint32_t dst = sbase + (uint32_t)s * kPjStageBytes;
+      mbar_arrive_expect_tx(full(s), (uint32_t)kPjStageBytes);
+      tma_load_2d(dst, &tmX, kb * kPjBK, m0, full(s));
+      tma_load_2d(dst + kPjABytes, &tmW, kb * kPjBK, n0, full(s));
+    }
+    misc[4] = kb;
+  } else if (threadIdx.x == 32) {
+    // ------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(kPjBM, kPjBN);
+    int kb = 0;
+    for (; kb < KB; ++kb) {
+      const int s = kb % kPjStages;
+      if (!mbar_wait_bounded(full(s), (uint32_t)(kb / kPjStages) & 1u, abort, kPjWaitNs)) break;
+      tc_fence_after();
+      const uint32_t a = sbase + (uint32_t)s * kPjStageBytes;
+      const uint64_t da = smem_desc(a, 16, 1024, 2u);
+      const uint64_t db = smem_desc(a + kPjABytes, 16, 1024, 2u);
+#pragma unroll
+      for (int kk = 0; kk < kPjBK / 16; ++kk)          // 16 bf16 = 32 bytes per step
+        mma_bf16(tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+      mma_commit(empty(s));
+    }
+    misc[5] = kb;
+    mma_commit(acc_bar);   // arrives once every MMA issued above has completed
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------ epilogue
+  // every thread waits for the accumulator; the decision to run the epilogue
+  // is taken after a CTA barrier, so it is the same in every warp (the TMEM
+  // loads are warp-collective)
+  mbar_wait_bounded(acc_bar, 0u, abort, kPjWaitNs);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const bool acc_ok = !*abort;
+  const int H = r.H, C = r.C;
+  const int tok = m0 + (int)threadIdx.x;          // TMEM lane = accumulator row = token
+  const bool write = (prm.flags & PJ_WRITE) != 0, store_kv = (prm.flags & PJ_STORE_KV) != 0;
+  const int head0 = misc[2], next0 = misc[3];
+  constexpr int HPT = kPjBN / D;                  // heads per tile
+  if (acc_ok) {
+#pragma unroll 1
+    for (int sub = 0; sub < HPT; ++sub) {
+      const int blk = blockIdx.y * HPT + sub;       // column block: kind * H + head
+      if (blk >= 3 * H) break;                      // CTA-uniform
+      const int kind = blk / H, h = blk % H;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t acc[32];
+        __syncwarp();
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(sub * D + c * 32), acc);
+        tmem_wait_ld();
+        if (tok >= prm.n) continue;
+        // the projection's bf16 outputs, and their fp32 values
+        uint32_t w16[16];
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          w16[i] = bf16_bits_rn(__uint_as_float(acc[2 * i])) | (bf16_bits_rn(__uint_as_float(acc[2 * i + 1])) << 16);
+          x[2 * i] = __uint_as_float(w16[i] << 16);
+          x[2 * i + 1] = __uint_as_float(w16[i] & 0xFFFF0000u);
+        }
+        const uint4 o[4] = {make_uint4(w16[0], w16[1], w16[2], w16[3]), make_uint4(w16[4], w16[5], w16[6], w16[7]),
+                            make_uint4(w16[8], w16[9], w16[10], w16[11]),
+                            make_uint4(w16[12], w16[13], w16[14], w16[15])};
+        if (kind == 0) {
+          if (prm.q_out) {
+            uint4* dst = reinterpret_cast<uint4*>(prm.q_out + ((size_t)tok * H + h) * D + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = o[i];
+          }
+          continue;
+        }
+        if (store_kv) {
+          uint4* dst = reinterpret_cast<uint4*>(prm.kv_out + (((size_t)(kind - 1) * prm.n + tok) * H + h) * D + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = o[i];
+        }
+        if (!write) continue;
+        // the write's arithmetic on two 16-value chunks (a head's row is in slot
+        // head0 + tok, past the prefix after a wrap)
+        int slot = head0 + tok;
+        if (slot >= C) slot -= C - r.P;
+        const float inv = r.scales[(kind == 2 ? 3 : 2) * H + h];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int chunk = 2 * c + half;
+          float y[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = x[16 * half + i];
+          bool ok = true;
+          if (kind == 1) {
+            const int p = prm.pos ? rope_pos(r, prm.pos, tok, 8 * chunk) : next0 + tok;
+            if (p < 0 || p >= r.max_pos) {
+              ok = false;
+              atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+            } else {
+              float4 cs[4];
+              load_table16(r.table, D, p, chunk, cs);
+              rope_pinned(y, cs);
+            }
+            if (h == 0 && chunk == 0) r.slot_pos[slot] = p;
+          }
+          if (ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], inv);
+            *reinterpret_cast<uint4*>((kind == 2 ? r.v : r.k) + ((size_t)h * C + slot) * D + chunk * 16) =
+                pack_e4m3x16(y);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) {
+    // a wait gave up: let every slice already requested land before the
+    // CTA's shared memory is released (bounded, on a fresh flag)
+    volatile int drain_abort = 0;
+    for (int kb = misc[5]; kb < misc[4]; ++kb)
+      if (!mbar_wait_bounded(full(kb % kPjStages), (uint32_t)(kb / kPjStages) & 1u, &drain_abort, kPjWaitNs)) break;
+    drain_abort = 0;
+    mbar_wait_bounded(acc_bar, 0u, &drain_abort, kPjWaitNs);   // the issued MMAs, before TMEM is freed
+    atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_TIMEOUT);
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPjBN);
+  }
+  if (write && threadIdx.x == 0) {
+    __threadfence();
+    const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
+    if (tk == (int)(gridDim.x * gridDim.y) - 1) {
+      __threadfence();
+      publish_write(r, head0, next0, prm.n);
+    }
+  }
+}
+
 unsigned grid_for(long long items) { return (unsigned)((items + kThreads - 1) / kThreads); }
 
 }  // namespace
@@ -1127,6 +1392,37 @@ cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStr
   const unsigned g = (unsigned)((pairs + kThreads - 1) / kThreads);
   k_encode<<<g, kThreads, 0, s>>>(in, out, n);
   return cudaGetLastError();
+}
+
+// the projection as a programmatic dependent.
+cudaError_t launch_project(const RingDev& r, const CUtensorMap* tmX, const CUtensorMap* tmW, const int32_t* pos,
+                           void* q_out, void* kv_out, int n, int dm, int flags, cudaStream_t s) {
+  ProjParams p;
+  p.r = r;
+  p.pos = pos;
+  p.q_out = static_cast<uint16_t*>(q_out);
+  p.kv_out = static_cast<uint16_t*>(kv_out);
+  p.n = n;
+  p.dm = dm;
+  p.flags = flags;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + kPjBM - 1) / kPjBM, (3 * r.H * r.D + kPjBN - 1) / kPjBN);
+  cfg.blockDim = dim3(kPjThreads);
+  cfg.dynamicSmemBytes = kPjSmem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_project<128>, *tmX, *tmW, p);
+  return cudaLaunchKernelEx(&cfg, k_project<64>, *tmX, *tmW, p);
+}
+
+cudaError_t project_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(k_project<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPjSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_project<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPjSmem);
+  return e;
 }
 
 }  // namespace kvr

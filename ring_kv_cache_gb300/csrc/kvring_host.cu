@@ -156,6 +156,22 @@ bool make_cache_map(CUtensorMap* m, void* base, int H, int C, int D) {
   return res == CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major bf16 matrix [rows][cols]: tiles of box_rows rows
+// by 64 columns (128 bytes) with the 128-byte swizzle the MMA descriptors
+// expect; rows past the end read 0.
+bool make_bf16_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -217,7 +233,8 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   d.pt = cfg->rope_pairs_t;
   d.py = cfg->rope_pairs_y;
 
-  if (kvr::attention_prepare(d.D) != cudaSuccess || kvr::cache_prepare() != cudaSuccess) {
+  if (kvr::attention_prepare(d.D) != cudaSuccess || kvr::cache_prepare() != cudaSuccess ||
+      kvr::project_prepare() != cudaSuccess) {
     delete r;
     return KVRING_ERR_CUDA;
   }
@@ -356,6 +373,26 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, in
     b.r[i] = r->dev;
   }
   return cuda_status(kvr::launch_delta_many(b, count, delta, (cudaStream_t)stream));
+}
+
+kvring_status kvring_project_write(kvring_t* r, const void* x, const void* w, int32_t d_model, const int32_t* pos,
+                                   int32_t n, void* q_out, void* kv_out, int32_t flags, void* stream) {
+  if (!r || !x || !w || !aligned(x, 16) || !aligned(w, 16) || n < 1) return KVRING_ERR_INVALID_ARG;
+  if (flags & ~(KVRING_PROJECT_WRITE | KVRING_PROJECT_STORE_KV)) return KVRING_ERR_INVALID_ARG;
+  if ((flags & KVRING_PROJECT_STORE_KV) && (!kv_out || !aligned(kv_out, 16))) return KVRING_ERR_INVALID_ARG;
+  if ((q_out && !aligned(q_out, 16)) || (pos && !aligned(pos, 4))) return KVRING_ERR_INVALID_ARG;
+  if (d_model < 64 || d_model % 64 != 0 || d_model > (1 << 20)) return KVRING_ERR_INVALID_ARG;
+  const bool write = (flags & KVRING_PROJECT_WRITE) != 0;
+  if (write && r->dev.pt && !pos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
+  if (!on_device(r)) return KVRING_ERR_INVALID_ARG;
+  if (write && !r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
+  if (n > r->cfg.max_tokens || (write && n > r->cfg.capacity - r->cfg.pinned_prefix)) return KVRING_ERR_CAPACITY;
+  CUtensorMap tmX, tmW;
+  if (!make_bf16_map(&tmX, x, n, d_model, 128) ||
+      !make_bf16_map(&tmW, w, 3 * r->dev.H * r->dev.D, d_model, 256))
+    return KVRING_ERR_INVALID_ARG;
+  return cuda_status(kvr::launch_project(r->dev, &tmX, &tmW, pos, q_out, kv_out, n, d_model, flags,
+                                         (cudaStream_t)stream));
 }
 
 kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* wv_in, void* wk_out, void* wv_out,

@@ -546,6 +546,10 @@ cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const i
 cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s);
 cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s);
 cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
+cudaError_t launch_project(const RingDev& r, const CUtensorMap* tmX, const CUtensorMap* tmW,
+                           const int32_t* pos, void* q_out, void* kv_out, int n, int dm, int flags,
+                           cudaStream_t s);
+cudaError_t project_prepare();
 
 struct AttnLaunch {
   const void* q;

@@ -167,3 +167,24 @@ def test_device_position_out_of_table_sets_error_word():
     ring.write(k, k, pos)
     st = ring.export()["state"].cpu().numpy()
     assert st[kv.STATE["error"]] & kv.DEVERR_POSITION
+
+
+def test_write_floor_leaves_the_ring_unchanged():
+    """The measurement kernel for the write's fixed cost (the write's grid,
+    launch, wait, state read, ticket and state publication with no data)
+    leaves codes, positions and state exactly as they were, before and after
+    the ring has wrapped, and a write after it still matches the oracle."""
+    frames = tiny_session()
+    ring, orc = make_pair(TINY, Ring)
+    ring.calibrate(dev(frames[0][1]), dev(frames[0][2]))
+    orc.calibrate(f(frames[0][1]), f(frames[0][2]))
+    for i, (q, k, v) in enumerate(frames):
+        ring.write(dev(k), dev(v))
+        orc.write(f(k), f(v))
+        if i in (1, 6):
+            for _ in range(3):
+                ring.write_floor(TINY.tokens)
+            assert_ring_equal(ring, orc, f"after floor launches at frame {i}")
+    assert_ring_equal(ring, orc, "after the last write")
+    with pytest.raises(kv.KvRingError):
+        ring.write_floor(TINY.capacity + 1)
