@@ -56,6 +56,8 @@ CALLS_PER_STEP = 240  # attention calls per step (4 passes x 60 blocks): where t
 # the original upkeep per call with a full window: copy the shifted bf16 window
 # (read + write), read it again to rotate and quantise, write the FP8 cache
 LEGACY_BYTES = 3 * 2 * C * H * D * 2 + 2 * C * H * D
+# extra measurements after the headline step (bench --legs)
+EXTRA_LEGS = ("batched", "legacy", "project", "full_step", "stress")
 H2D_BYTES = 3 * N_NEW * H * D * 2
 D2H_BYTES = N_Q * H * D * 4
 
@@ -385,12 +387,12 @@ def gpu_arm(args, rank, world):
         levels.append(lv)
     levels = np.concatenate(levels).ravel()
     errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
-    batched = batched_upkeep(args, dev, stream) if not args.no_batched else None
-    legacy_us = legacy_upkeep_us(dev, stream) if not args.no_batched else None
-    proj = project_write_us(dev, stream) if not args.no_batched else None
+    batched = batched_upkeep(args, dev, stream) if "batched" in args.legs else None
+    legacy_us = legacy_upkeep_us(dev, stream) if "legacy" in args.legs else None
+    proj = project_write_us(dev, stream) if "project" in args.legs else None
     del g_warm, g_timed, g_attn, g_write, g_delta, g_wfloor, g_dfloor, g_e2e
-    full_step = full_step_60_layers(dev, stream) if not args.no_batched else None
-    stress = stress_40_heads(dev, stream) if not args.no_batched else None
+    full_step = full_step_60_layers(dev, stream) if "full_step" in args.legs else None
+    stress = stress_40_heads(dev, stream) if "stress" in args.legs else None
     return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, wf_us=wf_us, df_us=df_us,
                 full_step=full_step, stress=stress, e2e_ms=e2e_ms, copy_us=copy_us,
                 clocks=clk.summary(),
@@ -811,9 +813,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvring", choices=["kvring", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-batched", action="store_true", help="skip the 60-ring batched upkeep measurement")
+    ap.add_argument("--no-batched", action="store_true", help="run none of the extra legs (same as --legs none)")
+    ap.add_argument("--legs", default=",".join(EXTRA_LEGS),
+                    help="extra measurements after the headline step, comma-separated from "
+                         f"{','.join(EXTRA_LEGS)} (or 'none')")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.legs = set() if args.no_batched else {x for x in args.legs.split(",") if x in EXTRA_LEGS}
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
