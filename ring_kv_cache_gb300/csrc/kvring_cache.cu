@@ -1004,15 +1004,18 @@ __global__ void k_encode(const float* __restrict__ in, uint8_t* __restrict__ out
 // positions set and the ring state advanced by the last CTA -- byte for byte
 // what kvring_write_frame does with the same bf16 keys and values.
 //
-// One CTA per 128 tokens x 256 output columns (two heads of 128 of one kind,
-// or four of 64): a 4-stage TMA pipeline of 64-wide reduction slices (A 16 KB
-// + B 32 KB), one thread loading, one thread issuing M128 N256 K16 bf16 MMAs
-// (66 ns each, longer than one thread's issue cost), the accumulator in 256
-// TMEM columns, and all four warps in the epilogue with one token row per
-// thread.
+// One CTA per 128 tokens x 160 output columns (five 32-column chunks, each
+// inside one head of one kind): 6 x 24 = 144 CTAs for a production frame
+// (757 tokens, 3 x 10 heads of 128), nearly one per SM.  A 5-stage TMA
+// pipeline of 64-wide reduction slices (A 16 KB + B 20 KB), one thread
+// loading, one thread issuing M128 N160 K16 bf16 MMAs, the accumulator in
+// TMEM (160 of 256 allocated columns), and all four warps in the epilogue
+// with one token row per thread.
 constexpr int kPjThreads = 128;
-constexpr int kPjBM = 128, kPjBN = 256, kPjBK = 64;
-constexpr int kPjStages = 4;
+constexpr int kPjBM = 128, kPjBN = kProjTileN, kPjBK = 64;
+constexpr int kPjStages = 5;
+constexpr uint32_t kPjTmemCols = 256;   // a power of two >= kPjBN
+static_assert(kPjBN % 32 == 0 && kPjBN % 16 == 0 && kPjBN <= 256, "tile of whole 32-column chunks");
 constexpr int kPjABytes = kPjBM * kPjBK * 2;
 constexpr int kPjBBytes = kPjBN * kPjBK * 2;
 constexpr int kPjStageBytes = kPjABytes + kPjBBytes;
@@ -1096,7 +1099,7 @@ __global__ void __launch_bounds__(kPjThreads, 1)
   }
   if (warp == 0) {
     __syncwarp();                                  // warp-collective allocation
-    tmem_alloc(smem_u32(misc), kPjBN);
+    tmem_alloc(smem_u32(misc), kPjTmemCols);
     tmem_relinquish();
   }
   // The activations come from the preceding kernel; the ring as well.
@@ -1158,18 +1161,18 @@ __global__ void __launch_bounds__(kPjThreads, 1)
   const int tok = m0 + (int)threadIdx.x;          // TMEM lane = accumulator row = token
   const bool write = (prm.flags & PJ_WRITE) != 0, store_kv = (prm.flags & PJ_STORE_KV) != 0;
   const int head0 = misc[2], next0 = misc[3];
-  constexpr int HPT = kPjBN / D;                  // heads per tile
   if (acc_ok) {
+    // 32-column chunk k of the tile is output column n0 + 32 k: kind (0 =
+    // query, 1 = key, 2 = value), head h, chunk c of the head's D columns
 #pragma unroll 1
-    for (int sub = 0; sub < HPT; ++sub) {
-      const int blk = blockIdx.y * HPT + sub;       // column block: kind * H + head
-      if (blk >= 3 * H) break;                      // CTA-uniform
-      const int kind = blk / H, h = blk % H;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+    for (int k = 0; k < kPjBN / 32; ++k) {
+      const int col = n0 + 32 * k;
+      if (col >= 3 * H * D) break;                  // CTA-uniform
+      const int kind = col / (H * D), h = (col % (H * D)) / D, c = (col % D) / 32;
+      {
         uint32_t acc[32];
         __syncwarp();
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(sub * D + c * 32), acc);
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(32 * k), acc);
         tmem_wait_ld();
         if (tok >= prm.n) continue;
         // the projection's bf16 outputs, and their fp32 values
@@ -1246,7 +1249,7 @@ __global__ void __launch_bounds__(kPjThreads, 1)
   }
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kPjBN);
+    tmem_dealloc(tmem, kPjTmemCols);
   }
   if (write && threadIdx.x == 0) {
     __threadfence();

@@ -389,7 +389,7 @@ kvring_status kvring_project_write(kvring_t* r, const void* x, const void* w, in
   if (n > r->cfg.max_tokens || (write && n > r->cfg.capacity - r->cfg.pinned_prefix)) return KVRING_ERR_CAPACITY;
   CUtensorMap tmX, tmW;
   if (!make_bf16_map(&tmX, x, n, d_model, 128) ||
-      !make_bf16_map(&tmW, w, 3 * r->dev.H * r->dev.D, d_model, 256))
+      !make_bf16_map(&tmW, w, 3 * r->dev.H * r->dev.D, d_model, kvr::kProjTileN))
     return KVRING_ERR_INVALID_ARG;
   return cuda_status(kvr::launch_project(r->dev, &tmX, &tmW, pos, q_out, kv_out, n, d_model, flags,
                                          (cudaStream_t)stream));

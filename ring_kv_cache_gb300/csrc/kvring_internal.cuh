@@ -32,6 +32,7 @@ enum : int {
 };
 
 constexpr int kTile = 128;          // slots per key/value tile, queries per query tile
+constexpr int kProjTileN = 160;     // output columns per QKV-projection CTA (the weight tile's rows)
 constexpr int kEmptyPos = INT32_MIN;
 
 // Device-side view of one ring (plain pointers into the caller's buffer).
