@@ -174,6 +174,47 @@ __device__ __forceinline__ void publish_write(const RingDev& r, int head0, int n
   __threadfence();
 }
 
+// The single-ring write publishes its state from values every block's
+// thread 0 gathers right after the wait, so the last block's publication is
+// stores only.  token_of_slot: the index of this frame's token that goes to
+// slot s (token t goes to head0 + t, wrapped past the prefix), or -1.
+__device__ __forceinline__ int token_of_slot(const RingDev& r, int head0, int n, int s) {
+  int t = s - head0;
+  if (t < 0) {
+    if (s < r.P) return -1;
+    t += r.C - r.P;
+  }
+  return t < n ? t : -1;
+}
+struct WritePlan {
+  int head, nv, tot_lo, tot_hi, next, oldest, prefix_end;
+};
+// From the state at the start of a write of n tokens (read after the wait):
+// the state after it.  The position of the oldest rolling slot and of the
+// prefix's last slot come from this frame's positions when this frame
+// writes those slots, else from their current entries (which this write
+// leaves alone), loaded here.
+__device__ __forceinline__ WritePlan plan_write(const RingDev& r, const int32_t* pos, int head0, int nv0,
+                                                unsigned long long total, int next0, int n) {
+  const int C = r.C, P = r.P;
+  WritePlan w;
+  w.head = head0 + n;
+  if (w.head >= C) w.head -= C - P;   // the wrap skips the pinned prefix
+  w.nv = nv0 + n < C ? nv0 + n : C;
+  const unsigned long long tot = total + (unsigned long long)n;
+  w.tot_lo = (int)(unsigned)(tot & 0xFFFFFFFFull);
+  w.tot_hi = (int)(unsigned)(tot >> 32);
+  w.next = next0 + n;
+  auto position = [&](int s) {
+    const int t = token_of_slot(r, head0, n, s);
+    return t >= 0 ? (pos ? rope_pos(r, pos, t, 0) : next0 + t) : __ldcg(r.slot_pos + s);
+  };
+  // oldest rolling slot: the next one to be overwritten once full, else slot P
+  w.oldest = w.nv > P ? position(w.nv >= C ? w.head : P) : kEmptyPos;
+  w.prefix_end = (P > 0 && w.nv >= P) ? position(P - 1) + 1 : 0;
+  return w;
+}
+
 // Each thread owns kWriteU chunks, (block * kWriteU + u) * 256 + tid, so a
 // warp's accesses stay contiguous; all input loads are issued before the
 // ring state is read, which hides one DRAM round trip.
@@ -237,11 +278,19 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
   // kernel: the inputs above were complete before that kernel started; the
   // ring (state, cache, positions) is read and written only after it is done.
   griddep_wait();
+  int nv0 = 0;
+  unsigned long long total0 = 0;
   if (threadIdx.x == 0) {
-    s_head = __ldcg(r.state + ST_HEAD);
+    const int4 st = __ldcg(reinterpret_cast<const int4*>(r.state));   // head, n_valid, total lo, hi
+    s_head = st.x;
+    nv0 = st.y;
+    total0 = (unsigned long long)(unsigned)st.w << 32 | (unsigned)st.z;
     s_next = __ldcg(r.state + ST_NEXT_POS);
   }
   __syncthreads();
+  // thread 0 gathers the state after this write while the block works
+  WritePlan plan{};
+  if (threadIdx.x == 0) plan = plan_write(r, pos, s_head, nv0, total0, s_next, n);
   if (pos || s_next != s_guess) load_rows(s_next);
 #pragma unroll
   for (int u = 0; u < U; ++u) {
@@ -278,18 +327,27 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
     }
   }
   __syncthreads();
+  // The last block to finish publishes the state.  No fence before the
+  // ticket: the publication reads nothing another block wrote (the plan was
+  // gathered at the start), every block read the old state before its
+  // ticket, and the next kernel sees the cache through this grid's end.
   if (threadIdx.x == 0) {
-    __threadfence();
     const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
     if (tk == nblk - 1) {
-      __threadfence();
-      publish_write(r, s_head, s_next, n);
+      r.state[ST_HEAD] = plan.head;
+      r.state[ST_NVALID] = plan.nv;
+      r.state[ST_TOTAL_LO] = plan.tot_lo;
+      r.state[ST_TOTAL_HI] = plan.tot_hi;
+      r.state[ST_NEXT_POS] = plan.next;
+      r.state[ST_OLDEST_POS] = plan.oldest;
+      if (r.P > 0 && plan.nv >= r.P) r.state[ST_PREFIX_END] = plan.prefix_end;
+      r.state[ST_TICKET_WRITE] = 0;
     }
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* __restrict__ k,
+__global__ void __launch_bounds__(kThreads, 3) k_write(RingDev r, const uint16_t* __restrict__ k,
                                                     const uint16_t* __restrict__ v,
                                                     const int32_t* __restrict__ pos, int n) {
   write_body<D, kWriteU>(r, k, v, pos, n, blockIdx.x, gridDim.x);
@@ -300,7 +358,7 @@ __global__ void __launch_bounds__(kThreads) k_write(RingDev r, const uint16_t* _
 // and state publication by the last block, with no data (zero tokens, so the
 // published state equals the state read and the ring is unchanged).
 template <int D>
-__global__ void __launch_bounds__(kThreads) k_write_floor(RingDev r) {
+__global__ void __launch_bounds__(kThreads, 3) k_write_floor(RingDev r) {
   write_body<D, kWriteU>(r, nullptr, nullptr, nullptr, 0, blockIdx.x, gridDim.x);
 }
 
@@ -791,7 +849,10 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
     if (ring_end || u + 1 == u_end) {
       __syncwarp();
       if (lane == 0) {
-        __threadfence();
+        // no fence before the ticket: the publication reads nothing the
+        // other warps wrote (every block's producer read this ring's state
+        // before any of its units could finish), and the next kernel sees
+        // the rotated keys and positions through this grid's end
         const int tk = atomicAdd(r.state + ST_TICKET_DELTA, done);
         if (tk + done == kDpConsumerWarps * (int)up) {
           __threadfence();
@@ -1076,7 +1137,8 @@ __global__ void __launch_bounds__(kPjThreads, 1)
   auto empty = [&](int s) -> uint32_t { return bars + 8u * (uint32_t)(kPjStages + s); };
   const uint32_t acc_bar = bars + 8u * (2 * kPjStages);
   int* misc = reinterpret_cast<int*>(sm + kPjStages * kPjStageBytes + 8 * (2 * kPjStages + 1));
-  // misc: [0] TMEM base, [1] abort, [2] head, [3] next position, [4] slices issued, [5] slices consumed
+  // misc: [0] TMEM base, [1] abort, [2] head, [3] next position, [4] slices issued, [5] slices consumed,
+  // [6..8] fill level and tokens written (lo, hi), [9..15] the ring state after this frame
   volatile int* abort = misc + 1;
 
   const RingDev& r = prm.r;
@@ -1105,14 +1167,32 @@ __global__ void __launch_bounds__(kPjThreads, 1)
   // The activations come from the preceding kernel; the ring as well.
   griddep_wait();
   if (threadIdx.x == 0) {
-    misc[2] = __ldcg(r.state + ST_HEAD);
+    const int4 st = __ldcg(reinterpret_cast<const int4*>(r.state));   // head, n_valid, total lo, hi
+    misc[2] = st.x;
     misc[3] = __ldcg(r.state + ST_NEXT_POS);
+    misc[6] = st.y;
+    misc[7] = st.z;
+    misc[8] = st.w;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   griddep_launch_dependents();
   const uint32_t tmem = (uint32_t)misc[0];
+  // With the write: a thread that idles through the main loop gathers the
+  // ring state after this frame (misc[9..15]), so the last CTA's
+  // publication is stores only.
+  if ((prm.flags & PJ_WRITE) && threadIdx.x == 64) {
+    const unsigned long long total0 = (unsigned long long)(unsigned)misc[8] << 32 | (unsigned)misc[7];
+    const WritePlan w = plan_write(r, prm.pos, misc[2], misc[6], total0, misc[3], prm.n);
+    misc[9] = w.head;
+    misc[10] = w.nv;
+    misc[11] = w.tot_lo;
+    misc[12] = w.tot_hi;
+    misc[13] = w.next;
+    misc[14] = w.oldest;
+    misc[15] = w.prefix_end;
+  }
 
   if (threadIdx.x == 0) {
     // ------------------------------------------------------ TMA producer
@@ -1251,12 +1331,20 @@ __global__ void __launch_bounds__(kPjThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kPjTmemCols);
   }
+  // The last CTA to finish publishes the gathered state (no fence before
+  // the ticket: the publication reads nothing another CTA wrote).  The CTA
+  // barrier above follows thread 64's gathering.
   if (write && threadIdx.x == 0) {
-    __threadfence();
     const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
     if (tk == (int)(gridDim.x * gridDim.y) - 1) {
-      __threadfence();
-      publish_write(r, head0, next0, prm.n);
+      r.state[ST_HEAD] = misc[9];
+      r.state[ST_NVALID] = misc[10];
+      r.state[ST_TOTAL_LO] = misc[11];
+      r.state[ST_TOTAL_HI] = misc[12];
+      r.state[ST_NEXT_POS] = misc[13];
+      r.state[ST_OLDEST_POS] = misc[14];
+      if (r.P > 0 && misc[10] >= r.P) r.state[ST_PREFIX_END] = misc[15];
+      r.state[ST_TICKET_WRITE] = 0;
     }
   }
 }
