@@ -151,29 +151,6 @@ __global__ void __launch_bounds__(kThreads) k_calibrate(RingDev r, const uint16_
 }
 
 // ---------------------------------------------------------------- write ---
-// Ring state after a write of n tokens that started at slot head0 with
-// default position next0; run by the one thread that completes the write.
-__device__ __forceinline__ void publish_write(const RingDev& r, int head0, int next0, int n) {
-  const int C = r.C, P = r.P;
-  int head = head0 + n;
-  if (head >= C) head -= C - P;   // the wrap skips the pinned prefix
-  int nv = r.state[ST_NVALID] + n;
-  nv = nv < C ? nv : C;
-  r.state[ST_HEAD] = head;
-  r.state[ST_NVALID] = nv;
-  const unsigned long long tot =
-      ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
-      (unsigned long long)n;
-  r.state[ST_TOTAL_LO] = (int)(unsigned)(tot & 0xFFFFFFFFull);
-  r.state[ST_TOTAL_HI] = (int)(unsigned)(tot >> 32);
-  r.state[ST_NEXT_POS] = next0 + n;
-  // oldest rolling slot: the next one to be overwritten once full, else slot P
-  r.state[ST_OLDEST_POS] = nv > P ? __ldcg(r.slot_pos + (nv >= C ? head : P)) : kEmptyPos;
-  if (P > 0 && nv >= P) r.state[ST_PREFIX_END] = __ldcg(r.slot_pos + P - 1) + 1;
-  r.state[ST_TICKET_WRITE] = 0;
-  __threadfence();
-}
-
 // The single-ring write publishes its state from values every block's
 // thread 0 gathers right after the wait, so the last block's publication is
 // stores only.  token_of_slot: the index of this frame's token that goes to
@@ -213,6 +190,18 @@ __device__ __forceinline__ WritePlan plan_write(const RingDev& r, const int32_t*
   w.oldest = w.nv > P ? position(w.nv >= C ? w.head : P) : kEmptyPos;
   w.prefix_end = (P > 0 && w.nv >= P) ? position(P - 1) + 1 : 0;
   return w;
+}
+
+// Store a gathered plan as the ring's state (the publication of a write).
+__device__ __forceinline__ void store_write_plan(const RingDev& r, const WritePlan& w) {
+  r.state[ST_HEAD] = w.head;
+  r.state[ST_NVALID] = w.nv;
+  r.state[ST_TOTAL_LO] = w.tot_lo;
+  r.state[ST_TOTAL_HI] = w.tot_hi;
+  r.state[ST_NEXT_POS] = w.next;
+  r.state[ST_OLDEST_POS] = w.oldest;
+  if (r.P > 0 && w.nv >= r.P) r.state[ST_PREFIX_END] = w.prefix_end;
+  r.state[ST_TICKET_WRITE] = 0;
 }
 
 // Each thread owns kWriteU chunks, (block * kWriteU + u) * 256 + tid, so a
@@ -333,16 +322,7 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
   // ticket, and the next kernel sees the cache through this grid's end.
   if (threadIdx.x == 0) {
     const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
-    if (tk == nblk - 1) {
-      r.state[ST_HEAD] = plan.head;
-      r.state[ST_NVALID] = plan.nv;
-      r.state[ST_TOTAL_LO] = plan.tot_lo;
-      r.state[ST_TOTAL_HI] = plan.tot_hi;
-      r.state[ST_NEXT_POS] = plan.next;
-      r.state[ST_OLDEST_POS] = plan.oldest;
-      if (r.P > 0 && plan.nv >= r.P) r.state[ST_PREFIX_END] = plan.prefix_end;
-      r.state[ST_TICKET_WRITE] = 0;
-    }
+    if (tk == nblk - 1) store_write_plan(r, plan);
   }
 }
 
@@ -637,16 +617,19 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
     }
     // Ring done for this block: every consumer warp adds its units to the
     // ring's ticket; the warp that completes (consumer warps) x (units per
-    // ring) publishes the new ring state.
+    // ring) publishes the new ring state, planned from the state as it still
+    // stands and this frame's own positions for the slots this frame writes,
+    // so it reads nothing another warp wrote and no fence precedes the
+    // tickets (the next kernel sees the cache through this grid's end).
     const bool ring_end = jv + 1 == (int)up;
     if (ring_end || u + 1 == u_end) {
       __syncwarp();
       if (lane == 0) {
-        __threadfence();
         const int tk = atomicAdd(r.state + ST_TICKET_WRITE, done);
         if (tk + done == kWmConsumerWarps * (int)up) {
-          __threadfence();
-          publish_write(r, head, next, n);
+          const int4 st4 = __ldcg(reinterpret_cast<const int4*>(r.state));   // head, n_valid, total lo, hi
+          const unsigned long long total0 = (unsigned long long)(unsigned)st4.w << 32 | (unsigned)st4.z;
+          store_write_plan(r, plan_write(r, b.pos[ring], head, st4.y, total0, next, n));
         }
       }
       done = 0;
