@@ -456,6 +456,7 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
   extern __shared__ __align__(128) uint8_t wsm[];
   __shared__ __align__(8) uint64_t full[kWmMaxStages], empty[kWmMaxStages];
   __shared__ int s_abort;
+  __shared__ int s_warps_done[kMaxBatch];   // per ring: consumer warps of this block past their last unit of it
   const int H = b.r[0].H, C = b.r[0].C;
   const WmGeom g = wm_geom(H, D);
   const int S = g.stages;
@@ -473,6 +474,7 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
     s_abort = 0;
     mbar_fence_init();
   }
+  for (int i = threadIdx.x; i < kMaxBatch; i += blockDim.x) s_warps_done[i] = 0;
   griddep_launch_dependents();
   griddep_wait();  // the rings are touched only after the preceding kernel
   __syncthreads();
@@ -624,9 +626,13 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
     const bool ring_end = jv + 1 == (int)up;
     if (ring_end || u + 1 == u_end) {
       __syncwarp();
-      if (lane == 0) {
-        const int tk = atomicAdd(r.state + ST_TICKET_WRITE, done);
-        if (tk + done == kWmConsumerWarps * (int)up) {
+      // (every consumer warp takes part in every unit, so the block's warps
+      // count themselves in shared memory and its last one takes the ring's
+      // ticket for all of them: one global atomic per block and ring, and
+      // no warp ever waits for another)
+      if (lane == 0 && atomicAdd(&s_warps_done[ring], 1) == kWmConsumerWarps - 1) {
+        const int tk = atomicAdd(r.state + ST_TICKET_WRITE, done * kWmConsumerWarps);
+        if (tk + done * kWmConsumerWarps == kWmConsumerWarps * (int)up) {
           const int4 st4 = __ldcg(reinterpret_cast<const int4*>(r.state));   // head, n_valid, total lo, hi
           const unsigned long long total0 = (unsigned long long)(unsigned)st4.w << 32 | (unsigned)st4.z;
           store_write_plan(r, plan_write(r, b.pos[ring], head, st4.y, total0, next, n));
@@ -676,6 +682,7 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
   __shared__ __align__(8) uint64_t full[kDpStages], empty[kDpStages];
   __shared__ int hdr[kDpStages][2];  // filled rows of the unit, its ring's delta (-1: none)
   __shared__ int s_abort;
+  __shared__ int s_warps_done[kMaxBatch];   // per ring: consumer warps of this block past their last unit of it
   const int H = b.r[0].H, C = b.r[0].C;
   const int P = b.r[0].P;                  // pinned prefix: never rotated
   const int runs = (C - P + RU - 1) / RU;  // runs of rolling slots per head
@@ -692,6 +699,7 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
     s_abort = 0;
     mbar_fence_init();
   }
+  for (int i = threadIdx.x; i < kMaxBatch; i += blockDim.x) s_warps_done[i] = 0;
   griddep_launch_dependents();
   griddep_wait();  // the rings are touched only after the preceding kernel
   __syncthreads();
@@ -831,13 +839,16 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
     const bool ring_end = h == H - 1 && run == runs - 1;
     if (ring_end || u + 1 == u_end) {
       __syncwarp();
-      if (lane == 0) {
-        // no fence before the ticket: the publication reads nothing the
-        // other warps wrote (every block's producer read this ring's state
-        // before any of its units could finish), and the next kernel sees
-        // the rotated keys and positions through this grid's end
-        const int tk = atomicAdd(r.state + ST_TICKET_DELTA, done);
-        if (tk + done == kDpConsumerWarps * (int)up) {
+      // No fence before the ticket: the publication reads nothing the
+      // other warps wrote (every block's producer read this ring's state
+      // before any of its units could finish), and the next kernel sees the
+      // rotated keys and positions through this grid's end.  Every consumer
+      // warp takes part in every unit, so the block's warps count themselves
+      // in shared memory and its last one takes the ring's ticket for all of
+      // them (no warp ever waits for another).
+      if (lane == 0 && atomicAdd(&s_warps_done[ring], 1) == kDpConsumerWarps - 1) {
+        const int tk = atomicAdd(r.state + ST_TICKET_DELTA, done * kDpConsumerWarps);
+        if (tk + done * kDpConsumerWarps == kDpConsumerWarps * (int)up) {
           __threadfence();
           if (d >= 0) {
             r.state[ST_NEXT_POS] -= d;
