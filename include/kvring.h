@@ -46,6 +46,18 @@
  *   - The ring's head, fill level and next position live in device memory,
  *     so a CUDA graph that captured a write or an attention call advances
  *     the ring correctly on every replay.
+ *   - Kernels overlap their predecessor on the stream (programmatic
+ *     dependent launch): each may start before the kernel enqueued just
+ *     before it has finished, and waits for it before touching anything
+ *     that kernel may write.  kvring_write_frame reads its frame, and
+ *     kvring_attention its queries, before that wait, except when a library
+ *     kernel that may still be running writes a caller buffer overlapping
+ *     them (kvring_project_write's q_out or kv_out, an attention output,
+ *     the legacy window): the library records those buffers per stream and
+ *     the call then reads after the wait.  A caller's own kernel launched
+ *     with programmatic stream serialisation that triggers its dependents
+ *     before it has written these inputs must not precede the library call
+ *     that reads them.
  */
 #ifndef KVRING_H
 #define KVRING_H
@@ -340,6 +352,12 @@ kvring_status kvring_debug_set_attention_wait(kvring_t* ring, int64_t limit_ns, 
  * last kvring_attention call, int32 [ceil(n_q/128)][H], copied to `levels`
  * (device or pinned host) on `stream`. */
 kvring_status kvring_debug_attention_levels(kvring_t* ring, int32_t* levels, void* stream);
+
+/* Test support: how many kvring_write_frame and kvring_attention calls so
+ * far (in this process, all rings and streams) found that the previous
+ * library kernel on their stream may write their frame or queries, and so
+ * read them only after waiting for it. */
+int64_t kvring_debug_late_reads(void);
 
 /* Static text for a status code. */
 const char* kvring_status_string(kvring_status s);

@@ -99,6 +99,7 @@ def lib():
         "kvring_debug_attention_levels": (i32, [vp, vp, vp]),
         "kvring_debug_set_attention_wait": (i32, [vp, i64, i32]),
         "kvring_debug_write_floor": (i32, [vp, i32, vp]),
+        "kvring_debug_late_reads": (i64, []),
         "kvring_status_string": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -301,6 +302,13 @@ def kvring_project_write(handle, x, w, d_model, pos, n, q_out, kv_out, flags, st
 def kvring_export(handle, k_out, v_out, scales, slot_pos, state, stream_ptr) -> None:
     _check(lib().kvring_export(handle, _ptr(k_out), _ptr(v_out), _ptr(scales), _ptr(slot_pos),
                                _ptr(state), stream_ptr), "kvring_export")
+
+
+def late_reads() -> int:
+    """How many write and attention calls so far read their frame or queries
+    after waiting for the preceding kernel, because the library's previous
+    kernel on their stream writes a buffer overlapping them."""
+    return int(lib().kvring_debug_late_reads())
 
 
 def encode_e4m3(x: torch.Tensor, stream=None) -> torch.Tensor:

@@ -169,6 +169,7 @@ struct AttnParams {
   int forced_level;
   int cluster_merge;   // the splits of a query tile form one cluster (2..8 CTAs)
   int debug_stall;     // 1: the QK issuer first waits on a barrier nothing arrives on
+  int q_late;          // 1: the preceding kernel may write the queries: read them after the wait
   unsigned long long wait_ns;   // limit of every bounded wait
 };
 
@@ -231,12 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto q_stage = [&](int rr) -> uint32_t {
     return sbase + (rr < 64 ? L::kK : L::kV) + 2 * L::kKVTile + (uint32_t)(rr & 63) * (2 * D);
   };
-  // the queries were complete before the preceding kernel started
-  for (int k = threadIdx.x; k < rows_in * (D / 8); k += kThreads) {
-    const int rr = k / (D / 8), c = k % (D / 8);
-    cp_async16(q_stage(rr) + 16u * c, prm.q + ((size_t)(qt * kTile + rr) * H + h) * D + 8 * c);
-  }
-  cp_async_commit();
+  // The query rows: before the wait for the preceding kernel unless the
+  // host found that a kernel possibly still in flight writes them.
+  auto copy_queries = [&]() {
+    for (int k = threadIdx.x; k < rows_in * (D / 8); k += kThreads) {
+      const int rr = k / (D / 8), c = k % (D / 8);
+      cp_async16(q_stage(rr) + 16u * c, prm.q + ((size_t)(qt * kTile + rr) * H + h) * D + 8 * c);
+    }
+    cp_async_commit();
+  };
+  if (!prm.q_late) copy_queries();
   // Set-up that touches nothing a preceding kernel writes runs before the
   // wait: barriers, TMEM, and an L2 prefetch of the RoPE rows the default
   // query positions will most likely need (a hint only: the state word is
@@ -283,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // This kernel is a programmatic dependent of the preceding kernel (a write,
   // or an earlier attention): the ring (state, cache) is read only after it.
   griddep_wait();
+  if (prm.q_late) copy_queries();
   const int nvalid = __ldcg(r.state + ST_NVALID);
   // the head's scales, loaded once here (the level choice, the softmax, the
   // epilogue and the split merge need them; a load there would sit on
@@ -1170,11 +1176,12 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   p.forced_level = a.forced_level;
   p.cluster_merge = (a.nsplit >= 2 && a.nsplit <= 8) ? 1 : 0;
   p.debug_stall = a.debug_stall;
+  p.q_late = a.q_late;
   p.wait_ns = a.wait_ns;
   const unsigned qtiles = (unsigned)((a.n_q + kTile - 1) / kTile);
   // A programmatic dependent of the preceding kernel: it may start while
-  // that kernel still runs, copies its query rows, and waits
-  // (griddepcontrol.wait) before it reads the ring.
+  // that kernel still runs, copies its query rows (unless that kernel may
+  // write them), and waits (griddepcontrol.wait) before it reads the ring.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(qtiles, (unsigned)r.H, (unsigned)a.nsplit);
   cfg.blockDim = dim3(kThreads);

@@ -215,15 +215,20 @@ constexpr int kWriteU = 2;
 template <int D, int U>
 __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __restrict__ k,
                                            const uint16_t* __restrict__ v, const int32_t* __restrict__ pos,
-                                           int n, int blk, int nblk) {
+                                           int n, int blk, int nblk, bool late) {
   constexpr int CH = D / 16;
   __shared__ int s_head, s_next;
   // A following kernel launched as a programmatic dependent (an attention's
   // query preparation, or the next write) may start now: each waits for
-  // this grid before it touches the ring.
+  // this grid before it touches the ring.  (This kernel writes no caller
+  // buffer; the host's record of which caller buffers kernels still in
+  // flight may write carries over it to the next call.)
   griddep_launch_dependents();
   const int H = r.H, C = r.C;
   const long long per = (long long)n * H * CH;
+  // The frame is loaded before the wait for the preceding kernel unless the
+  // host found that a kernel still in flight may write it.
+  if (late) griddep_wait();
   uint4 in[U][2];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
@@ -264,8 +269,8 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
     load_rows(s_guess);
   }
   // This kernel is launched as a programmatic dependent of the preceding
-  // kernel: the inputs above were complete before that kernel started; the
-  // ring (state, cache, positions) is read and written only after it is done.
+  // kernel: the ring (state, cache, positions) is read and written only
+  // after it is done.
   griddep_wait();
   int nv0 = 0;
   unsigned long long total0 = 0;
@@ -329,8 +334,8 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
 template <int D>
 __global__ void __launch_bounds__(kThreads, 3) k_write(RingDev r, const uint16_t* __restrict__ k,
                                                     const uint16_t* __restrict__ v,
-                                                    const int32_t* __restrict__ pos, int n) {
-  write_body<D, kWriteU>(r, k, v, pos, n, blockIdx.x, gridDim.x);
+                                                    const int32_t* __restrict__ pos, int n, int late) {
+  write_body<D, kWriteU>(r, k, v, pos, n, blockIdx.x, gridDim.x, late != 0);
 }
 
 // The write's fixed cost alone: the grid of an n-token write, the same
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_write(RingDev r, const uint16_t
 // published state equals the state read and the ring is unchanged).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 3) k_write_floor(RingDev r) {
-  write_body<D, kWriteU>(r, nullptr, nullptr, nullptr, 0, blockIdx.x, gridDim.x);
+  write_body<D, kWriteU>(r, nullptr, nullptr, nullptr, 0, blockIdx.x, gridDim.x, false);
 }
 
 // Many rings of one shape in one launch, as a bulk-copy pipeline.  The work
@@ -1374,14 +1379,15 @@ cudaLaunchConfig_t pdl_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* at
 }
 
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
-                         cudaStream_t s) {
+                         bool late, cudaStream_t s) {
   const long long items = 2LL * n * r.H * (r.D / 16);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteU - 1) / kWriteU)), s, attr);
   const uint16_t* kk = static_cast<const uint16_t*>(k);
   const uint16_t* vv = static_cast<const uint16_t*>(v);
-  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write<128>, r, kk, vv, pos, n);
-  return cudaLaunchKernelEx(&cfg, k_write<64>, r, kk, vv, pos, n);
+  const int lt = late ? 1 : 0;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write<128>, r, kk, vv, pos, n, lt);
+  return cudaLaunchKernelEx(&cfg, k_write<64>, r, kk, vv, pos, n, lt);
 }
 
 cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s) {

@@ -6,7 +6,10 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
+#include <mutex>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "kvring_internal.cuh"
@@ -172,6 +175,109 @@ bool make_bf16_map(CUtensorMap* m, const void* base, int rows, int cols, int box
   return res == CUDA_SUCCESS;
 }
 
+// ---------------------------------------------------------------------------
+// Which caller buffers kernels of this library that may still be running
+// write, per stream.
+//
+// Every kernel here is launched as a programmatic dependent of the kernel
+// before it on its stream.  The attention and the projection let their own
+// dependents start only once their wait for their predecessor has returned,
+// so after one of them, only that kernel itself may still be running.  The
+// writes and delta rotations let theirs start at once, so a kernel after
+// them may start while kernels before them still run -- but they write no
+// caller buffer.  The attention reads its queries, and the write its frame,
+// before its wait -- unless a kernel possibly still in flight writes them.
+// So a library kernel that stores into caller buffers (attention output, the
+// projection's queries and keys/values, the legacy window, the E4M3 test
+// encoder) replaces its stream's record with those ranges; an attention or a
+// projection with no such output clears it; a write or delta leaves it as it
+// is (it lets older kernels stay in flight and adds nothing to them); and a
+// call whose early inputs overlap the record reads them after the wait.  A
+// caller kernel that does not use programmatic launch lets its successor
+// start only at its end, so it needs no record.  The decision and the launch
+// happen under one lock, in launch order, so calls from several threads on
+// one stream see the record of the kernels that really precede theirs.
+struct Range {
+  const void* p;
+  size_t n;
+};
+
+struct OutRec {
+  cudaStream_t s;
+  std::thread::id tid;     // for the per-thread default stream, which each thread has its own of
+  uint64_t used;           // LRU stamp; 0 = free entry
+  uintptr_t lo[2], hi[2];  // written ranges [lo, hi); empty when lo == hi
+};
+
+constexpr int kOutRecs = 64;
+std::mutex g_out_mu;
+OutRec g_out[kOutRecs];
+uint64_t g_out_clock = 0;
+bool g_out_lost = false;   // a record was evicted: a stream without one reads late
+long long g_late_reads = 0;
+
+// Under g_out_mu.
+OutRec* find_rec(cudaStream_t s, bool create) {
+  const std::thread::id tid = s == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id();
+  OutRec* oldest = &g_out[0];
+  for (OutRec& e : g_out) {
+    if (e.used && e.s == s && e.tid == tid) return &e;
+    if (e.used < oldest->used) oldest = &e;
+  }
+  if (!create) return nullptr;
+  if (oldest->used) g_out_lost = true;
+  oldest->s = s;
+  oldest->tid = tid;
+  oldest->used = ++g_out_clock;
+  oldest->lo[0] = oldest->hi[0] = oldest->lo[1] = oldest->hi[1] = 0;
+  return oldest;
+}
+
+// Under g_out_mu: whether the last library kernel on s may write any of the
+// ranges (a call with these early inputs then reads them after its wait).
+bool late_inputs(cudaStream_t s, std::initializer_list<Range> in) {
+  const OutRec* e = find_rec(s, false);
+  bool late = false;
+  if (!e) {
+    late = g_out_lost;
+  } else {
+    for (const Range& r : in) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(r.p), b = a + r.n;
+      for (int i = 0; i < 2; ++i)
+        if (e->lo[i] < e->hi[i] && a < e->hi[i] && e->lo[i] < b) late = true;
+    }
+  }
+  if (late) ++g_late_reads;
+  return late;
+}
+
+// Under g_out_mu, after a launch on s succeeded: its kernel is now the last
+// one there, writing the given caller ranges (none for most calls).
+void note_launch(cudaStream_t s, Range a = {nullptr, 0}, Range b = {nullptr, 0}) {
+  OutRec* e = find_rec(s, true);
+  e->used = ++g_out_clock;
+  const Range rr[2] = {a, b};
+  for (int i = 0; i < 2; ++i) {
+    e->lo[i] = reinterpret_cast<uintptr_t>(rr[i].p);
+    e->hi[i] = rr[i].p ? e->lo[i] + rr[i].n : e->lo[i];
+  }
+}
+
+// Launches under the lock and records the launch when it succeeded.
+template <typename F>
+kvring_status tracked(cudaStream_t s, F launch, Range a = {nullptr, 0}, Range b = {nullptr, 0}) {
+  const cudaError_t e = launch();
+  if (e == cudaSuccess) note_launch(s, a, b);
+  return cuda_status(e);
+}
+
+// A launch whose kernel lets its dependents start before its own wait and
+// writes no caller buffer: the stream's record stays as it is.
+template <typename F>
+kvring_status passed_through(F launch) {
+  return cuda_status(launch());
+}
+
 }  // namespace
 
 extern "C" {
@@ -297,7 +403,9 @@ kvring_status kvring_calibrate_scales(kvring_t* r, const void* k, const void* v,
   if (r->dev.pt && !pos) return KVRING_ERR_INVALID_ARG;   // 3-D positions must be given
   if (!on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
-  const kvring_status st = cuda_status(kvr::launch_calibrate(r->dev, k, v, pos, n, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  const kvring_status st = tracked(s, [&] { return kvr::launch_calibrate(r->dev, k, v, pos, n, s); });
   if (st == KVRING_OK) r->calibrated = true;
   return st;
 }
@@ -310,14 +418,20 @@ kvring_status kvring_write_frame(kvring_t* r, const void* k, const void* v, cons
   if (!on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (!r->calibrated) return KVRING_ERR_NOT_CALIBRATED;
   if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
-  return cuda_status(kvr::launch_write(r->dev, k, v, pos, n, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t frame = (size_t)n * r->dev.H * r->dev.D * 2;
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  const bool late = late_inputs(s, {{k, frame}, {v, frame}});
+  return passed_through([&] { return kvr::launch_write(r->dev, k, v, pos, n, late, s); });
 }
 
 kvring_status kvring_delta_rotate(kvring_t* r, int32_t delta, void* stream) {
   if (!r || !on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (delta != KVRING_DELTA_TO_OLDEST && (delta < 0 || delta >= r->cfg.max_position))
     return KVRING_ERR_INVALID_ARG;
-  return cuda_status(kvr::launch_delta(r->dev, delta, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  return passed_through([&] { return kvr::launch_delta(r->dev, delta, s); });
 }
 
 namespace {
@@ -359,7 +473,9 @@ kvring_status kvring_write_frames_many(kvring_t* const* rings, int32_t count, co
     b.v[i] = static_cast<const uint16_t*>(v[i]);
     b.pos[i] = p;
   }
-  return cuda_status(kvr::launch_write_many(b, count, n, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_out_mu);   // (frames are read after the wait: nothing to check)
+  return passed_through([&] { return kvr::launch_write_many(b, count, n, s); });
 }
 
 kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, int32_t delta, void* stream) {
@@ -372,7 +488,9 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, in
       return KVRING_ERR_INVALID_ARG;
     b.r[i] = r->dev;
   }
-  return cuda_status(kvr::launch_delta_many(b, count, delta, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  return passed_through([&] { return kvr::launch_delta_many(b, count, delta, s); });
 }
 
 kvring_status kvring_project_write(kvring_t* r, const void* x, const void* w, int32_t d_model, const int32_t* pos,
@@ -391,8 +509,14 @@ kvring_status kvring_project_write(kvring_t* r, const void* x, const void* w, in
   if (!make_bf16_map(&tmX, x, n, d_model, 128) ||
       !make_bf16_map(&tmW, w, 3 * r->dev.H * r->dev.D, d_model, kvr::kProjTileN))
     return KVRING_ERR_INVALID_ARG;
-  return cuda_status(kvr::launch_project(r->dev, &tmX, &tmW, pos, q_out, kv_out, n, d_model, flags,
-                                         (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)n * r->dev.H * r->dev.D * 2;   // bytes of one bf16 [n][H][d] output
+  const Range qr{q_out, q_out ? rows : 0};
+  const bool kv = (flags & KVRING_PROJECT_STORE_KV) != 0;
+  const Range kvo{kv ? kv_out : nullptr, kv ? 2 * rows : 0};
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  return tracked(
+      s, [&] { return kvr::launch_project(r->dev, &tmX, &tmW, pos, q_out, kv_out, n, d_model, flags, s); }, qr, kvo);
 }
 
 kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* wv_in, void* wk_out, void* wv_out,
@@ -406,8 +530,12 @@ kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* w
   // the original upkeep had neither a prefix nor 3-D RoPE
   if (r->cfg.pinned_prefix != 0 || r->dev.pt != 0) return KVRING_ERR_UNSUPPORTED;
   if (n > r->cfg.capacity || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
-  const kvring_status st = cuda_status(
-      kvr::launch_legacy_upkeep(r->dev, wk_in, wv_in, wk_out, wv_out, k, v, n, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t window = (size_t)r->cfg.capacity * r->dev.H * r->dev.D * 2;
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  const kvring_status st = tracked(
+      s, [&] { return kvr::launch_legacy_upkeep(r->dev, wk_in, wv_in, wk_out, wv_out, k, v, n, s); },
+      Range{wk_out, window}, Range{wv_out, window});
   if (st == KVRING_OK) r->calibrated = true;   // the path sets its own scales
   return st;
 }
@@ -431,7 +559,12 @@ kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, 
   a.debug_stall = r->attn_debug_stall;
   a.wait_ns = r->attn_wait_ns;
   choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
-  return cuda_status(kvr::launch_attention(r->dev, &r->tmK, &r->tmV, a, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)n_q * r->dev.H * r->dev.D;
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  a.q_late = late_inputs(s, {{q, 2 * rows}}) ? 1 : 0;
+  return tracked(s, [&] { return kvr::launch_attention(r->dev, &r->tmK, &r->tmV, a, s); },
+                 Range{out, rows * (a.out_bf16 ? 2 : 4)});
 }
 
 kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t* qpos, int32_t n_q,
@@ -475,7 +608,11 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
   d.qtiles_max = (int)qtiles;
   d.max_splits = a.nsplit;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return cuda_status(kvr::launch_attention(d, &r->tmK, &r->tmV, a, s));
+  const size_t rows = (size_t)n_q * r->dev.H * r->dev.D;
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  a.q_late = late_inputs(s, {{q, 2 * rows}}) ? 1 : 0;
+  return tracked(s, [&] { return kvr::launch_attention(d, &r->tmK, &r->tmV, a, s); },
+                 Range{out, rows * (a.out_bf16 ? 2 : 4)});
 }
 
 kvring_status kvring_export(kvring_t* r, void* k_out, void* v_out, float* scales, int32_t* slot_pos,
@@ -498,13 +635,17 @@ kvring_status kvring_export(kvring_t* r, void* k_out, void* v_out, float* scales
 kvring_status kvring_debug_encode_e4m3(const float* in, uint8_t* out, int64_t n, void* stream) {
   if ((!in || !out) && n > 0) return KVRING_ERR_INVALID_ARG;
   if (n < 0) return KVRING_ERR_INVALID_ARG;
-  return cuda_status(kvr::launch_encode_e4m3(in, out, n, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  return tracked(s, [&] { return kvr::launch_encode_e4m3(in, out, n, s); }, Range{out, (size_t)n});
 }
 
 kvring_status kvring_debug_write_floor(kvring_t* r, int32_t n, void* stream) {
   if (!r || n < 1 || !on_device(r)) return KVRING_ERR_INVALID_ARG;
   if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
-  return cuda_status(kvr::launch_write_floor(r->dev, n, (cudaStream_t)stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  return passed_through([&] { return kvr::launch_write_floor(r->dev, n, s); });
 }
 
 kvring_status kvring_debug_set_attention_wait(kvring_t* r, int64_t limit_ns, int32_t stall) {
@@ -519,6 +660,11 @@ kvring_status kvring_debug_attention_levels(kvring_t* r, int32_t* levels, void* 
   if (!r || !levels || !on_device(r)) return KVRING_ERR_INVALID_ARG;
   const size_t bytes = (size_t)r->qtiles_max * r->dev.H * sizeof(int32_t);
   return cuda_status(cudaMemcpyAsync(levels, r->dev.levels, bytes, cudaMemcpyDefault, (cudaStream_t)stream));
+}
+
+int64_t kvring_debug_late_reads(void) {
+  std::lock_guard<std::mutex> lk(g_out_mu);
+  return g_late_reads;
 }
 
 const char* kvring_status_string(kvring_status s) {

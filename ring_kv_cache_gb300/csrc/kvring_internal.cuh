@@ -542,8 +542,10 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int chunk, int row_bytes
 namespace kvr {
 cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, const int32_t* pos,
                              int n, cudaStream_t s);
+// late: the preceding kernel may write k or v, so the frame is read only
+// after the wait for it
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
-                         cudaStream_t s);
+                         bool late, cudaStream_t s);
 cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s);
 cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s);
 cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
@@ -562,6 +564,7 @@ struct AttnLaunch {
   int tiles_per_split;
   int forced_level;
   int debug_stall;                 // test support: make the first QK wait time out
+  int q_late;                      // the preceding kernel may write q: read it after the wait
   unsigned long long wait_ns;      // limit of every bounded wait in the kernel
 };
 // Batched write / delta over rings of one shape (kernel parameters: no

@@ -25,7 +25,7 @@ from oracle import Ring, e4m3
 from oracle.projection import project_qkv
 from workloads import PROD, TINY, bf16_from_f32
 
-from _ringcheck import dev, export_np, f
+from _ringcheck import MAX_ABS, MEAN_ABS, dev, export_np, f, sampled_attention_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -151,3 +151,66 @@ def test_projection_argument_errors():
     assert e.value.status == 2
     with pytest.raises(ValueError):                   # d_model not a multiple of 64
         ring.project_write(x[:, :96].contiguous(), w[:, :96].contiguous(), write=False)
+
+
+def test_projection_outputs_consumed_at_once():
+    """The projection's outputs read by the very next call on the stream, with
+    no host synchronisation between: its stored keys and values by a write,
+    its queries by an attention.  The projection lets its dependents start
+    before it has stored them, so both calls must read those inputs only
+    after waiting for it -- the library's per-stream record of the buffers
+    its last kernel writes makes them do so (counted by late_reads) -- and
+    the results match the oracle.  Inputs no library kernel wrote are still
+    read before the wait."""
+    shape, dm, scale = PROD, 5120, 0.015
+    w, xs = _session(shape, dm, 8, 33, scale)
+    H, d = shape.heads, shape.head_dim
+    ring = kv.KvRing(H, d, shape.capacity, max(shape.tokens, shape.queries), shape.max_position, shape.rope_base)
+    orc = Ring(H, d, shape.capacity, shape.max_position, shape.rope_base)
+    wd = dev(w)
+    rows = np.random.default_rng(5).choice(shape.queries, 48, replace=False)
+    q0, k0, v0 = project_qkv(xs[0], w, H, d)
+    (_, ek, ev), (_, ak, av) = _bound(xs[0], w, H, d)
+    ring.calibrate(dev(k0), dev(v0))
+    orc.calibrate(f(k0), f(v0))
+    # frame 0: stored keys and values, written by a separate write at once
+    x0 = dev(xs[0])
+    before = kv.late_reads()
+    _, kv_out = ring.project_write(x0, wd, write=False, store_kv=True)
+    ring.write(kv_out[0], kv_out[1])
+    assert kv.late_reads() == before + 1
+    slots = orc.write(f(k0), f(v0))
+    torch.cuda.synchronize()
+    kvn = kv_out.view(torch.int16).cpu().numpy().view(np.uint16)
+    same_k = _compare_bf16(kvn[0], k0, ek, ak, "k").all(axis=2)
+    same_v = _compare_bf16(kvn[1], v0, ev, av, "v").all(axis=2)
+    e = export_np(ring)
+    for t in range(shape.tokens):
+        for h in range(H):
+            if same_k[t, h]:
+                assert np.array_equal(e["k"][h, slots[t]], orc.K[h, slots[t]]), (t, h)
+            if same_v[t, h]:
+                assert np.array_equal(e["v"][h, slots[t]], orc.V[h, slots[t]]), (t, h)
+    assert np.array_equal(e["slot_pos"].astype(np.int64), orc.slot_pos)
+    # frames 1-7 (the ring wraps in frame 7): the fused write, then an
+    # attention over the queries it just stored
+    for i in range(1, 8):
+        q, k, v = project_qkv(xs[i], w, H, d)
+        x = dev(xs[i])
+        before = kv.late_reads()
+        q_out, _ = ring.project_write(x, wd)
+        out = ring.attention(q_out)
+        assert kv.late_reads() == before + 1, i
+        orc.write(f(k), f(v))
+        torch.cuda.synchronize()
+        mx, mn, _ = sampled_attention_errors(orc, q, out.cpu().numpy(), rows)
+        assert mx <= MAX_ABS and mn <= MEAN_ABS, (i, mx, mn)
+        assert export_np(ring)["state"][kv.STATE["error"]] == 0
+    # a frame and queries uploaded by the caller: read before the wait
+    q, k, v = project_qkv(xs[0], w, H, d)
+    kd, vd, qd = dev(k), dev(v), dev(q)
+    torch.cuda.synchronize()
+    before = kv.late_reads()
+    ring.write(kd, vd)
+    ring.attention(qd)
+    assert kv.late_reads() == before
