@@ -348,6 +348,18 @@ kvring_status kvring_debug_write_floor(kvring_t* ring, int32_t n, void* stream);
  * Errors: INVALID_ARG (limit_ns outside [1000, 6e10], stall not 0 or 1). */
 kvring_status kvring_debug_set_attention_wait(kvring_t* ring, int64_t limit_ns, int32_t stall);
 
+/* Test support for the attention's early query preparation.  With default
+ * positions the kernel prepares its queries before waiting for the
+ * preceding kernel, for the positions implied by a next-position hint that
+ * every write leaves as it starts, and after the wait redoes the
+ * preparation if the ring's next position turned out different.  With
+ * wrong = 1 the guess of every following attention call on this ring is
+ * off by max_position (so also outside the RoPE table, which must not be
+ * reported), which exercises the redo; wrong = 0 restores normal calls.
+ * Host-side setting only: takes effect on calls enqueued afterwards.
+ * Errors: INVALID_ARG (wrong not 0 or 1). */
+kvring_status kvring_debug_attention_guess(kvring_t* ring, int32_t wrong);
+
 /* Test support: the precision level (1..4) each attention tile used in the
  * last kvring_attention call, int32 [ceil(n_q/128)][H], copied to `levels`
  * (device or pinned host) on `stream`. */

@@ -100,6 +100,7 @@ def lib():
         "kvring_debug_set_attention_wait": (i32, [vp, i64, i32]),
         "kvring_debug_write_floor": (i32, [vp, i32, vp]),
         "kvring_debug_late_reads": (i64, []),
+        "kvring_debug_attention_guess": (i32, [vp, i32]),
         "kvring_status_string": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -448,6 +449,11 @@ class KvRing:
         with torch.cuda.device(self.device):
             _check(lib().kvring_debug_write_floor(self.handle, int(n), self._s(stream)),
                    "kvring_debug_write_floor")
+
+    def set_attention_guess(self, wrong: bool = False) -> None:
+        """Test support: make the attention's early guess of the default
+        query positions wrong on purpose (kvring_debug_attention_guess)."""
+        _check(lib().kvring_debug_attention_guess(self.handle, int(bool(wrong))), "kvring_debug_attention_guess")
 
     def set_attention_wait(self, limit_ns: int = 1_000_000_000, stall: bool = False) -> None:
         """Test support: the attention kernel's wait limit, and a stall that

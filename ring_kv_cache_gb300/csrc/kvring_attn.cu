@@ -155,6 +155,8 @@ struct Misc {
   int level;
   int abort;
   int last;
+  int hint;      // the ring's next-position hint, read once before the wait
+  int pos_bad;   // a speculative query position fell outside the table
 };
 
 struct AttnParams {
@@ -170,6 +172,7 @@ struct AttnParams {
   int cluster_merge;   // the splits of a query tile form one cluster (2..8 CTAs)
   int debug_stall;     // 1: the QK issuer first waits on a barrier nothing arrives on
   int q_late;          // 1: the preceding kernel may write the queries: read them after the wait
+  int debug_guess;     // 1: guess the default positions wrong on purpose (test support)
   unsigned long long wait_ns;   // limit of every bounded wait
 };
 
@@ -243,10 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (!prm.q_late) copy_queries();
   // Set-up that touches nothing a preceding kernel writes runs before the
-  // wait: barriers, TMEM, and an L2 prefetch of the RoPE rows the default
-  // query positions will most likely need (a hint only: the state word is
-  // read before the preceding write may have advanced it, so both the
-  // positions before and after a write of n_q tokens are prefetched).
+  // wait: barriers, TMEM, and (below) the query prologue.
   if (threadIdx.x == kWarpTma * 32) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
@@ -277,55 +277,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (!prm.qpos && threadIdx.x < 2 * kTile) {
-    const int t = qt * kTile + (threadIdx.x & (kTile - 1));
-    if (t < prm.n_q) {
-      int p = __ldcg(r.state + ST_NEXT_POS) - prm.n_q + t + (threadIdx.x >= kTile ? prm.n_q : 0);
-      p = p < 0 ? 0 : (p >= r.max_pos ? r.max_pos - 1 : p);
-      bulk_prefetch_l2(r.table + (size_t)p * D, D * 4);
-    }
-  }
-  // This kernel is a programmatic dependent of the preceding kernel (a write,
-  // or an earlier attention): the ring (state, cache) is read only after it.
-  griddep_wait();
-  if (prm.q_late) copy_queries();
-  const int nvalid = __ldcg(r.state + ST_NVALID);
-  // the head's scales, loaded once here (the level choice, the softmax, the
-  // epilogue and the split merge need them; a load there would sit on
-  // their critical path)
+  // The head's scales, read once here (the level choice, the softmax, the
+  // epilogue and the split merge need them; a load there would sit on their
+  // critical path).  Only a calibration or the legacy upkeep writes them,
+  // and neither lets the kernel after it start early, so they may be read
+  // before the wait.
   const float scale_k = r.scales[h], scale_v = r.scales[H + h];
-  const int ntile_total = (nvalid + kTile - 1) / kTile;
-  const int tile0 = split * prm.tiles_per_split;
-  int ntiles = ntile_total - tile0;
-  ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
-
-  // ---------------------------------------------------------------- setup
-  const size_t unit = (size_t)qt * H + h;
-  if (threadIdx.x == kWarpTma * 32) {
-    // The producer starts the first two key/value copies at once; the third
-    // stage's space holds query rows until the query prologue is done.
-    const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
-    for (int j = 0; j < first; ++j) {
-      const int slot0 = (tile0 + j) * kTile;
-      mbar_arrive_expect_tx(bar(L::kBarKFull + j), (uint32_t)(kTile * D));
-      tma_load_3d(sbase + L::kK + j * L::kKVTile, &tmK, 0, slot0, h, bar(L::kBarKFull + j));
-      mbar_arrive_expect_tx(bar(L::kBarVFull + j), (uint32_t)(kTile * D));
-      tma_load_3d(sbase + L::kV + j * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarVFull + j));
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  // A following write (or query preparation) launched as a programmatic
-  // dependent may start on the idle SMs now: it loads its inputs and waits
-  // for this grid before it touches the ring.
-  griddep_launch_dependents();
-  const uint32_t tmem = misc->tmem_base;
-
-  {
-    // ------------------------------------------------ query prologue
-    // All twelve warps, before the roles split up (nothing can proceed
-    // without the query terms anyway).
+  // ------------------------------------------------ query prologue
+  // All twelve warps, before the roles split up (nothing can proceed without
+  // the query terms anyway).  first_pos: the position of query 0 when the
+  // positions are the default ones.
+  auto query_prologue = [&](int first_pos, bool speculative) {
       // (1) one position per query row; (2) the RoPE-table rows of those
       // positions copied into the f16 V tiles' space with 16-byte cp.async
       // (the query rows are already on their way, see above); (3) pass 1
@@ -343,9 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tq = qt * kTile + threadIdx.x;
         int p = 0;
         if (tq < prm.n_q) {
-          p = prm.qpos ? __ldg(prm.qpos + tq) : __ldcg(r.state + ST_NEXT_POS) - prm.n_q + tq;
+          p = prm.qpos ? __ldg(prm.qpos + tq) : first_pos + tq;
           if (p < 0 || p >= r.max_pos) {
-            atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+            // (a guessed position is reported only once it proves right)
+            if (speculative)
+              misc->pos_bad = 1;
+            else
+              atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
             p = 0;
           }
         }
@@ -463,13 +429,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (threadIdx.x == 0) {
-        misc->level = level;
-        if (split == 0) r.levels[unit] = level;
-      }
+      if (threadIdx.x == 0) misc->level = level;
       fence_proxy_async_smem();   // generic writes -> tensor-core reads
       __syncthreads();
+  };
+
+  // The query prologue runs before the wait for the preceding kernel when
+  // its inputs allow: the queries (and explicit positions) unless the host
+  // found that a kernel still in flight writes them, and the default
+  // positions from the ring's next-position hint, which a write sets as it
+  // starts.  After the wait the guess is checked against the ring's next
+  // position and the prologue repeated if it was wrong.
+  const bool early = !prm.q_late;
+  if (threadIdx.x == 0) {
+    misc->hint = prm.qpos ? 0 : ld_relaxed_gpu(r.state + ST_NEXT_POS_HINT) + (prm.debug_guess ? r.max_pos : 0);
+    misc->pos_bad = 0;
   }
+  __syncthreads();
+  const int hint = misc->hint;
+  if (early) query_prologue(hint - prm.n_q, prm.qpos == nullptr);
+  // This kernel is a programmatic dependent of the preceding kernel (a write,
+  // or an earlier attention): the ring (state, cache) is read only after it.
+  griddep_wait();
+  const int nvalid = __ldcg(r.state + ST_NVALID);
+  const int next_pos = __ldcg(r.state + ST_NEXT_POS);
+  const int ntile_total = (nvalid + kTile - 1) / kTile;
+  const int tile0 = split * prm.tiles_per_split;
+  int ntiles = ntile_total - tile0;
+  ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
+
+  // ---------------------------------------------------------------- setup
+  const size_t unit = (size_t)qt * H + h;
+  if (threadIdx.x == kWarpTma * 32) {
+    // The producer starts the first two key/value copies at once; the third
+    // stage's space holds query rows until the query prologue is done.
+    const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
+    for (int j = 0; j < first; ++j) {
+      const int slot0 = (tile0 + j) * kTile;
+      mbar_arrive_expect_tx(bar(L::kBarKFull + j), (uint32_t)(kTile * D));
+      tma_load_3d(sbase + L::kK + j * L::kKVTile, &tmK, 0, slot0, h, bar(L::kBarKFull + j));
+      mbar_arrive_expect_tx(bar(L::kBarVFull + j), (uint32_t)(kTile * D));
+      tma_load_3d(sbase + L::kV + j * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarVFull + j));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // A following write (or query preparation) launched as a programmatic
+  // dependent may start on the idle SMs now: it loads its inputs and waits
+  // for this grid before it touches the ring.
+  griddep_launch_dependents();
+  const uint32_t tmem = misc->tmem_base;
+  if (!(early && (prm.qpos != nullptr || next_pos == hint))) {
+    // (the staged query rows may have been overwritten by a fourth term)
+    copy_queries();
+    query_prologue(next_pos - prm.n_q, false);
+  } else if (threadIdx.x == 0 && misc->pos_bad) {
+    atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+  }
+  if (threadIdx.x == 0 && split == 0) r.levels[unit] = misc->level;
+
 
   if (warp == kWarpTma) {
     // ------------------------------------------ TMA producer + PV issuer
@@ -1177,6 +1196,7 @@ cudaError_t launch_attention(const RingDev& r, const CUtensorMap* tmK, const CUt
   p.cluster_merge = (a.nsplit >= 2 && a.nsplit <= 8) ? 1 : 0;
   p.debug_stall = a.debug_stall;
   p.q_late = a.q_late;
+  p.debug_guess = a.debug_guess;
   p.wait_ns = a.wait_ns;
   const unsigned qtiles = (unsigned)((a.n_q + kTile - 1) / kTile);
   // A programmatic dependent of the preceding kernel: it may start while

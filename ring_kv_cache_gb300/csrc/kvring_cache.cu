@@ -199,6 +199,7 @@ __device__ __forceinline__ void store_write_plan(const RingDev& r, const WritePl
   r.state[ST_TOTAL_LO] = w.tot_lo;
   r.state[ST_TOTAL_HI] = w.tot_hi;
   r.state[ST_NEXT_POS] = w.next;
+  st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, w.next);
   r.state[ST_OLDEST_POS] = w.oldest;
   if (r.P > 0 && w.nv >= r.P) r.state[ST_PREFIX_END] = w.prefix_end;
   r.state[ST_TICKET_WRITE] = 0;
@@ -222,7 +223,10 @@ __device__ __forceinline__ void write_body(const RingDev& r, const uint16_t* __r
   // query preparation, or the next write) may start now: each waits for
   // this grid before it touches the ring.  (This kernel writes no caller
   // buffer; the host's record of which caller buffers kernels still in
-  // flight may write carries over it to the next call.)
+  // flight may write carries over it to the next call.)  Block 0 first
+  // leaves the next position this write will publish as a hint for them.
+  if (blk == 0 && threadIdx.x == 0)
+    st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, ld_relaxed_gpu(r.state + ST_NEXT_POS) + n);
   griddep_launch_dependents();
   const int H = r.H, C = r.C;
   const long long per = (long long)n * H * CH;
@@ -480,6 +484,9 @@ __global__ void __maxnreg__(120) k_write_many(const __grid_constant__ WriteMany 
     mbar_fence_init();
   }
   for (int i = threadIdx.x; i < kMaxBatch; i += blockDim.x) s_warps_done[i] = 0;
+  // the next position each ring will have, as a hint for the kernels after
+  if (blockIdx.x == 0 && threadIdx.x < count)
+    st_relaxed_gpu(b.r[threadIdx.x].state + ST_NEXT_POS_HINT, ld_relaxed_gpu(b.r[threadIdx.x].state + ST_NEXT_POS) + n);
   griddep_launch_dependents();
   griddep_wait();  // the rings are touched only after the preceding kernel
   __syncthreads();
@@ -857,6 +864,7 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
           __threadfence();
           if (d >= 0) {
             r.state[ST_NEXT_POS] -= d;
+            st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, r.state[ST_NEXT_POS]);
             if (r.state[ST_OLDEST_POS] != kEmptyPos) r.state[ST_OLDEST_POS] -= d;
             r.state[ST_LAST_DELTA] = d;
           }
@@ -1029,6 +1037,7 @@ __global__ void __launch_bounds__(kThreads) k_legacy_quantise(RingDev r, const u
       r.state[ST_NVALID] = nf;
       r.state[ST_HEAD] = nf % C;
       r.state[ST_NEXT_POS] = total + n;
+      st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, (int)(total + n));
       const unsigned long long tot =
           ((unsigned long long)(unsigned)r.state[ST_TOTAL_HI] << 32 | (unsigned)r.state[ST_TOTAL_LO]) +
           (unsigned long long)n;
@@ -1163,6 +1172,9 @@ __global__ void __launch_bounds__(kPjThreads, 1)
     tmem_alloc(smem_u32(misc), kPjTmemCols);
     tmem_relinquish();
   }
+  // the next position the write will publish, as a hint for the kernels after
+  if ((prm.flags & PJ_WRITE) && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 32)
+    st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, ld_relaxed_gpu(r.state + ST_NEXT_POS) + prm.n);
   // The activations come from the preceding kernel; the ring as well.
   griddep_wait();
   if (threadIdx.x == 0) {
@@ -1341,6 +1353,7 @@ __global__ void __launch_bounds__(kPjThreads, 1)
       r.state[ST_TOTAL_LO] = misc[11];
       r.state[ST_TOTAL_HI] = misc[12];
       r.state[ST_NEXT_POS] = misc[13];
+      st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, misc[13]);
       r.state[ST_OLDEST_POS] = misc[14];
       if (r.P > 0 && misc[10] >= r.P) r.state[ST_PREFIX_END] = misc[15];
       r.state[ST_TICKET_WRITE] = 0;

@@ -25,6 +25,7 @@ struct kvring {
   bool calibrated;   // host mirror: a calibration has been enqueued
   unsigned long long attn_wait_ns;   // limit of the attention kernel's bounded waits
   int attn_debug_stall;              // test support: the next attention calls time out on purpose
+  int attn_debug_guess;              // test support: the attention's position guess is wrong on purpose
 };
 
 namespace {
@@ -315,6 +316,7 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   r->calibrated = false;
   r->attn_wait_ns = kDefaultWaitNs;
   r->attn_debug_stall = 0;
+  r->attn_debug_guess = 0;
   uint8_t* b = static_cast<uint8_t*>(dev_buf);
   kvr::RingDev& d = r->dev;
   d.k = b + p.k;
@@ -557,6 +559,7 @@ kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, 
   a.out_bf16 = out_dtype == KVRING_OUT_BF16;
   a.forced_level = r->cfg.attn_precision;
   a.debug_stall = r->attn_debug_stall;
+  a.debug_guess = r->attn_debug_guess;
   a.wait_ns = r->attn_wait_ns;
   choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -591,6 +594,7 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
   a.out_bf16 = out_dtype == KVRING_OUT_BF16;
   a.forced_level = r->cfg.attn_precision;
   a.debug_stall = r->attn_debug_stall;
+  a.debug_guess = r->attn_debug_guess;
   a.wait_ns = r->attn_wait_ns;
   choose_splits(r, n_q, &a.nsplit, &a.tiles_per_split);
   const int ctiles = (r->cfg.capacity + kvr::kTile - 1) / kvr::kTile;
@@ -653,6 +657,12 @@ kvring_status kvring_debug_set_attention_wait(kvring_t* r, int64_t limit_ns, int
     return KVRING_ERR_INVALID_ARG;
   r->attn_wait_ns = (unsigned long long)limit_ns;
   r->attn_debug_stall = stall;
+  return KVRING_OK;
+}
+
+kvring_status kvring_debug_attention_guess(kvring_t* r, int32_t wrong) {
+  if (!r || (wrong != 0 && wrong != 1)) return KVRING_ERR_INVALID_ARG;
+  r->attn_debug_guess = wrong;
   return KVRING_OK;
 }
 

@@ -28,6 +28,13 @@ enum : int {
   ST_TICKET_DELTA = 10,
   ST_OLDEST_POS = 11,   // position of the oldest rolling slot (the default reset delta)
   ST_PREFIX_END = 12,   // with a pinned prefix: position of its last slot + 1
+  // The next position as it will be once the write in flight is done: set
+  // at the start of every write (from a relaxed read of ST_NEXT_POS plus the
+  // frame's length) and with every change of ST_NEXT_POS.  Only a guess:
+  // the attention prepares its queries for the positions it implies while
+  // the preceding kernel still runs, and checks them against ST_NEXT_POS
+  // once that kernel is done.
+  ST_NEXT_POS_HINT = 13,
   ST_WORDS_ALLOC = 16,
 };
 
@@ -187,6 +194,11 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int32_t* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// The matching relaxed store, for a word that is only ever a guess.
+__device__ __forceinline__ void st_relaxed_gpu(int32_t* p, int v) {
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Non-blocking probe of the phase with the given parity.
@@ -565,6 +577,7 @@ struct AttnLaunch {
   int forced_level;
   int debug_stall;                 // test support: make the first QK wait time out
   int q_late;                      // the preceding kernel may write q: read it after the wait
+  int debug_guess;                 // test support: speculate on wrong default positions
   unsigned long long wait_ns;      // limit of every bounded wait in the kernel
 };
 // Batched write / delta over rings of one shape (kernel parameters: no
