@@ -351,6 +351,130 @@ __global__ void __launch_bounds__(kThreads, 3) k_write_floor(RingDev r) {
   write_body<D, kWriteU>(r, nullptr, nullptr, nullptr, 0, blockIdx.x, gridDim.x, false);
 }
 
+// One ring's write staged through shared memory.  Block b takes the tb
+// whole tokens [b TB, b TB + tb) of the frame, keys and values of all heads,
+// so a block is fat (about 40 KB of frame) and a production frame needs
+// under a hundred of them, a few per SM: the grid fits on the SMs that the
+// preceding attention leaves idle, and the frame and the RoPE rows (for the
+// ring's next position, read with a relaxed load) are copied into shared
+// memory with cp.async while that attention still runs.  After the wait
+// only the ring state is read, and the tokens rotated, scaled, converted and
+// stored from shared memory.  Shared memory: the frame, bf16 [2][tb][H][D],
+// then one assembled table row per token, fp32 [tb][D] (chunk c's 16 values
+// from the row of its section's position).  nodata: the fixed cost alone
+// (same grid, launch, hint, wait, state read, plan, ticket and publication;
+// nothing read from the frame, nothing written to the cache, n = 0 tokens
+// published).
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_t* __restrict__ k,
+                                                       const uint16_t* __restrict__ v,
+                                                       const int32_t* __restrict__ pos, int n, int TB, int late,
+                                                       int nodata) {
+  constexpr int CH = D / 16;
+  extern __shared__ __align__(16) uint8_t wts_sm[];
+  __shared__ int s_head, s_next, s_guess;
+  const int H = r.H, C = r.C;
+  const int t0 = blockIdx.x * TB;
+  const int tb = nodata ? 0 : (n - t0 < TB ? n - t0 : TB);
+  const int npub = nodata ? 0 : n;                       // tokens the publication accounts for
+  const uint32_t fr = smem_u32(wts_sm);
+  const size_t fbytes = (size_t)tb * H * D * 2;          // one tensor's bytes in this block
+  const uint32_t rows = fr + (uint32_t)(2 * (size_t)TB * H * D * 2);
+  // The next position this write will publish, as a hint for the kernels
+  // after it; then they may start (this kernel writes no caller buffer: the
+  // host's record of caller buffers written by kernels in flight carries
+  // over it).
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, ld_relaxed_gpu(r.state + ST_NEXT_POS) + npub);
+  griddep_launch_dependents();
+  // The frame before the wait for the preceding kernel, unless the host
+  // found that a kernel still in flight may write it.
+  if (late) griddep_wait();
+  const uint8_t* kb = reinterpret_cast<const uint8_t*>(k) + (size_t)t0 * H * D * 2;
+  const uint8_t* vb = reinterpret_cast<const uint8_t*>(v) + (size_t)t0 * H * D * 2;
+  for (size_t i = (size_t)threadIdx.x * 16; i < fbytes; i += kThreads * 16) {
+    cp_async16(fr + (uint32_t)i, kb + i);
+    cp_async16(fr + (uint32_t)(fbytes + i), vb + i);
+  }
+  // table rows: 16-byte piece q of chunk c of token tl
+  auto stage_rows = [&](int next) {
+    for (int i = threadIdx.x; i < tb * CH * 4; i += kThreads) {
+      const int tl = i / (CH * 4), c = (i / 4) % CH, q = i % 4;
+      const int p = pos ? rope_pos(r, pos, t0 + tl, 8 * c) : next + t0 + tl;
+      if (p >= 0 && p < r.max_pos)
+        cp_async16(rows + (uint32_t)((tl * D + 16 * c + 4 * q) * 4), r.table + (size_t)p * D + 16 * c + 4 * q);
+    }
+  };
+  if (!pos) {
+    if (threadIdx.x == 0) s_guess = ld_relaxed_gpu(r.state + ST_NEXT_POS);
+    __syncthreads();
+    stage_rows(s_guess);
+  }
+  cp_async_commit();
+  // The ring (state, cache, positions) only after the preceding kernel.
+  griddep_wait();
+  int nv0 = 0;
+  unsigned long long total0 = 0;
+  if (threadIdx.x == 0) {
+    const int4 st = __ldcg(reinterpret_cast<const int4*>(r.state));   // head, n_valid, total lo, hi
+    s_head = st.x;
+    nv0 = st.y;
+    total0 = (unsigned long long)(unsigned)st.w << 32 | (unsigned)st.z;
+    s_next = __ldcg(r.state + ST_NEXT_POS);
+  }
+  __syncthreads();
+  if (pos || s_next != s_guess) {
+    stage_rows(s_next);
+    cp_async_commit();
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  // Thread 0 plans the state after this write (a slot-position load or two)
+  // while the other threads rotate, convert and store the block's chunks.
+  WritePlan plan{};
+  if (threadIdx.x == 0) plan = plan_write(r, pos, s_head, nv0, total0, s_next, npub);
+  const int per = tb * H * CH;   // chunks of one tensor in this block
+  for (int i = (int)threadIdx.x - 1; threadIdx.x > 0 && i < 2 * per; i += kThreads - 1) {
+    const int isv = i >= per;
+    const int w = isv ? i - per : i;
+    const int chunk = w % CH, th = w / CH;
+    const int h = th % H, tl = th / H, t = t0 + tl;
+    // head < C and t < n <= C - P: at most one wrap, which skips the prefix
+    int slot = s_head + t;
+    if (slot >= C) slot -= C - r.P;
+    const uint8_t* src = wts_sm + (size_t)isv * fbytes + ((size_t)th * D + 16 * chunk) * 2;
+    float x[16];
+    unpack_bf16x16(*reinterpret_cast<const uint4*>(src), *reinterpret_cast<const uint4*>(src + 16), x);
+    bool ok = true;
+    if (!isv) {
+      const int p = pos ? rope_pos(r, pos, t, 8 * chunk) : s_next + t;
+      if (p < 0 || p >= r.max_pos) {
+        ok = false;
+        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+      } else {
+        const float4* rw = reinterpret_cast<const float4*>(wts_sm + (size_t)(rows - fr) + (size_t)(tl * D + 16 * chunk) * 4);
+        const float4 cs[4] = {rw[0], rw[1], rw[2], rw[3]};
+        rope_pinned(x, cs);
+      }
+      if (h == 0 && chunk == 0) r.slot_pos[slot] = p;
+    }
+    if (ok) {
+      const float inv = r.scales[(isv ? 3 : 2) * H + h];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = __fmul_rn(x[e], inv);
+      uint8_t* dst = (isv ? r.v : r.k) + ((size_t)h * C + slot) * D + chunk * 16;
+      *reinterpret_cast<uint4*>(dst) = pack_e4m3x16(x);
+    }
+  }
+  __syncthreads();
+  // The last block to finish publishes the state (planned at the start, so
+  // it reads nothing another block wrote and no fence precedes the ticket).
+  if (threadIdx.x == 0) {
+    const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
+    if (tk == (int)gridDim.x - 1) store_write_plan(r, plan);
+  }
+}
+
 // Many rings of one shape in one launch, as a bulk-copy pipeline.  The work
 // is cut into units of whole tokens (TU = RU / H tokens of all H heads, RU =
 // 8192 / D rows, 16 KB of bf16) -- or, when one token's heads exceed RU rows,
@@ -1391,8 +1515,38 @@ cudaLaunchConfig_t pdl_config(dim3 grid, cudaStream_t s, cudaLaunchAttribute* at
   return cfg;
 }
 
+// The staged write takes whole tokens per block, up to this many bytes of
+// shared memory (frame + table rows) per block: five tokens of a 10 x 128
+// frame, 152 blocks for 757 tokens, about five per SM (measured against 8
+// and 3 tokens per block: 8 made the writes of back-to-back calls slower,
+// 3 lost the overlap).  A ring whose single token needs more (over 55 heads
+// of 128) keeps the register-staged kernel.
+constexpr int kWriteTokBudget = 28 * 1024;
+
+// Tokens per block of the staged write, or 0 when a token does not fit.
+int write_tok_tokens(const RingDev& r, int n) {
+  const int per_token = 4 * r.H * r.D + 4 * r.D;
+  if (per_token > kWriteTokBudget) return 0;
+  const int tb = kWriteTokBudget / per_token;
+  return tb < n ? tb : n;
+}
+
+cudaError_t launch_write_tok(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n, int tb,
+                             bool late, bool nodata, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((n + tb - 1) / tb)), s, attr);
+  cfg.dynamicSmemBytes = (size_t)2 * tb * r.H * r.D * 2 + (size_t)tb * r.D * 4;
+  const uint16_t* kk = static_cast<const uint16_t*>(k);
+  const uint16_t* vv = static_cast<const uint16_t*>(v);
+  const int lt = late ? 1 : 0, nd = nodata ? 1 : 0;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write_tok<128>, r, kk, vv, pos, n, tb, lt, nd);
+  return cudaLaunchKernelEx(&cfg, k_write_tok<64>, r, kk, vv, pos, n, tb, lt, nd);
+}
+
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
                          bool late, cudaStream_t s) {
+  const int tb = write_tok_tokens(r, n);
+  if (tb > 0) return launch_write_tok(r, k, v, pos, n, tb, late, false, s);
   const long long items = 2LL * n * r.H * (r.D / 16);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteU - 1) / kWriteU)), s, attr);
@@ -1404,6 +1558,8 @@ cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const i
 }
 
 cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s) {
+  const int tb = write_tok_tokens(r, n);
+  if (tb > 0) return launch_write_tok(r, nullptr, nullptr, nullptr, n, tb, false, true, s);
   const long long items = 2LL * n * r.H * (r.D / 16);   // the grid of an n-token write
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteU - 1) / kWriteU)), s, attr);
