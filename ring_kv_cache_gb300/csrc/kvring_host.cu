@@ -326,8 +326,9 @@ kvring_status kvring_create(const kvring_config* cfg, void* dev_buf, size_t byte
   d.state = reinterpret_cast<int32_t*>(b + p.state);
   d.amax = reinterpret_cast<uint32_t*>(b + p.amax);
   d.table = reinterpret_cast<const float*>(b + p.table);
-  d.part_o = reinterpret_cast<float*>(b + p.part_o);
-  d.part_lse = reinterpret_cast<float*>(b + p.part_lse);
+  // split partials exist only for rings allowing more than 8 splits
+  d.part_o = cfg->max_kv_splits > 8 ? reinterpret_cast<float*>(b + p.part_o) : nullptr;
+  d.part_lse = cfg->max_kv_splits > 8 ? reinterpret_cast<float*>(b + p.part_lse) : nullptr;
   d.tickets = reinterpret_cast<int32_t*>(b + p.tickets);
   d.levels = reinterpret_cast<int32_t*>(b + p.levels);
   d.H = cfg->num_heads;

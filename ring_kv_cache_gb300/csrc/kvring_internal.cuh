@@ -51,7 +51,8 @@ struct RingDev {
   int32_t* state;      // [ST_WORDS_ALLOC]
   uint32_t* amax;      // [2H] calibration maxima as float bits (0 between calls)
   const float* table;  // [max_position][D/2][2] fp32 (cos, sin)
-  float* part_o;       // [max_splits][qtiles][H][128][D] attention partials (more than 8 splits)
+  float* part_o;       // [max_splits][qtiles][H][128][D] attention partials (rings allowing more
+                       // than 8 splits only; NULL otherwise)
   float* part_lse;     // [max_splits][qtiles][H][128]
   int32_t* tickets;    // [qtiles][H] split completion counters (0 between calls)
   int32_t* levels;     // [qtiles][H] precision level of each query tile

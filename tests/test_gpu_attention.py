@@ -184,6 +184,33 @@ def test_split_merge_consistent(splits):
     assert mx <= MAX_ABS and mn <= MEAN_ABS, (splits, mx, mn)
 
 
+@pytest.mark.parametrize("heads,out_dtype", [(4, torch.float32), (8, torch.bfloat16), (20, torch.float32)])
+def test_cluster_merge_production_scale(heads, out_dtype):
+    """The cluster merge at production scale: a 757-query call over a wrapped
+    5,788-slot ring on 4, 8 or 20 heads makes the host choose about 6, 3 or
+    2 splits of each query tile (each CTA of the cluster owns 128 / splits
+    rows, not a multiple of 32 for most split counts); sampled rows of every
+    query tile and head must match the float64 reference, in f32 and bf16
+    output."""
+    rng = np.random.default_rng(11 + heads)
+    shape = RingShape(heads=heads, head_dim=128, capacity=5788, tokens=757, queries=757, max_position=40960)
+    ring, orc = make_pair(shape, Ring, max_kv_splits=16)
+    for i in range(9):                       # 6,813 tokens: wrapped
+        q, k, v = frame(rng, shape, 757)
+        if i == 0:
+            ring.calibrate(dev(k), dev(v))
+            orc.calibrate(f(k), f(v))
+        ring.write(dev(k), dev(v))
+        orc.write(f(k), f(v))
+    q, _, _ = frame(rng, shape, 757)
+    out = ring.attention(dev(q), out_dtype=out_dtype).float().cpu().numpy()
+    rows = np.concatenate([np.arange(0, 757, 41), [36, 37, 38, 63, 64, 127, 128, 756]])
+    want = attention_exact(orc, f(q[rows]), orc.next_pos - 757 + rows)
+    mx, mn = attn_errors(out[rows], want)
+    assert mx <= MAX_ABS and mn <= MEAN_ABS, (heads, mx, mn)
+    assert ring.export()["state"][kv.STATE["error"]].item() == 0
+
+
 def test_bf16_output_close_to_f32_output():
     ring, orc, frames = _tiny_loaded(5)
     q = dev(frames[5][0])
