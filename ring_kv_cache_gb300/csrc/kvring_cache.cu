@@ -353,18 +353,21 @@ __global__ void __launch_bounds__(kThreads, 3) k_write_floor(RingDev r) {
 
 // One ring's write staged through shared memory.  Block b takes the tb
 // whole tokens [b TB, b TB + tb) of the frame, keys and values of all heads,
-// so a block is fat (about 40 KB of frame) and a production frame needs
-// under a hundred of them, a few per SM: the grid fits on the SMs that the
-// preceding attention leaves idle, and the frame and the RoPE rows (for the
-// ring's next position, read with a relaxed load) are copied into shared
-// memory with cp.async while that attention still runs.  After the wait
-// only the ring state is read, and the tokens rotated, scaled, converted and
-// stored from shared memory.  Shared memory: the frame, bf16 [2][tb][H][D],
-// then one assembled table row per token, fp32 [tb][D] (chunk c's 16 values
-// from the row of its section's position).  nodata: the fixed cost alone
-// (same grid, launch, hint, wait, state read, plan, ticket and publication;
-// nothing read from the frame, nothing written to the cache, n = 0 tokens
-// published).
+// so a block is fat (about 28 KB of shared memory) and a production frame
+// needs 152 of them, a few per SM: the grid fits on the SMs that the
+// preceding attention leaves idle.  Before the wait for the preceding
+// kernel the block copies the frame and the RoPE rows (for the ring's next
+// position, read with a relaxed load) into shared memory with cp.async and
+// encodes every chunk (rotation, scale, E4M3) in place; after the wait it
+// only reads the ring state and copies the codes into their slots.  If the
+// next position turned out different, or the positions are explicit (they
+// are read only after the wait), the rows are staged again and the chunks
+// encoded after the wait.  Shared memory: the frame, bf16 [2][tb][H][D] (a
+// chunk's 16 codes land in the first half of its own 32 bytes), then one
+// assembled table row per token, fp32 [tb][D] (chunk c's 16 values from the
+// row of its section's position).  nodata: the fixed cost alone (same grid,
+// launch, hint, wait, state read, plan, ticket and publication; nothing read
+// from the frame, nothing written to the cache, 0 tokens published).
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_t* __restrict__ k,
                                                        const uint16_t* __restrict__ v,
@@ -380,6 +383,7 @@ __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_
   const uint32_t fr = smem_u32(wts_sm);
   const size_t fbytes = (size_t)tb * H * D * 2;          // one tensor's bytes in this block
   const uint32_t rows = fr + (uint32_t)(2 * (size_t)TB * H * D * 2);
+  const int per = tb * H * CH;                           // chunks of one tensor in this block
   // The next position this write will publish, as a hint for the kernels
   // after it; then they may start (this kernel writes no caller buffer: the
   // host's record of caller buffers written by kernels in flight carries
@@ -405,12 +409,45 @@ __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_
         cp_async16(rows + (uint32_t)((tl * D + 16 * c + 4 * q) * 4), r.table + (size_t)p * D + 16 * c + 4 * q);
     }
   };
+  // Every chunk rotated (keys), scaled and converted, its codes written over
+  // the first half of its own 32 bytes (each thread reads its chunks before
+  // it writes them).  A key chunk whose position is outside the table keeps
+  // whatever it holds: the copy below skips it.
+  auto encode = [&](int next) {
+    for (int i = threadIdx.x; i < 2 * per; i += kThreads) {
+      const int isv = i >= per;
+      const int w = isv ? i - per : i;
+      const int chunk = w % CH, th = w / CH;
+      const int h = th % H, tl = th / H;
+      uint8_t* src = wts_sm + (size_t)isv * fbytes + ((size_t)th * D + 16 * chunk) * 2;
+      float x[16];
+      unpack_bf16x16(*reinterpret_cast<const uint4*>(src), *reinterpret_cast<const uint4*>(src + 16), x);
+      if (!isv) {
+        const int p = pos ? rope_pos(r, pos, t0 + tl, 8 * chunk) : next + t0 + tl;
+        if (p < 0 || p >= r.max_pos) continue;
+        const float4* rw = reinterpret_cast<const float4*>(wts_sm + (size_t)(rows - fr) + (size_t)(tl * D + 16 * chunk) * 4);
+        const float4 cs[4] = {rw[0], rw[1], rw[2], rw[3]};
+        rope_pinned(x, cs);
+      }
+      const float inv = r.scales[(isv ? 3 : 2) * H + h];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = __fmul_rn(x[e], inv);
+      *reinterpret_cast<uint4*>(src) = pack_e4m3x16(x);
+    }
+  };
   if (!pos) {
     if (threadIdx.x == 0) s_guess = ld_relaxed_gpu(r.state + ST_NEXT_POS);
     __syncthreads();
     stage_rows(s_guess);
   }
   cp_async_commit();
+  if (!pos) {
+    // (the scales are written only by a calibration, which never overlaps
+    // a following kernel)
+    cp_async_wait_all();
+    __syncthreads();
+    encode(s_guess);
+  }
   // The ring (state, cache, positions) only after the preceding kernel.
   griddep_wait();
   int nv0 = 0;
@@ -424,46 +461,46 @@ __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_
   }
   __syncthreads();
   if (pos || s_next != s_guess) {
+    // explicit positions, or a wrong guess: rows and codes after the wait
+    // (a wrong guess encoded the frame in place: load it again first)
+    if (!pos) {
+      for (size_t i = (size_t)threadIdx.x * 16; i < fbytes; i += kThreads * 16) {
+        cp_async16(fr + (uint32_t)i, kb + i);
+        cp_async16(fr + (uint32_t)(fbytes + i), vb + i);
+      }
+    }
     stage_rows(s_next);
     cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    encode(s_next);
   }
-  cp_async_wait_all();
   __syncthreads();
   // Thread 0 plans the state after this write (a slot-position load or two)
-  // while the other threads rotate, convert and store the block's chunks.
+  // while the other threads copy the codes into their slots: thread c + 1
+  // takes (tensor, head, chunk) c for every token of the block.
   WritePlan plan{};
   if (threadIdx.x == 0) plan = plan_write(r, pos, s_head, nv0, total0, s_next, npub);
-  const int per = tb * H * CH;   // chunks of one tensor in this block
-  for (int i = (int)threadIdx.x - 1; threadIdx.x > 0 && i < 2 * per; i += kThreads - 1) {
-    const int isv = i >= per;
-    const int w = isv ? i - per : i;
-    const int chunk = w % CH, th = w / CH;
-    const int h = th % H, tl = th / H, t = t0 + tl;
-    // head < C and t < n <= C - P: at most one wrap, which skips the prefix
-    int slot = s_head + t;
-    if (slot >= C) slot -= C - r.P;
-    const uint8_t* src = wts_sm + (size_t)isv * fbytes + ((size_t)th * D + 16 * chunk) * 2;
-    float x[16];
-    unpack_bf16x16(*reinterpret_cast<const uint4*>(src), *reinterpret_cast<const uint4*>(src + 16), x);
-    bool ok = true;
-    if (!isv) {
-      const int p = pos ? rope_pos(r, pos, t, 8 * chunk) : s_next + t;
-      if (p < 0 || p >= r.max_pos) {
-        ok = false;
-        atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
-      } else {
-        const float4* rw = reinterpret_cast<const float4*>(wts_sm + (size_t)(rows - fr) + (size_t)(tl * D + 16 * chunk) * 4);
-        const float4 cs[4] = {rw[0], rw[1], rw[2], rw[3]};
-        rope_pinned(x, cs);
+  for (int c = (int)threadIdx.x - 1; threadIdx.x > 0 && c < 2 * H * CH; c += kThreads - 1) {
+    const int isv = c >= H * CH;
+    const int rem = isv ? c - H * CH : c;
+    const int h = rem / CH, chunk = rem % CH;
+    uint8_t* const base = (isv ? r.v : r.k) + (size_t)h * C * D + chunk * 16;
+    const uint8_t* src = wts_sm + (size_t)isv * fbytes + ((size_t)h * D + 16 * chunk) * 2;
+    for (int tl = 0; tl < tb; ++tl, src += (size_t)H * D * 2) {
+      const int t = t0 + tl;
+      // head < C and t < n <= C - P: at most one wrap, which skips the prefix
+      int slot = s_head + t;
+      if (slot >= C) slot -= C - r.P;
+      if (!isv) {
+        const int p = pos ? rope_pos(r, pos, t, 8 * chunk) : s_next + t;
+        if (h == 0 && chunk == 0) r.slot_pos[slot] = p;
+        if (p < 0 || p >= r.max_pos) {
+          atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_POSITION);
+          continue;
+        }
       }
-      if (h == 0 && chunk == 0) r.slot_pos[slot] = p;
-    }
-    if (ok) {
-      const float inv = r.scales[(isv ? 3 : 2) * H + h];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] = __fmul_rn(x[e], inv);
-      uint8_t* dst = (isv ? r.v : r.k) + ((size_t)h * C + slot) * D + chunk * 16;
-      *reinterpret_cast<uint4*>(dst) = pack_e4m3x16(x);
+      *reinterpret_cast<uint4*>(base + (size_t)slot * D) = *reinterpret_cast<const uint4*>(src);
     }
   }
   __syncthreads();
