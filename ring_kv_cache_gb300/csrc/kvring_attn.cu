@@ -290,13 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto query_prologue = [&](int first_pos, bool speculative) {
       // (1) one position per query row; (2) the RoPE-table rows of those
       // positions copied into the f16 V tiles' space with 16-byte cp.async
-      // (the query rows are already on their way, see above); (3) pass 1
+      // (the query rows are already on their way, see above); (3) one pass
       // over 8-value chunks: chunk task k = i * 384 + tid is query row
       // k / CPR, chunk k % CPR, so a warp holds every chunk of its rows and a
-      // row's amax is a shuffle reduction, and the warps' maxima give the
-      // tile's precision level; (4) pass 2 writes the level's E4M3 terms of
-      // the rotated values it kept in registers straight into the swizzled
-      // images the QK MMA reads.
+      // row's amax is a shuffle reduction; the chunk's first two E4M3 terms
+      // go straight into the swizzled images the QK MMA reads; (4) the warps'
+      // maxima give the tile's precision level, and levels 3 and 4 add their
+      // terms from the residuals kept in registers.
       constexpr int CPR = D / 8;                           // 16-byte q chunks per row
       constexpr int TPR = D / 4;                           // 16-byte table chunks per row
       constexpr int PQ = (kTile * CPR + kThreads - 1) / kThreads;   // chunk tasks per thread
@@ -350,13 +350,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return cmax;
       };
-      // Pass 1 rotates every chunk once and keeps the values in registers
-      // (u[i], the row maximum in rm[i]); after the CTA barrier that gives
-      // the tile's maximum and level, pass 2 scales them and writes the terms.
-      // Chunk tasks of one iteration cover whole warps (rows x CPR is a
-      // multiple of 32), so every shuffle has all lanes.
-      float u[PQ][8], rm[PQ];
+      // One pass rotates every chunk, takes its row's maximum (the CPR
+      // consecutive lanes that hold the row), scales by it and writes the
+      // first two E4M3 terms at once, keeping the exact fp32 residual in
+      // registers (u[i]); after the CTA barrier that gives the tile's
+      // maximum and level, the tiles whose level needs them get terms 3 and 4
+      // from the residuals (term 4 goes to the third K stage, whose staged
+      // query rows every thread has read by then).  Chunk tasks of one
+      // iteration cover whole warps (rows x CPR is a multiple of 32), so
+      // every shuffle has all lanes.
+      float u[PQ][8];
       float wmax = 0.f;
+      auto put_term = [&](int term, uint32_t off, float (&v)[8], bool residual) {
+        uint16_t c4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(v[2 * e], v[2 * e + 1]);
+        *reinterpret_cast<uint2*>(sm + L::q_term(term) + off) =
+            make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
+        if (residual) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 dq = e4m3x2_to_f32x2(c4[e]);
+            v[2 * e] -= dq.x;
+            v[2 * e + 1] -= dq.y;
+          }
+        }
+      };
 #pragma unroll
       for (int i = 0; i < PQ; ++i) {
         const int k = i * kThreads + threadIdx.x;
@@ -368,12 +387,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) u[i][e] = 0.f;
         }
-        // row maximum over the CPR consecutive lanes that hold the row
 #pragma unroll
         for (int off = CPR / 2; off > 0; off >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, off));
-        rm[i] = cmax;
-        if (k < kTile * CPR && chunk == 0) epi[rrow] = cmax;
         wmax = fmaxf(wmax, cmax);
+        if (k < kTile * CPR) {
+          if (chunk == 0) epi[rrow] = cmax;
+          // E4M3 terms of q / sigma_q (sigma_q = amax/448 of the row), exact
+          // fp32 residuals; 8 bytes per chunk per term at the chunk's
+          // swizzled place in the query images
+          float sq = cmax / 448.0f;
+          if (!(sq >= 0x1p-126f)) sq = 1.0f;
+          // only invq * sq matters (the logit factor uses sq): a fast
+          // reciprocal (a couple of ulp) leaves it 1 within 2^-21
+          const float invq = __fdividef(1.0f, sq);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[i][e] *= invq;
+          const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
+          put_term(0, off, u[i], true);
+          put_term(1, off, u[i], true);
+        }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xFFFFFFFFu, wmax, off));
@@ -391,42 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 : (lg * vmax <= kLevel2MaxLV)                   ? 2
                                                                 : 3;
       }
+      if (level >= 3) {
 #pragma unroll
-      for (int i = 0; i < PQ; ++i) {
-        const int k = i * kThreads + threadIdx.x;
-        if (k >= kTile * CPR) break;
-        const int rrow = k / CPR, chunk = k % CPR;
-        // E4M3 terms of q / sigma_q (sigma_q = amax/448 of the row), exact
-        // fp32 residuals; 8 bytes per chunk per term at the chunk's swizzled
-        // place in the query images
-        float sq = rm[i] / 448.0f;
-        if (!(sq >= 0x1p-126f)) sq = 1.0f;
-        // only invq * sq matters (the logit factor uses sq): a fast
-        // reciprocal (a couple of ulp) leaves it 1 within 2^-21
-        const float invq = __fdividef(1.0f, sq);
-        float* v = u[i];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] *= invq;
-        const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
-#pragma unroll
-        for (int term = 0; term < 4; ++term) {
-          if (term < level) {
-            uint16_t c4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) c4[e] = f32x2_to_e4m3x2(v[2 * e], v[2 * e + 1]);
-            // (term 3 overwrites the third K stage, whose staged query rows
-            // pass 1 read before the CTA barrier)
-            *reinterpret_cast<uint2*>(sm + L::q_term(term) + off) =
-                make_uint2((uint32_t)c4[0] | ((uint32_t)c4[1] << 16), (uint32_t)c4[2] | ((uint32_t)c4[3] << 16));
-            if (term + 1 < level) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 dq = e4m3x2_to_f32x2(c4[e]);
-                v[2 * e] -= dq.x;
-                v[2 * e + 1] -= dq.y;
-              }
-            }
-          }
+        for (int i = 0; i < PQ; ++i) {
+          const int k = i * kThreads + threadIdx.x;
+          if (k >= kTile * CPR) break;
+          const int rrow = k / CPR, chunk = k % CPR;
+          const uint32_t off = swz_offset(rrow, chunk >> 1, D) + (chunk & 1) * 8;
+          put_term(2, off, u[i], level >= 4);
+          if (level >= 4) put_term(3, off, u[i], false);
         }
       }
       if (threadIdx.x == 0) misc->level = level;
