@@ -132,7 +132,8 @@ struct Layout {
   static constexpr int kBarVFull = 2 * kStages + 12;    // V tile of a stage landed
   static constexpr int kBarVEmpty = 3 * kStages + 12;   // ... widened to f16 by the converters
   static constexpr int kBarNever = 4 * kStages + 12;    // never arrived on: the debug stall waits here
-  static constexpr int kNumBars = 4 * kStages + 13;
+  static constexpr int kBarRows = 4 * kStages + 13;     // the query prologue's RoPE rows have landed
+  static constexpr int kNumBars = 4 * kStages + 14;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kLseAll = kMisc + 64;             // float [8 splits][128]: the cluster's log2-sum-exps
   static constexpr int kBytes = kLseAll + 8 * kTile * 4;
@@ -244,6 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cp_async_commit();
   };
+  // The ring's next-position hint, read first of all (its latency overlaps
+  // the set-up below; see the query prologue).
+  const int hint0 = (threadIdx.x == 0 && !prm.qpos) ? ld_relaxed_gpu(r.state + ST_NEXT_POS_HINT) : 0;
   if (!prm.q_late) copy_queries();
   // Set-up that touches nothing a preceding kernel writes runs before the
   // wait: barriers, TMEM, and (below) the query prologue.
@@ -269,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::kBarMerge), 1);
     mbar_init(bar(L::kBarPvIssuerDone), 1);
     mbar_init(bar(L::kBarNever), 1);
+    mbar_init(bar(L::kBarRows), 1);
     misc->abort = 0;
     misc->last = 0;
     mbar_fence_init();
@@ -287,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // All twelve warps, before the roles split up (nothing can proceed without
   // the query terms anyway).  first_pos: the position of query 0 when the
   // positions are the default ones.
+  int rows_phase = 0;   // completed phases of kBarRows (one per bulk row copy)
   auto query_prologue = [&](int first_pos, bool speculative) {
       // (1) one position per query row; (2) the RoPE-table rows of those
       // positions copied into the f16 V tiles' space with 16-byte cp.async
@@ -301,7 +307,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int TPR = D / 4;                           // 16-byte table chunks per row
       constexpr int PQ = (kTile * CPR + kThreads - 1) / kThreads;   // chunk tasks per thread
       int* qpos_s = reinterpret_cast<int*>(epi + 2 * kTile);   // [128] (1-D) or [128][3] (3-D)
-      if (!R3 && threadIdx.x < kTile) {
+      // Default positions that all lie in the table: the tile's rows are
+      // consecutive table rows, one bulk copy (completing on kBarRows).
+      const int p0 = first_pos + qt * kTile;
+      const bool bulk_rows = !R3 && !prm.qpos && p0 >= 0 && p0 + rows_in <= r.max_pos;
+      if (bulk_rows) {
+        if (threadIdx.x == 0) {
+          fence_proxy_async_smem();   // (a second pass rewrites rows the first one read)
+          mbar_arrive_expect_tx(bar(L::kBarRows), (uint32_t)(rows_in * D * 4));
+          bulk_load(sbase + L::kVh, r.table + (size_t)p0 * D, (uint32_t)(rows_in * D * 4), bar(L::kBarRows));
+        }
+      } else if (!R3 && threadIdx.x < kTile) {
         const int tq = qt * kTile + threadIdx.x;
         int p = 0;
         if (tq < prm.n_q) {
@@ -318,15 +334,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         qpos_s[threadIdx.x] = p;
       }
       if constexpr (R3) stage_rows_3d<D>(r, prm.qpos, prm.n_q, qt, rows_in, qpos_s, sbase + L::kVh);
-      __syncthreads();
-      if constexpr (!R3) {
-        for (int k = threadIdx.x; k < rows_in * TPR; k += kThreads) {
-          const int rr = k / TPR, c = k % TPR;
-          cp_async16(sbase + L::kVh + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)qpos_s[rr] * D + 4 * c);
+      if (!bulk_rows) {
+        __syncthreads();
+        if constexpr (!R3) {
+          for (int k = threadIdx.x; k < rows_in * TPR; k += kThreads) {
+            const int rr = k / TPR, c = k % TPR;
+            cp_async16(sbase + L::kVh + (uint32_t)(rr * TPR + c) * 16u, r.table + (size_t)qpos_s[rr] * D + 4 * c);
+          }
         }
+        cp_async_commit();
       }
-      cp_async_commit();
       cp_async_wait_all();
+      if (bulk_rows) {
+        volatile int no_abort = 0;
+        if (!mbar_wait_bounded(bar(L::kBarRows), (uint32_t)(rows_phase & 1), &no_abort, wait_ns))
+          misc->abort = 1;
+        ++rows_phase;
+      }
       __syncthreads();
       auto rotate = [&](int rrow, int chunk, float (&u)[8]) -> float {
         float cmax = 0.f;
@@ -447,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // position and the prologue repeated if it was wrong.
   const bool early = !prm.q_late;
   if (threadIdx.x == 0) {
-    misc->hint = prm.qpos ? 0 : ld_relaxed_gpu(r.state + ST_NEXT_POS_HINT) + (prm.debug_guess ? r.max_pos : 0);
+    misc->hint = prm.qpos ? 0 : hint0 + (prm.debug_guess ? r.max_pos : 0);
     misc->pos_bad = 0;
   }
   __syncthreads();
