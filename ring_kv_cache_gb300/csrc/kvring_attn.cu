@@ -158,6 +158,7 @@ struct Misc {
   int last;
   int hint;      // the ring's next-position hint, read once before the wait
   int pos_bad;   // a speculative query position fell outside the table
+  int nvalid_pre;   // the ring's fill level, read once before the wait
 };
 
 struct AttnParams {
@@ -248,6 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The ring's next-position hint, read first of all (its latency overlaps
   // the set-up below; see the query prologue).
   const int hint0 = (threadIdx.x == 0 && !prm.qpos) ? ld_relaxed_gpu(r.state + ST_NEXT_POS_HINT) : 0;
+  // The fill level as well, for the producer: once it equals the capacity
+  // it never changes again, so the first key/value copies can then be
+  // issued as soon as the wait returns, without the state read after it.
+  const int nvalid_pre = threadIdx.x == 32 ? ld_relaxed_gpu(r.state + ST_NVALID) : 0;
   if (!prm.q_late) copy_queries();
   // Set-up that touches nothing a preceding kernel writes runs before the
   // wait: barriers, TMEM, and (below) the query prologue.
@@ -474,25 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc->hint = prm.qpos ? 0 : hint0 + (prm.debug_guess ? r.max_pos : 0);
     misc->pos_bad = 0;
   }
+  if (threadIdx.x == 32) misc->nvalid_pre = nvalid_pre;
   __syncthreads();
   const int hint = misc->hint;
   if (early) query_prologue(hint - prm.n_q, prm.qpos == nullptr);
-  // This kernel is a programmatic dependent of the preceding kernel (a write,
-  // or an earlier attention): the ring (state, cache) is read only after it.
-  griddep_wait();
-  const int nvalid = __ldcg(r.state + ST_NVALID);
-  const int next_pos = __ldcg(r.state + ST_NEXT_POS);
-  const int ntile_total = (nvalid + kTile - 1) / kTile;
   const int tile0 = split * prm.tiles_per_split;
-  int ntiles = ntile_total - tile0;
-  ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
-
-  // ---------------------------------------------------------------- setup
-  const size_t unit = (size_t)qt * H + h;
-  if (threadIdx.x == kWarpTma * 32) {
+  auto first_copies = [&](int nv) {
     // The producer starts the first two key/value copies at once; the third
     // stage's space holds query rows until the query prologue is done.
-    const int first = ntiles < kStages - 1 ? ntiles : kStages - 1;
+    int nt = (nv + kTile - 1) / kTile - tile0;
+    nt = nt < 0 ? 0 : (nt > prm.tiles_per_split ? prm.tiles_per_split : nt);
+    const int first = nt < kStages - 1 ? nt : kStages - 1;
     for (int j = 0; j < first; ++j) {
       const int slot0 = (tile0 + j) * kTile;
       mbar_arrive_expect_tx(bar(L::kBarKFull + j), (uint32_t)(kTile * D));
@@ -500,7 +497,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar(L::kBarVFull + j), (uint32_t)(kTile * D));
       tma_load_3d(sbase + L::kV + j * L::kKVTile, &tmV, 0, slot0, h, bar(L::kBarVFull + j));
     }
-  }
+  };
+  // This kernel is a programmatic dependent of the preceding kernel (a write,
+  // or an earlier attention): the ring (state, cache) is read only after it.
+  griddep_wait();
+  if (threadIdx.x == kWarpTma * 32) first_copies(misc->nvalid_pre == r.C ? r.C : __ldcg(r.state + ST_NVALID));
+  const int nvalid = __ldcg(r.state + ST_NVALID);
+  const int next_pos = __ldcg(r.state + ST_NEXT_POS);
+  const int ntile_total = (nvalid + kTile - 1) / kTile;
+  int ntiles = ntile_total - tile0;
+  ntiles = ntiles < 0 ? 0 : (ntiles > prm.tiles_per_split ? prm.tiles_per_split : ntiles);
+
+  // ---------------------------------------------------------------- setup
+  const size_t unit = (size_t)qt * H + h;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
