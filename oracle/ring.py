@@ -193,7 +193,10 @@ class Ring:
         if delta < 0:
             raise ValueError("delta must be >= 0")
         lo, nv = self.P, self.n_valid
-        if nv > lo:
+        # A rotation by zero is the identity: every code stays as it is.  (The
+        # fp32 arithmetic below with c = 1, s = 0 would not be: a -0 code next
+        # to a positive partner becomes -0 + 0 = +0 and would re-encode as 0x00.)
+        if nv > lo and delta != 0:
             c, s = self.table.row(delta)
             dims = self.d if self.rope3d is None else 2 * self.rope3d[0]   # 3-D: temporal pairs only
             a = e4m3.decode(self.K[:, lo:nv, :dims]).astype(np.float32)   # exact

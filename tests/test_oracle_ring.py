@@ -179,6 +179,29 @@ def test_delta_zero_is_identity_and_rotation_is_deterministic():
     assert np.array_equal(r.V, v_before)          # values are never rotated
 
 
+def test_delta_zero_keeps_negative_zero_codes():
+    """A zero delta is the identity on every code, signed zeros included: a
+    -0 code (0x80) paired with a positive value keeps its sign, in both
+    positions of the pair, while a nonzero delta rotates it like any value."""
+    r = _ring()
+    k = np.zeros((TINY.tokens, TINY.heads, TINY.head_dim), np.float32)
+    k[:, :, 0::2] = 1.0                 # positive first elements
+    k[:, :, 3::4] = -1e-30              # second elements of odd pairs round to -0
+    k[:, :, 2::4] = -1e-30              # first elements of odd pairs too, partners above
+    k[:, :, 1::4] = 0.5
+    v = np.ones_like(k)
+    r.calibrate(k, v, np.zeros(TINY.tokens, np.int32))
+    r.write(k, v, np.zeros(TINY.tokens, np.int32))
+    assert (r.K[:, :TINY.tokens] == 0x80).any()
+    before = r.K.copy()
+    assert r.delta_rotate(TO_OLDEST) == 0          # the window already starts at position 0
+    assert np.array_equal(r.K, before)
+    r.delta_rotate(0)
+    assert np.array_equal(r.K, before)
+    r.delta_rotate(3)
+    assert not np.array_equal(r.K, before)
+
+
 def test_delta_to_oldest_reads_the_oldest_slot():
     frames = tiny_session()
     r = _ring()
