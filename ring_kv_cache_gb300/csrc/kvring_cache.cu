@@ -368,11 +368,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_write_floor(RingDev r) {
 // row of its section's position).  nodata: the fixed cost alone (same grid,
 // launch, hint, wait, state read, plan, ticket and publication; nothing read
 // from the frame, nothing written to the cache, 0 tokens published).
+// idle: no kernel that may still run reads or writes this ring (the host
+// keeps track); then, with default positions and early inputs, the ring
+// state read before the wait is exact and the whole write -- codes into
+// their slots, ticket, publication -- happens before it.  Block 0 then
+// waits, so that the kernels of the stream still complete in order; the
+// other blocks leave at once.
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_t* __restrict__ k,
                                                        const uint16_t* __restrict__ v,
                                                        const int32_t* __restrict__ pos, int n, int TB, int late,
-                                                       int nodata) {
+                                                       int nodata, int idle) {
   constexpr int CH = D / 16;
   extern __shared__ __align__(16) uint8_t wts_sm[];
   __shared__ int s_head, s_next, s_guess;
@@ -435,8 +441,22 @@ __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_
       *reinterpret_cast<uint4*>(src) = pack_e4m3x16(x);
     }
   };
+  const bool pre = idle && !pos && !late;
+  int nv0 = 0;
+  unsigned long long total0 = 0;
   if (!pos) {
-    if (threadIdx.x == 0) s_guess = ld_relaxed_gpu(r.state + ST_NEXT_POS);
+    if (threadIdx.x == 0) {
+      if (pre) {
+        const int4 st = ld_relaxed_gpu_v4(r.state);   // head, n_valid, total lo, hi
+        s_head = st.x;
+        nv0 = st.y;
+        total0 = (unsigned long long)(unsigned)st.w << 32 | (unsigned)st.z;
+        s_next = ld_relaxed_gpu(r.state + ST_NEXT_POS);
+        s_guess = s_next;
+      } else {
+        s_guess = ld_relaxed_gpu(r.state + ST_NEXT_POS);
+      }
+    }
     __syncthreads();
     stage_rows(s_guess);
   }
@@ -448,16 +468,16 @@ __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_
     __syncthreads();
     encode(s_guess);
   }
-  // The ring (state, cache, positions) only after the preceding kernel.
-  griddep_wait();
-  int nv0 = 0;
-  unsigned long long total0 = 0;
-  if (threadIdx.x == 0) {
-    const int4 st = __ldcg(reinterpret_cast<const int4*>(r.state));   // head, n_valid, total lo, hi
-    s_head = st.x;
-    nv0 = st.y;
-    total0 = (unsigned long long)(unsigned)st.w << 32 | (unsigned)st.z;
-    s_next = __ldcg(r.state + ST_NEXT_POS);
+  if (!pre) {
+    // The ring (state, cache, positions) only after the preceding kernel.
+    griddep_wait();
+    if (threadIdx.x == 0) {
+      const int4 st = __ldcg(reinterpret_cast<const int4*>(r.state));   // head, n_valid, total lo, hi
+      s_head = st.x;
+      nv0 = st.y;
+      total0 = (unsigned long long)(unsigned)st.w << 32 | (unsigned)st.z;
+      s_next = __ldcg(r.state + ST_NEXT_POS);
+    }
   }
   __syncthreads();
   if (pos || s_next != s_guess) {
@@ -510,6 +530,9 @@ __global__ void __launch_bounds__(kThreads) k_write_tok(RingDev r, const uint16_
     const int tk = atomicAdd(r.state + ST_TICKET_WRITE, 1);
     if (tk == (int)gridDim.x - 1) store_write_plan(r, plan);
   }
+  // (one block waiting is enough to keep the grid from completing before
+  // the preceding kernel; the others leave now and free their SMs)
+  if (pre && blockIdx.x == 0) griddep_wait();
 }
 
 // Many rings of one shape in one launch, as a bulk-copy pipeline.  The work
@@ -1569,21 +1592,21 @@ int write_tok_tokens(const RingDev& r, int n) {
 }
 
 cudaError_t launch_write_tok(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n, int tb,
-                             bool late, bool nodata, cudaStream_t s) {
+                             bool late, bool nodata, bool idle, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((n + tb - 1) / tb)), s, attr);
   cfg.dynamicSmemBytes = (size_t)2 * tb * r.H * r.D * 2 + (size_t)tb * r.D * 4;
   const uint16_t* kk = static_cast<const uint16_t*>(k);
   const uint16_t* vv = static_cast<const uint16_t*>(v);
-  const int lt = late ? 1 : 0, nd = nodata ? 1 : 0;
-  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write_tok<128>, r, kk, vv, pos, n, tb, lt, nd);
-  return cudaLaunchKernelEx(&cfg, k_write_tok<64>, r, kk, vv, pos, n, tb, lt, nd);
+  const int lt = late ? 1 : 0, nd = nodata ? 1 : 0, id = idle ? 1 : 0;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_write_tok<128>, r, kk, vv, pos, n, tb, lt, nd, id);
+  return cudaLaunchKernelEx(&cfg, k_write_tok<64>, r, kk, vv, pos, n, tb, lt, nd, id);
 }
 
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
-                         bool late, cudaStream_t s) {
+                         bool late, bool idle, cudaStream_t s) {
   const int tb = write_tok_tokens(r, n);
-  if (tb > 0) return launch_write_tok(r, k, v, pos, n, tb, late, false, s);
+  if (tb > 0) return launch_write_tok(r, k, v, pos, n, tb, late, false, idle, s);
   const long long items = 2LL * n * r.H * (r.D / 16);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteU - 1) / kWriteU)), s, attr);
@@ -1594,9 +1617,9 @@ cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const i
   return cudaLaunchKernelEx(&cfg, k_write<64>, r, kk, vv, pos, n, lt);
 }
 
-cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s) {
+cudaError_t launch_write_floor(const RingDev& r, int n, bool idle, cudaStream_t s) {
   const int tb = write_tok_tokens(r, n);
-  if (tb > 0) return launch_write_tok(r, nullptr, nullptr, nullptr, n, tb, false, true, s);
+  if (tb > 0) return launch_write_tok(r, nullptr, nullptr, nullptr, n, tb, false, true, idle, s);
   const long long items = 2LL * n * r.H * (r.D / 16);   // the grid of an n-token write
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid_for((items + kWriteU - 1) / kWriteU)), s, attr);

@@ -198,6 +198,13 @@ bool make_bf16_map(CUtensorMap* m, const void* base, int rows, int cols, int box
 // start only at its end, so it needs no record.  The decision and the launch
 // happen under one lock, in launch order, so calls from several threads on
 // one stream see the record of the kernels that really precede theirs.
+//
+// The record also lists the rings that kernels possibly still in flight may
+// read or write: a write or delta adds its rings (older kernels may still
+// run); an attention or a projection leaves its own ring only (a projection
+// that does not write, none); a kernel that lets no dependent start early
+// (calibration, legacy upkeep, the test encoder) leaves none.  A single-ring
+// write whose ring is not listed does its whole work before its wait.
 struct Range {
   const void* p;
   size_t n;
@@ -208,6 +215,8 @@ struct OutRec {
   std::thread::id tid;     // for the per-thread default stream, which each thread has its own of
   uint64_t used;           // LRU stamp; 0 = free entry
   uintptr_t lo[2], hi[2];  // written ranges [lo, hi); empty when lo == hi
+  const kvring* touched[4];   // rings a kernel possibly in flight may read or write
+  int ntouched;               // -1: more than fit (every ring counts as listed)
 };
 
 constexpr int kOutRecs = 64;
@@ -231,7 +240,19 @@ OutRec* find_rec(cudaStream_t s, bool create) {
   oldest->tid = tid;
   oldest->used = ++g_out_clock;
   oldest->lo[0] = oldest->hi[0] = oldest->lo[1] = oldest->hi[1] = 0;
+  oldest->ntouched = 0;
   return oldest;
+}
+
+// Under g_out_mu: whether no kernel possibly in flight on s reads or writes
+// the ring.
+bool ring_idle(cudaStream_t s, const kvring* ring) {
+  const OutRec* e = find_rec(s, false);
+  if (!e) return !g_out_lost;
+  if (e->ntouched < 0) return false;
+  for (int i = 0; i < e->ntouched; ++i)
+    if (e->touched[i] == ring) return false;
+  return true;
 }
 
 // Under g_out_mu: whether the last library kernel on s may write any of the
@@ -254,7 +275,7 @@ bool late_inputs(cudaStream_t s, std::initializer_list<Range> in) {
 
 // Under g_out_mu, after a launch on s succeeded: its kernel is now the last
 // one there, writing the given caller ranges (none for most calls).
-void note_launch(cudaStream_t s, Range a = {nullptr, 0}, Range b = {nullptr, 0}) {
+void note_launch(cudaStream_t s, Range a, Range b, const kvring* touches) {
   OutRec* e = find_rec(s, true);
   e->used = ++g_out_clock;
   const Range rr[2] = {a, b};
@@ -262,21 +283,42 @@ void note_launch(cudaStream_t s, Range a = {nullptr, 0}, Range b = {nullptr, 0})
     e->lo[i] = reinterpret_cast<uintptr_t>(rr[i].p);
     e->hi[i] = rr[i].p ? e->lo[i] + rr[i].n : e->lo[i];
   }
+  e->ntouched = 0;
+  if (touches) e->touched[e->ntouched++] = touches;
 }
 
-// Launches under the lock and records the launch when it succeeded.
+// Launches under the lock and records the launch when it succeeded (its
+// kernel lets its dependents start only after its own wait, or not early at
+// all; `touches`: the ring it reads or writes, if any).
 template <typename F>
-kvring_status tracked(cudaStream_t s, F launch, Range a = {nullptr, 0}, Range b = {nullptr, 0}) {
+kvring_status tracked(cudaStream_t s, F launch, Range a = {nullptr, 0}, Range b = {nullptr, 0},
+                      const kvring* touches = nullptr) {
   const cudaError_t e = launch();
-  if (e == cudaSuccess) note_launch(s, a, b);
+  if (e == cudaSuccess) note_launch(s, a, b, touches);
   return cuda_status(e);
 }
 
 // A launch whose kernel lets its dependents start before its own wait and
-// writes no caller buffer: the stream's record stays as it is.
+// writes no caller buffer: the stream's written ranges stay as they are and
+// its rings join the touched list.
 template <typename F>
-kvring_status passed_through(F launch) {
-  return cuda_status(launch());
+kvring_status passed_through(cudaStream_t s, F launch, kvring* const* rings, int count) {
+  const cudaError_t e = launch();
+  if (e == cudaSuccess) {
+    OutRec* rec = find_rec(s, true);
+    rec->used = ++g_out_clock;
+    for (int i = 0; i < count && rec->ntouched >= 0; ++i) {
+      bool listed = false;
+      for (int j = 0; j < rec->ntouched; ++j) listed = listed || rec->touched[j] == rings[i];
+      if (listed) continue;
+      if (rec->ntouched == 4) {
+        rec->ntouched = -1;
+      } else {
+        rec->touched[rec->ntouched++] = rings[i];
+      }
+    }
+  }
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -425,7 +467,8 @@ kvring_status kvring_write_frame(kvring_t* r, const void* k, const void* v, cons
   const size_t frame = (size_t)n * r->dev.H * r->dev.D * 2;
   std::lock_guard<std::mutex> lk(g_out_mu);
   const bool late = late_inputs(s, {{k, frame}, {v, frame}});
-  return passed_through([&] { return kvr::launch_write(r->dev, k, v, pos, n, late, s); });
+  const bool idle = ring_idle(s, r);
+  return passed_through(s, [&] { return kvr::launch_write(r->dev, k, v, pos, n, late, idle, s); }, &r, 1);
 }
 
 kvring_status kvring_delta_rotate(kvring_t* r, int32_t delta, void* stream) {
@@ -434,7 +477,7 @@ kvring_status kvring_delta_rotate(kvring_t* r, int32_t delta, void* stream) {
     return KVRING_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lk(g_out_mu);
-  return passed_through([&] { return kvr::launch_delta(r->dev, delta, s); });
+  return passed_through(s, [&] { return kvr::launch_delta(r->dev, delta, s); }, &r, 1);
 }
 
 namespace {
@@ -478,7 +521,7 @@ kvring_status kvring_write_frames_many(kvring_t* const* rings, int32_t count, co
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lk(g_out_mu);   // (frames are read after the wait: nothing to check)
-  return passed_through([&] { return kvr::launch_write_many(b, count, n, s); });
+  return passed_through(s, [&] { return kvr::launch_write_many(b, count, n, s); }, rings, count);
 }
 
 kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, int32_t delta, void* stream) {
@@ -493,7 +536,7 @@ kvring_status kvring_delta_rotate_many(kvring_t* const* rings, int32_t count, in
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lk(g_out_mu);
-  return passed_through([&] { return kvr::launch_delta_many(b, count, delta, s); });
+  return passed_through(s, [&] { return kvr::launch_delta_many(b, count, delta, s); }, rings, count);
 }
 
 kvring_status kvring_project_write(kvring_t* r, const void* x, const void* w, int32_t d_model, const int32_t* pos,
@@ -519,7 +562,8 @@ kvring_status kvring_project_write(kvring_t* r, const void* x, const void* w, in
   const Range kvo{kv ? kv_out : nullptr, kv ? 2 * rows : 0};
   std::lock_guard<std::mutex> lk(g_out_mu);
   return tracked(
-      s, [&] { return kvr::launch_project(r->dev, &tmX, &tmW, pos, q_out, kv_out, n, d_model, flags, s); }, qr, kvo);
+      s, [&] { return kvr::launch_project(r->dev, &tmX, &tmW, pos, q_out, kv_out, n, d_model, flags, s); }, qr, kvo,
+      write ? r : nullptr);
 }
 
 kvring_status kvring_legacy_upkeep(kvring_t* r, const void* wk_in, const void* wv_in, void* wk_out, void* wv_out,
@@ -568,7 +612,7 @@ kvring_status kvring_attention(kvring_t* r, const void* q, const int32_t* qpos, 
   std::lock_guard<std::mutex> lk(g_out_mu);
   a.q_late = late_inputs(s, {{q, 2 * rows}}) ? 1 : 0;
   return tracked(s, [&] { return kvr::launch_attention(r->dev, &r->tmK, &r->tmV, a, s); },
-                 Range{out, rows * (a.out_bf16 ? 2 : 4)});
+                 Range{out, rows * (a.out_bf16 ? 2 : 4)}, Range{nullptr, 0}, r);
 }
 
 kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t* qpos, int32_t n_q,
@@ -617,7 +661,7 @@ kvring_status kvring_attention_noalloc(kvring_t* r, const void* q, const int32_t
   std::lock_guard<std::mutex> lk(g_out_mu);
   a.q_late = late_inputs(s, {{q, 2 * rows}}) ? 1 : 0;
   return tracked(s, [&] { return kvr::launch_attention(d, &r->tmK, &r->tmV, a, s); },
-                 Range{out, rows * (a.out_bf16 ? 2 : 4)});
+                 Range{out, rows * (a.out_bf16 ? 2 : 4)}, Range{nullptr, 0}, r);
 }
 
 kvring_status kvring_export(kvring_t* r, void* k_out, void* v_out, float* scales, int32_t* slot_pos,
@@ -650,7 +694,8 @@ kvring_status kvring_debug_write_floor(kvring_t* r, int32_t n, void* stream) {
   if (n > r->cfg.capacity - r->cfg.pinned_prefix || n > r->cfg.max_tokens) return KVRING_ERR_CAPACITY;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lk(g_out_mu);
-  return passed_through([&] { return kvr::launch_write_floor(r->dev, n, s); });
+  const bool idle = ring_idle(s, r);
+  return passed_through(s, [&] { return kvr::launch_write_floor(r->dev, n, idle, s); }, &r, 1);
 }
 
 kvring_status kvring_debug_set_attention_wait(kvring_t* r, int64_t limit_ns, int32_t stall) {

@@ -197,6 +197,16 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int32_t* p) {
   return v;
 }
 
+// Four consecutive words by one relaxed load at device scope (16-byte aligned).
+__device__ __forceinline__ int4 ld_relaxed_gpu_v4(const int32_t* p) {
+  int4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
 // The matching relaxed store, for a word that is only ever a guess.
 __device__ __forceinline__ void st_relaxed_gpu(int32_t* p, int v) {
   asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -556,11 +566,12 @@ namespace kvr {
 cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, const int32_t* pos,
                              int n, cudaStream_t s);
 // late: the preceding kernel may write k or v, so the frame is read only
-// after the wait for it
+// after the wait for it; idle: no kernel that may still run touches the
+// ring, so (with default positions) the whole write happens before the wait
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
-                         bool late, cudaStream_t s);
+                         bool late, bool idle, cudaStream_t s);
 cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s);
-cudaError_t launch_write_floor(const RingDev& r, int n, cudaStream_t s);
+cudaError_t launch_write_floor(const RingDev& r, int n, bool idle, cudaStream_t s);
 cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
 cudaError_t launch_project(const RingDev& r, const CUtensorMap* tmX, const CUtensorMap* tmW,
                            const int32_t* pos, void* q_out, void* kv_out, int n, int dm, int flags,

@@ -188,3 +188,63 @@ def test_write_floor_leaves_the_ring_unchanged():
     assert_ring_equal(ring, orc, "after the last write")
     with pytest.raises(kv.KvRingError):
         ring.write_floor(TINY.capacity + 1)
+
+
+def test_writes_on_alternating_rings_match_the_oracle():
+    """Writes whose preceding kernel touches another ring (the host then lets
+    the whole write -- state read, codes, ticket, publication -- happen
+    before its wait for that kernel), mixed with writes that follow a kernel
+    on their own ring, resets and attention calls, eager and captured in a
+    CUDA graph: every ring equals the oracle byte for byte and every
+    attention meets the bar."""
+    frames = tiny_session(frames=12)
+    pairs = [make_pair(TINY, Ring) for _ in range(2)]
+    for ring, orc in pairs:
+        ring.calibrate(dev(frames[0][1]), dev(frames[0][2]))
+        orc.calibrate(f(frames[0][1]), f(frames[0][2]))
+    dframes = [tuple(dev(x) for x in fr) for fr in frames]
+    outs = [torch.empty((TINY.queries, TINY.heads, TINY.head_dim), device="cuda") for _ in pairs]
+    s = torch.cuda.Stream()
+
+    def step(i, eager_check):
+        q, k, v = dframes[i]
+        for j, (ring, orc) in enumerate(pairs):
+            if i == 9 and j == 1:
+                ring.delta_rotate(kv.TO_OLDEST, stream=s)     # a reset on one ring only
+                if eager_check:
+                    orc.delta_rotate(TO_OLDEST)
+            ring.write(k, v, stream=s)
+            if i % 3 == 2:
+                ring.write(k, v, stream=s)                    # right after a write on the same ring
+            ring.attention(q, out=outs[j], stream=s)
+
+    for i in range(6):
+        with torch.cuda.stream(s):
+            step(i, True)
+        s.synchronize()
+        for j, (ring, orc) in enumerate(pairs):
+            orc.write(f(frames[i][1]), f(frames[i][2]))
+            if i % 3 == 2:
+                orc.write(f(frames[i][1]), f(frames[i][2]))
+            assert_ring_equal(ring, orc, f"eager step {i}, ring {j}")
+            mx, mn = attn_errors(outs[j].cpu().numpy(), attention_exact(orc, f(frames[i][0])))
+            assert mx <= MAX_ABS and mn <= MEAN_ABS, (i, j, mx, mn)
+    # steps 6-11 captured once (the reset before step 9 on ring 1 included) and replayed
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(6, 12):
+            step(i, False)
+    with torch.cuda.stream(s):
+        g.replay()
+    s.synchronize()
+    for i in range(6, 12):
+        for j, (ring, orc) in enumerate(pairs):
+            if i == 9 and j == 1:
+                orc.delta_rotate(TO_OLDEST)
+            orc.write(f(frames[i][1]), f(frames[i][2]))
+            if i % 3 == 2:
+                orc.write(f(frames[i][1]), f(frames[i][2]))
+    for j, (ring, orc) in enumerate(pairs):
+        assert_ring_equal(ring, orc, f"after the graph, ring {j}")
+        mx, mn = attn_errors(outs[j].cpu().numpy(), attention_exact(orc, f(frames[11][0])))
+        assert mx <= MAX_ABS and mn <= MEAN_ABS, (j, mx, mn)
