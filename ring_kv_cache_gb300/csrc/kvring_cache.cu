@@ -1069,6 +1069,119 @@ __global__ void __launch_bounds__(kDpThreads, 1) k_delta_pipe(const __grid_const
   }
 }
 
+// The delta rotation of one ring: one block per (head, run of 128 rolling
+// slots), each thread four (d = 128) or two (d = 64) 16-byte chunks of the
+// run's key rows, all loaded before any arithmetic; the same rotation and
+// re-encoding as the batched pipeline (decoded codes turned by -delta with
+// the table row of delta, each product and sum rounded to fp32), the same
+// delta rule and the same state publication by the last block.  One ring's
+// key cache (7.4 MB at 10 heads x 5,788 slots x 128) is too small to fill a
+// pipeline of one block per SM; independent blocks keep more rows in
+// flight.  idle: no kernel that may still run reads or writes this ring
+// (the host keeps track); then the state read before the wait is final and
+// the whole rotation happens before it, block 0 then waiting so the
+// stream's kernels still complete in order.
+constexpr int kDeltaRows = 128;
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_delta_one(RingDev r, int delta_arg, int idle) {
+  constexpr int CH = D / 16;                         // 16-byte chunks per row
+  constexpr int RSTEP = kThreads / CH;               // rows between a thread's chunks
+  constexpr int PASSES = kDeltaRows / RSTEP;         // 4 (d = 128) or 2 (d = 64)
+  static_assert(PASSES * RSTEP == kDeltaRows, "block shape");
+  __shared__ int s_d, s_nv;
+  const int C = r.C, P = r.P;
+  const int runs = (C - P + kDeltaRows - 1) / kDeltaRows;
+  const int h = (int)blockIdx.x / runs, run = (int)blockIdx.x % runs;
+  const int r0 = P + run * kDeltaRows;
+  griddep_launch_dependents();
+  if (!idle) griddep_wait();   // the ring is touched only after the preceding kernel
+  if (threadIdx.x == 0) {
+    auto load = [&](int w) { return idle ? ld_relaxed_gpu(r.state + w) : __ldcg(r.state + w); };
+    const int nv = load(ST_NVALID);
+    int d = delta_arg;
+    if (d == KVRING_DELTA_TO_OLDEST) {
+      // the oldest rolling position, less the prefix's end with a prefix
+      const int oldest = load(ST_OLDEST_POS);
+      if (nv <= P || oldest == kEmptyPos) {
+        d = 0;
+      } else if (P == 0) {
+        d = oldest;
+      } else {
+        const int gap = oldest - load(ST_PREFIX_END);
+        d = gap > 0 ? gap : 0;
+      }
+    }
+    if (d < 0 || d >= r.max_pos) {
+      if (blockIdx.x == 0) atomicOr(reinterpret_cast<unsigned*>(r.state + ST_ERROR), KVRING_DEVERR_DELTA);
+      d = -1;   // skip the rotation entirely
+    }
+    s_d = d;
+    s_nv = nv;
+  }
+  __syncthreads();
+  const int d = s_d;
+  int rows = d > 0 ? s_nv - r0 : 0;
+  rows = rows < 0 ? 0 : (rows > kDeltaRows ? kDeltaRows : rows);
+  const int k = (int)threadIdx.x % CH, row0 = (int)threadIdx.x / CH;
+  // with 3-D RoPE only the temporal pairs turn: this thread's 8 pairs are
+  // temporal or not for every row (sections are whole chunks of 8 pairs)
+  const bool turns = r.pt == 0 || 8 * k < r.pt;
+  if (rows > 0 && turns) {
+    uint8_t* base = r.k + ((size_t)h * C + r0) * D + 16 * k;
+    uint4 in[PASSES];
+#pragma unroll
+    for (int j = 0; j < PASSES; ++j)
+      if (row0 + j * RSTEP < rows) in[j] = __ldcg(reinterpret_cast<const uint4*>(base + (size_t)(row0 + j * RSTEP) * D));
+    float c[8], sn[8];   // cos / sin of this thread's 8 pairs at delta
+    const float4* t = reinterpret_cast<const float4*>(r.table + (size_t)d * D + 16 * k);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 cs = __ldg(t + i);   // (c, s) of pairs 8k + 2i and 8k + 2i + 1
+      c[2 * i] = cs.x;
+      sn[2 * i] = cs.y;
+      c[2 * i + 1] = cs.z;
+      sn[2 * i + 1] = cs.w;
+    }
+#pragma unroll
+    for (int j = 0; j < PASSES; ++j) {
+      const int row = row0 + j * RSTEP;
+      if (row >= rows) continue;
+      const uint32_t w[4] = {in[j].x, in[j].y, in[j].z, in[j].w};
+      float y[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = e4m3x2_to_f32x2((uint16_t)(w[i] & 0xFFFF));
+        const float2 bb = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
+        y[4 * i + 0] = __fadd_rn(__fmul_rn(a.x, c[2 * i]), __fmul_rn(a.y, sn[2 * i]));
+        y[4 * i + 1] = __fsub_rn(__fmul_rn(a.y, c[2 * i]), __fmul_rn(a.x, sn[2 * i]));
+        y[4 * i + 2] = __fadd_rn(__fmul_rn(bb.x, c[2 * i + 1]), __fmul_rn(bb.y, sn[2 * i + 1]));
+        y[4 * i + 3] = __fsub_rn(__fmul_rn(bb.y, c[2 * i + 1]), __fmul_rn(bb.x, sn[2 * i + 1]));
+      }
+      *reinterpret_cast<uint4*>(base + (size_t)row * D) = pack_e4m3x16(y);
+    }
+  }
+  if (rows > 0 && h == 0 && (int)threadIdx.x < rows) r.slot_pos[r0 + threadIdx.x] -= d;
+  __syncthreads();
+  // The last block publishes (no fence before the ticket: the publication
+  // reads nothing another block wrote, and the next kernel sees the rotated
+  // keys and positions through this grid's end).
+  if (threadIdx.x == 0) {
+    const int tk = atomicAdd(r.state + ST_TICKET_DELTA, 1);
+    if (tk == (int)gridDim.x - 1) {
+      __threadfence();
+      if (d >= 0) {
+        r.state[ST_NEXT_POS] -= d;
+        st_relaxed_gpu(r.state + ST_NEXT_POS_HINT, r.state[ST_NEXT_POS]);
+        if (r.state[ST_OLDEST_POS] != kEmptyPos) r.state[ST_OLDEST_POS] -= d;
+        r.state[ST_LAST_DELTA] = d;
+      }
+      r.state[ST_TICKET_DELTA] = 0;
+      __threadfence();
+    }
+  }
+  if (idle && blockIdx.x == 0) griddep_wait();
+}
+
 // ------------------------------------------------------- legacy upkeep ---
 // The upkeep the ring replaced ("Where the Time Went": every call re-applied
 // RoPE to every cached key, re-quantised the cache and shifted the window by
@@ -1668,10 +1781,13 @@ cudaError_t launch_delta_many(const DeltaMany& b, int count, int delta, cudaStre
   return launch_delta_pipe(b, count, delta, s);
 }
 
-cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s) {
-  DeltaMany b;
-  b.r[0] = r;
-  return launch_delta_pipe(b, 1, delta, s);
+cudaError_t launch_delta(const RingDev& r, int delta, bool idle, cudaStream_t s) {
+  const unsigned runs = (unsigned)((r.C - r.P + kDeltaRows - 1) / kDeltaRows);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(runs * (unsigned)r.H), s, attr);
+  const int id = idle ? 1 : 0;
+  if (r.D == 128) return cudaLaunchKernelEx(&cfg, k_delta_one<128>, r, delta, id);
+  return cudaLaunchKernelEx(&cfg, k_delta_one<64>, r, delta, id);
 }
 
 cudaError_t cache_prepare() {

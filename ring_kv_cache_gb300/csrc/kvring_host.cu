@@ -215,8 +215,8 @@ struct OutRec {
   std::thread::id tid;     // for the per-thread default stream, which each thread has its own of
   uint64_t used;           // LRU stamp; 0 = free entry
   uintptr_t lo[2], hi[2];  // written ranges [lo, hi); empty when lo == hi
-  const kvring* touched[4];   // rings a kernel possibly in flight may read or write
-  int ntouched;               // -1: more than fit (every ring counts as listed)
+  const kvring* touched[KVRING_MAX_BATCH];   // rings a kernel possibly in flight may read or write
+  int ntouched;                              // -1: more than fit (every ring counts as listed)
 };
 
 constexpr int kOutRecs = 64;
@@ -311,7 +311,7 @@ kvring_status passed_through(cudaStream_t s, F launch, kvring* const* rings, int
       bool listed = false;
       for (int j = 0; j < rec->ntouched; ++j) listed = listed || rec->touched[j] == rings[i];
       if (listed) continue;
-      if (rec->ntouched == 4) {
+      if (rec->ntouched == KVRING_MAX_BATCH) {
         rec->ntouched = -1;
       } else {
         rec->touched[rec->ntouched++] = rings[i];
@@ -477,7 +477,8 @@ kvring_status kvring_delta_rotate(kvring_t* r, int32_t delta, void* stream) {
     return KVRING_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lk(g_out_mu);
-  return passed_through(s, [&] { return kvr::launch_delta(r->dev, delta, s); }, &r, 1);
+  const bool idle = ring_idle(s, r);
+  return passed_through(s, [&] { return kvr::launch_delta(r->dev, delta, idle, s); }, &r, 1);
 }
 
 namespace {

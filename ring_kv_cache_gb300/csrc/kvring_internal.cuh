@@ -570,7 +570,7 @@ cudaError_t launch_calibrate(const RingDev& r, const void* k, const void* v, con
 // ring, so (with default positions) the whole write happens before the wait
 cudaError_t launch_write(const RingDev& r, const void* k, const void* v, const int32_t* pos, int n,
                          bool late, bool idle, cudaStream_t s);
-cudaError_t launch_delta(const RingDev& r, int delta, cudaStream_t s);
+cudaError_t launch_delta(const RingDev& r, int delta, bool idle, cudaStream_t s);
 cudaError_t launch_write_floor(const RingDev& r, int n, bool idle, cudaStream_t s);
 cudaError_t launch_encode_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
 cudaError_t launch_project(const RingDev& r, const CUtensorMap* tmX, const CUtensorMap* tmW,
