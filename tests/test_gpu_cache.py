@@ -190,15 +190,19 @@ def test_write_floor_leaves_the_ring_unchanged():
         ring.write_floor(TINY.capacity + 1)
 
 
-def test_writes_on_alternating_rings_match_the_oracle():
-    """Writes whose preceding kernel touches another ring (the host then lets
-    the whole write -- state read, codes, ticket, publication -- happen
-    before its wait for that kernel), mixed with writes that follow a kernel
-    on their own ring, resets and attention calls, eager and captured in a
-    CUDA graph: every ring equals the oracle byte for byte and every
-    attention meets the bar."""
+@pytest.mark.parametrize("prefix", [0, 10])
+def test_writes_on_alternating_rings_match_the_oracle(prefix):
+    """Writes and resets whose preceding kernel touches another ring (the host
+    then lets the whole call -- state read, codes, ticket, publication --
+    happen before its wait for that kernel), mixed with writes that follow a
+    kernel on their own ring, and attention calls, eager and captured in a
+    CUDA graph, with and without a pinned prefix: every ring equals the
+    oracle byte for byte and every attention meets the bar."""
     frames = tiny_session(frames=12)
-    pairs = [make_pair(TINY, Ring) for _ in range(2)]
+    pairs = [(kv.KvRing(TINY.heads, TINY.head_dim, TINY.capacity, TINY.tokens, TINY.max_position,
+                        TINY.rope_base, pinned_prefix=prefix),
+              Ring(TINY.heads, TINY.head_dim, TINY.capacity, TINY.max_position, TINY.rope_base, prefix=prefix))
+             for _ in range(2)]
     for ring, orc in pairs:
         ring.calibrate(dev(frames[0][1]), dev(frames[0][2]))
         orc.calibrate(f(frames[0][1]), f(frames[0][2]))
