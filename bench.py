@@ -919,7 +919,9 @@ def main():
                 "attention_frac_fp8": res["stress"]["attention_tflops"] / fp8_peak,
                 "note": "40 heads x 128, Student-t (3 dof) keys and values, scales log-uniform in [0.1, 10]; "
                         "per call over a wrapped 5,788-slot ring, four rings round-robin"}}),
-            "timing": "per-kernel: CUDA graphs of 16 back-to-back calls on 16 rings, events around replays",
+            "timing": "per-kernel: CUDA graphs of 16 back-to-back calls on 16 rings, events around replays "
+                      "(a write or reset whose ring no kernel still in flight touches runs before its wait, "
+                      "so such calls overlap the call before them)",
             **({} if res["proj"] is None else {
                 "project_write": {
                     "avg_launch_us": res["proj"][0], "algorithmic_flops": res["proj"][1],
