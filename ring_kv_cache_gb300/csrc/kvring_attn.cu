@@ -78,6 +78,10 @@ constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpCvt = 10;
 constexpr uint32_t kTmemCols = 512;
+// The cluster merge moves each CTA's rows in chunks of kMergeRows, each on its
+// own barrier, so that merging a chunk overlaps the copies of the next.
+constexpr int kMergeChunks = 4;
+constexpr int kMergeRows = kTile / 2 / kMergeChunks;   // a CTA owns at most 64 rows
 // Probabilities carry a factor 2^kPShift relative to the running maximum,
 // which is raised only when a tile's maximum exceeds it by more than kTau:
 // the largest probability is 2^(kPShift + kTau) = 2^15, inside f16 (whose
@@ -127,13 +131,13 @@ struct Layout {
   static constexpr int kBarVhFull = 2 * kStages + 6;
   static constexpr int kBarMmaDone = 2 * kStages + 8;
   static constexpr int kBarSFree = 2 * kStages + 9;
-  static constexpr int kBarMerge = 2 * kStages + 10;    // peers' partial rows have landed
-  static constexpr int kBarPvIssuerDone = 2 * kStages + 11;  // every PV of the PV issuer has finished
-  static constexpr int kBarVFull = 2 * kStages + 12;    // V tile of a stage landed
-  static constexpr int kBarVEmpty = 3 * kStages + 12;   // ... widened to f16 by the converters
-  static constexpr int kBarNever = 4 * kStages + 12;    // never arrived on: the debug stall waits here
-  static constexpr int kBarRows = 4 * kStages + 13;     // the query prologue's RoPE rows have landed
-  static constexpr int kNumBars = 4 * kStages + 14;
+  static constexpr int kBarPvIssuerDone = 2 * kStages + 10;  // every PV of the PV issuer has finished
+  static constexpr int kBarVFull = 2 * kStages + 11;    // V tile of a stage landed
+  static constexpr int kBarVEmpty = 3 * kStages + 11;   // ... widened to f16 by the converters
+  static constexpr int kBarNever = 4 * kStages + 11;    // never arrived on: the debug stall waits here
+  static constexpr int kBarRows = 4 * kStages + 12;     // the query prologue's RoPE rows have landed
+  static constexpr int kBarMerge = 4 * kStages + 13;    // [kMergeChunks] a chunk of the peers' partial rows landed
+  static constexpr int kNumBars = 4 * kStages + 13 + kMergeChunks;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kLseAll = kMisc + 64;             // float [8 splits][128]: the cluster's log2-sum-exps
   static constexpr int kBytes = kLseAll + 8 * kTile * 4;
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(L::kBarMmaDone), 1);
     mbar_init(bar(L::kBarSFree), kGroupThreads / 32);  // a tile's S is in its group's registers
-    mbar_init(bar(L::kBarMerge), 1);
+    for (int c = 0; c < kMergeChunks; ++c) mbar_init(bar(L::kBarMerge + c), 1);
     mbar_init(bar(L::kBarPvIssuerDone), 1);
     mbar_init(bar(L::kBarNever), 1);
     mbar_init(bar(L::kBarRows), 1);
@@ -1073,9 +1077,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // before the barrier), and no CTA needs its f16 V tiles any more: each CTA
   // bulk-copies the rows every peer owns into that peer's f16 V space (one
   // slot per sender), completing on the peer's merge barrier, then merges
-  // its own rows from its own shared memory and stores them.  A CTA leaves
-  // once its outgoing copies have read its rows and its incoming ones have
-  // landed, so no second cluster barrier is needed.
+  // its own rows from its own shared memory and stores them.  Rows travel in
+  // chunks of kMergeRows, each completing on its own barrier, and a chunk is
+  // merged and stored as soon as it has landed.  A CTA leaves once its
+  // outgoing copies have read its rows and its incoming ones have landed, so
+  // no second cluster barrier is needed.
   if (prm.cluster_merge) {
     __syncwarp();
     cluster_sync_all();
@@ -1084,16 +1090,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ns = prm.nsplit;
     const int maxr = (kTile + ns - 1) / ns;        // rows of one slot
     const int r0 = split * kTile / ns, r1 = (split + 1) * kTile / ns, nr = r1 - r0;
+    auto chunk_rows = [&](int c, int rows) {
+      const int left = rows - c * kMergeRows;
+      return left < 0 ? 0 : (left < kMergeRows ? left : kMergeRows);
+    };
     if (threadIdx.x == kWarpTma * 32) {
-      mbar_arrive_expect_tx(bar(L::kBarMerge), (uint32_t)((ns - 1) * nr) * SPB);
-      for (int p = 0; p < ns; ++p) {
-        if (p == split) continue;
-        const int p0 = p * kTile / ns, p1 = (p + 1) * kTile / ns;
-        const int slot = split < p ? split : split - 1;
-        bulk_copy_to_cluster(dsmem_addr(sbase + L::kVh + (uint32_t)(slot * maxr) * SPB, (uint32_t)p),
-                             sbase + L::kK + (uint32_t)p0 * SPB, (uint32_t)(p1 - p0) * SPB,
-                             dsmem_addr(bar(L::kBarMerge), (uint32_t)p));
-      }
+      for (int c = 0; c < kMergeChunks; ++c)
+        if (chunk_rows(c, nr) > 0)
+          mbar_arrive_expect_tx(bar(L::kBarMerge + c), (uint32_t)((ns - 1) * chunk_rows(c, nr)) * SPB);
+      // chunk-major, so that every peer's first chunk is on its way first
+      for (int c = 0; c < kMergeChunks; ++c)
+        for (int p = 0; p < ns; ++p) {
+          if (p == split) continue;
+          const int p0 = p * kTile / ns, p1 = (p + 1) * kTile / ns;
+          const int rows = chunk_rows(c, p1 - p0);
+          if (rows == 0) continue;
+          const int slot = split < p ? split : split - 1;
+          bulk_copy_to_cluster(
+              dsmem_addr(sbase + L::kVh + (uint32_t)(slot * maxr + c * kMergeRows) * SPB, (uint32_t)p),
+              sbase + L::kK + (uint32_t)(p0 + c * kMergeRows) * SPB, (uint32_t)rows * SPB,
+              dsmem_addr(bar(L::kBarMerge + c), (uint32_t)p));
+        }
       bulk_commit();
     }
     if (warp < kSoftmaxThreads / 32) {
@@ -1123,65 +1140,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s2 = 0; s2 < 8; ++s2)
           if (s2 < ns) wts[s2 * kTile + threadIdx.x] = lv[s2] * gsc;
       }
+      sync_softmax();   // the weights
       // The peers' copies were issued unconditionally after the cluster
-      // barrier, so they land even on an aborted call: wait for them
+      // barrier, so they land even on an aborted call: wait for every chunk
       // whatever the abort flag says (a CTA must not exit while copies into
-      // its shared memory are in flight).
-      volatile int no_abort = 0;
-      const bool landed =
-          __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarMerge), 0, &no_abort, wait_ns));
-      sync_softmax();
+      // its shared memory are in flight); a chunk that never lands is a
+      // timeout.
       const int rows_live = prm.n_q - qt * kTile < kTile ? prm.n_q - qt * kTile : kTile;
-      float4 acc[MT];
-#pragma unroll
-      for (int i = 0; i < MT; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      // split s2's rows of this range: own staging, or the sender's slot;
-      // two splits at a time with all their loads issued before any use
+      // split s2's rows of this range: own staging, or the sender's slot
       auto rows_of = [&](int s2) -> const uint8_t* {
         return s2 == split ? sm + L::kK + (size_t)r0 * SPB
                            : sm + L::kVh + (size_t)((s2 < split ? s2 : s2 - 1) * maxr) * SPB;
       };
-      for (int s0 = 0; landed && s0 < ns; s0 += 2) {
-        float4 v[2][MT];
+      constexpr int IPC = MT / kMergeChunks;   // float4 tasks of a thread in one chunk
+      static_assert(MT % kMergeChunks == 0 && IPC * kSoftmaxThreads == kMergeRows * (D / 4),
+                    "a chunk is a whole number of task rounds");
+      bool landed = true;
+#pragma unroll 1
+      for (int c = 0; c < kMergeChunks && c * kMergeRows < nr; ++c) {
+        volatile int no_abort = 0;
+        landed = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar(L::kBarMerge + c), 0, &no_abort, wait_ns)) && landed;
+        if (!landed) continue;
+        float4 acc[IPC];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint8_t* src = rows_of(s0 + q < ns ? s0 + q : s0);
+        for (int i = 0; i < IPC; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // two splits at a time, all their loads issued before any use
+        for (int s0 = 0; s0 < ns; s0 += 2) {
+          float4 v[2][IPC];
 #pragma unroll
-          for (int i = 0; i < MT; ++i) {
-            const int idx = threadIdx.x + i * kSoftmaxThreads;
-            const int lr = idx / (D / 4), c4 = idx % (D / 4);
-            v[q][i] = idx < ntask ? *reinterpret_cast<const float4*>(src + (size_t)lr * SPB + 16 * c4)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < 2; ++q) {
+            const uint8_t* src = rows_of(s0 + q < ns ? s0 + q : s0);
+#pragma unroll
+            for (int i = 0; i < IPC; ++i) {
+              const int idx = threadIdx.x + (c * IPC + i) * kSoftmaxThreads;
+              const int lr = idx / (D / 4), c4 = idx % (D / 4);
+              v[q][i] = idx < ntask ? *reinterpret_cast<const float4*>(src + (size_t)lr * SPB + 16 * c4)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            if (s0 + q >= ns) break;
+#pragma unroll
+            for (int i = 0; i < IPC; ++i) {
+              const int idx = threadIdx.x + (c * IPC + i) * kSoftmaxThreads;
+              const float w = idx < ntask ? wts[(s0 + q) * kTile + idx / (D / 4)] : 0.f;
+              acc[i].x = fmaf(w, v[q][i].x, acc[i].x);
+              acc[i].y = fmaf(w, v[q][i].y, acc[i].y);
+              acc[i].z = fmaf(w, v[q][i].z, acc[i].z);
+              acc[i].w = fmaf(w, v[q][i].w, acc[i].w);
+            }
           }
         }
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          if (s0 + q >= ns) break;
-#pragma unroll
-          for (int i = 0; i < MT; ++i) {
-            const int idx = threadIdx.x + i * kSoftmaxThreads;
-            const float w = idx < ntask ? wts[(s0 + q) * kTile + idx / (D / 4)] : 0.f;
-            acc[i].x = fmaf(w, v[q][i].x, acc[i].x);
-            acc[i].y = fmaf(w, v[q][i].y, acc[i].y);
-            acc[i].z = fmaf(w, v[q][i].z, acc[i].z);
-            acc[i].w = fmaf(w, v[q][i].w, acc[i].w);
+        for (int i = 0; i < IPC; ++i) {
+          const int idx = threadIdx.x + (c * IPC + i) * kSoftmaxThreads;
+          const int row = r0 + idx / (D / 4), c4 = idx % (D / 4);
+          if (idx >= ntask || row >= rows_live) continue;
+          const size_t e = ((size_t)(qt * kTile + row) * H + h) * D + 4 * c4;
+          if (prm.out_bf16) {
+            const __nv_bfloat162 a0 = __floats2bfloat162_rn(acc[i].x, acc[i].y), a1 = __floats2bfloat162_rn(acc[i].z, acc[i].w);
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(prm.out) + e) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1));
+          } else {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + e) = acc[i];
           }
         }
       }
-#pragma unroll
-      for (int i = 0; i < MT; ++i) {
-        const int idx = threadIdx.x + i * kSoftmaxThreads;
-        const int row = r0 + idx / (D / 4), c4 = idx % (D / 4);
-        if (!landed || idx >= ntask || row >= rows_live) continue;
-        const size_t e = ((size_t)(qt * kTile + row) * H + h) * D + 4 * c4;
-        if (prm.out_bf16) {
-          const __nv_bfloat162 a0 = __floats2bfloat162_rn(acc[i].x, acc[i].y), a1 = __floats2bfloat162_rn(acc[i].z, acc[i].w);
-          *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(prm.out) + e) =
-              make_uint2(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1));
-        } else {
-          *reinterpret_cast<float4*>(reinterpret_cast<float*>(prm.out) + e) = acc[i];
-        }
-      }
+      if (!landed) misc->abort = 1;
     }
     // the outgoing copies have read this CTA's rows before it may leave
     if (threadIdx.x == kWarpTma * 32) bulk_wait_read();
