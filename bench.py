@@ -387,18 +387,33 @@ def gpu_arm(args, rank, world):
         levels.append(lv)
     levels = np.concatenate(levels).ravel()
     errs = [int(r.export()["state"][kv.STATE["error"]].item()) for r in rings]
-    batched = batched_upkeep(args, dev, stream) if "batched" in args.legs else None
-    legacy_us = legacy_upkeep_us(dev, stream) if "legacy" in args.legs else None
-    proj = project_write_us(dev, stream) if "project" in args.legs else None
+    leg_errors = {}
+    batched = run_leg(args.legs, "batched", lambda: batched_upkeep(args, dev, stream), leg_errors)
+    legacy_us = run_leg(args.legs, "legacy", lambda: legacy_upkeep_us(dev, stream), leg_errors)
+    proj = run_leg(args.legs, "project", lambda: project_write_us(dev, stream), leg_errors)
     del g_warm, g_timed, g_attn, g_write, g_delta, g_wfloor, g_dfloor, g_e2e
-    full_step = full_step_60_layers(dev, stream) if "full_step" in args.legs else None
-    stress = stress_40_heads(dev, stream) if "stress" in args.legs else None
-    return dict(total_ms=total_ms, w_us=w_us, a_us=a_us, d_us=d_us, wf_us=wf_us, df_us=df_us,
+    full_step = run_leg(args.legs, "full_step", lambda: full_step_60_layers(dev, stream), leg_errors)
+    stress = run_leg(args.legs, "stress", lambda: stress_40_heads(dev, stream), leg_errors)
+    return dict(total_ms=total_ms, leg_errors=leg_errors, w_us=w_us, a_us=a_us, d_us=d_us, wf_us=wf_us, df_us=df_us,
                 full_step=full_step, stress=stress, e2e_ms=e2e_ms, copy_us=copy_us,
                 clocks=clk.summary(),
                 batched=batched, legacy_us=legacy_us, proj=proj,
                 resets=timed_resets,
                 levels=levels, device_errors=int(np.bitwise_or.reduce(errs)))
+
+
+def run_leg(legs, name, fn, errors):
+    """Runs one extra measurement if it was asked for.  The headline step is
+    measured before any of them, so a leg that raises is reported under
+    `leg_errors` in the JSON line (and on stderr) instead of ending the run."""
+    if name not in legs:
+        return None
+    try:
+        return fn()
+    except Exception as e:  # noqa: BLE001 -- any failure of a leg is reported, not fatal
+        errors[name] = f"{type(e).__name__}: {e}"[:300]
+        print(f"bench: leg {name} failed: {errors[name]}", file=sys.stderr)
+        return None
 
 
 def batched_upkeep(args, dev, stream):
@@ -964,8 +979,13 @@ def main():
         "clocks": res["clocks"],
         "device_errors": res["device_errors"],
     }
+    errors = dict(res["leg_errors"])
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline()
+        cpu = run_leg({"cpu_baseline"}, "cpu_baseline", cpu_baseline, errors)
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+    if errors:
+        line["leg_errors"] = errors
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
