@@ -13,7 +13,8 @@ Modules:
   rope       RoPE table (fp32 from float64 libm) and rotations (pinned fp32,
              exact float64).
   ring       one layer's ring cache: calibrate, write, delta rotate.
-  attention  float64 attention over the cache (the reference), brute-force
+  attention  float64 attention over the cache (the reference), the same in
+             parts of the slots merged by their log-sum-exps, brute-force
              linear window, the slot-order-positions negative case, and a
              diagnostic that mirrors the kernel's FP8 operand choices.
   legacy     the original upkeep the ring replaced (window copy, RoPE of

@@ -15,6 +15,11 @@ queries in float64 without any quantisation, keys and values dequantised
 from the same FP8 cache bytes (code value times the fp32 scale, in float64),
 and a float64 softmax with the row maximum subtracted.
 
+``attention_part_f64`` / ``merge_parts_f64`` / ``attention_split`` restate
+the split of one query tile's slots among several workers: each part's
+normalised output with its log-sum-exp, and their combination, which is
+exact up to rounding (the merged parts equal the whole softmax).
+
 ``attention_emulated`` is a diagnostic that repeats the CUDA kernel's
 choices (queries split into FP8 terms with a per-row scale, probabilities
 scaled by 2^7 relative to a lazily raised running maximum and carried as FP8
@@ -61,6 +66,63 @@ def attention_exact(ring, q: np.ndarray, qpos=None) -> np.ndarray:
     qt = ring.rope_f64(q, qpos)
     k, v, _ = ring.dequantised()
     return softmax_attention_f64(qt, k, v)
+
+
+def attention_part_f64(qt: np.ndarray, k: np.ndarray, v: np.ndarray):
+    """Attention over one part of the slots, normalised within the part.
+
+    Returns (o, lse): o[t,h,:] = sum_j softmax_j(s) v[h,j,:] over the part's
+    slots j only, with s = qt[t,h]·k[h,j] / sqrt(d), and lse[t,h] =
+    log sum_j exp(s), the part's log-sum-exp in float64.  An empty part gives
+    zeros and lse = -inf.  This is the partial result a split of the keys
+    produces when one query tile's slots are shared among several workers.
+    """
+    n, H, d = qt.shape
+    if k.shape[1] == 0:
+        return np.zeros((n, H, d), dtype=np.float64), np.full((n, H), -np.inf)
+    s = np.einsum("thd,hjd->thj", qt, k) / math.sqrt(d)
+    m = s.max(axis=2)
+    p = np.exp(s - m[:, :, None])
+    ell = p.sum(axis=2)
+    o = np.einsum("thj,hjd->thd", p, v) / ell[:, :, None]
+    return o, m + np.log(ell)
+
+
+def merge_parts_f64(parts) -> np.ndarray:
+    """Combine partial results (o_s, lse_s) of disjoint parts of the slots.
+
+    With M = max_s lse_s and w_s = exp(lse_s - M), the whole softmax is
+    o = sum_s w_s o_s / sum_s w_s, because exp(lse_s) is part s's sum of
+    exponentials and o_s its normalised output.  Parts with lse = -inf
+    weigh nothing; a row whose parts are all empty is zero.
+    """
+    os_ = np.stack([np.asarray(o, dtype=np.float64) for o, _ in parts])      # [S, n, H, d]
+    lse = np.stack([np.asarray(l, dtype=np.float64) for _, l in parts])      # [S, n, H]
+    M = lse.max(axis=0)
+    finite = np.isfinite(M)
+    w = np.where(np.isfinite(lse), np.exp(lse - np.where(finite, M, 0.0)[None]), 0.0)
+    den = w.sum(axis=0)
+    num = (w[..., None] * os_).sum(axis=0)
+    return np.where(den[..., None] > 0, num / np.where(den > 0, den, 1.0)[..., None], 0.0)
+
+
+def attention_split(ring, q: np.ndarray, bounds, qpos=None) -> np.ndarray:
+    """``attention_exact`` computed in parts and merged: the filled slots (in
+    the ring's slot order) are cut at ``bounds`` (0 = b_0 <= b_1 <= ... <= b_S
+    = the number of filled slots; equal neighbours give empty parts), each
+    part gives its normalised output and log-sum-exp, and ``merge_parts_f64``
+    combines them."""
+    q = np.asarray(q, dtype=np.float64)
+    n = q.shape[0]
+    if qpos is None:
+        qpos = ring.next_pos - n + np.arange(n)
+    qt = ring.rope_f64(q, qpos)
+    k, v, _ = ring.dequantised()
+    b = [int(x) for x in bounds]
+    if b[0] != 0 or b[-1] != k.shape[1] or any(x > y for x, y in zip(b, b[1:])):
+        raise ValueError(f"bounds {b} do not cut the {k.shape[1]} filled slots")
+    parts = [attention_part_f64(qt, k[:, b0:b1], v[:, b0:b1]) for b0, b1 in zip(b, b[1:])]
+    return merge_parts_f64(parts)
 
 
 def attention_linear_window(history, q, qpos, ring) -> np.ndarray:

@@ -4,15 +4,19 @@ Checked against: closed forms (equal keys give the mean of the values, one
 filled slot returns its value), a pure-Python brute force on a tiny case,
 and torch's scaled_dot_product_attention in float64 (a library routine).
 The kernel-mirroring diagnostic is checked to converge to the reference as
-its FP8 term counts grow.
+its FP8 term counts grow.  The split of the slots into parts merged by their
+log-sum-exps is checked against the whole softmax for arbitrary cuts, a
+two-slot closed form and its degenerate cases.
 """
 import math
 
 import numpy as np
+import pytest
 import torch
 
 from oracle import e4m3, Ring
-from oracle.attention import attention_exact, attention_emulated
+from oracle.attention import (attention_emulated, attention_exact, attention_part_f64, attention_split,
+                              merge_parts_f64)
 from oracle.rope import rotate_f64
 from workloads import TINY, f32_from_bf16, tiny_session, prod_session, PROD
 
@@ -134,3 +138,83 @@ def test_kernel_mirror_two_f16_probability_terms():
     lo = (p - hi.astype(np.float32)).astype(np.float16)
     rel = np.abs(hi.astype(np.float64) + lo.astype(np.float64) - p) / p
     assert rel.max() <= 2.0 ** -21
+
+
+# ---------------------------------------------------------------- split merge
+# The slots of one query tile shared among several workers: each part's
+# normalised output with its log-sum-exp, merged.  Pinned by the identity
+# that the merged parts are the whole softmax, by a two-slot closed form,
+# and by the degenerate cases.
+
+
+
+def test_split_merge_equals_whole_softmax_for_any_cut():
+    r, frames = _tiny_ring(5)                       # wrapped tiny ring
+    q = f32_from_bf16(frames[5][0])
+    want = attention_exact(r, q)
+    nv = r.n_valid
+    rng = np.random.default_rng(21)
+    cuts = [[0, nv], [0, 1, nv], [0, nv - 1, nv], [0, nv // 2, nv // 2, nv],
+            [0, 0, nv, nv]]                         # empty parts at either end and inside
+    for s in (3, 5, 8):
+        inner = np.sort(rng.integers(0, nv + 1, size=s - 1))
+        cuts.append([0, *inner.tolist(), nv])
+    for b in cuts:
+        got = attention_split(r, q, b)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-13), b
+
+
+def test_split_merge_order_of_parts_does_not_matter():
+    rng = np.random.default_rng(5)
+    qt = rng.standard_normal((4, 2, 16)) * 3
+    k = rng.standard_normal((2, 30, 16))
+    v = rng.standard_normal((2, 30, 16))
+    parts = [attention_part_f64(qt, k[:, a:b], v[:, a:b]) for a, b in ((0, 7), (7, 7), (7, 19), (19, 30))]
+    fwd = merge_parts_f64(parts)
+    rev = merge_parts_f64(parts[::-1])
+    assert np.allclose(fwd, rev, rtol=1e-14, atol=1e-15)
+
+
+def test_split_merge_two_slots_closed_form():
+    # one query, one head, d = 4: scores s1 = 2 / sqrt(4) = 1 and s2 = 0
+    qt = np.array([[[1.0, 1.0, 0.0, 0.0]]])
+    k = np.array([[[1.0, 1.0, 0.0, 0.0], [1.0, -1.0, 0.0, 0.0]]])
+    v = np.array([[[3.0, 0.0, 0.0, 1.0], [-1.0, 2.0, 0.0, 1.0]]])
+    p1 = attention_part_f64(qt, k[:, :1], v[:, :1])
+    p2 = attention_part_f64(qt, k[:, 1:], v[:, 1:])
+    assert p1[1][0, 0] == 1.0 and p2[1][0, 0] == 0.0    # a one-slot part's lse is its score
+    e = math.e
+    want = (e * v[0, 0] + 1.0 * v[0, 1]) / (e + 1.0)
+    assert np.allclose(merge_parts_f64([p1, p2])[0, 0], want, rtol=1e-15)
+
+
+def test_split_merge_single_part_and_empty_parts():
+    rng = np.random.default_rng(8)
+    qt = rng.standard_normal((3, 2, 8))
+    k = rng.standard_normal((2, 5, 8))
+    v = rng.standard_normal((2, 5, 8))
+    whole = attention_part_f64(qt, k, v)
+    assert np.array_equal(merge_parts_f64([whole]), whole[0])          # weight exp(0) = 1
+    empty = attention_part_f64(qt, k[:, :0], v[:, :0])
+    assert np.all(empty[0] == 0) and np.all(np.isneginf(empty[1]))
+    assert np.array_equal(merge_parts_f64([empty, whole, empty]), whole[0])
+    got = merge_parts_f64([empty, empty])
+    assert np.all(got == 0) and not np.any(np.isnan(got))
+
+
+def test_split_part_lse_is_the_log_of_the_sum_of_exponentials():
+    rng = np.random.default_rng(13)
+    qt = rng.standard_normal((2, 1, 8)) * 4
+    k = rng.standard_normal((1, 6, 8))
+    v = rng.standard_normal((1, 6, 8))
+    _, lse = attention_part_f64(qt, k, v)
+    s = np.einsum("thd,hjd->thj", qt, k) / math.sqrt(8)
+    assert np.allclose(lse, np.log(np.exp(s).sum(axis=2)), rtol=1e-14)
+
+
+def test_split_rejects_bounds_that_do_not_cut_the_slots():
+    r, frames = _tiny_ring(2)
+    q = f32_from_bf16(frames[2][0])
+    for b in ([1, r.n_valid], [0, r.n_valid - 1], [0, 5, 3, r.n_valid]):
+        with pytest.raises(ValueError):
+            attention_split(r, q, b, np.arange(12))
